@@ -1,0 +1,385 @@
+#!/usr/bin/env python3
+"""Benchmark: cone-beam forward projection + matched backprojection (Siddon) on one B300.
+
+Workload: 256^3 float32 ellipsoid phantom, 360-view circular cone orbit (sid 500, sdd 1000),
+384 x 384 detector at 1.2, voxel spacing 1.0.  One step = one ct_project + one ct_backproject
+(the whole hot path; geometry staging happens once, before timing).
+
+Metric: ray-voxel updates per second of the pair, 2 U / (t_FP + t_BP), where U is the number of
+ray-voxel segments one pass walks (counted on the host in float64 from the geometry).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 it is launched under torchrun, one rank per GPU; each rank runs an independent replica
+of the workload (the path needs no exchange for replicas) and rank 0 prints one JSON line.
+`--impl reference` times the float64 CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from fan_beam_projector_siddon_b300 import workloads as W  # noqa: E402
+
+METRIC = "cone FP+BP ray-voxel updates/s at 256^3x360 views"
+UNIT = "updates/s"
+CONFIG_ID = 3
+
+
+# ----------------------------------------------------------------------------------------------
+# units of work
+# ----------------------------------------------------------------------------------------------
+
+def count_updates(w: W.Workload, views=None) -> int:
+    """Ray-voxel segments walked by one pass: per ray that meets the box, 1 + the number of
+    interior cell planes it crosses (float64, vectorised per view).  Independent of both the
+    CUDA path and the oracle."""
+    nz, ny, nx = w.vol_shape
+    s = w.voxel_spacing
+    dims = 2 if w.is_2d else 3
+    ncell = np.array([nx, ny, nz], dtype=np.float64)[:dims]
+    half = 0.5 * ncell * s
+    uu = (np.arange(w.n_u) - (w.n_u - 1) / 2.0) * w.du
+    vv = (np.arange(w.n_v) - (w.n_v - 1) / 2.0) * w.dv if not w.is_2d else np.zeros(1)
+    parallel = w.beam in (W.PARALLEL2D, W.PARALLEL3D)
+    total = 0
+    view_ids = range(w.n_views) if views is None else views
+    for k in view_ids:
+        r = w.views[k]
+        if w.is_2d:
+            first, ctr, du = r[0:2], r[2:4], r[4:6]
+            dv = np.zeros(2)
+        else:
+            first, ctr, du, dv = r[0:3], r[3:6], r[6:9], r[9:12]
+        pix = ctr + uu[:, None, None] * du + vv[None, :, None] * dv      # (U, V, dims)
+        if parallel:
+            e = pix
+            d = np.broadcast_to(first, pix.shape)
+            amin = np.full(pix.shape[:2], -np.inf)
+            amax = np.full(pix.shape[:2], np.inf)
+        else:
+            e = np.broadcast_to(first, pix.shape)
+            d = pix - first
+            amin = np.zeros(pix.shape[:2])
+            amax = np.ones(pix.shape[:2])
+        ok = np.ones(pix.shape[:2], dtype=bool)
+        with np.errstate(divide="ignore", invalid="ignore"):
+            for a in range(dims):
+                da, ea = d[..., a], e[..., a]
+                nzd = da != 0
+                t1 = np.where(nzd, (-half[a] - ea) / np.where(nzd, da, 1), -np.inf)
+                t2 = np.where(nzd, (half[a] - ea) / np.where(nzd, da, 1), np.inf)
+                amin = np.maximum(amin, np.minimum(t1, t2))
+                amax = np.minimum(amax, np.maximum(t1, t2))
+                ok &= nzd | ((ea >= -half[a]) & (ea < half[a]))
+        hit = ok & (amax > amin)
+        segs = np.where(hit, 1, 0).astype(np.int64)
+        for a in range(dims):
+            ci = (e[..., a] + np.where(hit, amin, 0) * d[..., a] + half[a]) / s
+            co = (e[..., a] + np.where(hit, amax, 0) * d[..., a] + half[a]) / s
+            lo, hi = np.minimum(ci, co), np.maximum(ci, co)
+            first_plane = np.maximum(np.floor(lo) + 1, 1)
+            last_plane = np.minimum(np.ceil(hi) - 1, ncell[a] - 1)
+            segs += np.where(hit, np.maximum(0, last_plane - first_plane + 1), 0).astype(np.int64)
+        total += int(segs.sum())
+    return total
+
+
+# ----------------------------------------------------------------------------------------------
+# clocks
+# ----------------------------------------------------------------------------------------------
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.25)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        mhz, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                mhz.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not mhz:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(mhz)}
+
+
+# ----------------------------------------------------------------------------------------------
+# CPU oracle timing (reference arm and cpu_baseline)
+# ----------------------------------------------------------------------------------------------
+
+def oracle_sample_rate(w: W.Workload, x: np.ndarray, n_views: int, threads: int):
+    """Oracle FP+BP over n_views evenly spaced views; returns (updates/s, seconds, updates)."""
+    import oracle
+    ids = np.linspace(0, w.n_views, n_views, endpoint=False).astype(int)
+    sub = w.subset(ids)
+    go = oracle.Geometry.from_workload(sub)
+    u = count_updates(sub)
+    y = W.random_sinogram(sub, 7)
+    t0 = time.perf_counter()
+    go.project(x, threads=threads)
+    go.backproject(y, threads=threads)
+    dt = time.perf_counter() - t0
+    return 2 * u / dt, dt, 2 * u
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    w = W.config(CONFIG_ID)
+    x = w.phantom()
+    cores = os.cpu_count() or 1
+    n_views = int(max(4, min(w.n_views, cores)))
+    rates, times = [], []
+    for _ in range(args.warmup):
+        oracle_sample_rate(w, x, max(1, n_views // 4), cores)
+    for _ in range(args.steps):
+        r, dt, _ = oracle_sample_rate(w, x, n_views, cores)
+        rates.append(r)
+        times.append(dt)
+    value = statistics.median(rates)
+    sample = (f"FP+BP of {n_views} evenly spaced views of {w.n_views} per step "
+              f"(float64 oracle, thread pool over views)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * statistics.median(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "volume": list(w.vol_shape), "views": w.n_views,
+                   "detector": [w.n_u, w.n_v], "sample_views": n_views},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------------------------
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6400.0, "fallback"
+
+
+def run_ours(args, rank, world):
+    import torch
+    import torch.distributed as dist
+    from fan_beam_projector_siddon_b300 import build as ct_build
+    if rank == 0 or not os.path.exists(ct_build.LIB):
+        ct_build.build()
+    if world > 1:
+        dist.barrier()
+    import fan_beam_projector_siddon_b300 as ct
+
+    dev = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(dev)
+    w = W.config(CONFIG_ID)
+    x_host = w.phantom()
+    U = count_updates(w)
+    g = ct.Geometry.from_workload(w)
+    vol = torch.from_numpy(x_host).cuda()
+    sino = torch.empty(w.sino_shape, dtype=torch.float32, device="cuda")
+    back = torch.empty(w.volume_shape, dtype=torch.float32, device="cuda")
+    ws = g.new_workspace()
+    wsb = 0 if ws is None else ws.numel()
+    wsp = None if ws is None else ws.data_ptr()
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")   # > 126 MB L2
+
+    def fp():
+        ct.ct_project(g.handle, vol.data_ptr(), sino.data_ptr(), wsp, wsb, sp)
+
+    def bp():
+        ct.ct_backproject(g.handle, sino.data_ptr(), back.data_ptr(), wsp, wsb, sp)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        fp()
+        bp()
+    torch.cuda.synchronize()
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev) as clk:
+        for k in range(args.steps):
+            flush.zero_()
+            ev[k][0].record(stream)
+            fp()
+            ev[k][1].record(stream)
+            bp()
+            ev[k][2].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    fp_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    bp_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    step_ms = [a + b for a, b in zip(fp_ms, bp_ms)]
+    mean_step = sum(step_ms) / len(step_ms)
+    if world > 1:
+        t = torch.tensor([mean_step], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        mean_step = float(t.item())
+    value = world * 2 * U / (mean_step * 1e-3)
+
+    # ---- end to end through the C ABI: pinned host in, host out, copies inside the region ----
+    vol_h = torch.from_numpy(x_host).pin_memory()
+    meas_h = torch.from_numpy(W.random_sinogram(w, 3)).pin_memory()
+    sino_h = torch.empty(w.sino_shape, dtype=torch.float32).pin_memory()
+    back_h = torch.empty(w.volume_shape, dtype=torch.float32).pin_memory()
+    meas = torch.empty_like(sino)
+    e2e_steps = max(2, min(args.steps, 5))
+
+    def e2e_step():
+        vol.copy_(vol_h, non_blocking=True)
+        meas.copy_(meas_h, non_blocking=True)
+        ct.ct_project(g.handle, vol.data_ptr(), sino.data_ptr(), wsp, wsb, sp)
+        sino_h.copy_(sino, non_blocking=True)
+        ct.ct_backproject(g.handle, meas.data_ptr(), back.data_ptr(), wsp, wsb, sp)
+        back_h.copy_(back, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = vol_h.numel() * 4 + meas_h.numel() * 4
+    d2h = sino_h.numel() * 4 + back_h.numel() * 4
+
+    if rank != 0:
+        return 0
+    # ---- roofline of the dominant kernel -----------------------------------------------------
+    peak, peak_kind = load_peaks()
+    fp_avg, bp_avg = sum(fp_ms) / len(fp_ms), sum(bp_ms) / len(bp_ms)
+    nrays, nvox = w.n_rays, w.n_voxels
+    fp_bytes = 4 * U + 4 * nrays + 4 * nvox
+    bp_bytes = 4 * U + 4 * nrays + 8 * nvox
+    dom = ("ct_backproject", bp_bytes, bp_avg) if bp_avg >= fp_avg else ("ct_project", fp_bytes,
+                                                                          fp_avg)
+    achieved = dom[1] / (dom[2] * 1e-3) / 1e9
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": mean_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "volume": list(w.vol_shape), "views": w.n_views,
+                   "detector": [w.n_u, w.n_v], "updates_per_pass": U,
+                   "l2": "flushed before each step (256 MiB write outside the timed events)",
+                   "parallelism": f"replicas x{world}"},
+        "fp_ms": statistics.mean(fp_ms), "bp_ms": statistics.mean(bp_ms),
+        "fp_updates_per_s": U / (fp_avg * 1e-3), "bp_updates_per_s": U / (bp_avg * 1e-3),
+        "views_per_s": {"fp": w.n_views / (fp_avg * 1e-3), "bp": w.n_views / (bp_avg * 1e-3)},
+        "roofline": {"bound": "hbm", "kernel": dom[0], "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                     "peak_source": peak_kind,
+                     "bytes_model": "4 B per ray-voxel update + 4 B per ray + volume once"},
+        "e2e": {"value": world * 2 * U / (e2e_ms * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        cores = os.cpu_count() or 1
+        n_views = int(max(4, min(w.n_views, cores)))
+        r, dt, nu = oracle_sample_rate(w, x_host, n_views, cores)
+        line["cpu_baseline"] = {"value": r, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": f"FP+BP of {n_views} evenly spaced views of "
+                                          f"{w.n_views} ({nu} updates, {dt:.1f} s)"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl")
+    try:
+        return run_ours(args, rank, world)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,233 @@
+"""ctypes binding of ``libctproj.so`` (declared in ``include/ct.h``).
+
+Argument marshalling only: every step of the projector runs in the library's CUDA kernels.
+PyTorch is used to allocate device memory and to name the current CUDA stream.  There is no
+fallback: if the shared library is missing or cannot be loaded, importing a binding function
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libctproj.so")
+
+CT_PARALLEL2D, CT_FAN2D, CT_CONE, CT_PARALLEL3D = 0, 1, 2, 3
+STATUS_NAMES = ["CT_OK", "CT_ERR_INVALID_ARGUMENT", "CT_ERR_INVALID_GEOMETRY",
+                "CT_ERR_NOT_DEVICE_POINTER", "CT_ERR_ALIASING", "CT_ERR_OUT_OF_MEMORY",
+                "CT_ERR_CUDA", "CT_ERR_WORKSPACE"]
+CT_OK = 0
+
+
+class CtError(RuntimeError):
+    """A libctproj call returned a status other than CT_OK."""
+
+    def __init__(self, status: int, call: str):
+        self.status = int(status)
+        name = STATUS_NAMES[status] if 0 <= status < len(STATUS_NAMES) else f"status {status}"
+        super().__init__(f"{call} failed: {name}")
+
+
+class GeometryInfo(ctypes.Structure):
+    _fields_ = [("beam", ctypes.c_int32), ("n_views", ctypes.c_int32),
+                ("nz", ctypes.c_int32), ("ny", ctypes.c_int32), ("nx", ctypes.c_int32),
+                ("n_u", ctypes.c_int32), ("n_v", ctypes.c_int32),
+                ("volume_layout", ctypes.c_int32),
+                ("n_rays", ctypes.c_int64), ("n_voxels", ctypes.c_int64),
+                ("workspace_bytes", ctypes.c_size_t), ("sirt_workspace_bytes", ctypes.c_size_t)]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libctproj once; raise ImportError if it is not built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"libctproj.so not built at {path}; run "
+                          "`python -m fan_beam_projector_siddon_b300.build` (nvcc, sm_103a)")
+    L = ctypes.CDLL(path)
+    vp, i32, i64, f32, f64, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
+                                  ctypes.c_float, ctypes.c_double, ctypes.c_size_t)
+    L.ct_geometry_create.argtypes = [i32, i32, ctypes.POINTER(f64), i32, i32, i32, f64, i32, i32,
+                                     f64, f64, ctypes.POINTER(vp)]
+    L.ct_geometry_create.restype = i32
+    L.ct_geometry_destroy.argtypes = [vp]
+    L.ct_geometry_destroy.restype = i32
+    L.ct_geometry_get_info.argtypes = [vp, ctypes.POINTER(GeometryInfo)]
+    L.ct_geometry_get_info.restype = i32
+    L.ct_project.argtypes = [vp, vp, vp, vp, sz, vp]
+    L.ct_project.restype = i32
+    L.ct_backproject.argtypes = [vp, vp, vp, vp, sz, vp]
+    L.ct_backproject.restype = i32
+    L.ct_sirt_workspace_bytes.argtypes = [vp]
+    L.ct_sirt_workspace_bytes.restype = sz
+    L.ct_sirt_iterate.argtypes = [vp, vp, vp, vp, sz, i32, f32, i32, vp]
+    L.ct_sirt_iterate.restype = i32
+    L.ct_status_string.argtypes = [i32]
+    L.ct_status_string.restype = ctypes.c_char_p
+    _lib = L
+    return L
+
+
+def _check(status: int, call: str) -> None:
+    if status != CT_OK:
+        raise CtError(status, call)
+
+
+# ---- the C entry points, same names, raw pointers ---------------------------------------------
+
+def ct_geometry_create(beam: int, views, vol_shape, voxel_spacing: float, n_u: int, n_v: int,
+                       du: float, dv: float) -> int:
+    """Create a handle; ``views`` is a host (n_views, 6|12) float64 array.  Returns the handle."""
+    L = load_library()
+    v = np.ascontiguousarray(np.asarray(views, dtype=np.float64))
+    nz, ny, nx = vol_shape
+    h = ctypes.c_void_p()
+    _check(L.ct_geometry_create(int(beam), int(v.shape[0]),
+                                v.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), int(nz),
+                                int(ny), int(nx), float(voxel_spacing), int(n_u), int(n_v),
+                                float(du), float(dv), ctypes.byref(h)), "ct_geometry_create")
+    return h.value
+
+
+def ct_geometry_destroy(handle: int) -> None:
+    _check(load_library().ct_geometry_destroy(handle), "ct_geometry_destroy")
+
+
+def ct_geometry_get_info(handle: int) -> GeometryInfo:
+    info = GeometryInfo()
+    _check(load_library().ct_geometry_get_info(handle, ctypes.byref(info)),
+           "ct_geometry_get_info")
+    return info
+
+
+def ct_project(handle: int, d_volume: int, d_sino: int, d_workspace: int | None,
+               workspace_bytes: int, stream: int | None) -> None:
+    _check(load_library().ct_project(handle, d_volume, d_sino, d_workspace, workspace_bytes,
+                                     stream), "ct_project")
+
+
+def ct_backproject(handle: int, d_sino: int, d_volume: int, d_workspace: int | None,
+                   workspace_bytes: int, stream: int | None) -> None:
+    _check(load_library().ct_backproject(handle, d_sino, d_volume, d_workspace,
+                                         workspace_bytes, stream), "ct_backproject")
+
+
+def ct_sirt_workspace_bytes(handle: int) -> int:
+    return int(load_library().ct_sirt_workspace_bytes(handle))
+
+
+def ct_sirt_iterate(handle: int, d_x: int, d_y: int, d_workspace: int, workspace_bytes: int,
+                    n_iters: int, relaxation: float, workspace_initialised: bool,
+                    stream: int | None) -> None:
+    _check(load_library().ct_sirt_iterate(handle, d_x, d_y, d_workspace, workspace_bytes,
+                                          int(n_iters), float(relaxation),
+                                          1 if workspace_initialised else 0, stream),
+           "ct_sirt_iterate")
+
+
+def ct_status_string(status: int) -> str:
+    return load_library().ct_status_string(int(status)).decode()
+
+
+# ---- a small object wrapper over torch tensors -------------------------------------------------
+
+class Geometry:
+    """Owns one ``ct_geometry`` handle; methods take and return CUDA float32 torch tensors."""
+
+    def __init__(self, beam: int, views, vol_shape, voxel_spacing: float, n_u: int, n_v: int,
+                 du: float, dv: float):
+        self.handle = ct_geometry_create(beam, views, vol_shape, voxel_spacing, n_u, n_v, du, dv)
+        self.info = ct_geometry_get_info(self.handle)
+        self.beam = int(beam)
+        self.is_2d = self.beam in (CT_PARALLEL2D, CT_FAN2D)
+
+    @classmethod
+    def from_workload(cls, w) -> "Geometry":
+        return cls(w.beam, w.views, w.vol_shape, w.voxel_spacing, w.n_u, w.n_v, w.du, w.dv)
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            ct_geometry_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def volume_shape(self):
+        i = self.info
+        return (i.ny, i.nx) if self.is_2d else (i.nz, i.ny, i.nx)
+
+    @property
+    def sino_shape(self):
+        i = self.info
+        return (i.n_views, i.n_u) if self.is_2d else (i.n_views, i.n_u, i.n_v)
+
+    @property
+    def workspace_bytes(self) -> int:
+        return int(self.info.workspace_bytes)
+
+    @property
+    def sirt_workspace_bytes(self) -> int:
+        return int(self.info.sirt_workspace_bytes)
+
+    def new_workspace(self, sirt: bool = False):
+        import torch
+        n = self.sirt_workspace_bytes if sirt else self.workspace_bytes
+        return torch.empty(max(n, 1), dtype=torch.uint8, device="cuda") if n else None
+
+    @staticmethod
+    def _stream(stream):
+        import torch
+        s = torch.cuda.current_stream() if stream is None else stream
+        return s.cuda_stream
+
+    def _ws(self, workspace, sirt=False):
+        need = self.sirt_workspace_bytes if sirt else self.workspace_bytes
+        if need == 0:
+            return None, 0
+        if workspace is None:
+            workspace = self.new_workspace(sirt)
+        return workspace.data_ptr(), workspace.numel() * workspace.element_size()
+
+    def project(self, volume, out=None, workspace=None, stream=None):
+        import torch
+        assert volume.is_cuda and volume.dtype == torch.float32 and volume.is_contiguous()
+        assert tuple(volume.shape) == tuple(self.volume_shape)
+        if out is None:
+            out = torch.empty(self.sino_shape, dtype=torch.float32, device=volume.device)
+        ws, wsb = self._ws(workspace)
+        ct_project(self.handle, volume.data_ptr(), out.data_ptr(), ws, wsb, self._stream(stream))
+        return out
+
+    def backproject(self, sino, out=None, workspace=None, stream=None):
+        import torch
+        assert sino.is_cuda and sino.dtype == torch.float32 and sino.is_contiguous()
+        assert tuple(sino.shape) == tuple(self.sino_shape)
+        if out is None:
+            out = torch.empty(self.volume_shape, dtype=torch.float32, device=sino.device)
+        ws, wsb = self._ws(workspace)
+        ct_backproject(self.handle, sino.data_ptr(), out.data_ptr(), ws, wsb,
+                       self._stream(stream))
+        return out
+
+    def sirt(self, x, y, n_iters: int, workspace, initialised: bool, relaxation: float = 1.0,
+             stream=None):
+        """``n_iters`` SIRT updates of ``x`` in place; ``workspace`` caches C between calls."""
+        import torch
+        assert x.is_cuda and x.dtype == torch.float32 and x.is_contiguous()
+        assert y.is_cuda and y.dtype == torch.float32 and y.is_contiguous()
+        ws, wsb = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+        ct_sirt_iterate(self.handle, x.data_ptr(), y.data_ptr(), ws, wsb, n_iters, relaxation,
+                        initialised, self._stream(stream))
+        return x

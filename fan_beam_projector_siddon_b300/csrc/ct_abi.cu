@@ -1,0 +1,408 @@
+// C ABI of libctproj (declared in include/ct.h): geometry admission, per-view record staging,
+// internal volume order, workspace carving and kernel dispatch.  Host code only.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "ct.h"
+#include "ct_internal.h"
+
+struct ct_geometry {
+    ct_geometry_info info;
+    double spacing;
+    double du, dv;
+    int device;
+    ct::Grid grid;          // strides of the internal layout
+    ct::Tiling tiling;
+    ct::ViewRec* d_views;   // device table, n_views records
+    std::vector<double> host_views;
+};
+
+namespace {
+
+using ct::Layout;
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t n) { return (n + kAlign - 1) / kAlign * kAlign; }
+
+bool is_2d(int beam) { return beam == CT_PARALLEL2D || beam == CT_FAN2D; }
+bool is_parallel(int beam) { return beam == CT_PARALLEL2D || beam == CT_PARALLEL3D; }
+
+double dot3(const double* a, const double* b) { return a[0] * b[0] + a[1] * b[1] + a[2] * b[2]; }
+double norm3(const double* a) { return std::sqrt(dot3(a, a)); }
+void cross3(const double* a, const double* b, double* c) {
+    c[0] = a[1] * b[2] - a[2] * b[1];
+    c[1] = a[2] * b[0] - a[0] * b[2];
+    c[2] = a[0] * b[1] - a[1] * b[0];
+}
+
+// Unpack one record into 3-vectors (2D records get z = 0; their det_v is +z, unused).
+void unpack(int beam, const double* r, double* first, double* ctr, double* u, double* v) {
+    if (is_2d(beam)) {
+        first[0] = r[0]; first[1] = r[1]; first[2] = 0.0;
+        ctr[0] = r[2]; ctr[1] = r[3]; ctr[2] = 0.0;
+        u[0] = r[4]; u[1] = r[5]; u[2] = 0.0;
+        v[0] = 0.0; v[1] = 0.0; v[2] = 1.0;
+    } else {
+        for (int k = 0; k < 3; ++k) {
+            first[k] = r[k]; ctr[k] = r[3 + k]; u[k] = r[6 + k]; v[k] = r[9 + k];
+        }
+    }
+}
+
+// Admission checks (diffct "Trajectories and Geometry", validation paragraph), float64.
+bool admit_view(int beam, const double* r, double s) {
+    const int w = is_2d(beam) ? 6 : 12;
+    for (int k = 0; k < w; ++k)
+        if (!std::isfinite(r[k])) return false;
+    double first[3], ctr[3], u[3], v[3];
+    unpack(beam, r, first, ctr, u, v);
+    const double tol = 1e-6;
+    if (std::fabs(norm3(u) - 1.0) > tol) return false;
+    if (!is_2d(beam) && std::fabs(norm3(v) - 1.0) > tol) return false;
+    if (!is_2d(beam) && std::fabs(dot3(u, v)) > tol) return false;
+    double n[3];
+    if (is_2d(beam)) {
+        n[0] = u[1]; n[1] = -u[0]; n[2] = 0.0;
+    } else {
+        cross3(u, v, n);
+    }
+    if (is_parallel(beam)) {
+        if (std::fabs(norm3(first) - 1.0) > tol) return false;
+        if (beam == CT_PARALLEL2D && std::fabs(dot3(first, u)) > tol) return false;
+        if (beam == CT_PARALLEL3D && std::fabs(dot3(first, n)) <= tol) return false;
+        if (norm3(ctr) > 1e6 * s) return false;
+    } else {
+        double sd[3] = {ctr[0] - first[0], ctr[1] - first[1], ctr[2] - first[2]};
+        const double dist = norm3(sd);
+        if (!(dist > 0.0)) return false;
+        if (std::fabs(dot3(sd, n)) <= tol * dist) return false;  // edge-on detector
+        const double rs = norm3(first), rc = norm3(ctr);
+        if ((rs < rc ? rs : rc) > 1e6 * s) return false;
+        if ((rs > rc ? rs : rc) > 1e15 * s) return false;
+    }
+    return true;
+}
+
+// Internal volume order: the axis that the 32 lanes of a warp run along (det_v or det_u,
+// whichever is better aligned with it, view by view) should be the fastest in memory, so that
+// a warp's 32 gathers or atomics fall into one or two 128-byte lines.
+Layout choose_layout(int beam, int n_views, const double* views, int nz) {
+    if (is_2d(beam) || nz == 1) return ct::LAYOUT_ZYX;
+    const int w = 12;
+    double score[3] = {0, 0, 0};
+    for (int i = 0; i < n_views; ++i) {
+        double first[3], ctr[3], u[3], v[3];
+        unpack(beam, views + (int64_t)i * w, first, ctr, u, v);
+        for (int a = 0; a < 3; ++a) score[a] += std::fmax(std::fabs(u[a]), std::fabs(v[a]));
+    }
+    // keep the caller's order unless another axis is clearly better (it costs two copies)
+    int best = 0;
+    for (int a = 1; a < 3; ++a)
+        if (score[a] > 1.1 * score[best] && score[a] > score[best]) best = a;
+    if (best == 2) return ct::LAYOUT_YXZ;
+    if (best == 1) return ct::LAYOUT_ZXY;
+    return ct::LAYOUT_ZYX;
+}
+
+void strides_for(Layout L, int nx, int ny, int nz, int32_t st[3]) {
+    switch (L) {
+        case ct::LAYOUT_YXZ:  // [y][x][z]
+            st[2] = 1; st[0] = nz; st[1] = nz * nx;
+            break;
+        case ct::LAYOUT_ZXY:  // [z][x][y]
+            st[1] = 1; st[0] = ny; st[2] = nx * ny;
+            break;
+        default:              // [z][y][x]
+            st[0] = 1; st[1] = nx; st[2] = nx * ny;
+            break;
+    }
+}
+
+ct_status from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return CT_OK;
+    if (e == cudaErrorMemoryAllocation) return CT_ERR_OUT_OF_MEMORY;
+    return CT_ERR_CUDA;
+}
+
+// A pointer must be device or managed memory of the handle's device.
+ct_status check_device_ptr(const void* p, int device) {
+    if (p == nullptr) return CT_ERR_INVALID_ARGUMENT;
+    cudaPointerAttributes at;
+    cudaError_t e = cudaPointerGetAttributes(&at, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return CT_ERR_NOT_DEVICE_POINTER;
+    }
+    if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged)
+        return CT_ERR_NOT_DEVICE_POINTER;
+    if (at.type == cudaMemoryTypeDevice && at.device != device) return CT_ERR_NOT_DEVICE_POINTER;
+    return CT_OK;
+}
+
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+    if (a == nullptr || b == nullptr || na == 0 || nb == 0) return false;
+    const uintptr_t x0 = (uintptr_t)a, x1 = x0 + na, y0 = (uintptr_t)b, y1 = y0 + nb;
+    return x0 < y1 && y0 < x1;
+}
+
+size_t volume_bytes(const ct_geometry* g) { return (size_t)g->info.n_voxels * sizeof(float); }
+size_t sino_bytes(const ct_geometry* g) { return (size_t)g->info.n_rays * sizeof(float); }
+
+// Convert between the caller's [z][y][x] order and the internal order.
+cudaError_t to_internal(const ct_geometry* g, const float* src, float* dst, cudaStream_t s) {
+    const int64_t nx = g->info.nx, ny = g->info.ny, nz = g->info.nz;
+    switch (g->info.volume_layout) {
+        case ct::LAYOUT_YXZ: return ct::launch_transpose(src, dst, nz, ny * nx, 1, s);
+        case ct::LAYOUT_ZXY: return ct::launch_transpose(src, dst, ny, nx, nz, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+cudaError_t from_internal(const ct_geometry* g, const float* src, float* dst, cudaStream_t s) {
+    const int64_t nx = g->info.nx, ny = g->info.ny, nz = g->info.nz;
+    switch (g->info.volume_layout) {
+        case ct::LAYOUT_YXZ: return ct::launch_transpose(src, dst, ny * nx, nz, 1, s);
+        case ct::LAYOUT_ZXY: return ct::launch_transpose(src, dst, nx, ny, nz, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+// Common argument checks for project/backproject.
+ct_status check_call(const ct_geometry* g, const void* in, size_t in_bytes, const void* out,
+                     size_t out_bytes, const void* ws, size_t ws_bytes, size_t ws_needed) {
+    if (g == nullptr || in == nullptr || out == nullptr) return CT_ERR_INVALID_ARGUMENT;
+    ct_status st;
+    if ((st = check_device_ptr(in, g->device)) != CT_OK) return st;
+    if ((st = check_device_ptr(out, g->device)) != CT_OK) return st;
+    if (ws_needed > 0) {
+        if (ws == nullptr || ws_bytes < ws_needed) return CT_ERR_WORKSPACE;
+        if ((st = check_device_ptr(ws, g->device)) != CT_OK) return st;
+    }
+    if (overlap(in, in_bytes, out, out_bytes)) return CT_ERR_ALIASING;
+    if (ws_needed > 0 && (overlap(ws, ws_needed, in, in_bytes) ||
+                          overlap(ws, ws_needed, out, out_bytes)))
+        return CT_ERR_ALIASING;
+    // surface errors of earlier asynchronous work before queueing more
+    cudaError_t e = cudaPeekAtLastError();
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return CT_ERR_CUDA;
+    }
+    return CT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ct_status_string(ct_status s) {
+    switch (s) {
+        case CT_OK: return "CT_OK";
+        case CT_ERR_INVALID_ARGUMENT: return "CT_ERR_INVALID_ARGUMENT";
+        case CT_ERR_INVALID_GEOMETRY: return "CT_ERR_INVALID_GEOMETRY";
+        case CT_ERR_NOT_DEVICE_POINTER: return "CT_ERR_NOT_DEVICE_POINTER";
+        case CT_ERR_ALIASING: return "CT_ERR_ALIASING";
+        case CT_ERR_OUT_OF_MEMORY: return "CT_ERR_OUT_OF_MEMORY";
+        case CT_ERR_CUDA: return "CT_ERR_CUDA";
+        case CT_ERR_WORKSPACE: return "CT_ERR_WORKSPACE";
+    }
+    return "CT_ERR_UNKNOWN";
+}
+
+ct_status ct_geometry_create(ct_beam beam, int32_t n_views, const double* views, int32_t nz,
+                             int32_t ny, int32_t nx, double voxel_spacing, int32_t n_u,
+                             int32_t n_v, double du, double dv, ct_geometry** out) {
+    if (out == nullptr) return CT_ERR_INVALID_ARGUMENT;
+    *out = nullptr;
+    const int b = (int)beam;
+    if (b < CT_PARALLEL2D || b > CT_PARALLEL3D) return CT_ERR_INVALID_ARGUMENT;
+    if (views == nullptr || n_views <= 0 || nz <= 0 || ny <= 0 || nx <= 0 || n_u <= 0 ||
+        n_v <= 0)
+        return CT_ERR_INVALID_ARGUMENT;
+    if (is_2d(b)) {
+        if (nz != 1 || n_v != 1) return CT_ERR_INVALID_ARGUMENT;
+        dv = 1.0;
+    }
+    if (!(std::isfinite(voxel_spacing) && voxel_spacing > 0.0) ||
+        !(std::isfinite(du) && du > 0.0) || !(std::isfinite(dv) && dv > 0.0))
+        return CT_ERR_INVALID_ARGUMENT;
+    const int64_t nvox = (int64_t)nz * ny * nx;
+    if (nvox > (int64_t)INT32_MAX) return CT_ERR_INVALID_ARGUMENT;  // 32-bit voxel indices
+    const int64_t tiles_u = is_2d(b) ? (n_u + 255) / 256 : (n_u + 31) / 32;
+    const int64_t tiles_v = is_2d(b) ? 1 : (n_v + 31) / 32;
+    if (tiles_u * tiles_v * n_views > (int64_t)INT32_MAX) return CT_ERR_INVALID_ARGUMENT;
+    const int w = is_2d(b) ? 6 : 12;
+    for (int i = 0; i < n_views; ++i)
+        if (!admit_view(b, views + (int64_t)i * w, voxel_spacing)) return CT_ERR_INVALID_GEOMETRY;
+
+    ct_geometry* g = new (std::nothrow) ct_geometry();
+    if (g == nullptr) return CT_ERR_OUT_OF_MEMORY;
+    g->host_views.assign(views, views + (int64_t)n_views * w);
+    g->spacing = voxel_spacing;
+    g->du = du;
+    g->dv = dv;
+    ct_geometry_info& I = g->info;
+    I.beam = b;
+    I.n_views = n_views;
+    I.nz = nz; I.ny = ny; I.nx = nx;
+    I.n_u = n_u; I.n_v = n_v;
+    I.n_rays = (int64_t)n_views * n_u * n_v;
+    I.n_voxels = nvox;
+    I.volume_layout = choose_layout(b, n_views, views, nz);
+    I.workspace_bytes = I.volume_layout == ct::LAYOUT_ZYX ? 0 : align_up(volume_bytes(g));
+    // SIRT: C, b (and x in the internal order), residual sinogram
+    I.sirt_workspace_bytes = 2 * align_up(volume_bytes(g)) +
+                             (I.volume_layout == ct::LAYOUT_ZYX ? 0 : align_up(volume_bytes(g))) +
+                             align_up(sino_bytes(g));
+
+    ct::Grid& G = g->grid;
+    G.n[0] = nx; G.n[1] = ny; G.n[2] = nz;
+    G.nd[0] = nx; G.nd[1] = ny; G.nd[2] = nz;
+    strides_for((Layout)I.volume_layout, nx, ny, nz, G.stride);
+    G.spacing = (float)voxel_spacing;
+    G.parallel = is_parallel(b) ? 1 : 0;
+    ct::Tiling& T = g->tiling;
+    T.n_views = n_views;
+    T.n_u = n_u; T.n_v = n_v;
+    T.tiles_u = (int32_t)tiles_u;
+    T.tiles_v = (int32_t)tiles_v;
+    T.two_d = is_2d(b) ? 1 : 0;
+
+    // Per-view records in voxel units, origin at the lower box corner.
+    const int fast = I.volume_layout == ct::LAYOUT_YXZ ? 2 : (I.volume_layout == ct::LAYOUT_ZXY ? 1 : 0);
+    std::vector<ct::ViewRec> recs((size_t)n_views);
+    const double half[3] = {0.5 * nx * voxel_spacing, 0.5 * ny * voxel_spacing,
+                            0.5 * nz * voxel_spacing};
+    const double is = 1.0 / voxel_spacing;
+    for (int i = 0; i < n_views; ++i) {
+        double first[3], ctr[3], u[3], v[3];
+        unpack(b, views + (int64_t)i * w, first, ctr, u, v);
+        ct::ViewRec& R = recs[(size_t)i];
+        std::memset(&R, 0, sizeof(R));
+        const double cu = 0.5 * (n_u - 1), cv = is_2d(b) ? 0.0 : 0.5 * (n_v - 1);
+        const double dvv = is_2d(b) ? 0.0 : dv;
+        for (int a = 0; a < 3; ++a) {
+            R.pu[a] = du * is * u[a];
+            R.pv[a] = dvv * is * v[a];
+            R.pb[a] = (ctr[a] + half[a]) * is - cu * R.pu[a] - cv * R.pv[a];
+        }
+        if (is_parallel(b)) {
+            const double nr = norm3(first);
+            for (int a = 0; a < 3; ++a) R.q[a] = first[a] / nr;
+        } else {
+            for (int a = 0; a < 3; ++a) {
+                R.q[a] = (first[a] + half[a]) * is;
+                R.pb[a] -= R.q[a];
+            }
+        }
+        R.lanes_along_v = (!is_2d(b) && std::fabs(v[fast]) >= std::fabs(u[fast])) ? 1 : 0;
+    }
+    cudaError_t e = cudaGetDevice(&g->device);
+    if (e == cudaSuccess) e = cudaMalloc(&g->d_views, sizeof(ct::ViewRec) * (size_t)n_views);
+    if (e == cudaSuccess)
+        e = cudaMemcpy(g->d_views, recs.data(), sizeof(ct::ViewRec) * (size_t)n_views,
+                       cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        if (g->d_views) cudaFree(g->d_views);
+        delete g;
+        return from_cuda(e);
+    }
+    *out = g;
+    return CT_OK;
+}
+
+ct_status ct_geometry_destroy(ct_geometry* g) {
+    if (g == nullptr) return CT_OK;
+    cudaError_t e = cudaSuccess;
+    if (g->d_views) e = cudaFree(g->d_views);
+    delete g;
+    return from_cuda(e);
+}
+
+ct_status ct_geometry_get_info(const ct_geometry* g, ct_geometry_info* info) {
+    if (g == nullptr || info == nullptr) return CT_ERR_INVALID_ARGUMENT;
+    *info = g->info;
+    return CT_OK;
+}
+
+ct_status ct_project(const ct_geometry* g, const float* d_volume, float* d_sino,
+                     void* d_workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (g == nullptr) return CT_ERR_INVALID_ARGUMENT;
+    ct_status st = check_call(g, d_volume, volume_bytes(g), d_sino, sino_bytes(g), d_workspace,
+                              workspace_bytes, g->info.workspace_bytes);
+    if (st != CT_OK) return st;
+    const float* vol = d_volume;
+    if (g->info.volume_layout != ct::LAYOUT_ZYX) {
+        float* tmp = static_cast<float*>(d_workspace);
+        if ((st = from_cuda(to_internal(g, d_volume, tmp, stream))) != CT_OK) return st;
+        vol = tmp;
+    }
+    return from_cuda(ct::launch_project(g->d_views, g->grid, g->tiling, vol, d_sino, stream));
+}
+
+ct_status ct_backproject(const ct_geometry* g, const float* d_sino, float* d_volume,
+                         void* d_workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (g == nullptr) return CT_ERR_INVALID_ARGUMENT;
+    ct_status st = check_call(g, d_sino, sino_bytes(g), d_volume, volume_bytes(g), d_workspace,
+                              workspace_bytes, g->info.workspace_bytes);
+    if (st != CT_OK) return st;
+    float* acc = g->info.volume_layout == ct::LAYOUT_ZYX ? d_volume
+                                                          : static_cast<float*>(d_workspace);
+    if ((st = from_cuda(cudaMemsetAsync(acc, 0, volume_bytes(g), stream))) != CT_OK) return st;
+    if ((st = from_cuda(ct::launch_backproject(g->d_views, g->grid, g->tiling, d_sino, acc,
+                                               stream))) != CT_OK)
+        return st;
+    if (acc != d_volume) return from_cuda(from_internal(g, acc, d_volume, stream));
+    return CT_OK;
+}
+
+size_t ct_sirt_workspace_bytes(const ct_geometry* g) {
+    return g == nullptr ? 0 : g->info.sirt_workspace_bytes;
+}
+
+ct_status ct_sirt_iterate(const ct_geometry* g, float* d_x, const float* d_y, void* d_workspace,
+                          size_t workspace_bytes, int32_t n_iters, float relaxation,
+                          int32_t workspace_initialised, cudaStream_t stream) {
+    if (g == nullptr || n_iters < 0 || !(relaxation > 0.0f && relaxation < 2.0f))
+        return CT_ERR_INVALID_ARGUMENT;
+    ct_status st = check_call(g, d_y, sino_bytes(g), d_x, volume_bytes(g), d_workspace,
+                              workspace_bytes, g->info.sirt_workspace_bytes);
+    if (st != CT_OK) return st;
+    if (overlap(d_x, volume_bytes(g), d_y, sino_bytes(g))) return CT_ERR_ALIASING;
+    const int64_t nvox = g->info.n_voxels;
+    const size_t vb = align_up(volume_bytes(g));
+    char* ws = static_cast<char*>(d_workspace);
+    float* C = reinterpret_cast<float*>(ws);
+    float* B = reinterpret_cast<float*>(ws + vb);
+    const bool native = g->info.volume_layout == ct::LAYOUT_ZYX;
+    float* X = native ? d_x : reinterpret_cast<float*>(ws + 2 * vb);
+    float* Rres = reinterpret_cast<float*>(ws + (native ? 2 : 3) * vb);
+    cudaError_t e = cudaSuccess;
+    if (!workspace_initialised) {
+        // C = 1 / (A^T 1), b = 0
+        e = cudaMemsetAsync(C, 0, volume_bytes(g), stream);
+        if (e == cudaSuccess)
+            e = ct::launch_backproject_ones(g->d_views, g->grid, g->tiling, C, stream);
+        if (e == cudaSuccess) e = ct::launch_invert(C, nvox, stream);
+        if (e == cudaSuccess) e = cudaMemsetAsync(B, 0, volume_bytes(g), stream);
+        if (e != cudaSuccess) return from_cuda(e);
+    }
+    if (n_iters == 0) return CT_OK;
+    if (!native && (e = to_internal(g, d_x, X, stream)) != cudaSuccess) return from_cuda(e);
+    for (int it = 0; it < n_iters && e == cudaSuccess; ++it) {
+        e = ct::launch_project_residual(g->d_views, g->grid, g->tiling, X, d_y, Rres, stream);
+        if (e == cudaSuccess)
+            e = ct::launch_backproject(g->d_views, g->grid, g->tiling, Rres, B, stream);
+        if (e == cudaSuccess) e = ct::launch_sirt_update(X, B, C, relaxation, nvox, stream);
+    }
+    if (e == cudaSuccess && !native) e = from_internal(g, X, d_x, stream);
+    return from_cuda(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,69 @@
+// Internal declarations shared by the C-ABI layer and the kernels of libctproj.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace ct {
+
+// Internal volume orders (the kernels' memory layout of the volume).
+enum Layout : int32_t {
+    LAYOUT_ZYX = 0,  // caller's order, x fastest
+    LAYOUT_YXZ = 1,  // z fastest: one 2D transpose of (nz) x (ny*nx)
+    LAYOUT_ZXY = 2,  // y fastest: nz transposes of (ny) x (nx)
+};
+
+// Per-view record as the kernels read it.  All positions are in voxel units, with the origin at
+// the volume's lower corner, so the volume is the box [0, nx] x [0, ny] x [0, nz] and voxel
+// (i, j, k) is the unit cell [i, i+1) x [j, j+1) x [k, k+1).  Pixel (u, v) sits at
+//     P(u, v) = pb + u * pu + v * pv        (pb already holds the -(U-1)/2, -(V-1)/2 offsets)
+// Parallel beams: the ray is P(u, v) + t * q   (q = unit ray direction), t over all reals.
+// Point sources:  the ray is q + a * (P(u, v) - q) for a in [0, 1]; pb is stored minus q, so
+//                 the direction is directly pb + u * pu + v * pv.
+struct ViewRec {
+    double pb[3];
+    double pu[3];
+    double pv[3];
+    double q[3];
+    int32_t lanes_along_v;  // 1: a warp's 32 lanes take 32 consecutive v; 0: consecutive u
+    int32_t pad;
+};
+static_assert(sizeof(ViewRec) == 104, "ViewRec layout");
+
+// Volume grid as the kernels see it.
+struct Grid {
+    int32_t n[3];        // cells along x, y, z
+    int32_t stride[3];   // element stride of x, y, z in the internal layout
+    double nd[3];        // n as doubles (box upper corner)
+    float spacing;       // physical voxel pitch
+    int32_t parallel;    // 1: infinite lines, 0: source-to-pixel segments
+};
+
+// Detector tiling of one launch.
+struct Tiling {
+    int32_t n_views;
+    int32_t n_u, n_v;
+    int32_t tiles_u, tiles_v;  // 32 x 32 pixel tiles (2D: 256 x 1)
+    int32_t two_d;
+};
+
+// Launchers (kernels in siddon_kernels.cu).  All asynchronous on `stream`.
+cudaError_t launch_project(const ViewRec* views, const Grid& g, const Tiling& t,
+                           const float* vol, float* sino, cudaStream_t stream);
+cudaError_t launch_backproject(const ViewRec* views, const Grid& g, const Tiling& t,
+                               const float* sino, float* vol, cudaStream_t stream);
+cudaError_t launch_backproject_ones(const ViewRec* views, const Grid& g, const Tiling& t,
+                                    float* vol, cudaStream_t stream);
+cudaError_t launch_project_residual(const ViewRec* views, const Grid& g, const Tiling& t,
+                                    const float* x, const float* y, float* r,
+                                    cudaStream_t stream);
+cudaError_t launch_invert(float* c, int64_t n, cudaStream_t stream);
+cudaError_t launch_sirt_update(float* x, float* b, const float* c, float relax, int64_t n,
+                               cudaStream_t stream);
+// out[b][c][r] = in[b][r][c] for b < batch, r < rows, c < cols.
+cudaError_t launch_transpose(const float* in, float* out, int64_t rows, int64_t cols,
+                             int64_t batch, cudaStream_t stream);
+
+}  // namespace ct

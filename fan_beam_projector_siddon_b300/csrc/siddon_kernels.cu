@@ -1,0 +1,419 @@
+// Siddon forward projector, matched adjoint and SIRT kernels for sm_103a.
+//
+// Operator: the cell-constant Siddon line integral (diffct documentation, "Differentiable
+// analytical reconstruction": cell-constant Siddon forward operator and matched adjoint), one ray
+// per detector pixel (diffct "Trajectories and Geometry", detector-surface section), pixel
+// positions from that page's flat-detector formula.
+//
+// Per ray:
+//   1. float64: pixel point, ray origin/direction, slab clip of the parameter range against the
+//      box [0, nx] x [0, ny] x [0, nz] (voxel units), entry and exit points;
+//   2. float32: per-axis first-crossing distance t0, crossing pitch dt and crossing count n from
+//      the entry/exit voxels, then the incremental Siddon walk.  The k-th crossing of axis a is
+//      always fmaf(k, dt_a, t0_a) (no running sums), so any kernel that walks the same ray gets
+//      bit-identical crossing positions and therefore bit-identical chord weights.
+// The walk takes exactly n_x + n_y + n_z steps and moves each axis at most n_a times from an
+// entry voxel inside the grid towards an exit voxel inside the grid, so every index it forms is
+// in bounds whatever the float rounding does to the order of near-simultaneous crossings.
+#include "ct_internal.h"
+
+#include <cuda_runtime.h>
+
+namespace ct {
+namespace {
+
+constexpr int kThreads = 256;  // 8 warps
+constexpr int kRows = 4;       // 3D tiles: 8 warps x 4 rows = 32 pixels along the warp axis
+constexpr int kTile = 32;      // 3D tiles are 32 x 32 pixels
+constexpr int kTile2D = 256;   // 2D tiles are 256 detector pixels
+
+__device__ __forceinline__ float f_inf() { return __int_as_float(0x7f800000); }
+
+// Reciprocal of a nonzero double: hardware estimate refined by two Newton-Raphson steps
+// r <- r + r (1 - d r), each of which squares the relative error.
+__device__ __forceinline__ double rcp64(double d) {
+    double r;
+    asm("rcp.approx.ftz.f64 %0, %1;" : "=d"(r) : "d"(d));
+    double e = __fma_rn(-d, r, 1.0);
+    r = __fma_rn(r, e, r);
+    e = __fma_rn(-d, r, 1.0);
+    return __fma_rn(r, e, r);
+}
+
+struct Ray {
+    float t0[3];   // distance (voxel units, along the ray) from entry to the first crossing
+    float dt[3];   // distance between successive crossings
+    int n[3];      // number of crossings
+    int step[3];   // signed element stride per crossing
+    int idx;       // entry voxel, linear index in the internal layout
+    float tend;    // chord length inside the box (voxel units)
+};
+
+// Ray set-up for pixel (u, v).  Returns false when the ray misses the volume.
+__device__ __forceinline__ bool setup_ray(const ViewRec& vr, const Grid& g, int u, int v,
+                                          Ray& r) {
+    const double fu = (double)u, fv = (double)v;
+    double o[3], d[3];
+    double amin, amax;
+    if (g.parallel) {
+#pragma unroll
+        for (int a = 0; a < 3; ++a) {
+            o[a] = __fma_rn(fv, vr.pv[a], __fma_rn(fu, vr.pu[a], vr.pb[a]));
+            d[a] = vr.q[a];
+        }
+        amin = -__longlong_as_double(0x7ff0000000000000ll);
+        amax = __longlong_as_double(0x7ff0000000000000ll);
+    } else {
+#pragma unroll
+        for (int a = 0; a < 3; ++a) {
+            o[a] = vr.q[a];
+            d[a] = __fma_rn(fv, vr.pv[a], __fma_rn(fu, vr.pu[a], vr.pb[a]));
+        }
+        amin = 0.0;
+        amax = 1.0;
+    }
+#pragma unroll
+    for (int a = 0; a < 3; ++a) {
+        if (d[a] != 0.0) {
+            const double ri = rcp64(d[a]);
+            const double t1 = -o[a] * ri;
+            const double t2 = (g.nd[a] - o[a]) * ri;
+            amin = fmax(amin, fmin(t1, t2));
+            amax = fmin(amax, fmax(t1, t2));
+        } else if (!(o[a] >= 0.0 && o[a] < g.nd[a])) {
+            return false;  // parallel to this slab and outside it (half-open box)
+        }
+    }
+    if (!(amax > amin)) return false;
+
+    const double dd = __fma_rn(d[2], d[2], __fma_rn(d[1], d[1], d[0] * d[0]));
+    const float dl = sqrtf((float)dd);
+    const float inv_dl = 1.0f / dl;
+    r.tend = __fmul_rn((float)(amax - amin), dl);
+    int idx = 0;
+#pragma unroll
+    for (int a = 0; a < 3; ++a) {
+        const float ci = (float)__fma_rn(amin, d[a], o[a]);
+        const float co = (float)__fma_rn(amax, d[a], o[a]);
+        const float dh = __fmul_rn((float)d[a], inv_dl);
+        const int top = g.n[a] - 1;
+        int i0, i1;
+        if (dh > 0.0f) {
+            i0 = (int)floorf(ci);
+            i1 = (int)ceilf(co) - 1;
+        } else if (dh < 0.0f) {
+            i0 = (int)ceilf(ci) - 1;
+            i1 = (int)floorf(co);
+        } else {
+            i0 = (int)floorf(ci);
+            i1 = i0;
+        }
+        i0 = min(max(i0, 0), top);
+        i1 = min(max(i1, 0), top);
+        // Crossing pitches are capped at 1e28 voxel lengths so that fmaf(k, dt, t0) stays
+        // finite for every k < 2^31: only axes with no crossing left ever read +inf.  (An axis
+        // with |dh| < 1e-28 has no crossing inside any admissible volume anyway.)
+        if (dh > 0.0f) {
+            const float inv = fminf(1.0f / dh, 1e28f);
+            r.n[a] = max(0, i1 - i0);
+            r.dt[a] = inv;
+            r.t0[a] = __fmul_rn(__fsub_rn((float)(i0 + 1), ci), inv);
+            r.step[a] = g.stride[a];
+        } else if (dh < 0.0f) {
+            const float inv = fminf(-1.0f / dh, 1e28f);
+            r.n[a] = max(0, i0 - i1);
+            r.dt[a] = inv;
+            r.t0[a] = __fmul_rn(__fsub_rn(ci, (float)i0), inv);
+            r.step[a] = -g.stride[a];
+        } else {
+            r.n[a] = 0;
+            r.dt[a] = f_inf();
+            r.t0[a] = f_inf();
+            r.step[a] = 0;
+        }
+        idx += i0 * g.stride[a];
+    }
+    r.idx = idx;
+    return true;
+}
+
+// The walk.  GATHER: returns sum_k vol[idx_k] * seg_k (voxel units).  SCATTER: adds
+// val * seg_k to vol[idx_k] for every segment and returns 0.  Both evaluate the segment lengths
+// with the same operations in the same order.
+template <bool SCATTER>
+__device__ __forceinline__ float walk(const Ray& r, const float* __restrict__ vin,
+                                      float* __restrict__ vout, float val) {
+    const float INF = f_inf();
+    float tx = r.n[0] > 0 ? r.t0[0] : INF;
+    float ty = r.n[1] > 0 ? r.t0[1] : INF;
+    float tz = r.n[2] > 0 ? r.t0[2] : INF;
+    float kx = 0.0f, ky = 0.0f, kz = 0.0f;
+    const float nx = (float)r.n[0], ny = (float)r.n[1], nz = (float)r.n[2];
+    int idx = r.idx;
+    float t = 0.0f, acc = 0.0f;
+    for (int rem = r.n[0] + r.n[1] + r.n[2]; rem > 0; --rem) {
+        const float tm = fminf(tx, fminf(ty, tz));
+        const float seg = __fsub_rn(tm, t);
+        if (SCATTER) {
+            atomicAdd(vout + idx, __fmul_rn(val, seg));
+        } else {
+            acc = __fmaf_rn(__ldg(vin + idx), seg, acc);
+        }
+        t = tm;
+        if (tx == tm) {
+            idx += r.step[0];
+            kx += 1.0f;
+            tx = kx < nx ? __fmaf_rn(kx, r.dt[0], r.t0[0]) : INF;
+        } else if (ty == tm) {
+            idx += r.step[1];
+            ky += 1.0f;
+            ty = ky < ny ? __fmaf_rn(ky, r.dt[1], r.t0[1]) : INF;
+        } else {
+            idx += r.step[2];
+            kz += 1.0f;
+            tz = kz < nz ? __fmaf_rn(kz, r.dt[2], r.t0[2]) : INF;
+        }
+    }
+    const float seg = __fsub_rn(r.tend, t);
+    if (SCATTER) {
+        atomicAdd(vout + idx, __fmul_rn(val, seg));
+    } else {
+        acc = __fmaf_rn(__ldg(vin + idx), seg, acc);
+    }
+    return acc;
+}
+
+// Block -> (view, pixel tile).  Tiles are ordered detector-v band first, then view, then u tile,
+// so that the blocks resident at one time walk one band of the volume across all views.
+struct TileCoord {
+    int view, ut, vt;
+};
+__device__ __forceinline__ TileCoord tile_of_block(const Tiling& t) {
+    int b = (int)blockIdx.x;
+    const int per_band = t.n_views * t.tiles_u;
+    TileCoord c;
+    c.vt = b / per_band;
+    b -= c.vt * per_band;
+    c.view = b / t.tiles_u;
+    c.ut = b - c.view * t.tiles_u;
+    return c;
+}
+
+__device__ __forceinline__ void load_view(const ViewRec* __restrict__ views, int view,
+                                          ViewRec& sv) {
+    constexpr int kWords = (int)(sizeof(ViewRec) / sizeof(double));
+    if (threadIdx.x < kWords)
+        reinterpret_cast<double*>(&sv)[threadIdx.x] =
+            reinterpret_cast<const double*>(views + view)[threadIdx.x];
+    __syncthreads();
+}
+
+// Pixel handled by this thread in row r of the tile (3D) or in the 2D tile.
+template <bool TWO_D>
+__device__ __forceinline__ void pixel_of(const TileCoord& c, const ViewRec& sv, int r, int& u,
+                                         int& v) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (TWO_D) {
+        u = c.ut * kTile2D + (int)threadIdx.x;
+        v = 0;
+    } else if (sv.lanes_along_v) {
+        v = c.vt * kTile + lane;
+        u = c.ut * kTile + warp * kRows + r;
+    } else {
+        u = c.ut * kTile + lane;
+        v = c.vt * kTile + warp * kRows + r;
+    }
+}
+
+template <bool TWO_D>
+__global__ void __launch_bounds__(kThreads) project_kernel(const ViewRec* __restrict__ views,
+                                                           const Grid g, const Tiling tl,
+                                                           const float* __restrict__ vol,
+                                                           float* __restrict__ sino) {
+    __shared__ ViewRec sv;
+    const TileCoord c = tile_of_block(tl);
+    load_view(views, c.view, sv);
+#pragma unroll 1
+    for (int row = 0; row < (TWO_D ? 1 : kRows); ++row) {
+        int u, v;
+        pixel_of<TWO_D>(c, sv, row, u, v);
+        if (u >= tl.n_u || v >= tl.n_v) continue;
+        Ray ray;
+        float acc = 0.0f;
+        if (setup_ray(sv, g, u, v, ray)) acc = walk<false>(ray, vol, nullptr, 0.0f);
+        sino[((int64_t)c.view * tl.n_u + u) * tl.n_v + v] = __fmul_rn(acc, g.spacing);
+    }
+}
+
+// MODE 0: scatter sino * spacing; MODE 1: scatter spacing (A^T 1).
+template <bool TWO_D, int MODE>
+__global__ void __launch_bounds__(kThreads) backproject_kernel(const ViewRec* __restrict__ views,
+                                                               const Grid g, const Tiling tl,
+                                                               const float* __restrict__ sino,
+                                                               float* __restrict__ vol) {
+    __shared__ ViewRec sv;
+    const TileCoord c = tile_of_block(tl);
+    load_view(views, c.view, sv);
+#pragma unroll 1
+    for (int row = 0; row < (TWO_D ? 1 : kRows); ++row) {
+        int u, v;
+        pixel_of<TWO_D>(c, sv, row, u, v);
+        if (u >= tl.n_u || v >= tl.n_v) continue;
+        float y = 1.0f;
+        if (MODE == 0) y = __ldg(sino + ((int64_t)c.view * tl.n_u + u) * tl.n_v + v);
+        if (y == 0.0f) continue;
+        Ray ray;
+        if (setup_ray(sv, g, u, v, ray)) walk<true>(ray, nullptr, vol, __fmul_rn(y, g.spacing));
+    }
+}
+
+// r = R (y - A x) with R = 1 / (A 1) = 1 / (spacing * chord); 0 for rays that miss.
+template <bool TWO_D>
+__global__ void __launch_bounds__(kThreads)
+    project_residual_kernel(const ViewRec* __restrict__ views, const Grid g, const Tiling tl,
+                            const float* __restrict__ x, const float* __restrict__ y,
+                            float* __restrict__ res) {
+    __shared__ ViewRec sv;
+    const TileCoord c = tile_of_block(tl);
+    load_view(views, c.view, sv);
+#pragma unroll 1
+    for (int row = 0; row < (TWO_D ? 1 : kRows); ++row) {
+        int u, v;
+        pixel_of<TWO_D>(c, sv, row, u, v);
+        if (u >= tl.n_u || v >= tl.n_v) continue;
+        const int64_t k = ((int64_t)c.view * tl.n_u + u) * tl.n_v + v;
+        Ray ray;
+        float out = 0.0f;
+        if (setup_ray(sv, g, u, v, ray) && ray.tend > 0.0f) {
+            const float ax = __fmul_rn(walk<false>(ray, x, nullptr, 0.0f), g.spacing);
+            out = __fdiv_rn(__fsub_rn(__ldg(y + k), ax), __fmul_rn(ray.tend, g.spacing));
+        }
+        res[k] = out;
+    }
+}
+
+__global__ void invert_kernel(float* __restrict__ c, int64_t n) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const float v = c[i];
+        c[i] = v > 0.0f ? __frcp_rn(v) : 0.0f;
+    }
+}
+
+// x += relax * c * b;  b = 0 (ready for the next backprojection).
+__global__ void sirt_update_kernel(float* __restrict__ x, float* __restrict__ b,
+                                   const float* __restrict__ c, float relax, int64_t n) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        x[i] = __fmaf_rn(relax, __fmul_rn(c[i], b[i]), x[i]);
+        b[i] = 0.0f;
+    }
+}
+
+// out[b][c][r] = in[b][r][c]; 32 x 32 tiles through shared memory.
+__global__ void __launch_bounds__(256) transpose_kernel(const float* __restrict__ in,
+                                                        float* __restrict__ out, int64_t rows,
+                                                        int64_t cols, int64_t tiles_r,
+                                                        int64_t tiles_c) {
+    __shared__ float tile[32][33];
+    int64_t t = blockIdx.x;
+    const int64_t tc = t % tiles_c;
+    t /= tiles_c;
+    const int64_t tr = t % tiles_r;
+    const int64_t b = t / tiles_r;
+    const int64_t base = b * rows * cols;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+#pragma unroll
+    for (int k = 0; k < 32; k += 8) {
+        const int64_t r = tr * 32 + ty + k, cc = tc * 32 + tx;
+        if (r < rows && cc < cols) tile[ty + k][tx] = __ldg(in + base + r * cols + cc);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < 32; k += 8) {
+        const int64_t cc = tc * 32 + ty + k, r = tr * 32 + tx;
+        if (r < rows && cc < cols) out[base + cc * rows + r] = tile[tx][ty + k];
+    }
+}
+
+int64_t grid_for(const Tiling& t) {
+    return (int64_t)t.tiles_v * t.n_views * t.tiles_u;
+}
+
+int elementwise_blocks(int64_t n) {
+    int64_t b = (n + 255) / 256;
+    return (int)(b < 148 * 16 ? (b > 0 ? b : 1) : 148 * 16);
+}
+
+}  // namespace
+
+cudaError_t launch_project(const ViewRec* views, const Grid& g, const Tiling& t, const float* vol,
+                           float* sino, cudaStream_t stream) {
+    const int64_t nb = grid_for(t);
+    if (nb <= 0) return cudaSuccess;
+    if (t.two_d)
+        project_kernel<true><<<(unsigned)nb, kThreads, 0, stream>>>(views, g, t, vol, sino);
+    else
+        project_kernel<false><<<(unsigned)nb, kThreads, 0, stream>>>(views, g, t, vol, sino);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_backproject(const ViewRec* views, const Grid& g, const Tiling& t,
+                               const float* sino, float* vol, cudaStream_t stream) {
+    const int64_t nb = grid_for(t);
+    if (nb <= 0) return cudaSuccess;
+    if (t.two_d)
+        backproject_kernel<true, 0><<<(unsigned)nb, kThreads, 0, stream>>>(views, g, t, sino, vol);
+    else
+        backproject_kernel<false, 0><<<(unsigned)nb, kThreads, 0, stream>>>(views, g, t, sino,
+                                                                             vol);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_backproject_ones(const ViewRec* views, const Grid& g, const Tiling& t,
+                                    float* vol, cudaStream_t stream) {
+    const int64_t nb = grid_for(t);
+    if (nb <= 0) return cudaSuccess;
+    if (t.two_d)
+        backproject_kernel<true, 1><<<(unsigned)nb, kThreads, 0, stream>>>(views, g, t, nullptr,
+                                                                            vol);
+    else
+        backproject_kernel<false, 1><<<(unsigned)nb, kThreads, 0, stream>>>(views, g, t, nullptr,
+                                                                             vol);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_project_residual(const ViewRec* views, const Grid& g, const Tiling& t,
+                                    const float* x, const float* y, float* r,
+                                    cudaStream_t stream) {
+    const int64_t nb = grid_for(t);
+    if (nb <= 0) return cudaSuccess;
+    if (t.two_d)
+        project_residual_kernel<true><<<(unsigned)nb, kThreads, 0, stream>>>(views, g, t, x, y, r);
+    else
+        project_residual_kernel<false><<<(unsigned)nb, kThreads, 0, stream>>>(views, g, t, x, y,
+                                                                              r);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_invert(float* c, int64_t n, cudaStream_t stream) {
+    invert_kernel<<<elementwise_blocks(n), 256, 0, stream>>>(c, n);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_sirt_update(float* x, float* b, const float* c, float relax, int64_t n,
+                               cudaStream_t stream) {
+    sirt_update_kernel<<<elementwise_blocks(n), 256, 0, stream>>>(x, b, c, relax, n);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_transpose(const float* in, float* out, int64_t rows, int64_t cols,
+                             int64_t batch, cudaStream_t stream) {
+    const int64_t tr = (rows + 31) / 32, tc = (cols + 31) / 32;
+    const int64_t nb = tr * tc * batch;
+    if (nb <= 0) return cudaSuccess;
+    transpose_kernel<<<(unsigned)nb, 256, 0, stream>>>(in, out, rows, cols, tr, tc);
+    return cudaGetLastError();
+}
+
+}  // namespace ct

@@ -1,0 +1,178 @@
+/*
+ * ct.h -- C ABI of libctproj: the cell-constant Siddon CT forward projector A, its matched
+ * adjoint A^T and a SIRT iteration built on the pair, for one NVIDIA B300 (sm_103a).
+ *
+ * Operator (diffct documentation, "Differentiable analytical reconstruction", first paragraph:
+ * "cell-constant Siddon forward operator and its matched adjoint"; "Trajectories and Geometry",
+ * detector-surface section: one ray per detector pixel, no detector-area integration):
+ *
+ *     y_ray = sum_v x_v * l_v(ray)          (A, ct_project)
+ *     b_v   = sum_ray y_ray * l_v(ray)      (A^T, ct_backproject)
+ *
+ * where l_v is the physical length of the ray inside voxel v of a piecewise-constant volume
+ * (half-open cells: a ray that lies exactly in a cell face belongs to the cell on the + side).
+ *
+ * Frame (diffct "Trajectories and Geometry", trajectory-format table and pixel formula):
+ * Cartesian (x, y[, z]), origin at the volume centre, one length unit for positions and both
+ * spacings.  Voxel i of an axis with n cells spans [-n s/2 + i s, -n s/2 + (i+1) s).
+ * Detector pixel (u, v) lies at
+ *     det_center + (u - (U-1)/2) du det_u + (v - (V-1)/2) dv det_v.
+ * Parallel beams: the ray is the infinite line through the pixel along ray_dir.
+ * Fan/cone beams: the ray is the segment from the source to the pixel.
+ *
+ * Layouts (all float32, C order, device memory owned by the caller):
+ *     volume    3D [z][y][x] = (nz, ny, nx);  2D [y][x] = (ny, nx)
+ *     sinogram  3D [view][u][v] (v fastest);  2D [view][u]
+ *
+ * Threading and streams: a geometry handle is immutable after creation; calls on different
+ * streams may share a handle, but not a workspace.  Every compute call is asynchronous on the
+ * given stream (NULL = legacy default stream), allocates nothing and never synchronises.
+ * Asynchronous CUDA errors surface as CT_ERR_CUDA on a later call.  No call aborts the process.
+ */
+#ifndef CT_H
+#define CT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t is `struct CUstream_st *`; pass it (or NULL) wherever `stream` appears. */
+struct CUstream_st;
+
+/* Exported symbols (the library is built with hidden default visibility). */
+#if defined(__GNUC__)
+#define CT_API __attribute__((visibility("default")))
+#else
+#define CT_API
+#endif
+
+/* Beam kinds (diffct "Trajectories and Geometry", trajectory-format table). */
+typedef enum {
+    CT_PARALLEL2D = 0, /* record: ray_dir(2), det_origin(2), det_u(2)             */
+    CT_FAN2D = 1,      /* record: src_pos(2), det_center(2), det_u(2)             */
+    CT_CONE = 2,       /* record: src_pos(3), det_center(3), det_u(3), det_v(3)   */
+    CT_PARALLEL3D = 3  /* record: ray_dir(3), det_center(3), det_u(3), det_v(3)   */
+} ct_beam;
+
+typedef enum {
+    CT_OK = 0,
+    CT_ERR_INVALID_ARGUMENT = 1,   /* NULL handle/pointer, bad size, bad enum, overflow        */
+    CT_ERR_INVALID_GEOMETRY = 2,   /* a view record fails the admission checks below          */
+    CT_ERR_NOT_DEVICE_POINTER = 3, /* a buffer is not device (or managed) memory of the
+                                      handle's device                                          */
+    CT_ERR_ALIASING = 4,           /* input, output and workspace ranges overlap               */
+    CT_ERR_OUT_OF_MEMORY = 5,      /* cudaMalloc failed in ct_geometry_create                  */
+    CT_ERR_CUDA = 6,               /* any other CUDA runtime error (incl. earlier async ones)  */
+    CT_ERR_WORKSPACE = 7           /* workspace missing or smaller than the reported size      */
+} ct_status;
+
+typedef struct ct_geometry ct_geometry; /* opaque, immutable after ct_geometry_create */
+
+/* Read-only description of a handle. */
+typedef struct {
+    int32_t beam;             /* ct_beam                                                  */
+    int32_t n_views;
+    int32_t nz, ny, nx;       /* 2D: nz == 1                                              */
+    int32_t n_u, n_v;         /* 2D: n_v == 1                                             */
+    int32_t volume_layout;    /* internal volume order used by the kernels:
+                                 0 = [z][y][x] (caller's order, no copy),
+                                 1 = [y][x][z] (z fastest), 2 = [z][x][y] (y fastest)      */
+    int64_t n_rays;           /* n_views * n_u * n_v                                      */
+    int64_t n_voxels;         /* nz * ny * nx                                             */
+    size_t workspace_bytes;   /* scratch needed by ct_project / ct_backproject            */
+    size_t sirt_workspace_bytes;
+} ct_geometry_info;
+
+/*
+ * Create a geometry handle.
+ *
+ * beam, n_views   ct_beam and number of views (> 0).
+ * views           HOST pointer, row-major n_views x 12 doubles (3D) or n_views x 6 (2D), one
+ *                 record per view as listed in ct_beam.  Copied; the caller keeps ownership.
+ * nz, ny, nx      volume size in voxels (2D: nz must be 1); nz*ny*nx < 2^31.
+ * voxel_spacing   scalar voxel pitch (> 0), same unit as the records.
+ * n_u, n_v        detector size in pixels (2D: n_v must be 1).
+ * du, dv          detector pitch along det_u / det_v (> 0; dv ignored for 2D).
+ * out             receives the handle on CT_OK, NULL otherwise.
+ *
+ * Admission checks, in float64 on the host (diffct "Trajectories and Geometry", the paragraph
+ * after the custom-acquisition example): every value finite; det_u (and det_v, ray_dir) unit
+ * length within 1e-6; 2D parallel: ray_dir . det_u = 0 within 1e-6; 3D: det_u . det_v = 0 within
+ * 1e-6; parallel3d: |ray_dir . (det_u x det_v)| > 1e-6 (not tangent to the detector); fan/cone:
+ * source and detector centre distinct, the detector not seen edge-on
+ * (|(det_center - src) . n| > 1e-6 |det_center - src|), and the nearer of the two within 1e6
+ * voxel spacings of the origin, both within 1e15; parallel beams: det_center within 1e6 voxel
+ * spacings.  Failing records give CT_ERR_INVALID_GEOMETRY; sizes give CT_ERR_INVALID_ARGUMENT.
+ *
+ * The handle allocates a small device table of per-view records on the current device and
+ * uploads it synchronously; the handle is bound to that device.
+ */
+CT_API ct_status ct_geometry_create(ct_beam beam, int32_t n_views, const double *views, int32_t nz,
+                             int32_t ny, int32_t nx, double voxel_spacing, int32_t n_u,
+                             int32_t n_v, double du, double dv, ct_geometry **out);
+
+/* Free a handle and its device table (synchronous).  NULL is accepted. */
+CT_API ct_status ct_geometry_destroy(ct_geometry *geom);
+
+/* Fill *info for a handle. */
+CT_API ct_status ct_geometry_get_info(const ct_geometry *geom, ct_geometry_info *info);
+
+/*
+ * Forward projection: d_sino = A d_volume.
+ *
+ * d_volume   device, (nz, ny, nx) float32, read only.
+ * d_sino     device, (n_views, n_u, n_v) float32; every entry is overwritten, rays that miss
+ *            the volume get 0 (diffct "Memory and chunking", resident layouts: forward kernels
+ *            overwrite each active ray, including missed rays).
+ * d_workspace, workspace_bytes
+ *            device scratch of at least info.workspace_bytes (may be NULL when that is 0);
+ *            used for the kernels' internal volume order.  Must not overlap the other buffers.
+ * Float32 walk with float64 entry/exit clipping; per-ray results match the float64 definition
+ * within 1e-4 of (ray chord length x max |x|).
+ */
+CT_API ct_status ct_project(const ct_geometry *geom, const float *d_volume, float *d_sino,
+                     void *d_workspace, size_t workspace_bytes, struct CUstream_st *stream);
+
+/*
+ * Matched adjoint: d_volume = A^T d_sino, with exactly the chord weights of ct_project (the same
+ * traversal code and the same float32 arithmetic).  d_volume is overwritten (cleared on the
+ * stream, then accumulated with float32 atomics, so the summation order, and thus the last bits,
+ * may vary from run to run).  Arguments as for ct_project.
+ */
+CT_API ct_status ct_backproject(const ct_geometry *geom, const float *d_sino, float *d_volume,
+                         void *d_workspace, size_t workspace_bytes,
+                         struct CUstream_st *stream);
+
+/* Scratch bytes needed by ct_sirt_iterate (= info.sirt_workspace_bytes). */
+CT_API size_t ct_sirt_workspace_bytes(const ct_geometry *geom);
+
+/*
+ * SIRT: n_iters updates  x <- x + relaxation * C . A^T( R . (y - A x) ),
+ * R = 1/(A 1) per ray, C = 1/(A^T 1) per voxel, each 0 where the sum is 0.  The pages name SIRT
+ * (ASTRA SIRT3D_CUDA in the HAADF-STEM article's timing table; diffct.solvers.sirt) without
+ * printing it; this is the textbook simultaneous iteration with those row/column normalisers.
+ *
+ * d_x        device volume, updated in place (start from zeros for a plain SIRT run).
+ * d_y        device sinogram (measurements), read only.
+ * d_workspace, workspace_bytes
+ *            at least ct_sirt_workspace_bytes(geom) of device scratch.  It caches C between
+ *            calls: pass workspace_initialised = 0 on the first call with a workspace (C is then
+ *            computed), 1 on later calls with the same handle and workspace.
+ * relaxation in (0, 2); n_iters >= 0.
+ */
+CT_API ct_status ct_sirt_iterate(const ct_geometry *geom, float *d_x, const float *d_y,
+                          void *d_workspace, size_t workspace_bytes, int32_t n_iters,
+                          float relaxation, int32_t workspace_initialised,
+                          struct CUstream_st *stream);
+
+/* Static, human-readable name of a status code. */
+CT_API const char *ct_status_string(ct_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CT_H */

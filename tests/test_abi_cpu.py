@@ -1,0 +1,92 @@
+"""Host-side checks of the C ABI that need no GPU: build, load, exported symbols, admission."""
+import ctypes
+import math
+import os
+import re
+
+import numpy as np
+import pytest
+
+from fan_beam_projector_siddon_b300 import build as ct_build
+from fan_beam_projector_siddon_b300 import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ct_build.build()
+    import fan_beam_projector_siddon_b300 as ct
+    return ct
+
+
+def _declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names |= set(re.findall(r"CT_API\s+[^;(]*?\b(ct_\w+)\s*\(", text, flags=re.S))
+    return names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    declared = _declared_symbols()
+    assert {"ct_geometry_create", "ct_project", "ct_backproject", "ct_sirt_iterate"} <= declared
+    so = ctypes.CDLL(ct_build.LIB)
+    for name in sorted(declared):
+        assert hasattr(so, name), f"{name} declared in include/ but not exported"
+
+
+def test_status_strings(lib):
+    assert lib.ct_status_string(0) == "CT_OK"
+    assert lib.ct_status_string(2) == "CT_ERR_INVALID_GEOMETRY"
+    assert lib.ct_status_string(99) == "CT_ERR_UNKNOWN"
+
+
+def _expect(lib, status, fn, *args):
+    with pytest.raises(lib.CtError) as ei:
+        fn(*args)
+    assert ei.value.status == status, str(ei.value)
+
+
+def test_admission_rejects_bad_geometry_before_touching_the_gpu(lib):
+    INV_GEOM, INV_ARG = 2, 1
+    w = W.config(3)
+    create = lib.ct_geometry_create
+    args = lambda views: (W.CONE, views, w.vol_shape, 1.0, 384, 384, 1.2, 1.2)
+    bad = w.views.copy(); bad[5, 0] = math.nan                       # non-finite
+    _expect(lib, INV_GEOM, create, *args(bad))
+    bad = w.views.copy(); bad[5, 6:9] *= 1.01                        # det_u not unit
+    _expect(lib, INV_GEOM, create, *args(bad))
+    bad = w.views.copy(); bad[5, 9:12] = bad[5, 6:9]                 # det_u not orthogonal to v
+    _expect(lib, INV_GEOM, create, *args(bad))
+    bad = w.views.copy(); bad[5, 0:3] = bad[5, 3:6]                  # source on detector centre
+    _expect(lib, INV_GEOM, create, *args(bad))
+    bad = w.views.copy(); bad[5, 0:3] = bad[5, 3:6] + 10 * bad[5, 6:9]   # edge-on detector
+    _expect(lib, INV_GEOM, create, *args(bad))
+    bad = w.views.copy(); bad[5, 0:6] *= 1e7                         # both endpoints too far
+    _expect(lib, INV_GEOM, create, *args(bad))
+    # parallel3d: ray tangent to the detector plane
+    p = W.config(5).views.copy(); p[3, 0:3] = p[3, 6:9]
+    _expect(lib, INV_GEOM, create, W.PARALLEL3D, p, (8, 8, 8), 1.0, 8, 8, 1.0, 1.0)
+    # 2D parallel: ray_dir not orthogonal to det_u
+    q = W.circular_parallel_2d(4); q[1, 4:6] = q[1, 0:2]
+    _expect(lib, INV_GEOM, create, W.PARALLEL2D, q, (1, 8, 8), 1.0, 8, 1, 1.0, 1.0)
+    # sizes
+    _expect(lib, INV_ARG, create, W.CONE, w.views, (0, 4, 4), 1.0, 4, 4, 1.0, 1.0)
+    _expect(lib, INV_ARG, create, W.CONE, w.views, (2048, 1024, 1024), 1.0, 4, 4, 1.0, 1.0)
+    _expect(lib, INV_ARG, create, W.CONE, w.views[:0], (4, 4, 4), 1.0, 4, 4, 1.0, 1.0)
+    _expect(lib, INV_ARG, create, W.CONE, w.views, (4, 4, 4), -1.0, 4, 4, 1.0, 1.0)
+    _expect(lib, INV_ARG, create, W.CONE, w.views, (4, 4, 4), 1.0, 4, 4, 0.0, 1.0)
+    _expect(lib, INV_ARG, create, W.FAN2D, W.config(2).views, (2, 8, 8), 1.0, 8, 1, 1.0, 1.0)
+    _expect(lib, INV_ARG, create, W.FAN2D, W.config(2).views, (1, 8, 8), 1.0, 8, 3, 1.0, 1.0)
+    _expect(lib, INV_ARG, create, 7, w.views, (4, 4, 4), 1.0, 4, 4, 1.0, 1.0)
+
+
+def test_null_arguments_are_rejected(lib):
+    L = lib.load_library()
+    assert L.ct_project(None, None, None, None, 0, None) == 1
+    assert L.ct_backproject(None, None, None, None, 0, None) == 1
+    assert L.ct_sirt_iterate(None, None, None, None, 0, 1, 1.0, 0, None) == 1
+    assert L.ct_geometry_destroy(None) == 0
+    assert L.ct_sirt_workspace_bytes(None) == 0

@@ -1,0 +1,269 @@
+"""CUDA path (through the C ABI) against the float64 oracle.
+
+* small twins of the five workloads (several tiles plus ragged tails): every ray of A, the whole
+  volume of A^T, the GPU adjoint identity;
+* the five full-size workloads, in the launch configuration the benchmark times: sampled rays of
+  A and sampled voxels of A^T against the oracle one by one, plus the adjoint identity;
+* edge cases: 1-8-voxel volumes, rays in cell faces, rays that all miss, bad pointers, aliasing,
+  short workspaces, determinism, non-default streams.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from fan_beam_projector_siddon_b300 import workloads as W
+from tests._parity import (ADJ_RTOL, BP_RTOL, adjoint_gap, fp_violations, rel_l2, sample_rays,
+                           sino_at, torch_cuda)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ct():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from fan_beam_projector_siddon_b300 import build
+    build.build()
+    import fan_beam_projector_siddon_b300 as ct
+    return ct
+
+
+def _cpu(t):
+    import torch
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+# ---------------------------------------------------------------------------------------------
+# small twins: elementwise
+# ---------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5])
+def test_small_forward_every_ray(ct, n):
+    w = W.small_config(n)
+    g = ct.Geometry.from_workload(w)
+    go = oracle.Geometry.from_workload(w)
+    x = w.phantom()
+    y_gpu = _cpu(g.project(torch_cuda(x)))
+    y_or = go.project(x, threads=8)
+    L, _ = go.ray_lengths()
+    bad = fp_violations(y_gpu, y_or, L, float(np.abs(x).max()))
+    assert bad.size == 0, (bad[:10], y_gpu.reshape(-1)[bad[:10]], y_or.reshape(-1)[bad[:10]])
+    assert (L > 0).mean() > 0.3
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5])
+def test_small_backprojection_whole_volume(ct, n):
+    w = W.small_config(n)
+    g = ct.Geometry.from_workload(w)
+    go = oracle.Geometry.from_workload(w)
+    for y in (W.random_sinogram(w, 5), np.abs(W.random_sinogram(w, 6))):
+        b_gpu = _cpu(g.backproject(torch_cuda(y)))
+        b_or = go.backproject(y, threads=8)
+        assert rel_l2(b_gpu, b_or) <= BP_RTOL
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5])
+def test_small_adjoint_identity_on_gpu(ct, n):
+    w = W.small_config(n)
+    g = ct.Geometry.from_workload(w)
+    rng = np.random.default_rng(n)
+    for lo in (0.0, -1.0):
+        x = rng.uniform(lo, 1.0, size=w.volume_shape).astype(np.float32)
+        y = rng.uniform(lo, 1.0, size=w.sino_shape).astype(np.float32)
+        Ax = _cpu(g.project(torch_cuda(x)))
+        Aty = _cpu(g.backproject(torch_cuda(y)))
+        gap, lhs, rhs = adjoint_gap(Ax, y, x, Aty)
+        assert gap <= ADJ_RTOL, (gap, lhs, rhs)
+
+
+def test_layouts_chosen_per_geometry(ct):
+    assert ct.Geometry.from_workload(W.config(3)).info.volume_layout == 1      # z fastest
+    assert ct.Geometry.from_workload(W.config(5)).info.volume_layout == 0      # caller order
+    assert ct.Geometry.from_workload(W.config(1)).info.volume_layout == 0
+    g = ct.Geometry.from_workload(W.config(3))
+    assert g.workspace_bytes >= 256 ** 3 * 4
+
+
+# ---------------------------------------------------------------------------------------------
+# full-size workloads: sampled
+# ---------------------------------------------------------------------------------------------
+
+_PHANTOMS = {}
+
+
+def _phantom(n):
+    if n not in _PHANTOMS:
+        _PHANTOMS.clear()
+        _PHANTOMS[n] = W.config(n).phantom()
+    return _PHANTOMS[n]
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5])
+def test_full_forward_sampled_rays(ct, n):
+    import torch
+    w = W.config(n)
+    x = _phantom(n)
+    g = ct.Geometry.from_workload(w)
+    go = oracle.Geometry.from_workload(w)
+    y_gpu = g.project(torch_cuda(x))
+    view, iu, iv = sample_rays(w, 4000, seed=n)
+    got = sino_at(_cpu(y_gpu), w, view, iu, iv)
+    want = go.project_rays(x, view, iu, iv)
+    L = go.project_rays(np.ones(w.volume_shape), view, iu, iv)
+    bad = fp_violations(got, want, L, float(np.abs(x).max()))
+    assert bad.size == 0, (bad[:5], got[bad[:5]], want[bad[:5]])
+    # every ray is written (no stale values): a second projection into a poisoned buffer agrees
+    out = torch.full(w.sino_shape, float("nan"), device="cuda")
+    g.project(torch_cuda(x), out=out)
+    assert torch.equal(out, y_gpu)
+    del y_gpu, out
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5])
+def test_full_backprojection_sampled_voxels(ct, n):
+    import torch
+    w = W.config(n)
+    g = ct.Geometry.from_workload(w)
+    go = oracle.Geometry.from_workload(w)
+    y = W.random_sinogram(w, 10 + n)
+    y = np.abs(y)   # positive: per-voxel sums without cancellation
+    b_gpu = _cpu(g.backproject(torch_cuda(y))).reshape(-1)
+    rng = np.random.default_rng(n)
+    vox = rng.choice(b_gpu.size, size=60 if n >= 4 else 150, replace=False)
+    want = go.backproject_voxels(y, vox)
+    assert rel_l2(b_gpu[vox], want) <= BP_RTOL
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5])
+def test_full_adjoint_identity(ct, n):
+    import torch
+    w = W.config(n)
+    g = ct.Geometry.from_workload(w)
+    x = W.random_volume(w, 1) * 0.5 + 0.5
+    y = W.random_sinogram(w, 2) * 0.5 + 0.5
+    Ax = _cpu(g.project(torch_cuda(x)))
+    Aty = _cpu(g.backproject(torch_cuda(y)))
+    gap, lhs, rhs = adjoint_gap(Ax, y, x, Aty)
+    assert gap <= ADJ_RTOL, (gap, lhs, rhs)
+    torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------------------------------------
+# edge cases
+# ---------------------------------------------------------------------------------------------
+
+def _random_frames(rng, n, beam):
+    views = []
+    for _ in range(n):
+        u = rng.standard_normal(3); u /= np.linalg.norm(u)
+        v = rng.standard_normal(3); v -= (v @ u) * u; v /= np.linalg.norm(v)
+        nrm = np.cross(u, v)
+        if beam == W.CONE:
+            views.append(np.concatenate([-5.0 * nrm + rng.uniform(-.3, .3, 3), 4.0 * nrm, u, v]))
+        else:
+            r = nrm + 0.4 * rng.standard_normal(3); r /= np.linalg.norm(r)
+            views.append(np.concatenate([r, rng.uniform(-.2, .2, 3), u, v]))
+    return np.array(views)
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 1), (2, 2, 2), (1, 2, 4), (8, 1, 1), (1, 1, 8),
+                                   (3, 1, 5)])
+@pytest.mark.parametrize("beam", [W.CONE, W.PARALLEL3D])
+def test_tiny_volumes(ct, shape, beam):
+    rng = np.random.default_rng(sum(shape) * 7 + beam)
+    views = _random_frames(rng, 6, beam)
+    s = 0.5
+    g = ct.Geometry(beam, views, shape, s, 37, 33, 0.11, 0.13)
+    go = oracle.Geometry(beam, views, shape, s, 37, 33, 0.11, 0.13)
+    x = rng.uniform(0.1, 1.0, size=shape).astype(np.float32)
+    y_gpu = _cpu(g.project(torch_cuda(x)))
+    y_or = go.project(x)
+    L, _ = go.ray_lengths()
+    assert fp_violations(y_gpu, y_or, L, float(x.max())).size == 0
+    yy = rng.uniform(0.1, 1.0, size=go.sino_shape).astype(np.float32)
+    assert rel_l2(_cpu(g.backproject(torch_cuda(yy))), go.backproject(yy)) <= BP_RTOL
+
+
+def test_face_rays_follow_the_half_open_rule(ct):
+    """Axis-aligned parallel rays lying exactly in cell faces belong to the + side cell."""
+    nz, ny, nx = 4, 6, 8
+    s = 1.0
+    x = np.random.default_rng(0).uniform(0, 1, size=(nz, ny, nx)).astype(np.float32)
+    # rays along +z; pixels on the integer lattice x, y in {-4..4} x {-3..3}: every ray lies in
+    # the corner line of four cells (or on the outer faces)
+    rec = np.array([[0, 0, 1.0, 0, 0, 0, 1.0, 0, 0, 0, 1.0, 0]])
+    g = ct.Geometry(W.PARALLEL3D, rec, (nz, ny, nx), s, 9, 7, 1.0, 1.0)
+    go = oracle.Geometry(W.PARALLEL3D, rec, (nz, ny, nx), s, 9, 7, 1.0, 1.0)
+    y_gpu = _cpu(g.project(torch_cuda(x)))[0]
+    y_or = go.project(x)[0]
+    np.testing.assert_allclose(y_gpu, y_or, rtol=1e-6, atol=1e-6)
+    # column u = 8 (x = +4) and row v = 6 (y = +3) lie on the outer + faces: exactly 0
+    assert np.all(y_gpu[8, :] == 0) and np.all(y_gpu[:, 6] == 0)
+    # the others equal the column sum of the + side cell
+    np.testing.assert_allclose(y_gpu[:8, :6], x.sum(axis=0).T, rtol=1e-6)
+    # 2D: rays along +x in the face planes y = k
+    rec2 = np.array([[1.0, 0, 0, 0, 0, 1.0]])
+    g2 = ct.Geometry(W.PARALLEL2D, rec2, (1, ny, nx), s, 7, 1, 1.0, 1.0)
+    img = x[0]
+    y2 = _cpu(g2.project(torch_cuda(img)))[0]
+    np.testing.assert_allclose(y2[:6], img.sum(axis=1), rtol=1e-6)
+    assert y2[6] == 0
+
+
+def test_rays_that_miss_give_exact_zeros(ct):
+    w = W.small_config(3)
+    views = w.views.copy()
+    views[:, 3:6] += np.array([0.0, 0.0, 400.0])     # detector far above: every ray misses
+    views[:, 0:3] += np.array([0.0, 0.0, 400.0])
+    g = ct.Geometry(W.CONE, views, w.vol_shape, 1.0, w.n_u, w.n_v, w.du, w.dv)
+    y = _cpu(g.project(torch_cuda(w.phantom())))
+    assert np.all(y == 0)
+    b = _cpu(g.backproject(torch_cuda(np.ones(w.sino_shape, np.float32))))
+    assert np.all(b == 0)
+
+
+def test_forward_is_deterministic_and_stream_aware(ct):
+    import torch
+    w = W.small_config(4)
+    g = ct.Geometry.from_workload(w)
+    x = torch_cuda(w.phantom())
+    a = g.project(x)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        b = g.project(x, stream=s)
+    s.synchronize()
+    assert torch.equal(a, b)
+
+
+def test_bad_pointers_aliasing_and_workspace(ct):
+    import torch
+    w = W.small_config(3)
+    g = ct.Geometry.from_workload(w)
+    vol = torch_cuda(w.phantom())
+    sino = torch.empty(w.sino_shape, device="cuda")
+    ws = g.new_workspace()
+    wsb = ws.numel()
+    host = np.zeros(w.sino_shape, np.float32)
+    with pytest.raises(ct.CtError) as e:
+        ct.ct_project(g.handle, vol.data_ptr(), host.ctypes.data, ws.data_ptr(), wsb, None)
+    assert e.value.status == 3
+    big = torch.empty(vol.numel() + sino.numel(), device="cuda")
+    with pytest.raises(ct.CtError) as e:       # output overlaps input
+        ct.ct_project(g.handle, big.data_ptr(), big.data_ptr() + 4 * 100, ws.data_ptr(), wsb,
+                      None)
+    assert e.value.status == 4
+    with pytest.raises(ct.CtError) as e:       # workspace too small
+        ct.ct_project(g.handle, vol.data_ptr(), sino.data_ptr(), ws.data_ptr(), wsb - 4, None)
+    assert e.value.status == 7
+    with pytest.raises(ct.CtError) as e:       # workspace overlapping the output
+        ct.ct_backproject(g.handle, sino.data_ptr(), vol.data_ptr(), vol.data_ptr(), wsb, None)
+    assert e.value.status in (4, 7)
+    # the handle still works afterwards
+    g.project(vol, out=sino, workspace=ws)
+    torch.cuda.synchronize()
