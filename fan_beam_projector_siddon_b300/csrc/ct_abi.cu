@@ -266,6 +266,7 @@ ct_status ct_geometry_create(ct_beam beam, int32_t n_views, const double* views,
     strides_for((Layout)I.volume_layout, nx, ny, nz, G.stride);
     G.spacing = (float)voxel_spacing;
     G.parallel = is_parallel(b) ? 1 : 0;
+    G.fast = I.volume_layout == ct::LAYOUT_YXZ ? 2 : (I.volume_layout == ct::LAYOUT_ZXY ? 1 : 0);
     ct::Tiling& T = g->tiling;
     T.n_views = n_views;
     T.n_u = n_u; T.n_v = n_v;
@@ -274,7 +275,7 @@ ct_status ct_geometry_create(ct_beam beam, int32_t n_views, const double* views,
     T.two_d = is_2d(b) ? 1 : 0;
 
     // Per-view records in voxel units, origin at the lower box corner.
-    const int fast = I.volume_layout == ct::LAYOUT_YXZ ? 2 : (I.volume_layout == ct::LAYOUT_ZXY ? 1 : 0);
+    const int fast = G.fast;
     std::vector<ct::ViewRec> recs((size_t)n_views);
     const double half[3] = {0.5 * nx * voxel_spacing, 0.5 * ny * voxel_spacing,
                             0.5 * nz * voxel_spacing};

@@ -39,6 +39,7 @@ struct Grid {
     double nd[3];        // n as doubles (box upper corner)
     float spacing;       // physical voxel pitch
     int32_t parallel;    // 1: infinite lines, 0: source-to-pixel segments
+    int32_t fast;        // axis that is fastest in memory (0 x, 1 y, 2 z): the walk's inner axis
 };
 
 // Detector tiling of one launch.

@@ -26,20 +26,21 @@ constexpr int kThreads = 256;  // 8 warps
 constexpr int kRows = 4;       // 3D tiles: 8 warps x 4 rows = 32 pixels along the warp axis
 constexpr int kTile = 32;      // 3D tiles are 32 x 32 pixels
 constexpr int kTile2D = 256;   // 2D tiles are 256 detector pixels
+constexpr int kMinBlocks = 5;  // resident CTAs per SM the walk kernels are compiled for (<= 51 regs)
 
 __device__ __forceinline__ float f_inf() { return __int_as_float(0x7f800000); }
 
-// Reciprocal of a nonzero double: hardware estimate refined by two Newton-Raphson steps
-// r <- r + r (1 - d r), each of which squares the relative error.
+// Reciprocal of a nonzero double: hardware estimate refined by one Newton-Raphson step
+// r <- r + r (1 - d r), which squares the estimate's relative error (to about 2^-44).
 __device__ __forceinline__ double rcp64(double d) {
     double r;
     asm("rcp.approx.ftz.f64 %0, %1;" : "=d"(r) : "d"(d));
-    double e = __fma_rn(-d, r, 1.0);
-    r = __fma_rn(r, e, r);
-    e = __fma_rn(-d, r, 1.0);
+    const double e = __fma_rn(-d, r, 1.0);
     return __fma_rn(r, e, r);
 }
 
+// Walk state of one ray.  Index 0 and 1 are the two "outer" axes, index 2 the "inner" axis,
+// which is the volume axis fastest in memory.
 struct Ray {
     float t0[3];   // distance (voxel units, along the ray) from entry to the first crossing
     float dt[3];   // distance between successive crossings
@@ -49,9 +50,13 @@ struct Ray {
     float tend;    // chord length inside the box (voxel units)
 };
 
-// Ray set-up for pixel (u, v).  Returns false when the ray misses the volume.
+// Ray set-up for pixel (u, v).  Returns false when the ray misses the volume.  F is the inner
+// (fast) axis; the outer axes are the other two in increasing order.
+template <int F>
 __device__ __forceinline__ bool setup_ray(const ViewRec& vr, const Grid& g, int u, int v,
                                           Ray& r) {
+    constexpr int A = F == 0 ? 1 : 0;
+    constexpr int B = F == 2 ? 1 : 2;
     const double fu = (double)u, fv = (double)v;
     double o[3], d[3];
     double amin, amax;
@@ -72,30 +77,36 @@ __device__ __forceinline__ bool setup_ray(const ViewRec& vr, const Grid& g, int 
         amin = 0.0;
         amax = 1.0;
     }
+    // slab clip against [0, n_a] per axis; the sign and zero tests read the bits (integer pipe)
 #pragma unroll
     for (int a = 0; a < 3; ++a) {
-        if (d[a] != 0.0) {
+        const long long bits = __double_as_longlong(d[a]);
+        if ((bits & 0x7fffffffffffffffll) != 0) {
             const double ri = rcp64(d[a]);
             const double t1 = -o[a] * ri;
             const double t2 = (g.nd[a] - o[a]) * ri;
-            amin = fmax(amin, fmin(t1, t2));
-            amax = fmin(amax, fmax(t1, t2));
+            const bool pos = bits >= 0;
+            amin = fmax(amin, pos ? t1 : t2);
+            amax = fmin(amax, pos ? t2 : t1);
         } else if (!(o[a] >= 0.0 && o[a] < g.nd[a])) {
             return false;  // parallel to this slab and outside it (half-open box)
         }
     }
     if (!(amax > amin)) return false;
 
-    const double dd = __fma_rn(d[2], d[2], __fma_rn(d[1], d[1], d[0] * d[0]));
-    const float dl = sqrtf((float)dd);
+    float df[3];
+#pragma unroll
+    for (int a = 0; a < 3; ++a) df[a] = (float)d[a];
+    const float dl = sqrtf(__fmaf_rn(df[2], df[2], __fmaf_rn(df[1], df[1], df[0] * df[0])));
     const float inv_dl = 1.0f / dl;
     r.tend = __fmul_rn((float)(amax - amin), dl);
     int idx = 0;
 #pragma unroll
     for (int a = 0; a < 3; ++a) {
+        const int slot = a == F ? 2 : (a == A ? 0 : 1);
         const float ci = (float)__fma_rn(amin, d[a], o[a]);
         const float co = (float)__fma_rn(amax, d[a], o[a]);
-        const float dh = __fmul_rn((float)d[a], inv_dl);
+        const float dh = __fmul_rn(df[a], inv_dl);
         const int top = g.n[a] - 1;
         int i0, i1;
         if (dh > 0.0f) {
@@ -115,21 +126,21 @@ __device__ __forceinline__ bool setup_ray(const ViewRec& vr, const Grid& g, int 
         // with |dh| < 1e-28 has no crossing inside any admissible volume anyway.)
         if (dh > 0.0f) {
             const float inv = fminf(1.0f / dh, 1e28f);
-            r.n[a] = max(0, i1 - i0);
-            r.dt[a] = inv;
-            r.t0[a] = __fmul_rn(__fsub_rn((float)(i0 + 1), ci), inv);
-            r.step[a] = g.stride[a];
+            r.n[slot] = max(0, i1 - i0);
+            r.dt[slot] = inv;
+            r.t0[slot] = __fmul_rn(__fsub_rn((float)(i0 + 1), ci), inv);
+            r.step[slot] = g.stride[a];
         } else if (dh < 0.0f) {
             const float inv = fminf(-1.0f / dh, 1e28f);
-            r.n[a] = max(0, i0 - i1);
-            r.dt[a] = inv;
-            r.t0[a] = __fmul_rn(__fsub_rn(ci, (float)i0), inv);
-            r.step[a] = -g.stride[a];
+            r.n[slot] = max(0, i0 - i1);
+            r.dt[slot] = inv;
+            r.t0[slot] = __fmul_rn(__fsub_rn(ci, (float)i0), inv);
+            r.step[slot] = -g.stride[a];
         } else {
-            r.n[a] = 0;
-            r.dt[a] = f_inf();
-            r.t0[a] = f_inf();
-            r.step[a] = 0;
+            r.n[slot] = 0;
+            r.dt[slot] = f_inf();
+            r.t0[slot] = f_inf();
+            r.step[slot] = 0;
         }
         idx += i0 * g.stride[a];
     }
@@ -137,49 +148,67 @@ __device__ __forceinline__ bool setup_ray(const ViewRec& vr, const Grid& g, int 
     return true;
 }
 
-// The walk.  GATHER: returns sum_k vol[idx_k] * seg_k (voxel units).  SCATTER: adds
-// val * seg_k to vol[idx_k] for every segment and returns 0.  Both evaluate the segment lengths
-// with the same operations in the same order.
+// One segment: gather or scatter.
+template <bool SCATTER>
+__device__ __forceinline__ void visit(int idx, float seg, const float* __restrict__ vin,
+                                      float* __restrict__ vout, float val, float& acc) {
+    if (SCATTER)
+        atomicAdd(vout + idx, __fmul_rn(val, seg));
+    else
+        acc = __fmaf_rn(__ldg(vin + idx), seg, acc);
+}
+
+// The walk.  GATHER returns sum_k vol[idx_k] * seg_k (voxel units); SCATTER adds val * seg_k to
+// vol[idx_k] and returns 0.  Both evaluate every segment length with the same operations.
+//
+// Order of work: the outer loop steps through the crossings of the two outer axes; before each
+// outer crossing, the inner loop takes the inner-axis crossings that come first.  A warp's lanes
+// cover neighbouring pixels along the detector axis that is aligned with the inner (fast) axis,
+// so they meet the same outer planes in the same order and stay in lock-step: each step's 32
+// gathers or atomics land in one or two 128-byte lines.
 template <bool SCATTER>
 __device__ __forceinline__ float walk(const Ray& r, const float* __restrict__ vin,
                                       float* __restrict__ vout, float val) {
     const float INF = f_inf();
-    float tx = r.n[0] > 0 ? r.t0[0] : INF;
-    float ty = r.n[1] > 0 ? r.t0[1] : INF;
-    float tz = r.n[2] > 0 ? r.t0[2] : INF;
-    float kx = 0.0f, ky = 0.0f, kz = 0.0f;
-    const float nx = (float)r.n[0], ny = (float)r.n[1], nz = (float)r.n[2];
+    float ta = r.n[0] > 0 ? r.t0[0] : INF;
+    float tb = r.n[1] > 0 ? r.t0[1] : INF;
+    float tf = r.n[2] > 0 ? r.t0[2] : INF;
+    float ka = 0.0f, kb = 0.0f, kf = 0.0f;
+    const float na = (float)r.n[0], nb = (float)r.n[1], nf = (float)r.n[2];
     int idx = r.idx;
     float t = 0.0f, acc = 0.0f;
-    for (int rem = r.n[0] + r.n[1] + r.n[2]; rem > 0; --rem) {
-        const float tm = fminf(tx, fminf(ty, tz));
-        const float seg = __fsub_rn(tm, t);
-        if (SCATTER) {
-            atomicAdd(vout + idx, __fmul_rn(val, seg));
-        } else {
-            acc = __fmaf_rn(__ldg(vin + idx), seg, acc);
-        }
-        t = tm;
-        if (tx == tm) {
-            idx += r.step[0];
-            kx += 1.0f;
-            tx = kx < nx ? __fmaf_rn(kx, r.dt[0], r.t0[0]) : INF;
-        } else if (ty == tm) {
-            idx += r.step[1];
-            ky += 1.0f;
-            ty = ky < ny ? __fmaf_rn(ky, r.dt[1], r.t0[1]) : INF;
-        } else {
+#pragma unroll 1
+    for (int outer = r.n[0] + r.n[1]; outer > 0; --outer) {
+        const float tstop = fminf(ta, tb);
+#pragma unroll 1
+        while (tf < tstop) {
+            visit<SCATTER>(idx, __fsub_rn(tf, t), vin, vout, val, acc);
+            t = tf;
             idx += r.step[2];
-            kz += 1.0f;
-            tz = kz < nz ? __fmaf_rn(kz, r.dt[2], r.t0[2]) : INF;
+            kf += 1.0f;
+            tf = kf < nf ? __fmaf_rn(kf, r.dt[2], r.t0[2]) : INF;
+        }
+        visit<SCATTER>(idx, __fsub_rn(tstop, t), vin, vout, val, acc);
+        t = tstop;
+        if (ta <= tb) {
+            idx += r.step[0];
+            ka += 1.0f;
+            ta = ka < na ? __fmaf_rn(ka, r.dt[0], r.t0[0]) : INF;
+        } else {
+            idx += r.step[1];
+            kb += 1.0f;
+            tb = kb < nb ? __fmaf_rn(kb, r.dt[1], r.t0[1]) : INF;
         }
     }
-    const float seg = __fsub_rn(r.tend, t);
-    if (SCATTER) {
-        atomicAdd(vout + idx, __fmul_rn(val, seg));
-    } else {
-        acc = __fmaf_rn(__ldg(vin + idx), seg, acc);
+#pragma unroll 1
+    while (tf < r.tend) {
+        visit<SCATTER>(idx, __fsub_rn(tf, t), vin, vout, val, acc);
+        t = tf;
+        idx += r.step[2];
+        kf += 1.0f;
+        tf = kf < nf ? __fmaf_rn(kf, r.dt[2], r.t0[2]) : INF;
     }
+    visit<SCATTER>(idx, __fsub_rn(r.tend, t), vin, vout, val, acc);
     return acc;
 }
 
@@ -225,8 +254,8 @@ __device__ __forceinline__ void pixel_of(const TileCoord& c, const ViewRec& sv, 
     }
 }
 
-template <bool TWO_D>
-__global__ void __launch_bounds__(kThreads) project_kernel(const ViewRec* __restrict__ views,
+template <bool TWO_D, int F>
+__global__ void __launch_bounds__(kThreads, kMinBlocks) project_kernel(const ViewRec* __restrict__ views,
                                                            const Grid g, const Tiling tl,
                                                            const float* __restrict__ vol,
                                                            float* __restrict__ sino) {
@@ -240,14 +269,14 @@ __global__ void __launch_bounds__(kThreads) project_kernel(const ViewRec* __rest
         if (u >= tl.n_u || v >= tl.n_v) continue;
         Ray ray;
         float acc = 0.0f;
-        if (setup_ray(sv, g, u, v, ray)) acc = walk<false>(ray, vol, nullptr, 0.0f);
+        if (setup_ray<F>(sv, g, u, v, ray)) acc = walk<false>(ray, vol, nullptr, 0.0f);
         sino[((int64_t)c.view * tl.n_u + u) * tl.n_v + v] = __fmul_rn(acc, g.spacing);
     }
 }
 
 // MODE 0: scatter sino * spacing; MODE 1: scatter spacing (A^T 1).
-template <bool TWO_D, int MODE>
-__global__ void __launch_bounds__(kThreads) backproject_kernel(const ViewRec* __restrict__ views,
+template <bool TWO_D, int F, int MODE>
+__global__ void __launch_bounds__(kThreads, kMinBlocks) backproject_kernel(const ViewRec* __restrict__ views,
                                                                const Grid g, const Tiling tl,
                                                                const float* __restrict__ sino,
                                                                float* __restrict__ vol) {
@@ -263,13 +292,14 @@ __global__ void __launch_bounds__(kThreads) backproject_kernel(const ViewRec* __
         if (MODE == 0) y = __ldg(sino + ((int64_t)c.view * tl.n_u + u) * tl.n_v + v);
         if (y == 0.0f) continue;
         Ray ray;
-        if (setup_ray(sv, g, u, v, ray)) walk<true>(ray, nullptr, vol, __fmul_rn(y, g.spacing));
+        if (setup_ray<F>(sv, g, u, v, ray))
+            walk<true>(ray, nullptr, vol, __fmul_rn(y, g.spacing));
     }
 }
 
 // r = R (y - A x) with R = 1 / (A 1) = 1 / (spacing * chord); 0 for rays that miss.
-template <bool TWO_D>
-__global__ void __launch_bounds__(kThreads)
+template <bool TWO_D, int F>
+__global__ void __launch_bounds__(kThreads, kMinBlocks)
     project_residual_kernel(const ViewRec* __restrict__ views, const Grid g, const Tiling tl,
                             const float* __restrict__ x, const float* __restrict__ y,
                             float* __restrict__ res) {
@@ -284,7 +314,7 @@ __global__ void __launch_bounds__(kThreads)
         const int64_t k = ((int64_t)c.view * tl.n_u + u) * tl.n_v + v;
         Ray ray;
         float out = 0.0f;
-        if (setup_ray(sv, g, u, v, ray) && ray.tend > 0.0f) {
+        if (setup_ray<F>(sv, g, u, v, ray) && ray.tend > 0.0f) {
             const float ax = __fmul_rn(walk<false>(ray, x, nullptr, 0.0f), g.spacing);
             out = __fdiv_rn(__fsub_rn(__ldg(y + k), ax), __fmul_rn(ray.tend, g.spacing));
         }
@@ -347,53 +377,45 @@ int elementwise_blocks(int64_t n) {
 
 }  // namespace
 
+// Instantiation by (2D, inner axis).  2D grids are always walked with x inner.
+#define CT_LAUNCH_BY_AXIS(KERNEL, EXTRA, ...)                                                 \
+    do {                                                                                     \
+        const unsigned nb_ = (unsigned)grid_for(t);                                          \
+        if (nb_ == 0) return cudaSuccess;                                                    \
+        if (t.two_d)                                                                         \
+            KERNEL<true, 0 EXTRA><<<nb_, kThreads, 0, stream>>>(__VA_ARGS__);                \
+        else if (g.fast == 2)                                                                \
+            KERNEL<false, 2 EXTRA><<<nb_, kThreads, 0, stream>>>(__VA_ARGS__);               \
+        else if (g.fast == 1)                                                                \
+            KERNEL<false, 1 EXTRA><<<nb_, kThreads, 0, stream>>>(__VA_ARGS__);               \
+        else                                                                                 \
+            KERNEL<false, 0 EXTRA><<<nb_, kThreads, 0, stream>>>(__VA_ARGS__);               \
+        return cudaGetLastError();                                                           \
+    } while (0)
+
+#define CT_NO_EXTRA
+#define CT_MODE0 , 0
+#define CT_MODE1 , 1
+
 cudaError_t launch_project(const ViewRec* views, const Grid& g, const Tiling& t, const float* vol,
                            float* sino, cudaStream_t stream) {
-    const int64_t nb = grid_for(t);
-    if (nb <= 0) return cudaSuccess;
-    if (t.two_d)
-        project_kernel<true><<<(unsigned)nb, kThreads, 0, stream>>>(views, g, t, vol, sino);
-    else
-        project_kernel<false><<<(unsigned)nb, kThreads, 0, stream>>>(views, g, t, vol, sino);
-    return cudaGetLastError();
+    CT_LAUNCH_BY_AXIS(project_kernel, CT_NO_EXTRA, views, g, t, vol, sino);
 }
 
 cudaError_t launch_backproject(const ViewRec* views, const Grid& g, const Tiling& t,
                                const float* sino, float* vol, cudaStream_t stream) {
-    const int64_t nb = grid_for(t);
-    if (nb <= 0) return cudaSuccess;
-    if (t.two_d)
-        backproject_kernel<true, 0><<<(unsigned)nb, kThreads, 0, stream>>>(views, g, t, sino, vol);
-    else
-        backproject_kernel<false, 0><<<(unsigned)nb, kThreads, 0, stream>>>(views, g, t, sino,
-                                                                             vol);
-    return cudaGetLastError();
+    CT_LAUNCH_BY_AXIS(backproject_kernel, CT_MODE0, views, g, t, sino, vol);
 }
 
 cudaError_t launch_backproject_ones(const ViewRec* views, const Grid& g, const Tiling& t,
                                     float* vol, cudaStream_t stream) {
-    const int64_t nb = grid_for(t);
-    if (nb <= 0) return cudaSuccess;
-    if (t.two_d)
-        backproject_kernel<true, 1><<<(unsigned)nb, kThreads, 0, stream>>>(views, g, t, nullptr,
-                                                                            vol);
-    else
-        backproject_kernel<false, 1><<<(unsigned)nb, kThreads, 0, stream>>>(views, g, t, nullptr,
-                                                                             vol);
-    return cudaGetLastError();
+    CT_LAUNCH_BY_AXIS(backproject_kernel, CT_MODE1, views, g, t, nullptr, vol);
 }
 
 cudaError_t launch_project_residual(const ViewRec* views, const Grid& g, const Tiling& t,
                                     const float* x, const float* y, float* r,
                                     cudaStream_t stream) {
-    const int64_t nb = grid_for(t);
-    if (nb <= 0) return cudaSuccess;
-    if (t.two_d)
-        project_residual_kernel<true><<<(unsigned)nb, kThreads, 0, stream>>>(views, g, t, x, y, r);
-    else
-        project_residual_kernel<false><<<(unsigned)nb, kThreads, 0, stream>>>(views, g, t, x, y,
-                                                                              r);
-    return cudaGetLastError();
+    CT_LAUNCH_BY_AXIS(project_residual_kernel, CT_NO_EXTRA, views, g, t, x, y, r);
 }
 
 cudaError_t launch_invert(float* c, int64_t n, cudaStream_t stream) {
