@@ -26,7 +26,7 @@ constexpr int kThreads = 256;  // 8 warps
 constexpr int kRows = 4;       // 3D tiles: 8 warps x 4 rows = 32 pixels along the warp axis
 constexpr int kTile = 32;      // 3D tiles are 32 x 32 pixels
 constexpr int kTile2D = 256;   // 2D tiles are 256 detector pixels
-constexpr int kMinBlocks = 5;  // resident CTAs per SM the walk kernels are compiled for (<= 51 regs)
+constexpr int kMinBlocks = 6;  // resident CTAs per SM the walk kernels are compiled for (<= 51 regs)
 
 __device__ __forceinline__ float f_inf() { return __int_as_float(0x7f800000); }
 
@@ -56,7 +56,6 @@ template <int F>
 __device__ __forceinline__ bool setup_ray(const ViewRec& vr, const Grid& g, int u, int v,
                                           Ray& r) {
     constexpr int A = F == 0 ? 1 : 0;
-    constexpr int B = F == 2 ? 1 : 2;
     const double fu = (double)u, fv = (double)v;
     double o[3], d[3];
     double amin, amax;
@@ -177,18 +176,29 @@ __device__ __forceinline__ float walk(const Ray& r, const float* __restrict__ vi
     const float na = (float)r.n[0], nb = (float)r.n[1], nf = (float)r.n[2];
     int idx = r.idx;
     float t = 0.0f, acc = 0.0f;
+    float v = 0.0f;
+    if (!SCATTER) v = __ldg(vin + idx);
 #pragma unroll 1
     for (int outer = r.n[0] + r.n[1]; outer > 0; --outer) {
         const float tstop = fminf(ta, tb);
 #pragma unroll 1
         while (tf < tstop) {
-            visit<SCATTER>(idx, __fsub_rn(tf, t), vin, vout, val, acc);
+            const float seg = __fsub_rn(tf, t);
+            if (SCATTER) {
+                atomicAdd(vout + idx, __fmul_rn(val, seg));
+                idx += r.step[2];
+            } else {
+                idx += r.step[2];
+                const float vn = __ldg(vin + idx);
+                acc = __fmaf_rn(v, seg, acc);
+                v = vn;
+            }
             t = tf;
-            idx += r.step[2];
             kf += 1.0f;
             tf = kf < nf ? __fmaf_rn(kf, r.dt[2], r.t0[2]) : INF;
         }
-        visit<SCATTER>(idx, __fsub_rn(tstop, t), vin, vout, val, acc);
+        const float seg = __fsub_rn(tstop, t);
+        if (SCATTER) atomicAdd(vout + idx, __fmul_rn(val, seg));
         t = tstop;
         if (ta <= tb) {
             idx += r.step[0];
@@ -199,16 +209,31 @@ __device__ __forceinline__ float walk(const Ray& r, const float* __restrict__ vi
             kb += 1.0f;
             tb = kb < nb ? __fmaf_rn(kb, r.dt[1], r.t0[1]) : INF;
         }
+        if (!SCATTER) {
+            const float vn = __ldg(vin + idx);
+            acc = __fmaf_rn(v, seg, acc);
+            v = vn;
+        }
     }
 #pragma unroll 1
     while (tf < r.tend) {
-        visit<SCATTER>(idx, __fsub_rn(tf, t), vin, vout, val, acc);
+        const float seg = __fsub_rn(tf, t);
+        if (SCATTER) {
+            atomicAdd(vout + idx, __fmul_rn(val, seg));
+            idx += r.step[2];
+        } else {
+            idx += r.step[2];
+            const float vn = __ldg(vin + idx);
+            acc = __fmaf_rn(v, seg, acc);
+            v = vn;
+        }
         t = tf;
-        idx += r.step[2];
         kf += 1.0f;
         tf = kf < nf ? __fmaf_rn(kf, r.dt[2], r.t0[2]) : INF;
     }
-    visit<SCATTER>(idx, __fsub_rn(r.tend, t), vin, vout, val, acc);
+    const float seg = __fsub_rn(r.tend, t);
+    if (SCATTER) atomicAdd(vout + idx, __fmul_rn(val, seg));
+    else acc = __fmaf_rn(v, seg, acc);
     return acc;
 }
 
@@ -247,10 +272,10 @@ __device__ __forceinline__ void pixel_of(const TileCoord& c, const ViewRec& sv, 
         v = 0;
     } else if (sv.lanes_along_v) {
         v = c.vt * kTile + lane;
-        u = c.ut * kTile + warp * kRows + r;
+        u = c.ut * kTile + r * 8 + warp;
     } else {
         u = c.ut * kTile + lane;
-        v = c.vt * kTile + warp * kRows + r;
+        v = c.vt * kTile + r * 8 + warp;
     }
 }
 
