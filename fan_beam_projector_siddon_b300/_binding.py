@@ -69,6 +69,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.ct_sirt_workspace_bytes.restype = sz
     L.ct_sirt_iterate.argtypes = [vp, vp, vp, vp, sz, i32, f32, i32, vp]
     L.ct_sirt_iterate.restype = i32
+    L.ct_backproject_static.argtypes = [vp, vp, vp, vp]
+    L.ct_backproject_static.restype = i32
     L.ct_status_string.argtypes = [i32]
     L.ct_status_string.restype = ctypes.c_char_p
     _lib = L
@@ -117,6 +119,12 @@ def ct_backproject(handle: int, d_sino: int, d_volume: int, d_workspace: int | N
                    workspace_bytes: int, stream: int | None) -> None:
     _check(load_library().ct_backproject(handle, d_sino, d_volume, d_workspace,
                                          workspace_bytes, stream), "ct_backproject")
+
+
+def ct_backproject_static(handle: int, d_sino: int, d_volume: int, stream: int | None) -> None:
+    """Backprojection without allocation or workspace (see ``include/ct.h``)."""
+    _check(load_library().ct_backproject_static(handle, d_sino, d_volume, stream),
+           "ct_backproject_static")
 
 
 def ct_sirt_workspace_bytes(handle: int) -> int:

@@ -3,6 +3,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -407,3 +408,67 @@ ct_status ct_sirt_iterate(const ct_geometry* g, float* d_x, const float* d_y, vo
 }
 
 }  // extern "C"
+
+// ---- backprojection without allocation (scratch in a fixed device array) -------------------
+//
+// Some callers cannot allocate device memory when they backproject: code running inside a
+// framework that hands it only a stream and its input/output pointers (a plugin or operator with
+// no access to an allocator), real-time pipelines that forbid allocation after start-up, and
+// programs that keep every device byte in a pool of their own.  For them the accumulator that
+// ct_backproject keeps in the caller's workspace lives here in one static device array instead.
+namespace {
+
+__device__ __align__(256) float g_ct_static_scratch[CT_STATIC_SCRATCH_VOXELS];
+
+constexpr int kMaxStaticDevices = 64;
+std::mutex g_static_mu;
+float* g_static_scratch_ptr[kMaxStaticDevices];  // device address of the array, per device
+
+// Device address of the static array on `device`, which must be the current device.  The
+// first call per device looks the address up (this may load the module on that device).
+ct_status static_scratch_on(int device, float** out) {
+    if (device < 0 || device >= kMaxStaticDevices) return CT_ERR_INVALID_ARGUMENT;
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (g_static_scratch_ptr[device] == nullptr) {
+        void* p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_ct_static_scratch);
+        if (e != cudaSuccess || p == nullptr) {
+            cudaGetLastError();
+            return CT_ERR_CUDA;
+        }
+        g_static_scratch_ptr[device] = static_cast<float*>(p);
+    }
+    *out = g_static_scratch_ptr[device];
+    return CT_OK;
+}
+
+}  // namespace
+
+extern "C" ct_status ct_backproject_static(const ct_geometry* g, const float* d_sino,
+                                           float* d_volume, cudaStream_t stream) {
+    if (g == nullptr) return CT_ERR_INVALID_ARGUMENT;
+    int current = -1;
+    if (cudaGetDevice(&current) != cudaSuccess) {
+        cudaGetLastError();
+        return CT_ERR_CUDA;
+    }
+    if (current != g->device) return CT_ERR_INVALID_ARGUMENT;
+    ct_status st = check_call(g, d_sino, sino_bytes(g), d_volume, volume_bytes(g), nullptr, 0, 0);
+    if (st != CT_OK) return st;
+    if (g->info.volume_layout == ct::LAYOUT_ZYX) {
+        // this geometry needs no scratch: accumulate straight into the caller's volume
+        cudaError_t e = cudaMemsetAsync(d_volume, 0, volume_bytes(g), stream);
+        if (e == cudaSuccess)
+            e = ct::launch_backproject(g->d_views, g->grid, g->tiling, d_sino, d_volume, stream);
+        return from_cuda(e);
+    }
+    if (g->info.n_voxels > (int64_t)CT_STATIC_SCRATCH_VOXELS) return CT_ERR_WORKSPACE;
+    float* acc = nullptr;
+    if ((st = static_scratch_on(g->device, &acc)) != CT_OK) return st;
+    // the array keeps the previous call's sums: clear the part this call accumulates into
+    cudaError_t e = cudaMemsetAsync(acc, 0, volume_bytes(g), stream);
+    if (e == cudaSuccess)
+        e = ct::launch_backproject(g->d_views, g->grid, g->tiling, d_sino, acc, stream);
+    if (e == cudaSuccess) e = from_internal(g, acc, d_volume, stream);
+    return from_cuda(e);
+}

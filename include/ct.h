@@ -168,6 +168,30 @@ CT_API ct_status ct_sirt_iterate(const ct_geometry *geom, float *d_x, const floa
                           float relaxation, int32_t workspace_initialised,
                           struct CUstream_st *stream);
 
+/*
+ * Backprojection that allocates nothing: d_volume = A^T d_sino, the same operator, kernels and
+ * weights as ct_backproject, for callers that cannot allocate device memory at the time they
+ * backproject (code that receives only a stream and its input/output pointers from a host
+ * framework, real-time pipelines that forbid allocation after start-up, programs that keep all
+ * device memory in their own pool).  It takes no workspace: when the geometry's internal volume
+ * order differs from the caller's (info.volume_layout != 0) the accumulator lives in one static
+ * device array of CT_STATIC_SCRATCH_VOXELS floats (16 MiB) that every GPU which loads the library
+ * holds until the process exits.  The pages describe no such entry point; it has no counterpart
+ * there.
+ *
+ * d_sino, d_volume  device buffers as for ct_backproject; d_volume is overwritten.
+ * Errors: CT_ERR_WORKSPACE if the geometry needs the static array and has more than
+ * CT_STATIC_SCRATCH_VOXELS voxels; CT_ERR_INVALID_ARGUMENT if the handle's device is not the
+ * current device; otherwise as ct_backproject.
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress, which may
+ * load the module on that device); make that first call before any stream capture.  Every call
+ * shares the one array: it is cleared on the stream at the start of each call, and calls whose
+ * work overlaps on the GPU (different streams, or graphs replayed concurrently) race on it.
+ */
+#define CT_STATIC_SCRATCH_VOXELS (1u << 22)
+CT_API ct_status ct_backproject_static(const ct_geometry *geom, const float *d_sino,
+                                       float *d_volume, struct CUstream_st *stream);
+
 /* Static, human-readable name of a status code. */
 CT_API const char *ct_status_string(ct_status status);
 
