@@ -147,40 +147,101 @@ __device__ __forceinline__ bool setup_ray(const ViewRec& vr, const Grid& g, int 
     return true;
 }
 
-// One segment: gather or scatter.
-template <bool SCATTER>
-__device__ __forceinline__ void visit(int idx, float seg, const float* __restrict__ vin,
-                                      float* __restrict__ vout, float val, float& acc) {
-    if (SCATTER)
-        atomicAdd(vout + idx, __fmul_rn(val, seg));
-    else
-        acc = __fmaf_rn(__ldg(vin + idx), seg, acc);
-}
-
 // The walk.  GATHER returns sum_k vol[idx_k] * seg_k (voxel units); SCATTER adds val * seg_k to
 // vol[idx_k] and returns 0.  Both evaluate every segment length with the same operations.
 //
 // Order of work: the outer loop steps through the crossings of the two outer axes; before each
-// outer crossing, the inner loop takes the inner-axis crossings that come first.  A warp's lanes
-// cover neighbouring pixels along the detector axis that is aligned with the inner (fast) axis,
-// so they meet the same outer planes in the same order and stay in lock-step: each step's 32
+// outer crossing, the inner-axis crossings that come first are taken.  A warp's lanes cover
+// neighbouring pixels along the detector axis that is aligned with the inner (fast) axis, so
+// they meet the same outer planes in the same order and stay in lock-step: each step's 32
 // gathers or atomics land in one or two 128-byte lines.
+//
+// Two phases.  The main phase runs while the next outer crossing lies strictly before the
+// earlier of the two outer axes' last crossings: there neither outer axis can run out, so its
+// next crossing is computed without a check, and the first inner crossing of an outer step is
+// handled inline (a second one is rare).  The gather issues the loads for the next outer step
+// (the voxel after the outer crossing, and the one after a pending inner crossing) one step
+// ahead.  The tail phase takes the remaining events with per-axis exhaustion checks.  Both
+// phases visit the same events in the same order with the same arithmetic.
 template <bool SCATTER>
 __device__ __forceinline__ float walk(const Ray& r, const float* __restrict__ vin,
                                       float* __restrict__ vout, float val) {
     const float INF = f_inf();
+    const float na = (float)r.n[0], nb = (float)r.n[1], nf = (float)r.n[2];
     float ta = r.n[0] > 0 ? r.t0[0] : INF;
     float tb = r.n[1] > 0 ? r.t0[1] : INF;
     float tf = r.n[2] > 0 ? r.t0[2] : INF;
     float ka = 0.0f, kb = 0.0f, kf = 0.0f;
-    const float na = (float)r.n[0], nb = (float)r.n[1], nf = (float)r.n[2];
     int idx = r.idx;
     float t = 0.0f, acc = 0.0f;
-    float v = 0.0f;
-    if (!SCATTER) v = __ldg(vin + idx);
+    // Main phase: outer crossings strictly before the earlier of the two outer axes' last
+    // crossings, so neither outer axis can run out here and its next crossing needs no check.
+    // (The last crossings use the same fmaf as the walk, so the comparison is exact.)
+    const float la = r.n[0] > 0 ? __fmaf_rn(na - 1.0f, r.dt[0], r.t0[0]) : INF;
+    const float lb = r.n[1] > 0 ? __fmaf_rn(nb - 1.0f, r.dt[1], r.t0[1]) : INF;
+    const float lim = fminf(la, lb);
+    float tstop = fminf(ta, tb);
+    bool p = tf < tstop;
+    float v0 = 0.0f, v1 = 0.0f;  // gather: values of the current voxel and of the next one inward
+    if (!SCATTER) {
+        v0 = __ldg(vin + idx);
+        if (p) v1 = __ldg(vin + idx + r.step[2]);
+    }
 #pragma unroll 1
-    for (int outer = r.n[0] + r.n[1]; outer > 0; --outer) {
-        const float tstop = fminf(ta, tb);
+    while (tstop < lim) {
+        const float seg0 = __fsub_rn(p ? tf : tstop, t);
+        if (SCATTER)
+            atomicAdd(vout + idx, __fmul_rn(val, seg0));
+        else
+            acc = __fmaf_rn(v0, seg0, acc);
+        if (p) {
+            idx += r.step[2];
+            t = tf;
+            kf += 1.0f;
+            tf = kf < nf ? __fmaf_rn(kf, r.dt[2], r.t0[2]) : INF;
+#pragma unroll 1
+            while (tf < tstop) {  // a second inner crossing before this outer one (rare)
+                const float seg = __fsub_rn(tf, t);
+                if (SCATTER) {
+                    atomicAdd(vout + idx, __fmul_rn(val, seg));
+                    idx += r.step[2];
+                } else {
+                    acc = __fmaf_rn(v1, seg, acc);
+                    idx += r.step[2];
+                    v1 = __ldg(vin + idx);
+                }
+                t = tf;
+                kf += 1.0f;
+                tf = kf < nf ? __fmaf_rn(kf, r.dt[2], r.t0[2]) : INF;
+            }
+            const float seg1 = __fsub_rn(tstop, t);
+            if (SCATTER)
+                atomicAdd(vout + idx, __fmul_rn(val, seg1));
+            else
+                acc = __fmaf_rn(v1, seg1, acc);
+        }
+        t = tstop;
+        if (ta <= tb) {
+            idx += r.step[0];
+            ka += 1.0f;
+            ta = __fmaf_rn(ka, r.dt[0], r.t0[0]);
+        } else {
+            idx += r.step[1];
+            kb += 1.0f;
+            tb = __fmaf_rn(kb, r.dt[1], r.t0[1]);
+        }
+        tstop = fminf(ta, tb);
+        p = tf < tstop;
+        if (!SCATTER) {
+            v0 = __ldg(vin + idx);
+            if (p) v1 = __ldg(vin + idx + r.step[2]);
+        }
+    }
+    // Tail: the remaining events with the per-axis checks.
+    float v = v0;
+#pragma unroll 1
+    for (int outer = (int)(na - ka) + (int)(nb - kb); outer > 0; --outer) {
+        tstop = fminf(ta, tb);
 #pragma unroll 1
         while (tf < tstop) {
             const float seg = __fsub_rn(tf, t);
@@ -232,8 +293,10 @@ __device__ __forceinline__ float walk(const Ray& r, const float* __restrict__ vi
         tf = kf < nf ? __fmaf_rn(kf, r.dt[2], r.t0[2]) : INF;
     }
     const float seg = __fsub_rn(r.tend, t);
-    if (SCATTER) atomicAdd(vout + idx, __fmul_rn(val, seg));
-    else acc = __fmaf_rn(v, seg, acc);
+    if (SCATTER)
+        atomicAdd(vout + idx, __fmul_rn(val, seg));
+    else
+        acc = __fmaf_rn(v, seg, acc);
     return acc;
 }
 
