@@ -180,7 +180,7 @@ def run_reference(args, rank, world):
     w = W.config(CONFIG_ID)
     x = w.phantom()
     cores = os.cpu_count() or 1
-    n_views = int(max(4, min(w.n_views, cores)))
+    n_views = sample_views(w, args.sample_views)
     rates, times = [], []
     for _ in range(args.warmup):
         oracle_sample_rate(w, x, max(1, n_views // 4), cores)
@@ -209,6 +209,25 @@ def run_reference(args, rank, world):
 # ----------------------------------------------------------------------------------------------
 # GPU arm
 # ----------------------------------------------------------------------------------------------
+
+def max_over_ranks(value: float, world: int) -> float:
+    """Largest `value` over all ranks of the default process group (NCCL or gloo)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sample_views(w: W.Workload, requested: int | None) -> int:
+    """Views per oracle step: one per host core (bounded), so a step is seconds of CPU work."""
+    cores = os.cpu_count() or 1
+    n = requested if requested else cores
+    return int(max(1, min(w.n_views, n)))
+
 
 def profiled_traffic(kernel: str):
     """DRAM bytes per launch of `kernel` from its committed ncu summary, or None when the kernel
@@ -297,10 +316,7 @@ def run_ours(args, rank, world):
     bp_ms = [e[1].elapsed_time(e[2]) for e in ev]
     step_ms = [a + b for a, b in zip(fp_ms, bp_ms)]
     mean_step = sum(step_ms) / len(step_ms)
-    if world > 1:
-        t = torch.tensor([mean_step], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        mean_step = float(t.item())
+    mean_step = max_over_ranks(mean_step, world)
     value = world * 2 * U / (mean_step * 1e-3)
 
     # ---- end to end through the C ABI: pinned host in, host out, copies inside the region ----
@@ -351,10 +367,7 @@ def run_ours(args, rank, world):
         e2e_step()
     torch.cuda.synchronize()
     e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, world)
     h2d = vol_h.numel() * 4 + meas_h.numel() * 4
     d2h = sino_h.numel() * 4 + back_h.numel() * 4
 
@@ -397,7 +410,7 @@ def run_ours(args, rank, world):
     }
     if world == 1 and not args.no_cpu_baseline:
         cores = os.cpu_count() or 1
-        n_views = int(max(4, min(w.n_views, cores)))
+        n_views = sample_views(w, args.sample_views)
         r, dt, nu = oracle_sample_rate(w, x_host, n_views, cores)
         line["cpu_baseline"] = {"value": r, "unit": UNIT, "cores": cores, "kind": "oracle",
                                 "sample": f"FP+BP of {n_views} evenly spaced views of "
@@ -413,6 +426,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sample-views", type=int, default=None,
+                    help="views per oracle step (default: one per host core)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -1,0 +1,92 @@
+"""Host-side parts of the benchmark: work counting, max-over-ranks with two gloo ranks, and the
+reference (oracle) arm's JSON line and rank behaviour.  No GPU."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+
+import oracle
+from fan_beam_projector_siddon_b300 import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5])
+def test_count_updates_matches_oracle_segments(n):
+    """1 + crossings per ray equals the oracle's positive-length segment count, except where a
+    ray crosses two planes at the same point (a zero-length segment the oracle merges)."""
+    w = W.small_config(n)
+    _, segs = oracle.Geometry.from_workload(w).ray_lengths()
+    counted = bench.count_updates(w)
+    assert counted >= int(segs.sum())
+    assert counted - int(segs.sum()) <= 1e-3 * counted
+
+
+def test_count_updates_jittered_workload_is_exact():
+    """With per-view jitter no ray meets two planes at one point: the counts agree exactly."""
+    w = W.small_config(4)
+    _, segs = oracle.Geometry.from_workload(w).ray_lengths()
+    assert bench.count_updates(w) == int(segs.sum())
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        got = bench.max_over_ranks(10.0 + 5.0 * rank, world)
+        out.put((rank, got))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_two_gloo_ranks():
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    got = dict(q.get(timeout=10) for _ in range(2))
+    assert got == {0: 15.0, 1: 15.0}
+
+
+def _run_reference(env_extra):
+    env = dict(os.environ, **env_extra)
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                           "--steps", "1", "--warmup", "0", "--sample-views", "2"],
+                          capture_output=True, text=True, env=env, timeout=600, cwd=ROOT)
+
+
+def test_reference_arm_prints_one_json_line():
+    r = _run_reference({"RANK": "0", "WORLD_SIZE": "1"})
+    assert r.returncode == 0, r.stderr
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "updates/s" and d["value"] > 0
+    assert d["higher_is_better"] is True and d["metric"] == bench.METRIC
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+
+
+def test_reference_arm_non_zero_rank_exits_quietly():
+    r = _run_reference({"RANK": "1", "WORLD_SIZE": "2"})
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == ""
