@@ -66,6 +66,7 @@ def _load():
         L.oracle_brute_row.argtypes = [gp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, dp]
         L.oracle_backproject_voxels.argtypes = [gp, dp, ctypes.c_int64, i64p, dp]
         L.oracle_sirt.argtypes = [gp, dp, dp, ctypes.c_int32, ctypes.c_double, dp]
+        L.oracle_cgls.argtypes = [gp, dp, dp, ctypes.c_int32, dp]
         _lib = L
     return _lib
 
@@ -200,6 +201,16 @@ class Geometry:
         res = np.zeros(max(n_iter, 1), dtype=np.float64)
         L.oracle_sirt(ctypes.byref(self._g), _dp(y), _dp(x), n_iter, relax, _dp(res))
         return x, res[:n_iter]
+
+    def cgls(self, y, n_iter: int, x0=None):
+        """(x after n_iter CGLS steps, ||y - A x||^2 before the first and after each step)."""
+        L = _load()
+        y = np.ascontiguousarray(np.asarray(y, dtype=np.float64).reshape(self.sino_shape))
+        x = (np.zeros(self.volume_shape, dtype=np.float64) if x0 is None
+             else np.array(x0, dtype=np.float64).reshape(self.volume_shape))
+        res = np.zeros(n_iter + 1, dtype=np.float64)
+        L.oracle_cgls(ctypes.byref(self._g), _dp(y), _dp(x), n_iter, _dp(res))
+        return x, res
 
 
 def line_segments(e, d, amin, amax, vol_shape, spacing, dims=3):

@@ -471,3 +471,61 @@ void oracle_sirt(const og_geom *g, const double *y, double *x, int32_t n_iter, d
     }
     free(R); free(C); free(ones_r); free(ones_v); free(ax); free(b);
 }
+
+/* ---- CGLS ------------------------------------------------------------------------------------ */
+
+/*
+ * n_iter steps of CGLS (conjugate gradients on the normal equations A^T A x = A^T y, in the
+ * form that never forms A^T A) from the given x, all vectors float64:
+ *   r = y - A x,  s = A^T r,  p = s,  gamma = <s, s>
+ *   repeat: q = A p;  alpha = gamma / <q, q>;  x += alpha p;  r -= alpha q;
+ *           s = A^T r;  gamma' = <s, s>;  beta = gamma' / gamma;  p = s + beta p;  gamma = gamma'
+ * A zero denominator (converged) gives alpha = 0 or beta = 0.  residual_norms (optional,
+ * n_iter + 1 entries) receives ||r||^2 before the first and after each step.
+ */
+void oracle_cgls(const og_geom *g, const double *y, double *x, int32_t n_iter,
+                 double *residual_norms) {
+    int64_t n[3];
+    axis_cells(g, n);
+    const int64_t nvox = n[0] * n[1] * n[2];
+    const int64_t nray = (int64_t)g->n_views * g->nu * g->nv;
+    double *r = (double *)malloc(sizeof(double) * (size_t)nray);
+    double *q = (double *)malloc(sizeof(double) * (size_t)nray);
+    double *s = (double *)malloc(sizeof(double) * (size_t)nvox);
+    double *p = (double *)malloc(sizeof(double) * (size_t)nvox);
+    oracle_project(g, x, q, 0, g->n_views);
+    double rn = 0.0;
+    for (int64_t i = 0; i < nray; ++i) {
+        r[i] = y[i] - q[i];
+        rn += r[i] * r[i];
+    }
+    if (residual_norms) residual_norms[0] = rn;
+    memset(s, 0, sizeof(double) * (size_t)nvox);
+    oracle_backproject(g, r, s, 0, g->n_views);
+    double gamma = 0.0;
+    for (int64_t i = 0; i < nvox; ++i) {
+        p[i] = s[i];
+        gamma += s[i] * s[i];
+    }
+    for (int it = 0; it < n_iter; ++it) {
+        oracle_project(g, p, q, 0, g->n_views);
+        double delta = 0.0;
+        for (int64_t i = 0; i < nray; ++i) delta += q[i] * q[i];
+        const double alpha = delta > 0.0 ? gamma / delta : 0.0;
+        for (int64_t i = 0; i < nvox; ++i) x[i] += alpha * p[i];
+        rn = 0.0;
+        for (int64_t i = 0; i < nray; ++i) {
+            r[i] -= alpha * q[i];
+            rn += r[i] * r[i];
+        }
+        if (residual_norms) residual_norms[it + 1] = rn;
+        memset(s, 0, sizeof(double) * (size_t)nvox);
+        oracle_backproject(g, r, s, 0, g->n_views);
+        double gamma_new = 0.0;
+        for (int64_t i = 0; i < nvox; ++i) gamma_new += s[i] * s[i];
+        const double beta = gamma > 0.0 ? gamma_new / gamma : 0.0;
+        for (int64_t i = 0; i < nvox; ++i) p[i] = s[i] + beta * p[i];
+        gamma = gamma_new;
+    }
+    free(r); free(q); free(s); free(p);
+}

@@ -455,3 +455,60 @@ def test_sirt_one_step_closed_forms():
     y = np.random.default_rng(2).uniform(-1, 1, size=(1, 3, 2))
     x1, _ = g.sirt(y, 1)
     np.testing.assert_allclose(x1[0], y[0].T / s, rtol=1e-14)
+
+
+# ---------------------------------------------------------------------------------------------
+# CGLS
+# ---------------------------------------------------------------------------------------------
+
+def _dense_matrix(g):
+    """Rows of A for every ray by the C brute force (tiny problems only)."""
+    rows = []
+    for view in range(g.n_views):
+        for iu in range(g.n_u):
+            for iv in range(g.n_v):
+                rows.append(g.brute_row(view, iu, iv).reshape(-1))
+    return np.array(rows)
+
+
+def test_cgls_reaches_the_least_squares_solution():
+    """In exact arithmetic CGLS from x = 0 reaches the minimum-norm least-squares solution of
+    min ||A x - y|| within rank(A) steps; checked against numpy's SVD-based lstsq of the explicit
+    matrix (rows from the per-voxel brute force) on a 3x3x2-voxel cone problem."""
+    rng = np.random.default_rng(4)
+    views = []
+    for k in range(5):
+        th = 2 * math.pi * k / 5
+        src = np.array([6 * math.cos(th), 6 * math.sin(th), 0.7 * math.sin(3 * th)])
+        u = np.array([-math.sin(th), math.cos(th), 0.0])
+        v = np.array([0.0, 0.0, 1.0])
+        views.append(np.concatenate([src, -4 * src / 6, u, v]))
+    g = _geom(W.CONE, np.array(views), (2, 3, 3), 0.8, 4, 3, 0.9, 0.9)
+    A = _dense_matrix(g)
+    y = rng.uniform(0, 1, size=A.shape[0])
+    x_ls = np.linalg.lstsq(A, y, rcond=None)[0]
+    rank = np.linalg.matrix_rank(A)
+    x, res = g.cgls(y.reshape(g.sino_shape), rank + 2)
+    np.testing.assert_allclose(x.reshape(-1), x_ls, rtol=0, atol=1e-8 * np.abs(x_ls).max())
+    # the residual norm never increases
+    assert np.all(np.diff(res) <= 1e-12 * res[0])
+    # A x agrees with the oracle's own projection of x (CGLS used A, not a stand-in)
+    np.testing.assert_allclose(A @ x.reshape(-1), g.project(x).reshape(-1), rtol=1e-12,
+                               atol=1e-12)
+
+
+def test_cgls_fixed_point_and_first_step():
+    """Consistent data from x_true is a fixed point; the first step from 0 is the exact line
+    search along A^T y: x_1 = (|A^T y|^2 / |A A^T y|^2) A^T y."""
+    w = W.small_config(1)
+    g = oracle.Geometry.from_workload(w)
+    x_true = w.phantom().astype(np.float64)
+    y = g.project(x_true)
+    x1, res = g.cgls(y, 2, x0=x_true)
+    np.testing.assert_allclose(x1, x_true, rtol=0, atol=1e-12)
+    assert res.max() < 1e-20
+    s = g.backproject(y)
+    q = g.project(s)
+    want = (np.sum(s * s) / np.sum(q * q)) * s
+    x1, _ = g.cgls(y, 1)
+    np.testing.assert_allclose(x1, want, rtol=1e-12, atol=1e-14)
