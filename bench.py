@@ -255,6 +255,96 @@ def load_peaks():
     return 6400.0, "fallback"
 
 
+def sirt_leg(ct, torch, n_iters: int = 10):
+    """SIRT on the dual-axis tilt-series workload (512^3, 280 parallel3d views, 512x512 detector),
+    the configuration the pages quote SIRT timings on: n_iters iterations from zero, timed with
+    CUDA events; the one-off C = 1/(A^T 1) initialisation is timed separately."""
+    w = W.config(5)
+    g = ct.Geometry.from_workload(w)
+    x_true = torch.from_numpy(w.phantom()).cuda()
+    y = g.project(x_true)
+    ws = g.new_workspace(sirt=True)
+    x = torch.zeros_like(x_true)
+    stream = torch.cuda.current_stream()
+    e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    torch.cuda.synchronize()
+    e0.record(stream)
+    g.sirt(x, y, 0, ws, initialised=False)
+    e1.record(stream)
+    g.sirt(x, y, n_iters, ws, initialised=True)
+    e2.record(stream)
+    torch.cuda.synchronize()
+    init_ms, run_ms = e0.elapsed_time(e1), e1.elapsed_time(e2)
+    U5 = count_updates(w)
+    rel = float((x - x_true).norm() / x_true.norm())
+    sirt = {"workload": w.name, "iterations": n_iters, "ms_per_iteration": run_ms / n_iters,
+            "init_ms": init_ms, "updates_per_pass": U5,
+            "updates_per_s": 2 * U5 * n_iters / (run_ms * 1e-3),
+            "rel_error_vs_phantom": rel,
+            "note": "iteration = residual projection + backprojection + update; "
+                    "the pages' RTX 8000 figure for this workload is ~2.2 s per iteration"}
+    del ws
+    wc = g.new_workspace(cgls=True)
+    x.zero_()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    g.cgls(x, y, 0, wc, initialised=False)
+    e1.record(stream)
+    g.cgls(x, y, n_iters, wc, initialised=True)
+    e2.record(stream)
+    torch.cuda.synchronize()
+    cgls = {"workload": w.name, "iterations": n_iters,
+            "ms_per_iteration": e1.elapsed_time(e2) / n_iters, "init_ms": e0.elapsed_time(e1),
+            "rel_error_vs_phantom": float((x - x_true).norm() / x_true.norm()),
+            "note": "iteration = projection (+|q|^2) + fused residual backprojection + |s|^2 "
+                    "+ update, scalars on the device"}
+    del wc, x, y, x_true
+    torch.cuda.empty_cache()
+    return sirt, cgls
+
+
+def context_leg(ct, torch):
+    """The pages' performance-table workload shape (512^3 volume, circular cone, 360 views,
+    1024x768 detector at pitch 1.25; sid/sdd are not printed, 1000/1500 is this build's
+    reading): one forward projection, one backprojection, one CGLS iteration, CUDA events."""
+    views = W.circular_cone(360, 1000.0, 1500.0)
+    w = W.Workload("cone-512^3-360v-1024x768", W.CONE, views, (512, 512, 512), 1.0, 1024, 768,
+                   1.25, 1.25, 0, None)
+    g = ct.Geometry.from_workload(w)
+    x = torch.rand(w.volume_shape, device="cuda")
+    sino = torch.empty(w.sino_shape, device="cuda")
+    back = torch.empty(w.volume_shape, device="cuda")
+    ws = g.new_workspace()
+    stream = torch.cuda.current_stream()
+
+    def timed(fn, reps=3):
+        fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    fp = timed(lambda: g.project(x, out=sino, workspace=ws))
+    bp = timed(lambda: g.backproject(sino, out=back, workspace=ws))
+    del ws
+    wc = g.new_workspace(cgls=True)
+    xc = torch.zeros_like(x)
+    g.cgls(xc, sino, 0, wc, initialised=False)
+    it = timed(lambda: g.cgls(xc, sino, 1, wc, initialised=True))
+    del wc, xc, x, sino, back
+    torch.cuda.empty_cache()
+    return {"workload": w.name, "fp_ms": fp, "bp_ms": bp, "cgls_iteration_ms": it,
+            "pages_a100_ms": {"fp": 566.79, "bp": 1060.77, "cgls_iteration": 1753.73},
+            "note": "context only: the pages' figures are diffct on one A100 with unstated "
+                    "sid/sdd; not the same measurement"}
+
+
 def run_ours(args, rank, world):
     import torch
     import torch.distributed as dist
@@ -408,6 +498,10 @@ def run_ours(args, rank, world):
         "gpu_launches": 4 * args.steps,
         "clocks": clocks,
     }
+    if not args.no_sirt:
+        line["sirt"], line["cgls"] = sirt_leg(ct, torch)
+    if args.context:
+        line["context_pages_table"] = context_leg(ct, torch)
     if world == 1 and not args.no_cpu_baseline:
         cores = os.cpu_count() or 1
         n_views = sample_views(w, args.sample_views)
@@ -426,6 +520,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sirt", action="store_true", help="skip the SIRT/CGLS leg")
+    ap.add_argument("--context", action="store_true",
+                    help="also time the pages' performance-table workload shape")
     ap.add_argument("--sample-views", type=int, default=None,
                     help="views per oracle step (default: one per host core)")
     args = ap.parse_args()

@@ -4,11 +4,13 @@ The compute path is the C-ABI library ``libctproj.so`` (CUDA, sm_103a); this pac
 thin ctypes binding plus the seeded input generators in ``workloads``.
 """
 from ._binding import (CT_CONE, CT_FAN2D, CT_PARALLEL2D, CT_PARALLEL3D, CtError, Geometry,
-                       GeometryInfo, ct_backproject, ct_backproject_static, ct_geometry_create, ct_geometry_destroy,
+                       GeometryInfo, ct_backproject, ct_backproject_static, ct_cgls_iterate,
+                       ct_cgls_workspace_bytes, ct_geometry_create, ct_geometry_destroy,
                        ct_geometry_get_info, ct_project, ct_sirt_iterate,
                        ct_sirt_workspace_bytes, ct_status_string, load_library)
 
 __all__ = ["CT_CONE", "CT_FAN2D", "CT_PARALLEL2D", "CT_PARALLEL3D", "CtError", "Geometry",
-           "GeometryInfo", "ct_backproject", "ct_backproject_static", "ct_geometry_create", "ct_geometry_destroy",
+           "GeometryInfo", "ct_backproject", "ct_backproject_static", "ct_cgls_iterate",
+           "ct_cgls_workspace_bytes", "ct_geometry_create", "ct_geometry_destroy",
            "ct_geometry_get_info", "ct_project", "ct_sirt_iterate", "ct_sirt_workspace_bytes",
            "ct_status_string", "load_library"]

@@ -69,6 +69,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.ct_sirt_workspace_bytes.restype = sz
     L.ct_sirt_iterate.argtypes = [vp, vp, vp, vp, sz, i32, f32, i32, vp]
     L.ct_sirt_iterate.restype = i32
+    L.ct_cgls_workspace_bytes.argtypes = [vp]
+    L.ct_cgls_workspace_bytes.restype = sz
+    L.ct_cgls_iterate.argtypes = [vp, vp, vp, vp, sz, i32, i32, vp]
+    L.ct_cgls_iterate.restype = i32
     L.ct_backproject_static.argtypes = [vp, vp, vp, vp]
     L.ct_backproject_static.restype = i32
     L.ct_status_string.argtypes = [i32]
@@ -140,6 +144,17 @@ def ct_sirt_iterate(handle: int, d_x: int, d_y: int, d_workspace: int, workspace
            "ct_sirt_iterate")
 
 
+def ct_cgls_workspace_bytes(handle: int) -> int:
+    return int(load_library().ct_cgls_workspace_bytes(handle))
+
+
+def ct_cgls_iterate(handle: int, d_x: int, d_y: int, d_workspace: int, workspace_bytes: int,
+                    n_iters: int, workspace_initialised: bool, stream: int | None) -> None:
+    _check(load_library().ct_cgls_iterate(handle, d_x, d_y, d_workspace, workspace_bytes,
+                                          int(n_iters), 1 if workspace_initialised else 0,
+                                          stream), "ct_cgls_iterate")
+
+
 def ct_status_string(status: int) -> str:
     return load_library().ct_status_string(int(status)).decode()
 
@@ -189,9 +204,14 @@ class Geometry:
     def sirt_workspace_bytes(self) -> int:
         return int(self.info.sirt_workspace_bytes)
 
-    def new_workspace(self, sirt: bool = False):
+    @property
+    def cgls_workspace_bytes(self) -> int:
+        return ct_cgls_workspace_bytes(self.handle)
+
+    def new_workspace(self, sirt: bool = False, cgls: bool = False):
         import torch
-        n = self.sirt_workspace_bytes if sirt else self.workspace_bytes
+        n = (self.cgls_workspace_bytes if cgls else
+             self.sirt_workspace_bytes if sirt else self.workspace_bytes)
         return torch.empty(max(n, 1), dtype=torch.uint8, device="cuda") if n else None
 
     @staticmethod
@@ -228,6 +248,17 @@ class Geometry:
         ct_backproject(self.handle, sino.data_ptr(), out.data_ptr(), ws, wsb,
                        self._stream(stream))
         return out
+
+    def cgls(self, x, y, n_iters: int, workspace, initialised: bool, stream=None):
+        """``n_iters`` CGLS steps on ``x`` in place; ``workspace`` carries the state between
+        calls (``initialised=False`` on the first call)."""
+        import torch
+        assert x.is_cuda and x.dtype == torch.float32 and x.is_contiguous()
+        assert y.is_cuda and y.dtype == torch.float32 and y.is_contiguous()
+        ws, wsb = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+        ct_cgls_iterate(self.handle, x.data_ptr(), y.data_ptr(), ws, wsb, n_iters, initialised,
+                        self._stream(stream))
+        return x
 
     def sirt(self, x, y, n_iters: int, workspace, initialised: bool, relaxation: float = 1.0,
              stream=None):

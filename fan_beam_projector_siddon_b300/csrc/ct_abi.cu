@@ -2,6 +2,7 @@
 // internal volume order, workspace carving and kernel dispatch.  Host code only.
 #include <cmath>
 #include <cstdint>
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -402,6 +403,85 @@ ct_status ct_sirt_iterate(const ct_geometry* g, float* d_x, const float* d_y, vo
         if (e == cudaSuccess)
             e = ct::launch_backproject(g->d_views, g->grid, g->tiling, Rres, B, stream);
         if (e == cudaSuccess) e = ct::launch_sirt_update(X, B, C, relaxation, nvox, stream);
+    }
+    if (e == cudaSuccess && !native) e = from_internal(g, X, d_x, stream);
+    return from_cuda(e);
+}
+
+// ---- CGLS -------------------------------------------------------------------------------------
+
+// Workspace of ct_cgls_iterate: x in the internal order (unless that is the caller's), p, s,
+// r, q, the partial sums of one reduction, and the four float64 scalars.
+struct CglsLayout {
+    size_t x, p, s, r, q, partials, scal, total;
+};
+
+static CglsLayout cgls_layout(const ct_geometry* g) {
+    const size_t vb = align_up(volume_bytes(g)), sb = align_up(sino_bytes(g));
+    const int64_t parts = std::max<int64_t>(ct::project_blocks(g->tiling), ct::norm_blocks());
+    CglsLayout L{};
+    size_t off = 0;
+    const bool native = g->info.volume_layout == ct::LAYOUT_ZYX;
+    L.x = off; off += native ? 0 : vb;
+    L.p = off; off += vb;
+    L.s = off; off += vb;
+    L.r = off; off += sb;
+    L.q = off; off += sb;
+    L.partials = off; off += align_up((size_t)parts * sizeof(double));
+    L.scal = off; off += align_up(4 * sizeof(double));
+    L.total = off;
+    return L;
+}
+
+size_t ct_cgls_workspace_bytes(const ct_geometry* g) {
+    return g == nullptr ? 0 : cgls_layout(g).total;
+}
+
+ct_status ct_cgls_iterate(const ct_geometry* g, float* d_x, const float* d_y, void* d_workspace,
+                          size_t workspace_bytes, int32_t n_iters, int32_t workspace_initialised,
+                          cudaStream_t stream) {
+    if (g == nullptr || n_iters < 0) return CT_ERR_INVALID_ARGUMENT;
+    const CglsLayout L = cgls_layout(g);
+    ct_status st = check_call(g, d_y, sino_bytes(g), d_x, volume_bytes(g), d_workspace,
+                              workspace_bytes, L.total);
+    if (st != CT_OK) return st;
+    const int64_t nvox = g->info.n_voxels, nray = g->info.n_rays;
+    char* ws = static_cast<char*>(d_workspace);
+    const bool native = g->info.volume_layout == ct::LAYOUT_ZYX;
+    float* X = native ? d_x : reinterpret_cast<float*>(ws + L.x);
+    float* P = reinterpret_cast<float*>(ws + L.p);
+    float* S = reinterpret_cast<float*>(ws + L.s);
+    float* R = reinterpret_cast<float*>(ws + L.r);
+    float* Q = reinterpret_cast<float*>(ws + L.q);
+    double* parts = reinterpret_cast<double*>(ws + L.partials);
+    double* scal = reinterpret_cast<double*>(ws + L.scal);
+    const int64_t fp_parts = ct::project_blocks(g->tiling), nrm_parts = ct::norm_blocks();
+    const ct::ViewRec* V = g->d_views;
+    cudaError_t e = cudaSuccess;
+    if (!native) e = to_internal(g, d_x, X, stream);
+    if (e == cudaSuccess && !workspace_initialised) {
+        // r = y - A x;  s = A^T r;  p = s;  gamma = |s|^2
+        e = ct::launch_project(V, g->grid, g->tiling, X, Q, stream);
+        if (e == cudaSuccess) e = ct::launch_sub(R, d_y, Q, nray, stream);
+        if (e == cudaSuccess) e = cudaMemsetAsync(S, 0, volume_bytes(g), stream);
+        if (e == cudaSuccess) e = ct::launch_backproject(V, g->grid, g->tiling, R, S, stream);
+        if (e == cudaSuccess) e = cudaMemsetAsync(P, 0, volume_bytes(g), stream);
+        if (e == cudaSuccess) e = ct::launch_norm_partials(S, nvox, parts, stream);
+        if (e == cudaSuccess) e = ct::launch_cgls_scalars(parts, nrm_parts, scal, 2, stream);
+        if (e == cudaSuccess) e = ct::launch_cgls_update(X, P, S, scal, nvox, stream);
+    }
+    for (int it = 0; it < n_iters && e == cudaSuccess; ++it) {
+        // q = A p, delta = |q|^2, alpha = gamma / delta
+        e = ct::launch_project_norm(V, g->grid, g->tiling, P, Q, parts, stream);
+        if (e == cudaSuccess) e = ct::launch_cgls_scalars(parts, fp_parts, scal, 0, stream);
+        // r -= alpha q, s = A^T r (s is zero here)
+        if (e == cudaSuccess)
+            e = ct::launch_backproject_residual(V, g->grid, g->tiling, R, Q, scal, S, stream);
+        // beta = |s|^2 / gamma, gamma = |s|^2
+        if (e == cudaSuccess) e = ct::launch_norm_partials(S, nvox, parts, stream);
+        if (e == cudaSuccess) e = ct::launch_cgls_scalars(parts, nrm_parts, scal, 1, stream);
+        // x += alpha p, p = s + beta p, s = 0
+        if (e == cudaSuccess) e = ct::launch_cgls_update(X, P, S, scal, nvox, stream);
     }
     if (e == cudaSuccess && !native) e = from_internal(g, X, d_x, stream);
     return from_cuda(e);

@@ -60,6 +60,22 @@ cudaError_t launch_backproject_ones(const ViewRec* views, const Grid& g, const T
 cudaError_t launch_project_residual(const ViewRec* views, const Grid& g, const Tiling& t,
                                     const float* x, const float* y, float* r,
                                     cudaStream_t stream);
+// CGLS pieces.  Scalars (float64, device): [gamma, delta, alpha, beta].
+int64_t project_blocks(const Tiling& t);  // blocks (= partial sums) of one projection launch
+int norm_blocks();                          // blocks (= partial sums) of launch_norm_partials
+cudaError_t launch_project_norm(const ViewRec* views, const Grid& g, const Tiling& t,
+                                const float* vol, float* sino, double* partials,
+                                cudaStream_t stream);
+cudaError_t launch_backproject_residual(const ViewRec* views, const Grid& g, const Tiling& t,
+                                        float* r, const float* q, const double* scal, float* vol,
+                                        cudaStream_t stream);
+cudaError_t launch_norm_partials(const float* v, int64_t n, double* partials,
+                                 cudaStream_t stream);
+cudaError_t launch_cgls_scalars(const double* partials, int64_t n, double* scal, int which,
+                                cudaStream_t stream);
+cudaError_t launch_cgls_update(float* x, float* p, float* s, const double* scal, int64_t n,
+                               cudaStream_t stream);
+cudaError_t launch_sub(float* r, const float* y, const float* q, int64_t n, cudaStream_t stream);
 cudaError_t launch_invert(float* c, int64_t n, cudaStream_t stream);
 cudaError_t launch_sirt_update(float* x, float* b, const float* c, float relax, int64_t n,
                                cudaStream_t stream);

@@ -410,6 +410,143 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
     }
 }
 
+// ---- CGLS ------------------------------------------------------------------------------------
+// Device-side scalars of a CGLS run: gamma = |s|^2, delta = |q|^2, alpha, beta (float64).
+enum { kGamma = 0, kDelta = 1, kAlpha = 2, kBeta = 3 };
+
+// Sum of a double over the block into partials[blockIdx.x] (all threads must call it).
+__device__ __forceinline__ void block_sum_to(double v, double* __restrict__ partials) {
+    __shared__ double warp_sums[kThreads / 32];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(0xffffffffu, v, o);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) warp_sums[warp] = v;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double s = 0.0;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) s += warp_sums[w];
+        partials[blockIdx.x] = s;
+    }
+}
+
+// q = A p, and per block the float64 sum of q^2 (for delta = |q|^2).
+template <bool TWO_D, int F>
+__global__ void __launch_bounds__(kThreads, kMinBlocks)
+    project_norm_kernel(const ViewRec* __restrict__ views, const Grid g, const Tiling tl,
+                        const float* __restrict__ vol, float* __restrict__ sino,
+                        double* __restrict__ partials) {
+    __shared__ ViewRec sv;
+    const TileCoord c = tile_of_block(tl);
+    load_view(views, c.view, sv);
+    double sq = 0.0;
+#pragma unroll 1
+    for (int row = 0; row < (TWO_D ? 1 : kRows); ++row) {
+        int u, v;
+        pixel_of<TWO_D>(c, sv, row, u, v);
+        if (u >= tl.n_u || v >= tl.n_v) continue;
+        Ray ray;
+        float acc = 0.0f;
+        if (setup_ray<F>(sv, g, u, v, ray)) acc = walk<false>(ray, vol, nullptr, 0.0f);
+        const float q = __fmul_rn(acc, g.spacing);
+        sino[((int64_t)c.view * tl.n_u + u) * tl.n_v + v] = q;
+        sq = __fma_rn((double)q, (double)q, sq);
+    }
+    block_sum_to(sq, partials);
+}
+
+// r <- r - alpha q, then scatter the new r (s = A^T r accumulates into vol).
+template <bool TWO_D, int F>
+__global__ void __launch_bounds__(kThreads, kMinBlocks)
+    backproject_residual_kernel(const ViewRec* __restrict__ views, const Grid g, const Tiling tl,
+                                float* __restrict__ r, const float* __restrict__ q,
+                                const double* __restrict__ scal, float* __restrict__ vol) {
+    __shared__ ViewRec sv;
+    const TileCoord c = tile_of_block(tl);
+    load_view(views, c.view, sv);
+    const float alpha = (float)scal[kAlpha];
+#pragma unroll 1
+    for (int row = 0; row < (TWO_D ? 1 : kRows); ++row) {
+        int u, v;
+        pixel_of<TWO_D>(c, sv, row, u, v);
+        if (u >= tl.n_u || v >= tl.n_v) continue;
+        const int64_t k = ((int64_t)c.view * tl.n_u + u) * tl.n_v + v;
+        const float y = __fmaf_rn(-alpha, __ldg(q + k), r[k]);
+        r[k] = y;
+        if (y == 0.0f) continue;
+        Ray ray;
+        if (setup_ray<F>(sv, g, u, v, ray))
+            walk<true>(ray, nullptr, vol, __fmul_rn(y, g.spacing));
+    }
+}
+
+// Per-block float64 sums of v^2 (grid-stride over n elements).
+__global__ void __launch_bounds__(kThreads) norm_partials_kernel(const float* __restrict__ v,
+                                                                  int64_t n,
+                                                                  double* __restrict__ partials) {
+    double s = 0.0;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const double x = (double)__ldg(v + i);
+        s = __fma_rn(x, x, s);
+    }
+    block_sum_to(s, partials);
+}
+
+// One block: total of the partials, then the CGLS scalar step `which`:
+//   0: delta = total, alpha = gamma / delta      (after q = A p)
+//   1: beta = total / gamma, gamma = total       (after s = A^T r)
+//   2: gamma = total, alpha = beta = 0           (start)
+// A zero denominator gives 0 (the run has converged).
+__global__ void __launch_bounds__(kThreads) cgls_scalars_kernel(const double* __restrict__ partials,
+                                                                 int32_t n, double* __restrict__ scal,
+                                                                 int32_t which) {
+    double s = 0.0;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) s += partials[i];
+    __shared__ double warp_sums[kThreads / 32];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(0xffffffffu, s, o);
+    if ((threadIdx.x & 31) == 0) warp_sums[threadIdx.x >> 5] = s;
+    __syncthreads();
+    if (threadIdx.x != 0) return;
+    double total = 0.0;
+    for (int w = 0; w < kThreads / 32; ++w) total += warp_sums[w];
+    if (which == 0) {
+        scal[kDelta] = total;
+        scal[kAlpha] = total > 0.0 ? scal[kGamma] / total : 0.0;
+    } else if (which == 1) {
+        const double gamma = scal[kGamma];
+        scal[kBeta] = gamma > 0.0 ? total / gamma : 0.0;
+        scal[kGamma] = total;
+    } else {
+        scal[kGamma] = total;
+        scal[kAlpha] = 0.0;
+        scal[kBeta] = 0.0;
+    }
+}
+
+// x += alpha p;  p = s + beta p;  s = 0 (ready for the next backprojection).
+__global__ void cgls_update_kernel(float* __restrict__ x, float* __restrict__ p,
+                                   float* __restrict__ s, const double* __restrict__ scal,
+                                   int64_t n) {
+    const float alpha = (float)scal[kAlpha], beta = (float)scal[kBeta];
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const float pv = p[i];
+        x[i] = __fmaf_rn(alpha, pv, x[i]);
+        p[i] = __fmaf_rn(beta, pv, s[i]);
+        s[i] = 0.0f;
+    }
+}
+
+// r = y - q.
+__global__ void sub_kernel(float* __restrict__ r, const float* __restrict__ y,
+                           const float* __restrict__ q, int64_t n) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x)
+        r[i] = __fsub_rn(__ldg(y + i), __ldg(q + i));
+}
+
 __global__ void invert_kernel(float* __restrict__ c, int64_t n) {
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
          i += (int64_t)gridDim.x * blockDim.x) {
@@ -504,6 +641,45 @@ cudaError_t launch_project_residual(const ViewRec* views, const Grid& g, const T
                                     const float* x, const float* y, float* r,
                                     cudaStream_t stream) {
     CT_LAUNCH_BY_AXIS(project_residual_kernel, CT_NO_EXTRA, views, g, t, x, y, r);
+}
+
+int64_t project_blocks(const Tiling& t) { return grid_for(t); }
+
+cudaError_t launch_project_norm(const ViewRec* views, const Grid& g, const Tiling& t,
+                                const float* vol, float* sino, double* partials,
+                                cudaStream_t stream) {
+    CT_LAUNCH_BY_AXIS(project_norm_kernel, CT_NO_EXTRA, views, g, t, vol, sino, partials);
+}
+
+cudaError_t launch_backproject_residual(const ViewRec* views, const Grid& g, const Tiling& t,
+                                        float* r, const float* q, const double* scal, float* vol,
+                                        cudaStream_t stream) {
+    CT_LAUNCH_BY_AXIS(backproject_residual_kernel, CT_NO_EXTRA, views, g, t, r, q, scal, vol);
+}
+
+int norm_blocks() { return 148 * 8; }
+
+cudaError_t launch_norm_partials(const float* v, int64_t n, double* partials,
+                                 cudaStream_t stream) {
+    norm_partials_kernel<<<norm_blocks(), kThreads, 0, stream>>>(v, n, partials);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_cgls_scalars(const double* partials, int64_t n, double* scal, int which,
+                                cudaStream_t stream) {
+    cgls_scalars_kernel<<<1, kThreads, 0, stream>>>(partials, (int32_t)n, scal, which);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_cgls_update(float* x, float* p, float* s, const double* scal, int64_t n,
+                               cudaStream_t stream) {
+    cgls_update_kernel<<<elementwise_blocks(n), 256, 0, stream>>>(x, p, s, scal, n);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_sub(float* r, const float* y, const float* q, int64_t n, cudaStream_t stream) {
+    sub_kernel<<<elementwise_blocks(n), 256, 0, stream>>>(r, y, q, n);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_invert(float* c, int64_t n, cudaStream_t stream) {

@@ -168,6 +168,32 @@ CT_API ct_status ct_sirt_iterate(const ct_geometry *geom, float *d_x, const floa
                           float relaxation, int32_t workspace_initialised,
                           struct CUstream_st *stream);
 
+/* Scratch bytes needed by ct_cgls_iterate. */
+CT_API size_t ct_cgls_workspace_bytes(const ct_geometry *geom);
+
+/*
+ * CGLS: n_iters steps of conjugate gradients on the normal equations A^T A x = A^T y, in the
+ * form that never forms A^T A (r = y - A x, s = A^T r, p = s, gamma = |s|^2; each step:
+ * q = A p, alpha = gamma / |q|^2, x += alpha p, r -= alpha q, s = A^T r, beta = |s|^2 / gamma,
+ * p = s + beta p).  The pages list a CGLS solver on this operator pair (diffct "Solvers" API
+ * entries cgls / cgls_into) and time one CGLS iteration in their performance table; they do not
+ * print the recurrences, which are the textbook ones.  Norms are accumulated in float64 on the
+ * device; alpha, beta and gamma stay on the device (no host synchronisation).  A zero
+ * denominator (an exact solution) gives alpha = 0 or beta = 0.
+ *
+ * d_x        device volume, updated in place; the starting point (zeros for a plain run).
+ * d_y        device sinogram (measurements), read only.
+ * d_workspace, workspace_bytes
+ *            at least ct_cgls_workspace_bytes(geom).  It carries the CGLS state (r, p, gamma)
+ *            between calls: pass workspace_initialised = 0 on the first call (the state is
+ *            set up from d_x), 1 to continue a run with the same handle, workspace and d_y, and
+ *            with d_x unchanged since the previous call.
+ * n_iters >= 0.
+ */
+CT_API ct_status ct_cgls_iterate(const ct_geometry *geom, float *d_x, const float *d_y,
+                                 void *d_workspace, size_t workspace_bytes, int32_t n_iters,
+                                 int32_t workspace_initialised, struct CUstream_st *stream);
+
 /*
  * Backprojection that allocates nothing: d_volume = A^T d_sino, the same operator, kernels and
  * weights as ct_backproject, for callers that cannot allocate device memory at the time they
