@@ -52,7 +52,7 @@ class Workload:
     beam: int
     views: np.ndarray            # (n_views, 6|12) float64, C-contiguous
     vol_shape: tuple             # (nz, ny, nx); 2D problems have nz == 1
-    voxel_spacing: float
+    voxel_spacing: float | tuple # scalar, or per axis in tensor order: (dy, dx) / (dz, dy, dx)
     n_u: int
     n_v: int                     # 1 for 2D problems
     du: float
@@ -356,6 +356,32 @@ def small_config(n: int, seed: int | None = None) -> Workload:
                                                    radius_range=(2.0, 6.0), half_thickness=12.0),
                                       (48, 56, 52)))
     raise ValueError(f"unknown workload {n}")
+
+
+def anisotropic_config(kind: str, seed: int = 7) -> Workload:
+    """Small workloads with a different voxel spacing per axis (tensor order), for parity tests:
+    'cone' (spacing (dz, dy, dx) = (1.1, 0.8, 0.6)), 'tilt' (parallel3d, (0.7, 1.3, 0.9)) and
+    'fan' (2D, (dy, dx) = (0.9, 0.7))."""
+    if kind == "cone":
+        views = circular_cone(19, 120.0, 240.0)
+        return Workload("cone-aniso", CONE, views, (29, 37, 41), (1.1, 0.8, 0.6), 63, 41, 1.0,
+                        1.3, seed, lambda: _crop(ellipsoids_3d(8, 41, np.random.default_rng(seed),
+                                                              axis_range=(3.0, 18.0)),
+                                                 (29, 37, 41)))
+    if kind == "tilt":
+        ang = np.arange(-60, 61, 10, dtype=np.float64)
+        views = dual_axis_tilt(ang, ang)
+        return Workload("tilt-aniso", PARALLEL3D, views, (23, 31, 27), (0.7, 1.3, 0.9), 49, 45,
+                        0.9, 1.1, seed,
+                        lambda: _crop(spheres_slab(30, 31, np.random.default_rng(seed),
+                                                   radius_range=(2.0, 5.0),
+                                                   half_thickness=10.0), (23, 31, 27)))
+    if kind == "fan":
+        views = circular_fan_2d(29, 200.0, 300.0)
+        return Workload("fan-aniso", FAN2D, views, (1, 53, 67), (0.9, 0.7), 97, 1, 0.8, 1.0,
+                        seed, lambda: ellipses_2d(6, 67, np.random.default_rng(seed),
+                                                  axis_range=(3.0, 20.0))[:53])
+    raise ValueError(kind)
 
 
 def _crop(vol: np.ndarray, shape) -> np.ndarray:

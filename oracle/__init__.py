@@ -36,7 +36,7 @@ class _Geom(ctypes.Structure):
     _fields_ = [("beam", ctypes.c_int32), ("n_views", ctypes.c_int32),
                 ("views", ctypes.POINTER(ctypes.c_double)),
                 ("nz", ctypes.c_int32), ("ny", ctypes.c_int32), ("nx", ctypes.c_int32),
-                ("s", ctypes.c_double), ("nu", ctypes.c_int32), ("nv", ctypes.c_int32),
+                ("s", ctypes.c_double * 3), ("nu", ctypes.c_int32), ("nv", ctypes.c_int32),
                 ("du", ctypes.c_double), ("dv", ctypes.c_double)]
 
 
@@ -58,7 +58,7 @@ def _load():
                                           i64p, dp, ctypes.c_int64]
         L.oracle_ray_segments.restype = ctypes.c_int64
         L.oracle_line_segments.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
-                                           ctypes.c_int32, ctypes.c_double, dp, dp,
+                                           ctypes.c_int32, dp, dp, dp,
                                            ctypes.c_double, ctypes.c_double, i64p, dp,
                                            ctypes.c_int64]
         L.oracle_line_segments.restype = ctypes.c_int64
@@ -75,6 +75,20 @@ def _dp(a: np.ndarray):
     return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
 
 
+def spacing_xyz(voxel_spacing, is_2d: bool):
+    """(sx, sy, sz) from a scalar or a tuple in tensor order: (dy, dx) for 2D, (dz, dy, dx) for
+    3D (diffct "Trajectories and Geometry", voxel spacing)."""
+    if np.ndim(voxel_spacing) == 0:
+        s = float(voxel_spacing)
+        return (s, s, s)
+    vs = [float(v) for v in voxel_spacing]
+    if is_2d:
+        assert len(vs) == 2
+        return (vs[1], vs[0], 1.0)
+    assert len(vs) == 3
+    return (vs[2], vs[1], vs[0])
+
+
 class Geometry:
     """Oracle-side view of an acquisition (same record layout as the C library's input)."""
 
@@ -86,9 +100,10 @@ class Geometry:
         self.vol_shape = (int(nz), int(ny), int(nx))
         self.is_2d = self.beam in (0, 1)
         self.n_u, self.n_v = int(n_u), (1 if self.is_2d else int(n_v))
-        self.spacing = float(voxel_spacing)
+        self.spacing_xyz = spacing_xyz(voxel_spacing, self.is_2d)
         self._g = _Geom(self.beam, self.views.shape[0], _dp(self.views), self.vol_shape[0],
-                        self.vol_shape[1], self.vol_shape[2], self.spacing, self.n_u, self.n_v,
+                        self.vol_shape[1], self.vol_shape[2],
+                        (ctypes.c_double * 3)(*self.spacing_xyz), self.n_u, self.n_v,
                         float(du), float(dv))
 
     @classmethod
@@ -214,15 +229,18 @@ class Geometry:
 
 
 def line_segments(e, d, amin, amax, vol_shape, spacing, dims=3):
-    """Segments (voxel indices, chords) of an explicit ray p(a) = e + a d, a in [amin, amax]."""
+    """Segments (voxel indices, chords) of an explicit ray p(a) = e + a d, a in [amin, amax];
+    `spacing` is a scalar or (dz, dy, dx)."""
     L = _load()
     nz, ny, nx = vol_shape
+    sp = np.ascontiguousarray(spacing_xyz(spacing, False) if dims == 3 or np.ndim(spacing) == 0
+                              else spacing_xyz(spacing, True), dtype=np.float64)
     e = np.ascontiguousarray(np.resize(np.asarray(e, dtype=np.float64), 3))
     d = np.ascontiguousarray(np.resize(np.asarray(d, dtype=np.float64), 3))
     cap = nx + ny + nz + 4
     idx = np.zeros(cap, dtype=np.int64)
     w = np.zeros(cap, dtype=np.float64)
-    cnt = L.oracle_line_segments(dims, nz, ny, nx, float(spacing), _dp(e), _dp(d), float(amin),
+    cnt = L.oracle_line_segments(dims, nz, ny, nx, _dp(sp), _dp(e), _dp(d), float(amin),
                                  float(amax), idx.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
                                  _dp(w), cap)
     return idx[:cnt].copy(), w[:cnt].copy()

@@ -17,9 +17,10 @@
  *
  * Conventions (diffct "Trajectories and Geometry", trajectory format and pixel formula):
  *   - Cartesian (x, y[, z]), origin at the volume centre, one length unit throughout.
- *   - Volume [z][y][x] (2D [y][x]); voxel i on an axis with n cells spans
+ *   - Volume [z][y][x] (2D [y][x]); voxel i on an axis with n cells of spacing s spans
  *     [-n s/2 + i s, -n s/2 + (i+1) s)  (half-open: a ray lying in a cell face belongs to the cell
- *     on the + side; the outer + face of the box belongs to no cell).
+ *     on the + side; the outer + face of the box belongs to no cell).  The spacing may differ per
+ *     axis ("Trajectories and Geometry": a scalar or a per-axis tuple in tensor order).
  *   - Pixel (u, v) at det_center + (u - (U-1)/2) du det_u + (v - (V-1)/2) dv det_v.
  *   - parallel / parallel3d: p(a) = pixel + a * ray_dir, a over all reals (infinite line).
  *   - fan / cone: p(a) = src + a * (pixel - src), a in [0, 1] (source-to-pixel segment; the
@@ -48,7 +49,7 @@ typedef struct {
     int32_t n_views;
     const double *views;   /* n_views x (6 | 12) */
     int32_t nz, ny, nx;    /* 2D: nz == 1 */
-    double s;              /* voxel spacing */
+    double s[3];           /* voxel spacing along x, y, z (2D: z unused) */
     int32_t nu, nv;        /* 2D: nv == 1 */
     double du, dv;
 } og_geom;
@@ -99,10 +100,10 @@ typedef void (*seg_fn)(void *ctx, int64_t voxel, double length);
  * `dims` = 2 or 3 (2D grids ignore the z component; their single slice is z in [-s/2, s/2)).
  * Returns the number of segments with positive length.
  */
-static int64_t siddon_ray(int dims, const int64_t n[3], double s, const double e[3],
+static int64_t siddon_ray(int dims, const int64_t n[3], const double s[3], const double e[3],
                           const double d[3], double amin, double amax, seg_fn fn, void *ctx) {
     double h[3];
-    for (int a = 0; a < 3; ++a) h[a] = 0.5 * (double)n[a] * s;
+    for (int a = 0; a < 3; ++a) h[a] = 0.5 * (double)n[a] * s[a];
     double lo = amin, hi = amax;
     for (int a = 0; a < dims; ++a) {
         if (d[a] != 0.0) {
@@ -130,7 +131,7 @@ static int64_t siddon_ray(int dims, const int64_t n[3], double s, const double e
         for (int64_t k = 1; k < n[a]; ++k) {
             /* visit planes in the order the ray meets them */
             int64_t kk = d[a] > 0 ? k : n[a] - k;
-            double al = (-h[a] + (double)kk * s - e[a]) / d[a];
+            double al = (-h[a] + (double)kk * s[a] - e[a]) / d[a];
             if (al > lo && al < hi) ax[a][cnt[a]++] = al;
         }
         used += cnt[a];
@@ -159,7 +160,7 @@ static int64_t siddon_ray(int dims, const int64_t n[3], double s, const double e
         double mid = 0.5 * (merged[k] + merged[k + 1]);
         int64_t idx[3] = {0, 0, 0};
         for (int a = 0; a < dims; ++a) {
-            double c = (e[a] + mid * d[a] + h[a]) / s;
+            double c = (e[a] + mid * d[a] + h[a]) / s[a];
             int64_t i = (int64_t)floor(c);
             if (i < 0) i = 0;
             if (i > n[a] - 1) i = n[a] - 1;
@@ -260,8 +261,9 @@ int64_t oracle_ray_segments(const og_geom *g, int32_t view, int32_t iu, int32_t 
     return L.cnt;
 }
 
-/* Same for an explicit ray (e, d, [amin, amax]) through an nx*ny*nz grid (dims = 2 or 3). */
-int64_t oracle_line_segments(int32_t dims, int32_t nz, int32_t ny, int32_t nx, double s,
+/* Same for an explicit ray (e, d, [amin, amax]) through an nx*ny*nz grid (dims = 2 or 3) of
+   spacing s[0..2] along x, y, z. */
+int64_t oracle_line_segments(int32_t dims, int32_t nz, int32_t ny, int32_t nx, const double *s,
                              const double *e, const double *d, double amin, double amax,
                              int64_t *idx, double *w, int64_t cap) {
     int64_t n[3] = {nx, ny, nz};
@@ -327,8 +329,8 @@ void oracle_brute_row(const og_geom *g, int32_t view, int32_t iu, int32_t iv, do
                 int64_t idx[3] = {x, y, z};
                 double lo[3], hi[3];
                 for (int a = 0; a < 3; ++a) {
-                    lo[a] = -0.5 * (double)n[a] * g->s + (double)idx[a] * g->s;
-                    hi[a] = lo[a] + g->s;
+                    lo[a] = -0.5 * (double)n[a] * g->s[a] + (double)idx[a] * g->s[a];
+                    hi[a] = lo[a] + g->s[a];
                 }
                 row[(z * n[1] + y) * n[0] + x] = cell_chord(dims, lo, hi, e, d, amin, amax);
             }
@@ -351,8 +353,8 @@ void oracle_backproject_voxels(const og_geom *g, const double *sino, int64_t nvo
         int64_t idx[3] = {lin % n[0], (lin / n[0]) % n[1], lin / (n[0] * n[1])};
         double lo[3], hi[3];
         for (int a = 0; a < 3; ++a) {
-            lo[a] = -0.5 * (double)n[a] * g->s + (double)idx[a] * g->s;
-            hi[a] = lo[a] + g->s;
+            lo[a] = -0.5 * (double)n[a] * g->s[a] + (double)idx[a] * g->s[a];
+            hi[a] = lo[a] + g->s[a];
         }
         double acc = 0.0;
         for (int view = 0; view < g->n_views; ++view) {
