@@ -303,6 +303,38 @@ def sirt_leg(ct, torch, n_iters: int = 10):
     return sirt, cgls
 
 
+def batch_leg(ct, torch, w, U, nb: int = 4, reps: int = 3):
+    """The metric workload with nb volumes at once (leading batch dimension): one walk per ray
+    serves all nb volumes.  Updates counted as nb x U per direction."""
+    g = ct.Geometry.from_workload(w)
+    vols = torch.rand((nb,) + tuple(w.volume_shape), device="cuda")
+    sinos = torch.empty((nb,) + tuple(w.sino_shape), device="cuda")
+    backs = torch.empty_like(vols)
+    need = ct.ct_batch_workspace_bytes(g.handle, nb)
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    fps, bps = [], []
+    for k in range(reps + 1):
+        flush.zero_()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record(stream)
+        g.project(vols, out=sinos, workspace=ws)
+        e[1].record(stream)
+        g.backproject(sinos, out=backs, workspace=ws)
+        e[2].record(stream)
+        torch.cuda.synchronize()
+        if k:
+            fps.append(e[0].elapsed_time(e[1]))
+            bps.append(e[1].elapsed_time(e[2]))
+    fp, bp = statistics.median(fps), statistics.median(bps)
+    del vols, sinos, backs, ws, flush
+    torch.cuda.empty_cache()
+    return {"batch": nb, "fp_ms": fp, "bp_ms": bp,
+            "fp_updates_per_s": nb * U / (fp * 1e-3), "bp_updates_per_s": nb * U / (bp * 1e-3),
+            "pair_updates_per_s": 2 * nb * U / ((fp + bp) * 1e-3)}
+
+
 def context_leg(ct, torch):
     """The pages' performance-table workload shape (512^3 volume, circular cone, 360 views,
     1024x768 detector at pitch 1.25; sid/sdd are not printed, 1000/1500 is this build's
@@ -498,6 +530,7 @@ def run_ours(args, rank, world):
         "gpu_launches": 4 * args.steps,
         "clocks": clocks,
     }
+    line["batch4"] = batch_leg(ct, torch, w, U)
     if not args.no_sirt:
         line["sirt"], line["cgls"] = sirt_leg(ct, torch)
     if args.context:

@@ -57,6 +57,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.ct_geometry_create.argtypes = [i32, i32, ctypes.POINTER(f64), i32, i32, i32, f64, i32, i32,
                                      f64, f64, ctypes.POINTER(vp)]
     L.ct_geometry_create.restype = i32
+    L.ct_geometry_create_ex.argtypes = [i32, i32, ctypes.POINTER(f64), i32, i32, i32,
+                                        ctypes.POINTER(f64), i32, i32, f64, f64,
+                                        ctypes.POINTER(vp)]
+    L.ct_geometry_create_ex.restype = i32
     L.ct_geometry_destroy.argtypes = [vp]
     L.ct_geometry_destroy.restype = i32
     L.ct_geometry_get_info.argtypes = [vp, ctypes.POINTER(GeometryInfo)]
@@ -69,6 +73,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.ct_sirt_workspace_bytes.restype = sz
     L.ct_sirt_iterate.argtypes = [vp, vp, vp, vp, sz, i32, f32, i32, vp]
     L.ct_sirt_iterate.restype = i32
+    L.ct_batch_workspace_bytes.argtypes = [vp, i32]
+    L.ct_batch_workspace_bytes.restype = sz
+    L.ct_project_batch.argtypes = [vp, i32, vp, vp, vp, sz, vp]
+    L.ct_project_batch.restype = i32
+    L.ct_backproject_batch.argtypes = [vp, i32, vp, vp, vp, sz, vp]
+    L.ct_backproject_batch.restype = i32
     L.ct_cgls_workspace_bytes.argtypes = [vp]
     L.ct_cgls_workspace_bytes.restype = sz
     L.ct_cgls_iterate.argtypes = [vp, vp, vp, vp, sz, i32, i32, vp]
@@ -88,17 +98,27 @@ def _check(status: int, call: str) -> None:
 
 # ---- the C entry points, same names, raw pointers ---------------------------------------------
 
-def ct_geometry_create(beam: int, views, vol_shape, voxel_spacing: float, n_u: int, n_v: int,
+def ct_geometry_create(beam: int, views, vol_shape, voxel_spacing, n_u: int, n_v: int,
                        du: float, dv: float) -> int:
-    """Create a handle; ``views`` is a host (n_views, 6|12) float64 array.  Returns the handle."""
+    """Create a handle; ``views`` is a host (n_views, 6|12) float64 array; ``voxel_spacing`` a
+    scalar (ct_geometry_create) or a tuple in tensor order, (dy, dx) for 2D or (dz, dy, dx) for
+    3D (ct_geometry_create_ex).  Returns the handle."""
     L = load_library()
     v = np.ascontiguousarray(np.asarray(views, dtype=np.float64))
     nz, ny, nx = vol_shape
     h = ctypes.c_void_p()
-    _check(L.ct_geometry_create(int(beam), int(v.shape[0]),
-                                v.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), int(nz),
-                                int(ny), int(nx), float(voxel_spacing), int(n_u), int(n_v),
-                                float(du), float(dv), ctypes.byref(h)), "ct_geometry_create")
+    vp = v.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+    if np.ndim(voxel_spacing) == 0:
+        _check(L.ct_geometry_create(int(beam), int(v.shape[0]), vp, int(nz), int(ny), int(nx),
+                                    float(voxel_spacing), int(n_u), int(n_v), float(du),
+                                    float(dv), ctypes.byref(h)), "ct_geometry_create")
+    else:
+        s = [float(x) for x in voxel_spacing]
+        s = [1.0] + s if len(s) == 2 else s
+        arr = (ctypes.c_double * 3)(*s)
+        _check(L.ct_geometry_create_ex(int(beam), int(v.shape[0]), vp, int(nz), int(ny), int(nx),
+                                       arr, int(n_u), int(n_v), float(du), float(dv),
+                                       ctypes.byref(h)), "ct_geometry_create_ex")
     return h.value
 
 
@@ -144,6 +164,24 @@ def ct_sirt_iterate(handle: int, d_x: int, d_y: int, d_workspace: int, workspace
            "ct_sirt_iterate")
 
 
+def ct_batch_workspace_bytes(handle: int, batch: int) -> int:
+    return int(load_library().ct_batch_workspace_bytes(handle, int(batch)))
+
+
+def ct_project_batch(handle: int, batch: int, d_volumes: int, d_sinos: int,
+                     d_workspace: int | None, workspace_bytes: int, stream: int | None) -> None:
+    _check(load_library().ct_project_batch(handle, int(batch), d_volumes, d_sinos, d_workspace,
+                                           workspace_bytes, stream), "ct_project_batch")
+
+
+def ct_backproject_batch(handle: int, batch: int, d_sinos: int, d_volumes: int,
+                         d_workspace: int | None, workspace_bytes: int,
+                         stream: int | None) -> None:
+    _check(load_library().ct_backproject_batch(handle, int(batch), d_sinos, d_volumes,
+                                               d_workspace, workspace_bytes, stream),
+           "ct_backproject_batch")
+
+
 def ct_cgls_workspace_bytes(handle: int) -> int:
     return int(load_library().ct_cgls_workspace_bytes(handle))
 
@@ -164,7 +202,7 @@ def ct_status_string(status: int) -> str:
 class Geometry:
     """Owns one ``ct_geometry`` handle; methods take and return CUDA float32 torch tensors."""
 
-    def __init__(self, beam: int, views, vol_shape, voxel_spacing: float, n_u: int, n_v: int,
+    def __init__(self, beam: int, views, vol_shape, voxel_spacing, n_u: int, n_v: int,
                  du: float, dv: float):
         self.handle = ct_geometry_create(beam, views, vol_shape, voxel_spacing, n_u, n_v, du, dv)
         self.info = ct_geometry_get_info(self.handle)
@@ -228,25 +266,59 @@ class Geometry:
             workspace = self.new_workspace(sirt)
         return workspace.data_ptr(), workspace.numel() * workspace.element_size()
 
+    def _batch_ws(self, batch, workspace):
+        need = ct_batch_workspace_bytes(self.handle, batch)
+        if need == 0:
+            return None, 0
+        if workspace is None:
+            import torch
+            workspace = torch.empty(need, dtype=torch.uint8, device="cuda")
+        return workspace.data_ptr(), workspace.numel() * workspace.element_size()
+
     def project(self, volume, out=None, workspace=None, stream=None):
+        """A volume -> sinogram; leading batch/channel dimensions are kept."""
         import torch
         assert volume.is_cuda and volume.dtype == torch.float32 and volume.is_contiguous()
-        assert tuple(volume.shape) == tuple(self.volume_shape)
+        nd = len(self.volume_shape)
+        assert tuple(volume.shape[volume.dim() - nd:]) == tuple(self.volume_shape)
+        lead = tuple(volume.shape[:volume.dim() - nd])
         if out is None:
-            out = torch.empty(self.sino_shape, dtype=torch.float32, device=volume.device)
-        ws, wsb = self._ws(workspace)
-        ct_project(self.handle, volume.data_ptr(), out.data_ptr(), ws, wsb, self._stream(stream))
+            out = torch.empty(lead + tuple(self.sino_shape), dtype=torch.float32,
+                              device=volume.device)
+        batch = int(np.prod(lead)) if lead else 0
+        if batch == 0 and lead:
+            return out
+        if not lead:
+            ws, wsb = self._ws(workspace)
+            ct_project(self.handle, volume.data_ptr(), out.data_ptr(), ws, wsb,
+                       self._stream(stream))
+        else:
+            ws, wsb = self._batch_ws(batch, workspace)
+            ct_project_batch(self.handle, batch, volume.data_ptr(), out.data_ptr(), ws, wsb,
+                             self._stream(stream))
         return out
 
     def backproject(self, sino, out=None, workspace=None, stream=None):
+        """A^T sinogram -> volume; leading batch/channel dimensions are kept."""
         import torch
         assert sino.is_cuda and sino.dtype == torch.float32 and sino.is_contiguous()
-        assert tuple(sino.shape) == tuple(self.sino_shape)
+        nd = len(self.sino_shape)
+        assert tuple(sino.shape[sino.dim() - nd:]) == tuple(self.sino_shape)
+        lead = tuple(sino.shape[:sino.dim() - nd])
         if out is None:
-            out = torch.empty(self.volume_shape, dtype=torch.float32, device=sino.device)
-        ws, wsb = self._ws(workspace)
-        ct_backproject(self.handle, sino.data_ptr(), out.data_ptr(), ws, wsb,
-                       self._stream(stream))
+            out = torch.empty(lead + tuple(self.volume_shape), dtype=torch.float32,
+                              device=sino.device)
+        batch = int(np.prod(lead)) if lead else 0
+        if batch == 0 and lead:
+            return out
+        if not lead:
+            ws, wsb = self._ws(workspace)
+            ct_backproject(self.handle, sino.data_ptr(), out.data_ptr(), ws, wsb,
+                           self._stream(stream))
+        else:
+            ws, wsb = self._batch_ws(batch, workspace)
+            ct_backproject_batch(self.handle, batch, sino.data_ptr(), out.data_ptr(), ws, wsb,
+                                 self._stream(stream))
         return out
 
     def cgls(self, x, y, n_iters: int, workspace, initialised: bool, stream=None):

@@ -219,6 +219,13 @@ const char* ct_status_string(ct_status s) {
 ct_status ct_geometry_create(ct_beam beam, int32_t n_views, const double* views, int32_t nz,
                              int32_t ny, int32_t nx, double voxel_spacing, int32_t n_u,
                              int32_t n_v, double du, double dv, ct_geometry** out) {
+    const double s3[3] = {voxel_spacing, voxel_spacing, voxel_spacing};
+    return ct_geometry_create_ex(beam, n_views, views, nz, ny, nx, s3, n_u, n_v, du, dv, out);
+}
+
+ct_status ct_geometry_create_ex(ct_beam beam, int32_t n_views, const double* views, int32_t nz,
+                                int32_t ny, int32_t nx, const double* spacing_zyx, int32_t n_u,
+                                int32_t n_v, double du, double dv, ct_geometry** out) {
     if (out == nullptr) return CT_ERR_INVALID_ARGUMENT;
     *out = nullptr;
     const int b = (int)beam;
@@ -230,9 +237,15 @@ ct_status ct_geometry_create(ct_beam beam, int32_t n_views, const double* views,
         if (nz != 1 || n_v != 1) return CT_ERR_INVALID_ARGUMENT;
         dv = 1.0;
     }
-    if (!(std::isfinite(voxel_spacing) && voxel_spacing > 0.0) ||
-        !(std::isfinite(du) && du > 0.0) || !(std::isfinite(dv) && dv > 0.0))
+    if (spacing_zyx == nullptr) return CT_ERR_INVALID_ARGUMENT;
+    // spacing along x, y, z; a 2D grid has no z extent, its z pitch is unused (set to 1)
+    const double sp[3] = {spacing_zyx[2], spacing_zyx[1], is_2d(b) ? 1.0 : spacing_zyx[0]};
+    for (int a = 0; a < 3; ++a)
+        if (!(std::isfinite(sp[a]) && sp[a] > 0.0)) return CT_ERR_INVALID_ARGUMENT;
+    if (!(std::isfinite(du) && du > 0.0) || !(std::isfinite(dv) && dv > 0.0))
         return CT_ERR_INVALID_ARGUMENT;
+    const double sp_min = std::min(sp[0], std::min(sp[1], is_2d(b) ? sp[1] : sp[2]));
+    const bool iso = sp[0] == sp[1] && (is_2d(b) || sp[1] == sp[2]);
     const int64_t nvox = (int64_t)nz * ny * nx;
     if (nvox > (int64_t)INT32_MAX) return CT_ERR_INVALID_ARGUMENT;  // 32-bit voxel indices
     const int64_t tiles_u = is_2d(b) ? (n_u + 255) / 256 : (n_u + 31) / 32;
@@ -240,12 +253,12 @@ ct_status ct_geometry_create(ct_beam beam, int32_t n_views, const double* views,
     if (tiles_u * tiles_v * n_views > (int64_t)INT32_MAX) return CT_ERR_INVALID_ARGUMENT;
     const int w = is_2d(b) ? 6 : 12;
     for (int i = 0; i < n_views; ++i)
-        if (!admit_view(b, views + (int64_t)i * w, voxel_spacing)) return CT_ERR_INVALID_GEOMETRY;
+        if (!admit_view(b, views + (int64_t)i * w, sp_min)) return CT_ERR_INVALID_GEOMETRY;
 
     ct_geometry* g = new (std::nothrow) ct_geometry();
     if (g == nullptr) return CT_ERR_OUT_OF_MEMORY;
     g->host_views.assign(views, views + (int64_t)n_views * w);
-    g->spacing = voxel_spacing;
+    g->spacing = sp_min;
     g->du = du;
     g->dv = dv;
     ct_geometry_info& I = g->info;
@@ -266,7 +279,8 @@ ct_status ct_geometry_create(ct_beam beam, int32_t n_views, const double* views,
     G.n[0] = nx; G.n[1] = ny; G.n[2] = nz;
     G.nd[0] = nx; G.nd[1] = ny; G.nd[2] = nz;
     strides_for((Layout)I.volume_layout, nx, ny, nz, G.stride);
-    G.spacing = (float)voxel_spacing;
+    for (int a = 0; a < 3; ++a) G.sp[a] = (float)sp[a];
+    G.iso = iso ? 1 : 0;
     G.parallel = is_parallel(b) ? 1 : 0;
     G.fast = I.volume_layout == ct::LAYOUT_YXZ ? 2 : (I.volume_layout == ct::LAYOUT_ZXY ? 1 : 0);
     ct::Tiling& T = g->tiling;
@@ -279,9 +293,8 @@ ct_status ct_geometry_create(ct_beam beam, int32_t n_views, const double* views,
     // Per-view records in voxel units, origin at the lower box corner.
     const int fast = G.fast;
     std::vector<ct::ViewRec> recs((size_t)n_views);
-    const double half[3] = {0.5 * nx * voxel_spacing, 0.5 * ny * voxel_spacing,
-                            0.5 * nz * voxel_spacing};
-    const double is = 1.0 / voxel_spacing;
+    const double half[3] = {0.5 * nx * sp[0], 0.5 * ny * sp[1], 0.5 * nz * sp[2]};
+    const double is[3] = {1.0 / sp[0], 1.0 / sp[1], 1.0 / sp[2]};
     for (int i = 0; i < n_views; ++i) {
         double first[3], ctr[3], u[3], v[3];
         unpack(b, views + (int64_t)i * w, first, ctr, u, v);
@@ -289,17 +302,20 @@ ct_status ct_geometry_create(ct_beam beam, int32_t n_views, const double* views,
         std::memset(&R, 0, sizeof(R));
         const double cu = 0.5 * (n_u - 1), cv = is_2d(b) ? 0.0 : 0.5 * (n_v - 1);
         const double dvv = is_2d(b) ? 0.0 : dv;
+        // coordinates in voxel units per axis (p_a + half_a) / spacing_a
         for (int a = 0; a < 3; ++a) {
-            R.pu[a] = du * is * u[a];
-            R.pv[a] = dvv * is * v[a];
-            R.pb[a] = (ctr[a] + half[a]) * is - cu * R.pu[a] - cv * R.pv[a];
+            R.pu[a] = du * is[a] * u[a];
+            R.pv[a] = dvv * is[a] * v[a];
+            R.pb[a] = (ctr[a] + half[a]) * is[a] - cu * R.pu[a] - cv * R.pv[a];
         }
         if (is_parallel(b)) {
+            // unit direction in physical space, expressed in voxel units per axis (for an
+            // isotropic grid this is the physical unit vector itself)
             const double nr = norm3(first);
-            for (int a = 0; a < 3; ++a) R.q[a] = first[a] / nr;
+            for (int a = 0; a < 3; ++a) R.q[a] = iso ? first[a] / nr : first[a] / nr * is[a];
         } else {
             for (int a = 0; a < 3; ++a) {
-                R.q[a] = (first[a] + half[a]) * is;
+                R.q[a] = (first[a] + half[a]) * is[a];
                 R.pb[a] -= R.q[a];
             }
         }
@@ -405,6 +421,79 @@ ct_status ct_sirt_iterate(const ct_geometry* g, float* d_x, const float* d_y, vo
         if (e == cudaSuccess) e = ct::launch_sirt_update(X, B, C, relaxation, nvox, stream);
     }
     if (e == cudaSuccess && !native) e = from_internal(g, X, d_x, stream);
+    return from_cuda(e);
+}
+
+// ---- batches of volumes ---------------------------------------------------------------------
+
+// Volumes per batched launch: 4, 2 or 1 (the kernels are instantiated for these).
+static int chunk_of(int remaining) { return remaining >= 4 ? 4 : (remaining >= 2 ? 2 : 1); }
+
+size_t ct_batch_workspace_bytes(const ct_geometry* g, int32_t batch) {
+    if (g == nullptr || batch <= 0) return 0;
+    if (g->info.volume_layout == ct::LAYOUT_ZYX) return 0;
+    return (size_t)std::min(batch, 4) * align_up(volume_bytes(g));
+}
+
+ct_status ct_project_batch(const ct_geometry* g, int32_t batch, const float* d_volumes,
+                           float* d_sinos, void* d_workspace, size_t workspace_bytes,
+                           cudaStream_t stream) {
+    if (g == nullptr || batch <= 0) return CT_ERR_INVALID_ARGUMENT;
+    ct_status st = check_call(g, d_volumes, (size_t)batch * volume_bytes(g), d_sinos,
+                              (size_t)batch * sino_bytes(g), d_workspace, workspace_bytes,
+                              ct_batch_workspace_bytes(g, batch));
+    if (st != CT_OK) return st;
+    const int64_t nvox = g->info.n_voxels, nray = g->info.n_rays;
+    const bool native = g->info.volume_layout == ct::LAYOUT_ZYX;
+    const int64_t wstride = (int64_t)(align_up(volume_bytes(g)) / sizeof(float));
+    float* ws = static_cast<float*>(d_workspace);
+    cudaError_t e = cudaSuccess;
+    for (int b0 = 0; b0 < batch && e == cudaSuccess;) {
+        const int nb = chunk_of(batch - b0);
+        const float* vol = d_volumes + (int64_t)b0 * nvox;
+        int64_t vstride = nvox;
+        if (!native) {
+            for (int j = 0; j < nb && e == cudaSuccess; ++j)
+                e = to_internal(g, d_volumes + (int64_t)(b0 + j) * nvox, ws + j * wstride, stream);
+            vol = ws;
+            vstride = wstride;
+        }
+        if (e == cudaSuccess)
+            e = ct::launch_project_batch(g->d_views, g->grid, g->tiling, nb, vol, vstride,
+                                         d_sinos + (int64_t)b0 * nray, nray, stream);
+        b0 += nb;
+    }
+    return from_cuda(e);
+}
+
+ct_status ct_backproject_batch(const ct_geometry* g, int32_t batch, const float* d_sinos,
+                               float* d_volumes, void* d_workspace, size_t workspace_bytes,
+                               cudaStream_t stream) {
+    if (g == nullptr || batch <= 0) return CT_ERR_INVALID_ARGUMENT;
+    ct_status st = check_call(g, d_sinos, (size_t)batch * sino_bytes(g), d_volumes,
+                              (size_t)batch * volume_bytes(g), d_workspace, workspace_bytes,
+                              ct_batch_workspace_bytes(g, batch));
+    if (st != CT_OK) return st;
+    const int64_t nvox = g->info.n_voxels, nray = g->info.n_rays;
+    const bool native = g->info.volume_layout == ct::LAYOUT_ZYX;
+    const int64_t wstride = (int64_t)(align_up(volume_bytes(g)) / sizeof(float));
+    float* ws = static_cast<float*>(d_workspace);
+    cudaError_t e = cudaSuccess;
+    for (int b0 = 0; b0 < batch && e == cudaSuccess;) {
+        const int nb = chunk_of(batch - b0);
+        float* acc = native ? d_volumes + (int64_t)b0 * nvox : ws;
+        const int64_t vstride = native ? nvox : wstride;
+        e = cudaMemsetAsync(acc, 0, (size_t)((nb - 1) * vstride + nvox) * sizeof(float), stream);
+        if (e == cudaSuccess)
+            e = ct::launch_backproject_batch(g->d_views, g->grid, g->tiling, nb,
+                                             d_sinos + (int64_t)b0 * nray, nray, acc, vstride,
+                                             stream);
+        if (!native)
+            for (int j = 0; j < nb && e == cudaSuccess; ++j)
+                e = from_internal(g, ws + j * wstride, d_volumes + (int64_t)(b0 + j) * nvox,
+                                  stream);
+        b0 += nb;
+    }
     return from_cuda(e);
 }
 

@@ -37,7 +37,8 @@ struct Grid {
     int32_t n[3];        // cells along x, y, z
     int32_t stride[3];   // element stride of x, y, z in the internal layout
     double nd[3];        // n as doubles (box upper corner)
-    float spacing;       // physical voxel pitch
+    float sp[3];         // physical voxel pitch along x, y, z
+    int32_t iso;         // 1 when the three pitches are equal
     int32_t parallel;    // 1: infinite lines, 0: source-to-pixel segments
     int32_t fast;        // axis that is fastest in memory (0 x, 1 y, 2 z): the walk's inner axis
 };
@@ -57,6 +58,14 @@ cudaError_t launch_backproject(const ViewRec* views, const Grid& g, const Tiling
                                const float* sino, float* vol, cudaStream_t stream);
 cudaError_t launch_backproject_ones(const ViewRec* views, const Grid& g, const Tiling& t,
                                     float* vol, cudaStream_t stream);
+// Batched forms: nb (1, 2 or 4) volumes at vol + b * vstride (internal order) and sinograms at
+// sino + b * sstride, one walk per ray for all of them.
+cudaError_t launch_project_batch(const ViewRec* views, const Grid& g, const Tiling& t, int nb,
+                                 const float* vol, int64_t vstride, float* sino, int64_t sstride,
+                                 cudaStream_t stream);
+cudaError_t launch_backproject_batch(const ViewRec* views, const Grid& g, const Tiling& t, int nb,
+                                     const float* sino, int64_t sstride, float* vol,
+                                     int64_t vstride, cudaStream_t stream);
 cudaError_t launch_project_residual(const ViewRec* views, const Grid& g, const Tiling& t,
                                     const float* x, const float* y, float* r,
                                     cudaStream_t stream);

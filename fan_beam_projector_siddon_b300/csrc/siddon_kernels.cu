@@ -48,6 +48,7 @@ struct Ray {
     int step[3];   // signed element stride per crossing
     int idx;       // entry voxel, linear index in the internal layout
     float tend;    // chord length inside the box (voxel units)
+    float scale;   // physical length per unit of voxel-space length along this ray
 };
 
 // Ray set-up for pixel (u, v).  Returns false when the ray misses the volume.  F is the inner
@@ -99,6 +100,15 @@ __device__ __forceinline__ bool setup_ray(const ViewRec& vr, const Grid& g, int 
     const float dl = sqrtf(__fmaf_rn(df[2], df[2], __fmaf_rn(df[1], df[1], df[0] * df[0])));
     const float inv_dl = 1.0f / dl;
     r.tend = __fmul_rn((float)(amax - amin), dl);
+    if (g.iso) {
+        r.scale = g.sp[0];
+    } else {
+        // the walk measures length in voxel units per axis; a segment of voxel-space length t
+        // has physical length t |d_phys| / |d_vox|, with d_phys_a = d_vox_a * spacing_a
+        const float px = __fmul_rn(df[0], g.sp[0]), py = __fmul_rn(df[1], g.sp[1]),
+                    pz = __fmul_rn(df[2], g.sp[2]);
+        r.scale = __fmul_rn(sqrtf(__fmaf_rn(pz, pz, __fmaf_rn(py, py, px * px))), inv_dl);
+    }
     int idx = 0;
 #pragma unroll
     for (int a = 0; a < 3; ++a) {
@@ -163,9 +173,10 @@ __device__ __forceinline__ bool setup_ray(const ViewRec& vr, const Grid& g, int 
 // (the voxel after the outer crossing, and the one after a pending inner crossing) one step
 // ahead.  The tail phase takes the remaining events with per-axis exhaustion checks.  Both
 // phases visit the same events in the same order with the same arithmetic.
-template <bool SCATTER>
-__device__ __forceinline__ float walk(const Ray& r, const float* __restrict__ vin,
-                                      float* __restrict__ vout, float val) {
+template <bool SCATTER, int NB>
+__device__ __forceinline__ void walk(const Ray& r, const float* __restrict__ vin,
+                                     float* __restrict__ vout, int64_t vstride,
+                                     const float (&val)[NB], float (&acc)[NB]) {
     const float INF = f_inf();
     const float na = (float)r.n[0], nb = (float)r.n[1], nf = (float)r.n[2];
     float ta = r.n[0] > 0 ? r.t0[0] : INF;
@@ -173,7 +184,22 @@ __device__ __forceinline__ float walk(const Ray& r, const float* __restrict__ vi
     float tf = r.n[2] > 0 ? r.t0[2] : INF;
     float ka = 0.0f, kb = 0.0f, kf = 0.0f;
     int idx = r.idx;
-    float t = 0.0f, acc = 0.0f;
+    float t = 0.0f;
+#pragma unroll
+    for (int b = 0; b < NB; ++b) acc[b] = 0.0f;
+    // segment [.., .. + seg) in voxel idx: gather from / scatter into every volume of the batch
+    auto scatter = [&](int i, float seg) {
+#pragma unroll
+        for (int b = 0; b < NB; ++b) atomicAdd(vout + b * vstride + i, __fmul_rn(val[b], seg));
+    };
+    auto load = [&](int i, float (&v)[NB]) {
+#pragma unroll
+        for (int b = 0; b < NB; ++b) v[b] = __ldg(vin + b * vstride + i);
+    };
+    auto gather = [&](const float (&v)[NB], float seg) {
+#pragma unroll
+        for (int b = 0; b < NB; ++b) acc[b] = __fmaf_rn(v[b], seg, acc[b]);
+    };
     // Main phase: outer crossings strictly before the earlier of the two outer axes' last
     // crossings, so neither outer axis can run out here and its next crossing needs no check.
     // (The last crossings use the same fmaf as the walk, so the comparison is exact.)
@@ -182,18 +208,18 @@ __device__ __forceinline__ float walk(const Ray& r, const float* __restrict__ vi
     const float lim = fminf(la, lb);
     float tstop = fminf(ta, tb);
     bool p = tf < tstop;
-    float v0 = 0.0f, v1 = 0.0f;  // gather: values of the current voxel and of the next one inward
+    float v0[NB], v1[NB];  // gather: values of the current voxel and of the next one inward
     if (!SCATTER) {
-        v0 = __ldg(vin + idx);
-        if (p) v1 = __ldg(vin + idx + r.step[2]);
+        load(idx, v0);
+        if (p) load(idx + r.step[2], v1);
     }
 #pragma unroll 1
     while (tstop < lim) {
         const float seg0 = __fsub_rn(p ? tf : tstop, t);
         if (SCATTER)
-            atomicAdd(vout + idx, __fmul_rn(val, seg0));
+            scatter(idx, seg0);
         else
-            acc = __fmaf_rn(v0, seg0, acc);
+            gather(v0, seg0);
         if (p) {
             idx += r.step[2];
             t = tf;
@@ -203,12 +229,12 @@ __device__ __forceinline__ float walk(const Ray& r, const float* __restrict__ vi
             while (tf < tstop) {  // a second inner crossing before this outer one (rare)
                 const float seg = __fsub_rn(tf, t);
                 if (SCATTER) {
-                    atomicAdd(vout + idx, __fmul_rn(val, seg));
+                    scatter(idx, seg);
                     idx += r.step[2];
                 } else {
-                    acc = __fmaf_rn(v1, seg, acc);
+                    gather(v1, seg);
                     idx += r.step[2];
-                    v1 = __ldg(vin + idx);
+                    load(idx, v1);
                 }
                 t = tf;
                 kf += 1.0f;
@@ -216,9 +242,9 @@ __device__ __forceinline__ float walk(const Ray& r, const float* __restrict__ vi
             }
             const float seg1 = __fsub_rn(tstop, t);
             if (SCATTER)
-                atomicAdd(vout + idx, __fmul_rn(val, seg1));
+                scatter(idx, seg1);
             else
-                acc = __fmaf_rn(v1, seg1, acc);
+                gather(v1, seg1);
         }
         t = tstop;
         if (ta <= tb) {
@@ -233,12 +259,11 @@ __device__ __forceinline__ float walk(const Ray& r, const float* __restrict__ vi
         tstop = fminf(ta, tb);
         p = tf < tstop;
         if (!SCATTER) {
-            v0 = __ldg(vin + idx);
-            if (p) v1 = __ldg(vin + idx + r.step[2]);
+            load(idx, v0);
+            if (p) load(idx + r.step[2], v1);
         }
     }
-    // Tail: the remaining events with the per-axis checks.
-    float v = v0;
+    // Tail: the remaining events with the per-axis checks.  v0 holds the current voxel's values.
 #pragma unroll 1
     for (int outer = (int)(na - ka) + (int)(nb - kb); outer > 0; --outer) {
         tstop = fminf(ta, tb);
@@ -246,20 +271,22 @@ __device__ __forceinline__ float walk(const Ray& r, const float* __restrict__ vi
         while (tf < tstop) {
             const float seg = __fsub_rn(tf, t);
             if (SCATTER) {
-                atomicAdd(vout + idx, __fmul_rn(val, seg));
+                scatter(idx, seg);
                 idx += r.step[2];
             } else {
                 idx += r.step[2];
-                const float vn = __ldg(vin + idx);
-                acc = __fmaf_rn(v, seg, acc);
-                v = vn;
+                float vn[NB];
+                load(idx, vn);
+                gather(v0, seg);
+#pragma unroll
+                for (int b = 0; b < NB; ++b) v0[b] = vn[b];
             }
             t = tf;
             kf += 1.0f;
             tf = kf < nf ? __fmaf_rn(kf, r.dt[2], r.t0[2]) : INF;
         }
         const float seg = __fsub_rn(tstop, t);
-        if (SCATTER) atomicAdd(vout + idx, __fmul_rn(val, seg));
+        if (SCATTER) scatter(idx, seg);
         t = tstop;
         if (ta <= tb) {
             idx += r.step[0];
@@ -271,22 +298,26 @@ __device__ __forceinline__ float walk(const Ray& r, const float* __restrict__ vi
             tb = kb < nb ? __fmaf_rn(kb, r.dt[1], r.t0[1]) : INF;
         }
         if (!SCATTER) {
-            const float vn = __ldg(vin + idx);
-            acc = __fmaf_rn(v, seg, acc);
-            v = vn;
+            float vn[NB];
+            load(idx, vn);
+            gather(v0, seg);
+#pragma unroll
+            for (int b = 0; b < NB; ++b) v0[b] = vn[b];
         }
     }
 #pragma unroll 1
     while (tf < r.tend) {
         const float seg = __fsub_rn(tf, t);
         if (SCATTER) {
-            atomicAdd(vout + idx, __fmul_rn(val, seg));
+            scatter(idx, seg);
             idx += r.step[2];
         } else {
             idx += r.step[2];
-            const float vn = __ldg(vin + idx);
-            acc = __fmaf_rn(v, seg, acc);
-            v = vn;
+            float vn[NB];
+            load(idx, vn);
+            gather(v0, seg);
+#pragma unroll
+            for (int b = 0; b < NB; ++b) v0[b] = vn[b];
         }
         t = tf;
         kf += 1.0f;
@@ -294,10 +325,22 @@ __device__ __forceinline__ float walk(const Ray& r, const float* __restrict__ vi
     }
     const float seg = __fsub_rn(r.tend, t);
     if (SCATTER)
-        atomicAdd(vout + idx, __fmul_rn(val, seg));
+        scatter(idx, seg);
     else
-        acc = __fmaf_rn(v, seg, acc);
-    return acc;
+        gather(v0, seg);
+}
+
+// Single-volume forms.
+__device__ __forceinline__ float walk_gather(const Ray& r, const float* __restrict__ vin) {
+    const float none[1] = {0.0f};
+    float acc[1];
+    walk<false, 1>(r, vin, nullptr, 0, none, acc);
+    return acc[0];
+}
+__device__ __forceinline__ void walk_scatter(const Ray& r, float* __restrict__ vout, float val) {
+    const float v[1] = {val};
+    float acc[1];
+    walk<true, 1>(r, nullptr, vout, 0, v, acc);
 }
 
 // Block -> (view, pixel tile).  Tiles are ordered detector-v band first, then view, then u tile,
@@ -342,11 +385,19 @@ __device__ __forceinline__ void pixel_of(const TileCoord& c, const ViewRec& sv, 
     }
 }
 
-template <bool TWO_D, int F>
-__global__ void __launch_bounds__(kThreads, kMinBlocks) project_kernel(const ViewRec* __restrict__ views,
-                                                           const Grid g, const Tiling tl,
-                                                           const float* __restrict__ vol,
-                                                           float* __restrict__ sino) {
+// Resident CTAs per SM for the batched walks (more registers per thread for NB values).
+template <int NB>
+struct BatchBlocks {
+    static constexpr int value = NB == 1 ? kMinBlocks : (NB == 2 ? 5 : 4);
+};
+
+// sino[b] = A vol[b] for the NB volumes vol + b * vstride (internal order) and sinograms
+// sino + b * sstride; one walk per ray serves all NB volumes.
+template <bool TWO_D, int F, int NB>
+__global__ void __launch_bounds__(kThreads, BatchBlocks<NB>::value)
+    project_kernel(const ViewRec* __restrict__ views, const Grid g, const Tiling tl,
+                   const float* __restrict__ vol, int64_t vstride, float* __restrict__ sino,
+                   int64_t sstride) {
     __shared__ ViewRec sv;
     const TileCoord c = tile_of_block(tl);
     load_view(views, c.view, sv);
@@ -355,19 +406,32 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) project_kernel(const Vie
         int u, v;
         pixel_of<TWO_D>(c, sv, row, u, v);
         if (u >= tl.n_u || v >= tl.n_v) continue;
+        const int64_t k = ((int64_t)c.view * tl.n_u + u) * tl.n_v + v;
         Ray ray;
-        float acc = 0.0f;
-        if (setup_ray<F>(sv, g, u, v, ray)) acc = walk<false>(ray, vol, nullptr, 0.0f);
-        sino[((int64_t)c.view * tl.n_u + u) * tl.n_v + v] = __fmul_rn(acc, g.spacing);
+        if (setup_ray<F>(sv, g, u, v, ray)) {
+            if (NB == 1) {
+                sino[k] = __fmul_rn(walk_gather(ray, vol), ray.scale);
+            } else {
+                const float none[NB] = {};
+                float acc[NB];
+                walk<false, NB>(ray, vol, nullptr, vstride, none, acc);
+#pragma unroll
+                for (int b = 0; b < NB; ++b) sino[b * sstride + k] = __fmul_rn(acc[b], ray.scale);
+            }
+        } else {
+#pragma unroll
+            for (int b = 0; b < NB; ++b) sino[b * sstride + k] = 0.0f;
+        }
     }
 }
 
-// MODE 0: scatter sino * spacing; MODE 1: scatter spacing (A^T 1).
-template <bool TWO_D, int F, int MODE>
-__global__ void __launch_bounds__(kThreads, kMinBlocks) backproject_kernel(const ViewRec* __restrict__ views,
-                                                               const Grid g, const Tiling tl,
-                                                               const float* __restrict__ sino,
-                                                               float* __restrict__ vol) {
+// MODE 0: scatter sino * (physical length per voxel-space length); MODE 1: the same for a sinogram
+// of ones (A^T 1).  NB volumes/sinograms at strides vstride/sstride, one walk per ray.
+template <bool TWO_D, int F, int MODE, int NB>
+__global__ void __launch_bounds__(kThreads, BatchBlocks<NB>::value)
+    backproject_kernel(const ViewRec* __restrict__ views, const Grid g, const Tiling tl,
+                       const float* __restrict__ sino, int64_t sstride, float* __restrict__ vol,
+                       int64_t vstride) {
     __shared__ ViewRec sv;
     const TileCoord c = tile_of_block(tl);
     load_view(views, c.view, sv);
@@ -376,16 +440,29 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) backproject_kernel(const
         int u, v;
         pixel_of<TWO_D>(c, sv, row, u, v);
         if (u >= tl.n_u || v >= tl.n_v) continue;
-        float y = 1.0f;
-        if (MODE == 0) y = __ldg(sino + ((int64_t)c.view * tl.n_u + u) * tl.n_v + v);
-        if (y == 0.0f) continue;
+        const int64_t k = ((int64_t)c.view * tl.n_u + u) * tl.n_v + v;
+        float y[NB];
+        bool any = false;
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            y[b] = MODE == 0 ? __ldg(sino + b * sstride + k) : 1.0f;
+            any |= y[b] != 0.0f;
+        }
+        if (!any) continue;
         Ray ray;
-        if (setup_ray<F>(sv, g, u, v, ray))
-            walk<true>(ray, nullptr, vol, __fmul_rn(y, g.spacing));
+        if (!setup_ray<F>(sv, g, u, v, ray)) continue;
+        if (NB == 1) {
+            walk_scatter(ray, vol, __fmul_rn(y[0], ray.scale));
+        } else {
+            float val[NB], unused[NB];
+#pragma unroll
+            for (int b = 0; b < NB; ++b) val[b] = __fmul_rn(y[b], ray.scale);
+            walk<true, NB>(ray, nullptr, vol, vstride, val, unused);
+        }
     }
 }
 
-// r = R (y - A x) with R = 1 / (A 1) = 1 / (spacing * chord); 0 for rays that miss.
+// r = R (y - A x) with R = 1 / (A 1) = 1 / (physical chord); 0 for rays that miss.
 template <bool TWO_D, int F>
 __global__ void __launch_bounds__(kThreads, kMinBlocks)
     project_residual_kernel(const ViewRec* __restrict__ views, const Grid g, const Tiling tl,
@@ -403,8 +480,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
         Ray ray;
         float out = 0.0f;
         if (setup_ray<F>(sv, g, u, v, ray) && ray.tend > 0.0f) {
-            const float ax = __fmul_rn(walk<false>(ray, x, nullptr, 0.0f), g.spacing);
-            out = __fdiv_rn(__fsub_rn(__ldg(y + k), ax), __fmul_rn(ray.tend, g.spacing));
+            const float ax = __fmul_rn(walk_gather(ray, x), ray.scale);
+            out = __fdiv_rn(__fsub_rn(__ldg(y + k), ax), __fmul_rn(ray.tend, ray.scale));
         }
         res[k] = out;
     }
@@ -446,9 +523,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
         pixel_of<TWO_D>(c, sv, row, u, v);
         if (u >= tl.n_u || v >= tl.n_v) continue;
         Ray ray;
-        float acc = 0.0f;
-        if (setup_ray<F>(sv, g, u, v, ray)) acc = walk<false>(ray, vol, nullptr, 0.0f);
-        const float q = __fmul_rn(acc, g.spacing);
+        float q = 0.0f;
+        if (setup_ray<F>(sv, g, u, v, ray))
+            q = __fmul_rn(walk_gather(ray, vol), ray.scale);
         sino[((int64_t)c.view * tl.n_u + u) * tl.n_v + v] = q;
         sq = __fma_rn((double)q, (double)q, sq);
     }
@@ -476,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
         if (y == 0.0f) continue;
         Ray ray;
         if (setup_ray<F>(sv, g, u, v, ray))
-            walk<true>(ray, nullptr, vol, __fmul_rn(y, g.spacing));
+            walk_scatter(ray, vol, __fmul_rn(y, ray.scale));
     }
 }
 
@@ -619,22 +696,51 @@ int elementwise_blocks(int64_t n) {
     } while (0)
 
 #define CT_NO_EXTRA
-#define CT_MODE0 , 0
-#define CT_MODE1 , 1
+
+#define CT_NB1 , 1
+#define CT_NB2 , 2
+#define CT_NB4 , 4
+#define CT_MODE0_NB1 , 0, 1
+#define CT_MODE0_NB2 , 0, 2
+#define CT_MODE0_NB4 , 0, 4
+#define CT_MODE1_NB1 , 1, 1
 
 cudaError_t launch_project(const ViewRec* views, const Grid& g, const Tiling& t, const float* vol,
                            float* sino, cudaStream_t stream) {
-    CT_LAUNCH_BY_AXIS(project_kernel, CT_NO_EXTRA, views, g, t, vol, sino);
+    CT_LAUNCH_BY_AXIS(project_kernel, CT_NB1, views, g, t, vol, (int64_t)0, sino, (int64_t)0);
 }
 
 cudaError_t launch_backproject(const ViewRec* views, const Grid& g, const Tiling& t,
                                const float* sino, float* vol, cudaStream_t stream) {
-    CT_LAUNCH_BY_AXIS(backproject_kernel, CT_MODE0, views, g, t, sino, vol);
+    CT_LAUNCH_BY_AXIS(backproject_kernel, CT_MODE0_NB1, views, g, t, sino, (int64_t)0, vol,
+                      (int64_t)0);
 }
 
 cudaError_t launch_backproject_ones(const ViewRec* views, const Grid& g, const Tiling& t,
                                     float* vol, cudaStream_t stream) {
-    CT_LAUNCH_BY_AXIS(backproject_kernel, CT_MODE1, views, g, t, nullptr, vol);
+    CT_LAUNCH_BY_AXIS(backproject_kernel, CT_MODE1_NB1, views, g, t, nullptr, (int64_t)0, vol,
+                      (int64_t)0);
+}
+
+cudaError_t launch_project_batch(const ViewRec* views, const Grid& g, const Tiling& t, int nb,
+                                 const float* vol, int64_t vstride, float* sino, int64_t sstride,
+                                 cudaStream_t stream) {
+    if (nb == 4) CT_LAUNCH_BY_AXIS(project_kernel, CT_NB4, views, g, t, vol, vstride, sino, sstride);
+    if (nb == 2) CT_LAUNCH_BY_AXIS(project_kernel, CT_NB2, views, g, t, vol, vstride, sino, sstride);
+    if (nb == 1) CT_LAUNCH_BY_AXIS(project_kernel, CT_NB1, views, g, t, vol, vstride, sino, sstride);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_backproject_batch(const ViewRec* views, const Grid& g, const Tiling& t, int nb,
+                                     const float* sino, int64_t sstride, float* vol,
+                                     int64_t vstride, cudaStream_t stream) {
+    if (nb == 4)
+        CT_LAUNCH_BY_AXIS(backproject_kernel, CT_MODE0_NB4, views, g, t, sino, sstride, vol, vstride);
+    if (nb == 2)
+        CT_LAUNCH_BY_AXIS(backproject_kernel, CT_MODE0_NB2, views, g, t, sino, sstride, vol, vstride);
+    if (nb == 1)
+        CT_LAUNCH_BY_AXIS(backproject_kernel, CT_MODE0_NB1, views, g, t, sino, sstride, vol, vstride);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_project_residual(const ViewRec* views, const Grid& g, const Tiling& t,

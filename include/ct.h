@@ -114,6 +114,19 @@ CT_API ct_status ct_geometry_create(ct_beam beam, int32_t n_views, const double 
                              int32_t ny, int32_t nx, double voxel_spacing, int32_t n_u,
                              int32_t n_v, double du, double dv, ct_geometry **out);
 
+/*
+ * As ct_geometry_create, with a voxel spacing per axis ("Trajectories and Geometry": voxel
+ * spacing is a positive scalar or a positive per-axis tuple in tensor order).
+ *
+ * spacing_zyx   HOST pointer to 3 doubles (dz, dy, dx), each > 0; for 2D beams dz is ignored.
+ * Voxel i of an axis with n cells and pitch s spans [-n s/2 + i s, -n s/2 + (i+1) s); chord
+ * lengths are physical.  The admission distance limit uses the smallest pitch.
+ */
+CT_API ct_status ct_geometry_create_ex(ct_beam beam, int32_t n_views, const double *views,
+                                       int32_t nz, int32_t ny, int32_t nx,
+                                       const double *spacing_zyx, int32_t n_u, int32_t n_v,
+                                       double du, double dv, ct_geometry **out);
+
 /* Free a handle and its device table (synchronous).  NULL is accepted. */
 CT_API ct_status ct_geometry_destroy(ct_geometry *geom);
 
@@ -167,6 +180,23 @@ CT_API ct_status ct_sirt_iterate(const ct_geometry *geom, float *d_x, const floa
                           void *d_workspace, size_t workspace_bytes, int32_t n_iters,
                           float relaxation, int32_t workspace_initialised,
                           struct CUstream_st *stream);
+
+/*
+ * Batches of volumes ("Leading batch/channel dimensions are preserved", diffct quickstart):
+ * d_volumes holds `batch` volumes back to back, (batch, nz, ny, nx); d_sinos holds `batch`
+ * sinograms, (batch, n_views, n_u, n_v).  Results equal `batch` separate ct_project /
+ * ct_backproject calls (the forward results bit for bit); the kernels walk each ray once for up
+ * to 4 volumes, so the per-update cost of the traversal is shared.  Workspace: at least
+ * ct_batch_workspace_bytes(geom, batch) (0 when the internal volume order is the caller's).
+ * Semantics, ownership and errors as for the single-volume calls.
+ */
+CT_API size_t ct_batch_workspace_bytes(const ct_geometry *geom, int32_t batch);
+CT_API ct_status ct_project_batch(const ct_geometry *geom, int32_t batch,
+                                  const float *d_volumes, float *d_sinos, void *d_workspace,
+                                  size_t workspace_bytes, struct CUstream_st *stream);
+CT_API ct_status ct_backproject_batch(const ct_geometry *geom, int32_t batch,
+                                      const float *d_sinos, float *d_volumes, void *d_workspace,
+                                      size_t workspace_bytes, struct CUstream_st *stream);
 
 /* Scratch bytes needed by ct_cgls_iterate. */
 CT_API size_t ct_cgls_workspace_bytes(const ct_geometry *geom);

@@ -267,3 +267,83 @@ def test_bad_pointers_aliasing_and_workspace(ct):
     # the handle still works afterwards
     g.project(vol, out=sino, workspace=ws)
     torch.cuda.synchronize()
+
+
+# ---------------------------------------------------------------------------------------------
+# per-axis voxel spacing
+# ---------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("kind", ["cone", "tilt", "fan"])
+def test_anisotropic_spacing_forward_backward_adjoint(ct, kind):
+    w = W.anisotropic_config(kind)
+    g = ct.Geometry.from_workload(w)
+    go = oracle.Geometry.from_workload(w)
+    x = w.phantom()
+    y_gpu = _cpu(g.project(torch_cuda(x)))
+    y_or = go.project(x, threads=8)
+    L, _ = go.ray_lengths()
+    bad = fp_violations(y_gpu, y_or, L, float(np.abs(x).max()))
+    assert bad.size == 0, (bad[:5], y_gpu.reshape(-1)[bad[:5]], y_or.reshape(-1)[bad[:5]])
+    yy = np.abs(W.random_sinogram(w, 4))
+    assert rel_l2(_cpu(g.backproject(torch_cuda(yy))), go.backproject(yy, threads=8)) <= BP_RTOL
+    rng = np.random.default_rng(5)
+    xr = rng.uniform(0, 1, size=w.volume_shape).astype(np.float32)
+    yr = rng.uniform(0, 1, size=w.sino_shape).astype(np.float32)
+    gap, lhs, rhs = adjoint_gap(_cpu(g.project(torch_cuda(xr))), yr, xr,
+                                _cpu(g.backproject(torch_cuda(yr))))
+    assert gap <= ADJ_RTOL, (gap, lhs, rhs)
+
+
+def test_anisotropic_spacing_rejects_bad_pitches(ct):
+    w = W.anisotropic_config("cone")
+    for bad in [(1.0, 0.0, 1.0), (1.0, -2.0, 1.0), (float("nan"), 1.0, 1.0)]:
+        with pytest.raises(ct.CtError) as e:
+            ct.Geometry(w.beam, w.views, w.vol_shape, bad, w.n_u, w.n_v, w.du, w.dv)
+        assert e.value.status == 1
+
+
+# ---------------------------------------------------------------------------------------------
+# batches of volumes (leading dimensions)
+# ---------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("n", [3, 5, 1])
+def test_batched_calls_equal_single_calls(ct, n):
+    """A batch of 7 volumes (chunks of 4 + 2 + 1 in the kernels) gives the single-volume forward
+    results bit for bit and the single-volume backprojections to float32 summation order."""
+    import torch
+    w = W.small_config(n)
+    g = ct.Geometry.from_workload(w)
+    rng = np.random.default_rng(n)
+    vols = torch_cuda(rng.uniform(0, 1, size=(7,) + tuple(w.volume_shape)))
+    sinos = g.project(vols)
+    assert tuple(sinos.shape) == (7,) + tuple(w.sino_shape)
+    for b in range(7):
+        assert torch.equal(sinos[b], g.project(vols[b].contiguous()))
+    ys = torch_cuda(rng.uniform(-1, 1, size=(7,) + tuple(w.sino_shape)))
+    backs = g.backproject(ys)
+    for b in range(7):
+        single = _cpu(g.backproject(ys[b].contiguous()))
+        assert rel_l2(_cpu(backs[b]), single) <= 1e-6
+    # two leading dimensions
+    v2 = vols[:6].reshape((2, 3) + tuple(w.volume_shape)).contiguous()
+    s2 = g.project(v2)
+    assert torch.equal(s2.reshape(sinos[:6].shape), sinos[:6])
+
+
+def test_batched_call_checks(ct):
+    import torch
+    w = W.small_config(3)
+    g = ct.Geometry.from_workload(w)
+    vols = torch.zeros((3,) + tuple(w.volume_shape), device="cuda")
+    sinos = torch.zeros((3,) + tuple(w.sino_shape), device="cuda")
+    need = ct.ct_batch_workspace_bytes(g.handle, 3)
+    assert need >= 3 * w.n_voxels * 4
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    with pytest.raises(ct.CtError) as e:
+        ct.ct_project_batch(g.handle, 3, vols.data_ptr(), sinos.data_ptr(), ws.data_ptr(),
+                            need - 4, None)
+    assert e.value.status == 7
+    with pytest.raises(ct.CtError) as e:
+        ct.ct_project_batch(g.handle, 0, vols.data_ptr(), sinos.data_ptr(), ws.data_ptr(), need,
+                            None)
+    assert e.value.status == 1
