@@ -59,6 +59,7 @@ class Workload:
     dv: float
     seed: int
     phantom_fn: Callable[[], np.ndarray] | None = None
+    offsets: np.ndarray | None = None  # (n_u, n_v, 3) local (u, v, n) pixel offsets, or flat
 
     @property
     def n_views(self) -> int:
@@ -381,6 +382,59 @@ def anisotropic_config(kind: str, seed: int = 7) -> Workload:
         return Workload("fan-aniso", FAN2D, views, (1, 53, 67), (0.9, 0.7), 97, 1, 0.8, 1.0,
                         seed, lambda: ellipses_2d(6, 67, np.random.default_rng(seed),
                                                   axis_range=(3.0, 20.0))[:53])
+    raise ValueError(kind)
+
+
+def flat_offsets(n_u: int, n_v: int, du: float, dv: float) -> np.ndarray:
+    """The flat detector written as per-pixel (u, v, n) offsets: ((u - (U-1)/2) du,
+    (v - (V-1)/2) dv, 0)."""
+    ou = (np.arange(n_u) - (n_u - 1) / 2.0) * du
+    ov = (np.arange(n_v) - (n_v - 1) / 2.0) * dv
+    off = np.zeros((n_u, n_v, 3))
+    off[:, :, 0] = ou[:, None]
+    off[:, :, 1] = ov[None, :]
+    return off
+
+
+def cylindrical_offsets(views: np.ndarray, is_2d: bool, n_u: int, n_v: int, du: float,
+                        dv: float, radius: float) -> np.ndarray:
+    """Cylindrical detector (axis along det_v) of the given radius, as in the diffct
+    detector-surface example: at arc length u, offsets (R sin(u/R), v, +/-R (1 - cos(u/R))).
+    The normal offset bends the detector towards the source (the sign follows the generated
+    frame's normal, checked on view 0), so radius = sdd centres the cylinder on the source."""
+    r = views[0]
+    if is_2d:
+        src, ctr, u = np.r_[r[0:2], 0.0], np.r_[r[2:4], 0.0], np.r_[r[4:6], 0.0]
+        nrm = np.array([u[1], -u[0], 0.0])
+    else:
+        src, ctr, u, v = r[0:3], r[3:6], r[6:9], r[9:12]
+        nrm = np.cross(u, v)
+    towards = 1.0 if float(nrm @ (src - ctr)) > 0 else -1.0
+    ang = (np.arange(n_u) - (n_u - 1) / 2.0) * du / radius
+    ov = (np.arange(n_v) - (n_v - 1) / 2.0) * dv if not is_2d else np.zeros(1)
+    off = np.zeros((n_u, n_v, 3))
+    off[:, :, 0] = (radius * np.sin(ang))[:, None]
+    off[:, :, 1] = ov[None, :]
+    off[:, :, 2] = (towards * radius * (1.0 - np.cos(ang)))[:, None]
+    return off
+
+
+def curved_config(kind: str, seed: int = 9) -> Workload:
+    """Small workloads with a cylindrical detector centred on the source ('cone', 'fan')."""
+    if kind == "cone":
+        views = circular_cone(17, 150.0, 300.0)
+        w = Workload("cone-cylindrical", CONE, views, (33, 41, 45), 1.0, 71, 37, 1.4, 1.2, seed,
+                     lambda: _crop(ellipsoids_3d(8, 45, np.random.default_rng(seed),
+                                                 axis_range=(3.0, 18.0)), (33, 41, 45)))
+        w.offsets = cylindrical_offsets(views, False, 71, 37, 1.4, 1.2, 300.0)
+        return w
+    if kind == "fan":
+        views = circular_fan_2d(23, 200.0, 350.0)
+        w = Workload("fan-cylindrical", FAN2D, views, (1, 57, 63), 1.0, 101, 1, 1.3, 1.0, seed,
+                     lambda: ellipses_2d(6, 63, np.random.default_rng(seed),
+                                         axis_range=(3.0, 20.0))[:57])
+        w.offsets = cylindrical_offsets(views, True, 101, 1, 1.3, 1.0, 350.0)
+        return w
     raise ValueError(kind)
 
 

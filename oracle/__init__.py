@@ -37,7 +37,8 @@ class _Geom(ctypes.Structure):
                 ("views", ctypes.POINTER(ctypes.c_double)),
                 ("nz", ctypes.c_int32), ("ny", ctypes.c_int32), ("nx", ctypes.c_int32),
                 ("s", ctypes.c_double * 3), ("nu", ctypes.c_int32), ("nv", ctypes.c_int32),
-                ("du", ctypes.c_double), ("dv", ctypes.c_double)]
+                ("du", ctypes.c_double), ("dv", ctypes.c_double),
+                ("offsets", ctypes.POINTER(ctypes.c_double))]
 
 
 _lib = None
@@ -67,6 +68,7 @@ def _load():
         L.oracle_backproject_voxels.argtypes = [gp, dp, ctypes.c_int64, i64p, dp]
         L.oracle_sirt.argtypes = [gp, dp, dp, ctypes.c_int32, ctypes.c_double, dp]
         L.oracle_cgls.argtypes = [gp, dp, dp, ctypes.c_int32, dp]
+        L.oracle_ray.argtypes = [gp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, dp, dp, dp]
         _lib = L
     return _lib
 
@@ -92,8 +94,8 @@ def spacing_xyz(voxel_spacing, is_2d: bool):
 class Geometry:
     """Oracle-side view of an acquisition (same record layout as the C library's input)."""
 
-    def __init__(self, beam: int, views, vol_shape, voxel_spacing: float, n_u: int, n_v: int,
-                 du: float, dv: float):
+    def __init__(self, beam: int, views, vol_shape, voxel_spacing, n_u: int, n_v: int,
+                 du: float, dv: float, offsets=None):
         self.beam = int(beam)
         self.views = np.ascontiguousarray(np.asarray(views, dtype=np.float64))
         nz, ny, nx = vol_shape
@@ -101,14 +103,28 @@ class Geometry:
         self.is_2d = self.beam in (0, 1)
         self.n_u, self.n_v = int(n_u), (1 if self.is_2d else int(n_v))
         self.spacing_xyz = spacing_xyz(voxel_spacing, self.is_2d)
+        # per-pixel (u, v, n) offsets of a parameterized detector surface, (n_u, n_v, 3)
+        self.offsets = None
+        if offsets is not None:
+            self.offsets = np.ascontiguousarray(
+                np.asarray(offsets, dtype=np.float64).reshape(self.n_u, self.n_v, 3))
         self._g = _Geom(self.beam, self.views.shape[0], _dp(self.views), self.vol_shape[0],
                         self.vol_shape[1], self.vol_shape[2],
                         (ctypes.c_double * 3)(*self.spacing_xyz), self.n_u, self.n_v,
-                        float(du), float(dv))
+                        float(du), float(dv),
+                        _dp(self.offsets) if self.offsets is not None else None)
 
     @classmethod
     def from_workload(cls, w) -> "Geometry":
-        return cls(w.beam, w.views, w.vol_shape, w.voxel_spacing, w.n_u, w.n_v, w.du, w.dv)
+        return cls(w.beam, w.views, w.vol_shape, w.voxel_spacing, w.n_u, w.n_v, w.du, w.dv,
+                   getattr(w, "offsets", None))
+
+    def ray(self, view: int, iu: int, iv: int = 0):
+        """(origin e, direction d, (amin, amax)) of one pixel's ray."""
+        L = _load()
+        e, d, rg = np.zeros(3), np.zeros(3), np.zeros(2)
+        L.oracle_ray(ctypes.byref(self._g), view, iu, iv, _dp(e), _dp(d), _dp(rg))
+        return e, d, (rg[0], rg[1])
 
     @property
     def n_views(self) -> int:

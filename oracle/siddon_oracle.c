@@ -52,6 +52,7 @@ typedef struct {
     double s[3];           /* voxel spacing along x, y, z (2D: z unused) */
     int32_t nu, nv;        /* 2D: nv == 1 */
     double du, dv;
+    const double *offsets; /* NULL: flat detector; else nu x nv x 3 local (u, v, n) offsets */
 } og_geom;
 
 static int is_2d(const og_geom *g) { return g->beam == OG_PARALLEL2D || g->beam == OG_FAN2D; }
@@ -79,10 +80,28 @@ static void make_ray(const og_geom *g, int view, int iu, int iv, double e[3], do
             first[k] = r[k]; ctr[k] = r[3 + k]; du[k] = r[6 + k]; dv[k] = r[9 + k];
         }
     }
-    const double cu = ((double)iu - (g->nu - 1) / 2.0) * g->du;
-    const double cv = is_2d(g) ? 0.0 : ((double)iv - (g->nv - 1) / 2.0) * g->dv;
     double pix[3];
-    for (int k = 0; k < 3; ++k) pix[k] = ctr[k] + cu * du[k] + cv * dv[k];
+    if (g->offsets == NULL) {
+        /* flat detector: the page's pixel formula */
+        const double cu = ((double)iu - (g->nu - 1) / 2.0) * g->du;
+        const double cv = is_2d(g) ? 0.0 : ((double)iv - (g->nv - 1) / 2.0) * g->dv;
+        for (int k = 0; k < 3; ++k) pix[k] = ctr[k] + cu * du[k] + cv * dv[k];
+    } else {
+        /* parameterized surface ("Trajectories and Geometry", detector surfaces): the pixel's
+           local (u, v, n) offsets along det_u, det_v and the normal, which is
+           cross(det_u, det_v) in 3D and (det_u_y, -det_u_x) in 2D */
+        const double *o = g->offsets + ((int64_t)iu * g->nv + iv) * 3;
+        double nrm[3];
+        if (is_2d(g)) {
+            nrm[0] = du[1]; nrm[1] = -du[0]; nrm[2] = 0.0;
+        } else {
+            nrm[0] = du[1] * dv[2] - du[2] * dv[1];
+            nrm[1] = du[2] * dv[0] - du[0] * dv[2];
+            nrm[2] = du[0] * dv[1] - du[1] * dv[0];
+        }
+        for (int k = 0; k < 3; ++k)
+            pix[k] = ctr[k] + o[0] * du[k] + (is_2d(g) ? 0.0 : o[1] * dv[k]) + o[2] * nrm[k];
+    }
     if (is_parallel(g)) {
         for (int k = 0; k < 3; ++k) { e[k] = pix[k]; d[k] = first[k]; }
         *amin = -INFINITY; *amax = INFINITY;
@@ -292,6 +311,12 @@ void oracle_ray_lengths(const og_geom *g, int32_t v0, int32_t v1, double *length
             }
 }
 
+/* The ray of pixel (iu, iv) of a view: origin e, direction d, parameter range (for tests). */
+void oracle_ray(const og_geom *g, int32_t view, int32_t iu, int32_t iv, double *e, double *d,
+                double *range) {
+    make_ray(g, view, iu, iv, e, d, &range[0], &range[1]);
+}
+
 /* ---- brute force: one voxel's own box against the ray --------------------------------------- */
 
 /*
@@ -413,6 +438,9 @@ void oracle_backproject_voxels(const og_geom *g, const double *sino, int64_t nvo
             }
             int64_t u0 = (int64_t)floor(umin) - 1, u1 = (int64_t)ceil(umax) + 1;
             int64_t w0 = (int64_t)floor(vmin) - 1, w1 = (int64_t)ceil(vmax) + 1;
+            if (g->offsets != NULL) {  /* not a plane: no bounding rectangle, try every pixel */
+                u0 = 0; u1 = g->nu - 1; w0 = 0; w1 = g->nv - 1;
+            }
             if (u0 < 0) u0 = 0;
             if (w0 < 0) w0 = 0;
             if (u1 > g->nu - 1) u1 = g->nu - 1;
