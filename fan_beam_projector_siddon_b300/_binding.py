@@ -61,6 +61,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                         ctypes.POINTER(f64), i32, i32, f64, f64,
                                         ctypes.POINTER(vp)]
     L.ct_geometry_create_ex.restype = i32
+    L.ct_geometry_create_surface.argtypes = [i32, i32, ctypes.POINTER(f64), i32, i32, i32,
+                                             ctypes.POINTER(f64), i32, i32, ctypes.POINTER(f64),
+                                             ctypes.POINTER(vp)]
+    L.ct_geometry_create_surface.restype = i32
     L.ct_geometry_destroy.argtypes = [vp]
     L.ct_geometry_destroy.restype = i32
     L.ct_geometry_get_info.argtypes = [vp, ctypes.POINTER(GeometryInfo)]
@@ -97,6 +101,31 @@ def _check(status: int, call: str) -> None:
 
 
 # ---- the C entry points, same names, raw pointers ---------------------------------------------
+
+def _spacing_zyx(voxel_spacing):
+    if np.ndim(voxel_spacing) == 0:
+        s = float(voxel_spacing)
+        return (ctypes.c_double * 3)(s, s, s)
+    s = [float(x) for x in voxel_spacing]
+    return (ctypes.c_double * 3)(*([1.0] + s if len(s) == 2 else s))
+
+
+def ct_geometry_create_surface(beam: int, views, vol_shape, voxel_spacing, n_u: int, n_v: int,
+                               offsets) -> int:
+    """Create a handle with a parameterized detector surface: ``offsets`` is (n_u, n_v, 3)
+    local (u, v, n) pixel offsets (2D: n_v = 1)."""
+    L = load_library()
+    v = np.ascontiguousarray(np.asarray(views, dtype=np.float64))
+    off = np.ascontiguousarray(np.asarray(offsets, dtype=np.float64).reshape(n_u, n_v, 3))
+    nz, ny, nx = vol_shape
+    h = ctypes.c_void_p()
+    dp = ctypes.POINTER(ctypes.c_double)
+    _check(L.ct_geometry_create_surface(int(beam), int(v.shape[0]), v.ctypes.data_as(dp),
+                                        int(nz), int(ny), int(nx), _spacing_zyx(voxel_spacing),
+                                        int(n_u), int(n_v), off.ctypes.data_as(dp),
+                                        ctypes.byref(h)), "ct_geometry_create_surface")
+    return h.value
+
 
 def ct_geometry_create(beam: int, views, vol_shape, voxel_spacing, n_u: int, n_v: int,
                        du: float, dv: float) -> int:
@@ -203,15 +232,21 @@ class Geometry:
     """Owns one ``ct_geometry`` handle; methods take and return CUDA float32 torch tensors."""
 
     def __init__(self, beam: int, views, vol_shape, voxel_spacing, n_u: int, n_v: int,
-                 du: float, dv: float):
-        self.handle = ct_geometry_create(beam, views, vol_shape, voxel_spacing, n_u, n_v, du, dv)
+                 du: float, dv: float, offsets=None):
+        if offsets is None:
+            self.handle = ct_geometry_create(beam, views, vol_shape, voxel_spacing, n_u, n_v, du,
+                                             dv)
+        else:
+            self.handle = ct_geometry_create_surface(beam, views, vol_shape, voxel_spacing, n_u,
+                                                     n_v, offsets)
         self.info = ct_geometry_get_info(self.handle)
         self.beam = int(beam)
         self.is_2d = self.beam in (CT_PARALLEL2D, CT_FAN2D)
 
     @classmethod
     def from_workload(cls, w) -> "Geometry":
-        return cls(w.beam, w.views, w.vol_shape, w.voxel_spacing, w.n_u, w.n_v, w.du, w.dv)
+        return cls(w.beam, w.views, w.vol_shape, w.voxel_spacing, w.n_u, w.n_v, w.du, w.dv,
+                   getattr(w, "offsets", None))
 
     def close(self) -> None:
         if getattr(self, "handle", None):

@@ -21,6 +21,7 @@ struct ct_geometry {
     ct::Grid grid;          // strides of the internal layout
     ct::Tiling tiling;
     ct::ViewRec* d_views;   // device table, n_views records
+    double* d_offsets;      // surface detectors: device (n_u, n_v, 3) offsets; else nullptr
     std::vector<double> host_views;
 };
 
@@ -58,7 +59,7 @@ void unpack(int beam, const double* r, double* first, double* ctr, double* u, do
 }
 
 // Admission checks (diffct "Trajectories and Geometry", validation paragraph), float64.
-bool admit_view(int beam, const double* r, double s) {
+bool admit_view(int beam, const double* r, double s, bool surface) {
     const int w = is_2d(beam) ? 6 : 12;
     for (int k = 0; k < w; ++k)
         if (!std::isfinite(r[k])) return false;
@@ -83,7 +84,7 @@ bool admit_view(int beam, const double* r, double s) {
         double sd[3] = {ctr[0] - first[0], ctr[1] - first[1], ctr[2] - first[2]};
         const double dist = norm3(sd);
         if (!(dist > 0.0)) return false;
-        if (std::fabs(dot3(sd, n)) <= tol * dist) return false;  // edge-on detector
+        if (!surface && std::fabs(dot3(sd, n)) <= tol * dist) return false;  // edge-on detector
         const double rs = norm3(first), rc = norm3(ctr);
         if ((rs < rc ? rs : rc) > 1e6 * s) return false;
         if ((rs > rc ? rs : rc) > 1e15 * s) return false;
@@ -223,9 +224,53 @@ ct_status ct_geometry_create(ct_beam beam, int32_t n_views, const double* views,
     return ct_geometry_create_ex(beam, n_views, views, nz, ny, nx, s3, n_u, n_v, du, dv, out);
 }
 
-ct_status ct_geometry_create_ex(ct_beam beam, int32_t n_views, const double* views, int32_t nz,
-                                int32_t ny, int32_t nx, const double* spacing_zyx, int32_t n_u,
-                                int32_t n_v, double du, double dv, ct_geometry** out) {
+}  // extern "C"
+
+namespace {
+
+// Per-pixel admission for surface detectors ("Trajectories and Geometry": surface detectors
+// validate each actual source/pixel pair): finite world points; for point sources every pixel
+// distinct from the source in float32; the nearer endpoint within 1e6 voxel spacings of the
+// origin and both within 1e15.
+bool admit_surface(int beam, int32_t n_views, const double* views, int32_t n_u, int32_t n_v,
+                   const double* off, double s) {
+    const int w = is_2d(beam) ? 6 : 12;
+    for (int64_t k = 0; k < (int64_t)n_u * n_v * 3; ++k)
+        if (!std::isfinite(off[k])) return false;
+    for (int i = 0; i < n_views; ++i) {
+        double first[3], ctr[3], u[3], v[3], n[3];
+        unpack(beam, views + (int64_t)i * w, first, ctr, u, v);
+        if (is_2d(beam)) {
+            n[0] = u[1]; n[1] = -u[0]; n[2] = 0.0;
+        } else {
+            cross3(u, v, n);
+        }
+        for (int64_t p = 0; p < (int64_t)n_u * n_v; ++p) {
+            const double* o = off + p * 3;
+            double pix[3];
+            for (int a = 0; a < 3; ++a)
+                pix[a] = ctr[a] + o[0] * u[a] + (is_2d(beam) ? 0.0 : o[1] * v[a]) + o[2] * n[a];
+            if (!(std::isfinite(pix[0]) && std::isfinite(pix[1]) && std::isfinite(pix[2])))
+                return false;
+            const double rp = norm3(pix);
+            if (is_parallel(beam)) {
+                if (rp > 1e6 * s) return false;
+            } else {
+                if ((float)pix[0] == (float)first[0] && (float)pix[1] == (float)first[1] &&
+                    (float)pix[2] == (float)first[2])
+                    return false;
+                const double rs = norm3(first);
+                if ((rs < rp ? rs : rp) > 1e6 * s) return false;
+                if ((rs > rp ? rs : rp) > 1e15 * s) return false;
+            }
+        }
+    }
+    return true;
+}
+
+ct_status create_impl(ct_beam beam, int32_t n_views, const double* views, int32_t nz, int32_t ny,
+                      int32_t nx, const double* spacing_zyx, int32_t n_u, int32_t n_v, double du,
+                      double dv, const double* offsets, ct_geometry** out) {
     if (out == nullptr) return CT_ERR_INVALID_ARGUMENT;
     *out = nullptr;
     const int b = (int)beam;
@@ -252,8 +297,12 @@ ct_status ct_geometry_create_ex(ct_beam beam, int32_t n_views, const double* vie
     const int64_t tiles_v = is_2d(b) ? 1 : (n_v + 31) / 32;
     if (tiles_u * tiles_v * n_views > (int64_t)INT32_MAX) return CT_ERR_INVALID_ARGUMENT;
     const int w = is_2d(b) ? 6 : 12;
+    const bool surface = offsets != nullptr;
     for (int i = 0; i < n_views; ++i)
-        if (!admit_view(b, views + (int64_t)i * w, sp_min)) return CT_ERR_INVALID_GEOMETRY;
+        if (!admit_view(b, views + (int64_t)i * w, sp_min, surface))
+            return CT_ERR_INVALID_GEOMETRY;
+    if (surface && !admit_surface(b, n_views, views, n_u, n_v, offsets, sp_min))
+        return CT_ERR_INVALID_GEOMETRY;
 
     ct_geometry* g = new (std::nothrow) ct_geometry();
     if (g == nullptr) return CT_ERR_OUT_OF_MEMORY;
@@ -300,13 +349,28 @@ ct_status ct_geometry_create_ex(ct_beam beam, int32_t n_views, const double* vie
         unpack(b, views + (int64_t)i * w, first, ctr, u, v);
         ct::ViewRec& R = recs[(size_t)i];
         std::memset(&R, 0, sizeof(R));
-        const double cu = 0.5 * (n_u - 1), cv = is_2d(b) ? 0.0 : 0.5 * (n_v - 1);
-        const double dvv = is_2d(b) ? 0.0 : dv;
         // coordinates in voxel units per axis (p_a + half_a) / spacing_a
-        for (int a = 0; a < 3; ++a) {
-            R.pu[a] = du * is[a] * u[a];
-            R.pv[a] = dvv * is[a] * v[a];
-            R.pb[a] = (ctr[a] + half[a]) * is[a] - cu * R.pu[a] - cv * R.pv[a];
+        if (!surface) {
+            const double cu = 0.5 * (n_u - 1), cv = is_2d(b) ? 0.0 : 0.5 * (n_v - 1);
+            const double dvv = is_2d(b) ? 0.0 : dv;
+            for (int a = 0; a < 3; ++a) {
+                R.pu[a] = du * is[a] * u[a];
+                R.pv[a] = dvv * is[a] * v[a];
+                R.pb[a] = (ctr[a] + half[a]) * is[a] - cu * R.pu[a] - cv * R.pv[a];
+            }
+        } else {
+            double n[3];
+            if (is_2d(b)) {
+                n[0] = u[1]; n[1] = -u[0]; n[2] = 0.0;
+            } else {
+                cross3(u, v, n);
+            }
+            for (int a = 0; a < 3; ++a) {
+                R.pu[a] = is[a] * u[a];
+                R.pv[a] = is_2d(b) ? 0.0 : is[a] * v[a];
+                R.pn[a] = is[a] * n[a];
+                R.pb[a] = (ctr[a] + half[a]) * is[a];
+            }
         }
         if (is_parallel(b)) {
             // unit direction in physical space, expressed in voxel units per axis (for an
@@ -326,20 +390,54 @@ ct_status ct_geometry_create_ex(ct_beam beam, int32_t n_views, const double* vie
     if (e == cudaSuccess)
         e = cudaMemcpy(g->d_views, recs.data(), sizeof(ct::ViewRec) * (size_t)n_views,
                        cudaMemcpyHostToDevice);
+    const size_t off_bytes = sizeof(double) * 3 * (size_t)n_u * (size_t)n_v;
+    if (e == cudaSuccess && surface) e = cudaMalloc(&g->d_offsets, off_bytes);
+    if (e == cudaSuccess && surface)
+        e = cudaMemcpy(g->d_offsets, offsets, off_bytes, cudaMemcpyHostToDevice);
     if (e != cudaSuccess) {
         cudaGetLastError();
         if (g->d_views) cudaFree(g->d_views);
+        if (g->d_offsets) cudaFree(g->d_offsets);
         delete g;
         return from_cuda(e);
     }
+    G.offsets = g->d_offsets;
+    G.nv = n_v;
     *out = g;
     return CT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ct_status ct_geometry_create_ex(ct_beam beam, int32_t n_views, const double* views, int32_t nz,
+                                int32_t ny, int32_t nx, const double* spacing_zyx, int32_t n_u,
+                                int32_t n_v, double du, double dv, ct_geometry** out) {
+    return create_impl(beam, n_views, views, nz, ny, nx, spacing_zyx, n_u, n_v, du, dv, nullptr,
+                       out);
+}
+
+ct_status ct_geometry_create_surface(ct_beam beam, int32_t n_views, const double* views,
+                                     int32_t nz, int32_t ny, int32_t nx,
+                                     const double* spacing_zyx, int32_t n_u, int32_t n_v,
+                                     const double* offsets_uvn, ct_geometry** out) {
+    if (offsets_uvn == nullptr) {
+        if (out) *out = nullptr;
+        return CT_ERR_INVALID_ARGUMENT;
+    }
+    return create_impl(beam, n_views, views, nz, ny, nx, spacing_zyx, n_u, n_v, 1.0, 1.0,
+                       offsets_uvn, out);
 }
 
 ct_status ct_geometry_destroy(ct_geometry* g) {
     if (g == nullptr) return CT_OK;
     cudaError_t e = cudaSuccess;
     if (g->d_views) e = cudaFree(g->d_views);
+    if (g->d_offsets) {
+        const cudaError_t e2 = cudaFree(g->d_offsets);
+        if (e == cudaSuccess) e = e2;
+    }
     delete g;
     return from_cuda(e);
 }

@@ -18,19 +18,21 @@ enum Layout : int32_t {
 // Per-view record as the kernels read it.  All positions are in voxel units, with the origin at
 // the volume's lower corner, so the volume is the box [0, nx] x [0, ny] x [0, nz] and voxel
 // (i, j, k) is the unit cell [i, i+1) x [j, j+1) x [k, k+1).  Pixel (u, v) sits at
-//     P(u, v) = pb + u * pu + v * pv        (pb already holds the -(U-1)/2, -(V-1)/2 offsets)
-// Parallel beams: the ray is P(u, v) + t * q   (q = unit ray direction), t over all reals.
+//     flat detector:  P(u, v) = pb + u * pu + v * pv   (pb holds the -(U-1)/2, -(V-1)/2 offsets)
+//     surface:        P(u, v) = pb + o_u * pu + o_v * pv + o_n * pn   (per-pixel offsets o)
+// Parallel beams: the ray is P(u, v) + t * q   (q = ray direction), t over all reals.
 // Point sources:  the ray is q + a * (P(u, v) - q) for a in [0, 1]; pb is stored minus q, so
-//                 the direction is directly pb + u * pu + v * pv.
+//                 the direction is directly P(u, v).
 struct ViewRec {
     double pb[3];
     double pu[3];
     double pv[3];
+    double pn[3];           // detector normal (surface detectors only)
     double q[3];
     int32_t lanes_along_v;  // 1: a warp's 32 lanes take 32 consecutive v; 0: consecutive u
     int32_t pad;
 };
-static_assert(sizeof(ViewRec) == 104, "ViewRec layout");
+static_assert(sizeof(ViewRec) == 128, "ViewRec layout");
 
 // Volume grid as the kernels see it.
 struct Grid {
@@ -41,6 +43,8 @@ struct Grid {
     int32_t iso;         // 1 when the three pitches are equal
     int32_t parallel;    // 1: infinite lines, 0: source-to-pixel segments
     int32_t fast;        // axis that is fastest in memory (0 x, 1 y, 2 z): the walk's inner axis
+    const double* offsets;  // surface detectors: (n_u, n_v, 3) local offsets; flat: nullptr
+    int32_t nv;             // detector pixels along v (row pitch of the offsets table)
 };
 
 // Detector tiling of one launch.

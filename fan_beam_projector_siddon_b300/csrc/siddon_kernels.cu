@@ -57,13 +57,25 @@ template <int F>
 __device__ __forceinline__ bool setup_ray(const ViewRec& vr, const Grid& g, int u, int v,
                                           Ray& r) {
     constexpr int A = F == 0 ? 1 : 0;
-    const double fu = (double)u, fv = (double)v;
+    // pixel point: flat formula, or the pixel's (u, v, n) offsets on a surface detector
+    double P[3];
+    if (g.offsets == nullptr) {
+        const double fu = (double)u, fv = (double)v;
+#pragma unroll
+        for (int a = 0; a < 3; ++a) P[a] = __fma_rn(fv, vr.pv[a], __fma_rn(fu, vr.pu[a], vr.pb[a]));
+    } else {
+        const double* off = g.offsets + ((int64_t)u * g.nv + v) * 3;
+        const double ou = __ldg(off), ov = __ldg(off + 1), on = __ldg(off + 2);
+#pragma unroll
+        for (int a = 0; a < 3; ++a)
+            P[a] = __fma_rn(on, vr.pn[a], __fma_rn(ov, vr.pv[a], __fma_rn(ou, vr.pu[a], vr.pb[a])));
+    }
     double o[3], d[3];
     double amin, amax;
     if (g.parallel) {
 #pragma unroll
         for (int a = 0; a < 3; ++a) {
-            o[a] = __fma_rn(fv, vr.pv[a], __fma_rn(fu, vr.pu[a], vr.pb[a]));
+            o[a] = P[a];
             d[a] = vr.q[a];
         }
         amin = -__longlong_as_double(0x7ff0000000000000ll);
@@ -72,7 +84,7 @@ __device__ __forceinline__ bool setup_ray(const ViewRec& vr, const Grid& g, int 
 #pragma unroll
         for (int a = 0; a < 3; ++a) {
             o[a] = vr.q[a];
-            d[a] = __fma_rn(fv, vr.pv[a], __fma_rn(fu, vr.pu[a], vr.pb[a]));
+            d[a] = P[a];
         }
         amin = 0.0;
         amax = 1.0;

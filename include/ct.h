@@ -127,6 +127,23 @@ CT_API ct_status ct_geometry_create_ex(ct_beam beam, int32_t n_views, const doub
                                        const double *spacing_zyx, int32_t n_u, int32_t n_v,
                                        double du, double dv, ct_geometry **out);
 
+/*
+ * As ct_geometry_create_ex, with a parameterized detector surface instead of the flat detector
+ * ("Trajectories and Geometry", detector surfaces): pixel (u, v) of a view sits at
+ *     det_center + o_u det_u + o_v det_v + o_n n,   n = det_u x det_v  (2D: (det_u_y, -det_u_x))
+ * with the pixel's local offsets o = offsets_uvn[(u * n_v + v) * 3 + {0, 1, 2}] (physical units,
+ * shared by all views; 2D: o_v is ignored).  A cylinder of radius R about det_v, for example, has
+ * o = (R sin(s/R), v, +-R (1 - cos(s/R))) at arc length s.  The record's det_u/det_v must still
+ * be orthonormal; instead of the flat edge-on test every source/pixel pair is checked: distinct
+ * in float32, nearer endpoint within 1e6 voxel spacings of the origin, both within 1e15.
+ * offsets_uvn is a HOST pointer to n_u x n_v x 3 doubles, copied to a device table that the
+ * handle owns.
+ */
+CT_API ct_status ct_geometry_create_surface(ct_beam beam, int32_t n_views, const double *views,
+                                            int32_t nz, int32_t ny, int32_t nx,
+                                            const double *spacing_zyx, int32_t n_u, int32_t n_v,
+                                            const double *offsets_uvn, ct_geometry **out);
+
 /* Free a handle and its device table (synchronous).  NULL is accepted. */
 CT_API ct_status ct_geometry_destroy(ct_geometry *geom);
 

@@ -90,3 +90,23 @@ def test_null_arguments_are_rejected(lib):
     assert L.ct_sirt_iterate(None, None, None, None, 0, 1, 1.0, 0, None) == 1
     assert L.ct_geometry_destroy(None) == 0
     assert L.ct_sirt_workspace_bytes(None) == 0
+
+
+def test_surface_admission_before_touching_the_gpu(lib):
+    """Surface detectors are checked pixel by pixel on the host: non-finite offsets and a pixel
+    on the source are rejected as invalid geometry."""
+    w = W.curved_config("cone")
+    bad = w.offsets.copy()
+    bad[3, 4, 2] = np.nan
+    _expect(lib, 2, lib.ct_geometry_create_surface, w.beam, w.views, w.vol_shape,
+            w.voxel_spacing, w.n_u, w.n_v, bad)
+    bad = w.offsets.copy()
+    src, ctr, u, v = w.views[0, 0:3], w.views[0, 3:6], w.views[0, 6:9], w.views[0, 9:12]
+    rel = src - ctr
+    bad[0, 0] = [rel @ u, rel @ v, rel @ np.cross(u, v)]
+    _expect(lib, 2, lib.ct_geometry_create_surface, w.beam, w.views, w.vol_shape,
+            w.voxel_spacing, w.n_u, w.n_v, bad)
+    # per-axis spacing: non-positive pitches are bad arguments
+    c = W.anisotropic_config("cone")
+    _expect(lib, 1, lib.ct_geometry_create, c.beam, c.views, c.vol_shape, (1.0, 0.0, 1.0),
+            c.n_u, c.n_v, c.du, c.dv)

@@ -347,3 +347,40 @@ def test_batched_call_checks(ct):
         ct.ct_project_batch(g.handle, 0, vols.data_ptr(), sinos.data_ptr(), ws.data_ptr(), need,
                             None)
     assert e.value.status == 1
+
+
+# ---------------------------------------------------------------------------------------------
+# parameterized detector surfaces
+# ---------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("kind", ["cone", "fan"])
+def test_cylindrical_detector_forward_backward_adjoint(ct, kind):
+    w = W.curved_config(kind)
+    g = ct.Geometry.from_workload(w)
+    go = oracle.Geometry.from_workload(w)
+    x = w.phantom()
+    y_gpu = _cpu(g.project(torch_cuda(x)))
+    y_or = go.project(x, threads=8)
+    L, _ = go.ray_lengths()
+    bad = fp_violations(y_gpu, y_or, L, float(np.abs(x).max()))
+    assert bad.size == 0, (bad[:5], y_gpu.reshape(-1)[bad[:5]], y_or.reshape(-1)[bad[:5]])
+    assert (L > 0).mean() > 0.5
+    yy = np.abs(W.random_sinogram(w, 4))
+    assert rel_l2(_cpu(g.backproject(torch_cuda(yy))), go.backproject(yy, threads=8)) <= BP_RTOL
+    rng = np.random.default_rng(6)
+    xr = rng.uniform(0, 1, size=w.volume_shape).astype(np.float32)
+    yr = rng.uniform(0, 1, size=w.sino_shape).astype(np.float32)
+    gap, lhs, rhs = adjoint_gap(_cpu(g.project(torch_cuda(xr))), yr, xr,
+                                _cpu(g.backproject(torch_cuda(yr))))
+    assert gap <= ADJ_RTOL, (gap, lhs, rhs)
+
+
+def test_flat_offsets_surface_equals_flat_detector(ct):
+    import torch
+    w = W.small_config(3)
+    flat = ct.Geometry.from_workload(w)
+    surf = ct.Geometry(w.beam, w.views, w.vol_shape, w.voxel_spacing, w.n_u, w.n_v, w.du, w.dv,
+                       offsets=W.flat_offsets(w.n_u, w.n_v, w.du, w.dv))
+    x = torch_cuda(w.phantom())
+    a, b = _cpu(flat.project(x)), _cpu(surf.project(x))
+    np.testing.assert_allclose(b, a, rtol=1e-5, atol=1e-5 * float(np.abs(a).max()))
