@@ -1,0 +1,136 @@
+"""Float64 reference of filtered backprojection (parallel FBP, fan FBP, cone FDK).
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py``).  Plain numpy; it shares nothing with the
+CUDA path.  The pages (diffct "Differentiable analytical reconstruction" and the parallel/fan/
+cone FBP example pages) name the stages -- detector cosine weights, a ramp filter along the
+detector u axis with physical sample spacing and an optional window (ram-lak, shepp-logan,
+cosine, hamming, hann), angular integration weights, and a voxel-driven distance-weighted gather
+-- without printing formulas.  This module writes out the textbook forms:
+
+* cosine weight of pixel p (fan/cone):  |(c - s) . n| / |p - s|, n the detector normal;
+* filter: Q(u_i) = tau * sum_j h((i - j) tau) p(u_j), with h the band-limited ramp
+  h(x) = 2 * int_0^{1/(2 tau)} f W(f) cos(2 pi f x) df, tau = du, evaluated here by adaptive
+  quadrature (scipy.integrate.quad) -- not by closed forms;
+* view weight w_k (default pi / n_views: a uniformly sampled full scan, i.e. pi for parallel
+  beams over 180 degrees, and 2 pi with the 1/2 redundancy factor for fan/cone over 360);
+* gather: f(X) = sum_k w_k g_k(X) Q_k(u_k(X), v_k(X)) with bilinear interpolation (0 outside the
+  detector), g = 1 for parallel beams and, for fan/cone, g = (D_sd / D_so) / U(X)^2 with
+  U(X) = ((X - s) . n) / ((iso - s) . n), D_so = |(iso - s) . n|, D_sd = |(c - s) . n|
+  (Feldkamp's distance weight for a detector at distance D_sd; the D_sd / D_so factor converts a
+  filter applied in physical detector units to the isocentre plane).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+WINDOWS = ("ram-lak", "shepp-logan", "cosine", "hamming", "hann")
+
+
+def window_response(name: str, f: np.ndarray, tau: float) -> np.ndarray:
+    """W(f) on [0, 1/(2 tau)] for the named window (frequency in cycles per unit length)."""
+    x = f * tau  # in [0, 1/2]
+    if name == "ram-lak":
+        return np.ones_like(f)
+    if name == "shepp-logan":
+        return np.sinc(x)                     # sin(pi x) / (pi x)
+    if name == "cosine":
+        return np.cos(np.pi * x)
+    if name == "hamming":
+        return 0.54 + 0.46 * np.cos(2 * np.pi * x)
+    if name == "hann":
+        return 0.5 + 0.5 * np.cos(2 * np.pi * x)
+    raise ValueError(name)
+
+
+def ramp_taps(n_u: int, tau: float, window: str) -> np.ndarray:
+    """h(n tau) for n = -(n_u - 1) .. n_u - 1, by quadrature of the band-limited windowed ramp."""
+    from scipy.integrate import quad
+    F = 0.5 / tau
+    taps = np.zeros(2 * n_u - 1)
+    for n in range(n_u):
+        x = n * tau
+        val, _ = quad(lambda f: f * window_response(window, np.array([f]), tau)[0]
+                      * math.cos(2 * math.pi * f * x), 0.0, F, limit=400,
+                      weight=None, epsabs=1e-14, epsrel=1e-12)
+        taps[n_u - 1 + n] = taps[n_u - 1 - n] = 2.0 * val
+    return taps
+
+
+def _frames(beam: int, rec: np.ndarray):
+    if beam in (0, 1):
+        first, ctr, u = np.r_[rec[0:2], 0.0], np.r_[rec[2:4], 0.0], np.r_[rec[4:6], 0.0]
+        v = np.array([0.0, 0.0, 1.0])
+        n = np.array([u[1], -u[0], 0.0])
+    else:
+        first, ctr, u, v = rec[0:3], rec[3:6], rec[6:9], rec[9:12]
+        n = np.cross(u, v)
+    return first, ctr, u, v, n
+
+
+def fbp(beam: int, views: np.ndarray, vol_shape, spacing: float, n_u: int, n_v: int, du: float,
+        dv: float, sino: np.ndarray, window: str = "ram-lak", view_weights=None, isocenter=None):
+    """Filtered backprojection of `sino` ((views, U) or (views, U, V)) onto the volume grid."""
+    assert beam in (0, 1, 2), "parallel (2D), fan (2D) and cone beams"
+    two_d = beam in (0, 1)
+    nz, ny, nx = vol_shape
+    n_views = views.shape[0]
+    p = np.asarray(sino, dtype=np.float64).reshape(n_views, n_u, 1 if two_d else n_v)
+    V = p.shape[2]
+    w = (np.full(n_views, math.pi / n_views) if view_weights is None
+         else np.asarray(view_weights, dtype=np.float64))
+    iso = np.zeros(3) if isocenter is None else np.r_[np.asarray(isocenter, float), [0.0] * (3 - len(isocenter))]
+    cu, cv = (n_u - 1) / 2.0, (V - 1) / 2.0
+    uu = (np.arange(n_u) - cu) * du
+    vv = (np.arange(V) - cv) * dv if not two_d else np.zeros(1)
+    taps = ramp_taps(n_u, du, window)
+    # voxel centres
+    zs = (np.arange(nz) + 0.5 - nz / 2.0) * spacing if not two_d else np.zeros(1)
+    ys = (np.arange(ny) + 0.5 - ny / 2.0) * spacing
+    xs = (np.arange(nx) + 0.5 - nx / 2.0) * spacing
+    Z, Y, X = np.meshgrid(zs, ys, xs, indexing="ij")
+    P = np.stack([X, Y, Z], axis=-1)                               # (nz|1, ny, nx, 3)
+    out = np.zeros(P.shape[:3])
+    for k in range(n_views):
+        first, ctr, u, v, n = _frames(beam, views[k])
+        q = p[k].copy()
+        if beam != 0:                                              # cosine pre-weights
+            pix = ctr[None, None, :] + uu[:, None, None] * u + vv[None, :, None] * v
+            q *= abs((ctr - first) @ n) / np.linalg.norm(pix - first, axis=-1)
+        # filter every detector column along u (linear convolution, no wrap-around)
+        Q = np.empty_like(q)
+        for j in range(V):
+            Q[:, j] = du * np.convolve(q[:, j], taps, mode="full")[n_u - 1:2 * n_u - 1]
+        # gather
+        if beam == 0:
+            upix = ((P - ctr) @ u) / du + cu
+            vpix = np.zeros_like(upix)
+            g = np.ones_like(upix)
+        else:
+            a = P - first
+            den = a @ n
+            D = (ctr - first) @ n
+            upix = ((first - ctr) @ u + D * (a @ u) / den) / du + cu
+            vpix = (((first - ctr) @ v + D * (a @ v) / den) / dv + cv) if not two_d else np.zeros_like(upix)
+            Uw = den / ((iso - first) @ n)
+            g = (abs(D) / abs((iso - first) @ n)) / (Uw * Uw)
+        out += w[k] * g * _bilinear(Q, upix, vpix)
+    return out[0] if two_d else out
+
+
+def _bilinear(Q: np.ndarray, up: np.ndarray, vp: np.ndarray) -> np.ndarray:
+    """Bilinear interpolation of Q[u, v] at fractional pixel indices, 0 outside the grid."""
+    nU, nV = Q.shape
+    u0 = np.floor(up).astype(np.int64)
+    v0 = np.floor(vp).astype(np.int64)
+    fu, fv = up - u0, vp - v0
+    res = np.zeros(up.shape)
+    for du_, wu in ((0, 1 - fu), (1, fu)):
+        for dv_, wv in ((0, 1 - fv), (1, fv)):
+            iu, iv = u0 + du_, v0 + dv_
+            ok = (iu >= 0) & (iu < nU) & (iv >= 0) & (iv < nV)
+            vals = np.zeros(up.shape)
+            vals[ok] = Q[iu[ok], iv[ok]]
+            res += wu * wv * vals
+    return res

@@ -1,0 +1,118 @@
+"""Pins for the float64 FBP/FDK reference (oracle/fbp.py).
+
+* filter taps from quadrature against the textbook closed forms of the band-limited Ram-Lak and
+  Shepp-Logan kernels (Kak & Slaney), and every window's taps against a direct Riemann sum of
+  their frequency response;
+* reconstructions of analytically projected objects (a disk in parallel and fan geometry, a ball
+  in cone geometry -- sinograms from chord lengths, not from any projector) come back close to 1
+  inside and close to 0 outside; this pins the filter scale, the view weights, the cosine weights
+  and the distance weights together.
+"""
+import math
+
+import numpy as np
+import pytest
+
+from fan_beam_projector_siddon_b300 import workloads as W
+from oracle import fbp as F
+
+
+@pytest.mark.parametrize("tau", [1.0, 0.5, 1.3])
+def test_ramlak_and_shepp_logan_taps_match_closed_forms(tau):
+    n = np.arange(-9, 10)
+    h = F.ramp_taps(10, tau, "ram-lak")
+    nn = np.where(n == 0, 1, n).astype(float)
+    want = np.where(n == 0, 1.0 / (4 * tau * tau),
+                    np.where(n % 2 == 0, 0.0, -1.0 / (np.pi ** 2 * nn ** 2 * tau ** 2)))
+    np.testing.assert_allclose(h, want, rtol=1e-9, atol=1e-12 / tau ** 2)
+    h = F.ramp_taps(10, tau, "shepp-logan")
+    want = -2.0 / (np.pi ** 2 * tau ** 2 * (4 * n.astype(float) ** 2 - 1))
+    np.testing.assert_allclose(h, want, rtol=1e-9, atol=1e-12 / tau ** 2)
+
+
+@pytest.mark.parametrize("window", F.WINDOWS)
+def test_window_taps_against_riemann_sum(window):
+    tau = 0.8
+    h = F.ramp_taps(6, tau, window)
+    f = (np.arange(200000) + 0.5) / 200000 * (0.5 / tau)
+    df = (0.5 / tau) / 200000
+    for n in range(6):
+        want = 2 * np.sum(f * F.window_response(window, f, tau) * np.cos(2 * np.pi * f * n * tau)) * df
+        assert abs(h[5 + n] - want) <= 1e-8 / tau ** 2
+
+
+def _disk_parallel_sino(views, n_u, du, R):
+    t = (np.arange(n_u) - (n_u - 1) / 2.0) * du
+    row = 2 * np.sqrt(np.clip(R * R - t * t, 0, None))
+    return np.tile(row, (views.shape[0], 1))
+
+
+def _chord_ball(src, pix, R):
+    """Chord of the segment src -> pix through the ball |x| <= R (all arrays (..., 3))."""
+    d = pix - src
+    L = np.linalg.norm(d, axis=-1)
+    dh = d / L[..., None]
+    b = np.sum(src * dh, axis=-1)
+    c = np.sum(src * src, axis=-1) - R * R
+    disc = b * b - c
+    return 2 * np.sqrt(np.clip(disc, 0, None))
+
+
+def _radius_grid(n, s):
+    c = (np.arange(n) + 0.5 - n / 2.0) * s
+    return c
+
+
+def test_parallel_fbp_of_a_disk():
+    n, R = 64, 20.0
+    views = W.circular_parallel_2d(180)
+    sino = _disk_parallel_sino(views, 129, 0.5, R)
+    img = F.fbp(0, views, (1, n, n), 1.0, 129, 1, 0.5, 1.0, sino)
+    c = _radius_grid(n, 1.0)
+    r = np.hypot(*np.meshgrid(c, c, indexing="ij"))
+    assert abs(np.median(img[r < 0.8 * R]) - 1.0) < 0.01
+    assert np.abs(img[r < 0.8 * R] - 1.0).max() < 0.05
+    fov = 0.95 * 64 * 0.5 / 2 * 2           # inside the detector's half-width (32)
+    assert np.abs(img[(r > 1.25 * R) & (r < fov)]).max() < 0.05
+
+
+def test_fan_fbp_of_a_disk():
+    n, R, sid, sdd = 64, 20.0, 160.0, 256.0
+    views = W.circular_fan_2d(240, sid, sdd)
+    n_u, du = 161, 0.8
+    sino = np.zeros((240, n_u))
+    uu = (np.arange(n_u) - (n_u - 1) / 2.0) * du
+    for k in range(240):
+        src = np.r_[views[k, 0:2], 0.0]
+        pix = np.r_[views[k, 2:4], 0.0][None, :] + uu[:, None] * np.r_[views[k, 4:6], 0.0][None, :]
+        sino[k] = _chord_ball(src[None, :], pix, R)      # a disk is the ball's z = 0 section
+    img = F.fbp(1, views, (1, n, n), 1.0, n_u, 1, du, 1.0, sino)
+    c = _radius_grid(n, 1.0)
+    r = np.hypot(*np.meshgrid(c, c, indexing="ij"))
+    assert abs(np.median(img[r < 0.8 * R]) - 1.0) < 0.01
+    assert np.abs(img[r < 0.8 * R] - 1.0).max() < 0.05
+    fov = 0.95 * (n_u - 1) / 2 * du * sid / sdd    # radius seen by every view
+    assert np.abs(img[(r > 1.25 * R) & (r < fov)]).max() < 0.05
+
+
+def test_cone_fdk_of_a_ball():
+    n, R, sid, sdd = 40, 12.0, 120.0, 200.0
+    views = W.circular_cone(120, sid, sdd)
+    n_u, n_v, du = 97, 81, 0.8
+    uu = (np.arange(n_u) - (n_u - 1) / 2.0) * du
+    vv = (np.arange(n_v) - (n_v - 1) / 2.0) * du
+    sino = np.zeros((120, n_u, n_v))
+    for k in range(120):
+        src, ctr, u, v = views[k, 0:3], views[k, 3:6], views[k, 6:9], views[k, 9:12]
+        pix = ctr + uu[:, None, None] * u + vv[None, :, None] * v
+        sino[k] = _chord_ball(src[None, None, :], pix, R)
+    vol = F.fbp(2, views, (n, n, n), 1.0, n_u, n_v, du, du, sino, window="hann")
+    c = _radius_grid(n, 1.0)
+    Z, Y, X = np.meshgrid(c, c, c, indexing="ij")
+    r = np.sqrt(X * X + Y * Y + Z * Z)
+    central = np.abs(Z) < 1.0
+    assert abs(np.median(vol[central & (r < 0.7 * R)]) - 1.0) < 0.02
+    assert abs(np.median(vol[r < 0.7 * R]) - 1.0) < 0.03
+    fov = 0.95 * (n_u - 1) / 2 * du * sid / sdd
+    rxy = np.sqrt(X * X + Y * Y)
+    assert np.abs(vol[(r > 1.4 * R) & (rxy < fov) & central]).max() < 0.1
