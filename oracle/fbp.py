@@ -69,9 +69,14 @@ def _frames(beam: int, rec: np.ndarray):
     return first, ctr, u, v, n
 
 
-def fbp(beam: int, views: np.ndarray, vol_shape, spacing: float, n_u: int, n_v: int, du: float,
-        dv: float, sino: np.ndarray, window: str = "ram-lak", view_weights=None, isocenter=None):
-    """Filtered backprojection of `sino` ((views, U) or (views, U, V)) onto the volume grid."""
+def fbp(beam: int, views: np.ndarray, vol_shape, spacing, n_u: int, n_v: int, du: float,
+        dv: float, sino: np.ndarray, window: str = "ram-lak", view_weights=None, isocenter=None,
+        voxels=None):
+    """Filtered backprojection of `sino` ((views, U) or (views, U, V)) onto the volume grid.
+
+    `spacing` is one pitch or per-axis pitches in tensor order ((dz, dy, dx), 2D (dy, dx)); voxel
+    centres sit at (i + 1/2 - n/2) * pitch on each axis.  With `voxels` (an (m, 3) array of
+    (iz, iy, ix) indices) only those voxels are reconstructed and an (m,) array is returned."""
     assert beam in (0, 1, 2), "parallel (2D), fan (2D) and cone beams"
     two_d = beam in (0, 1)
     nz, ny, nx = vol_shape
@@ -85,12 +90,18 @@ def fbp(beam: int, views: np.ndarray, vol_shape, spacing: float, n_u: int, n_v: 
     uu = (np.arange(n_u) - cu) * du
     vv = (np.arange(V) - cv) * dv if not two_d else np.zeros(1)
     taps = ramp_taps(n_u, du, window)
+    sp = np.broadcast_to(np.asarray(spacing, dtype=np.float64), (2 if two_d else 3,))
+    sz, sy, sx = (1.0, sp[0], sp[1]) if two_d else (sp[0], sp[1], sp[2])
     # voxel centres
-    zs = (np.arange(nz) + 0.5 - nz / 2.0) * spacing if not two_d else np.zeros(1)
-    ys = (np.arange(ny) + 0.5 - ny / 2.0) * spacing
-    xs = (np.arange(nx) + 0.5 - nx / 2.0) * spacing
-    Z, Y, X = np.meshgrid(zs, ys, xs, indexing="ij")
-    P = np.stack([X, Y, Z], axis=-1)                               # (nz|1, ny, nx, 3)
+    zs = (np.arange(nz) + 0.5 - nz / 2.0) * sz if not two_d else np.zeros(1)
+    ys = (np.arange(ny) + 0.5 - ny / 2.0) * sy
+    xs = (np.arange(nx) + 0.5 - nx / 2.0) * sx
+    if voxels is None:
+        Z, Y, X = np.meshgrid(zs, ys, xs, indexing="ij")
+        P = np.stack([X, Y, Z], axis=-1)                           # (nz|1, ny, nx, 3)
+    else:
+        vi = np.asarray(voxels, dtype=np.int64).reshape(-1, 3)
+        P = np.stack([xs[vi[:, 2]], ys[vi[:, 1]], zs[vi[:, 0]]], axis=-1)[None, None]  # (1,1,m,3)
     out = np.zeros(P.shape[:3])
     for k in range(n_views):
         first, ctr, u, v, n = _frames(beam, views[k])
@@ -116,6 +127,8 @@ def fbp(beam: int, views: np.ndarray, vol_shape, spacing: float, n_u: int, n_v: 
             Uw = den / ((iso - first) @ n)
             g = (abs(D) / abs((iso - first) @ n)) / (Uw * Uw)
         out += w[k] * g * _bilinear(Q, upix, vpix)
+    if voxels is not None:
+        return out[0, 0]
     return out[0] if two_d else out
 
 
