@@ -48,12 +48,18 @@ def ramp_taps(n_u: int, tau: float, window: str) -> np.ndarray:
     """h(n tau) for n = -(n_u - 1) .. n_u - 1, by quadrature of the band-limited windowed ramp."""
     from scipy.integrate import quad
     F = 0.5 / tau
+
+    def g(f):
+        return f * window_response(window, np.array([f]), tau)[0]
+
     taps = np.zeros(2 * n_u - 1)
     for n in range(n_u):
         x = n * tau
-        val, _ = quad(lambda f: f * window_response(window, np.array([f]), tau)[0]
-                      * math.cos(2 * math.pi * f * x), 0.0, F, limit=400,
-                      weight=None, epsabs=1e-14, epsrel=1e-12)
+        if n == 0:
+            val, _ = quad(g, 0.0, F, limit=400, epsabs=1e-14, epsrel=1e-12)
+        else:  # the cos(2 pi f x) factor as the rule's oscillatory weight (QAWO)
+            val, _ = quad(g, 0.0, F, weight="cos", wvar=2 * math.pi * x, limit=400,
+                          epsabs=1e-14)
         taps[n_u - 1 + n] = taps[n_u - 1 - n] = 2.0 * val
     return taps
 

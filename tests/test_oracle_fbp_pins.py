@@ -17,15 +17,15 @@ from fan_beam_projector_siddon_b300 import workloads as W
 from oracle import fbp as F
 
 
-@pytest.mark.parametrize("tau", [1.0, 0.5, 1.3])
-def test_ramlak_and_shepp_logan_taps_match_closed_forms(tau):
-    n = np.arange(-9, 10)
-    h = F.ramp_taps(10, tau, "ram-lak")
+@pytest.mark.parametrize("tau,n_u", [(1.0, 10), (0.5, 10), (1.3, 10), (1.2, 384)])
+def test_ramlak_and_shepp_logan_taps_match_closed_forms(tau, n_u):
+    n = np.arange(-(n_u - 1), n_u)
+    h = F.ramp_taps(n_u, tau, "ram-lak")
     nn = np.where(n == 0, 1, n).astype(float)
     want = np.where(n == 0, 1.0 / (4 * tau * tau),
                     np.where(n % 2 == 0, 0.0, -1.0 / (np.pi ** 2 * nn ** 2 * tau ** 2)))
     np.testing.assert_allclose(h, want, rtol=1e-9, atol=1e-12 / tau ** 2)
-    h = F.ramp_taps(10, tau, "shepp-logan")
+    h = F.ramp_taps(n_u, tau, "shepp-logan")
     want = -2.0 / (np.pi ** 2 * tau ** 2 * (4 * n.astype(float) ** 2 - 1))
     np.testing.assert_allclose(h, want, rtol=1e-9, atol=1e-12 / tau ** 2)
 
