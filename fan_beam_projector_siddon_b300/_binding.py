@@ -20,6 +20,7 @@ STATUS_NAMES = ["CT_OK", "CT_ERR_INVALID_ARGUMENT", "CT_ERR_INVALID_GEOMETRY",
                 "CT_ERR_NOT_DEVICE_POINTER", "CT_ERR_ALIASING", "CT_ERR_OUT_OF_MEMORY",
                 "CT_ERR_CUDA", "CT_ERR_WORKSPACE"]
 CT_OK = 0
+FBP_WINDOWS = {"ram-lak": 0, "shepp-logan": 1, "cosine": 2, "hamming": 3, "hann": 4}
 
 
 class CtError(RuntimeError):
@@ -89,6 +90,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.ct_cgls_iterate.restype = i32
     L.ct_backproject_static.argtypes = [vp, vp, vp, vp]
     L.ct_backproject_static.restype = i32
+    L.ct_fbp_workspace_bytes.argtypes = [vp]
+    L.ct_fbp_workspace_bytes.restype = sz
+    L.ct_fbp.argtypes = [vp, vp, vp, vp, ctypes.POINTER(f64), i32, vp, sz, vp]
+    L.ct_fbp.restype = i32
     L.ct_status_string.argtypes = [i32]
     L.ct_status_string.restype = ctypes.c_char_p
     _lib = L
@@ -220,6 +225,25 @@ def ct_cgls_iterate(handle: int, d_x: int, d_y: int, d_workspace: int, workspace
     _check(load_library().ct_cgls_iterate(handle, d_x, d_y, d_workspace, workspace_bytes,
                                           int(n_iters), 1 if workspace_initialised else 0,
                                           stream), "ct_cgls_iterate")
+
+
+def ct_fbp_workspace_bytes(handle: int) -> int:
+    return int(load_library().ct_fbp_workspace_bytes(handle))
+
+
+def ct_fbp(handle: int, d_sino: int, d_volume: int, d_view_weights: int | None, isocenter,
+           window, d_workspace: int, workspace_bytes: int, stream: int | None) -> None:
+    """Filtered backprojection; ``window`` is a name of ``FBP_WINDOWS`` or its code and
+    ``isocenter`` a host 3-vector or None."""
+    code = FBP_WINDOWS[window] if isinstance(window, str) else int(window)
+    iso = None
+    if isocenter is not None:
+        arr = np.zeros(3, dtype=np.float64)
+        vals = np.asarray(isocenter, dtype=np.float64).ravel()
+        arr[:len(vals)] = vals
+        iso = arr.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+    _check(load_library().ct_fbp(handle, d_sino, d_volume, d_view_weights, iso, code,
+                                 d_workspace, workspace_bytes, stream), "ct_fbp")
 
 
 def ct_status_string(status: int) -> str:
@@ -377,3 +401,32 @@ class Geometry:
         ct_sirt_iterate(self.handle, x.data_ptr(), y.data_ptr(), ws, wsb, n_iters, relaxation,
                         initialised, self._stream(stream))
         return x
+
+    def fbp(self, sino, out=None, window="ram-lak", view_weights=None, isocenter=None,
+            workspace=None, stream=None):
+        """Filtered backprojection (FBP / FDK) of a sinogram; leading dimensions are kept and
+        reconstructed one after another with the same workspace."""
+        import torch
+        assert sino.is_cuda and sino.dtype == torch.float32 and sino.is_contiguous()
+        nd = len(self.sino_shape)
+        assert tuple(sino.shape[sino.dim() - nd:]) == tuple(self.sino_shape)
+        lead = tuple(sino.shape[:sino.dim() - nd])
+        if out is None:
+            out = torch.empty(lead + tuple(self.volume_shape), dtype=torch.float32,
+                              device=sino.device)
+        need = ct_fbp_workspace_bytes(self.handle)
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=sino.device)
+        ws, wsb = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+        wptr = None
+        if view_weights is not None:
+            view_weights = torch.as_tensor(view_weights, dtype=torch.float32,
+                                           device=sino.device).contiguous()
+            assert view_weights.numel() == self.info.n_views
+            wptr = view_weights.data_ptr()
+        s2 = sino.reshape((-1,) + tuple(self.sino_shape))
+        o2 = out.view((-1,) + tuple(self.volume_shape))
+        for b in range(s2.shape[0]):
+            ct_fbp(self.handle, s2[b].data_ptr(), o2[b].data_ptr(), wptr, isocenter, window,
+                   ws, wsb, self._stream(stream))
+        return out

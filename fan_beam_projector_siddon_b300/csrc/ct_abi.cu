@@ -22,6 +22,7 @@ struct ct_geometry {
     ct::Tiling tiling;
     ct::ViewRec* d_views;   // device table, n_views records
     double* d_offsets;      // surface detectors: device (n_u, n_v, 3) offsets; else nullptr
+    double* d_raw;          // device copy of the caller's view records (physical units)
     std::vector<double> host_views;
 };
 
@@ -390,6 +391,9 @@ ct_status create_impl(ct_beam beam, int32_t n_views, const double* views, int32_
     if (e == cudaSuccess)
         e = cudaMemcpy(g->d_views, recs.data(), sizeof(ct::ViewRec) * (size_t)n_views,
                        cudaMemcpyHostToDevice);
+    const size_t raw_bytes = sizeof(double) * (size_t)n_views * (size_t)w;
+    if (e == cudaSuccess) e = cudaMalloc(&g->d_raw, raw_bytes);
+    if (e == cudaSuccess) e = cudaMemcpy(g->d_raw, views, raw_bytes, cudaMemcpyHostToDevice);
     const size_t off_bytes = sizeof(double) * 3 * (size_t)n_u * (size_t)n_v;
     if (e == cudaSuccess && surface) e = cudaMalloc(&g->d_offsets, off_bytes);
     if (e == cudaSuccess && surface)
@@ -398,6 +402,7 @@ ct_status create_impl(ct_beam beam, int32_t n_views, const double* views, int32_
         cudaGetLastError();
         if (g->d_views) cudaFree(g->d_views);
         if (g->d_offsets) cudaFree(g->d_offsets);
+        if (g->d_raw) cudaFree(g->d_raw);
         delete g;
         return from_cuda(e);
     }
@@ -436,6 +441,10 @@ ct_status ct_geometry_destroy(ct_geometry* g) {
     if (g->d_views) e = cudaFree(g->d_views);
     if (g->d_offsets) {
         const cudaError_t e2 = cudaFree(g->d_offsets);
+        if (e == cudaSuccess) e = e2;
+    }
+    if (g->d_raw) {
+        const cudaError_t e2 = cudaFree(g->d_raw);
         if (e == cudaSuccess) e = e2;
     }
     delete g;
@@ -738,4 +747,83 @@ extern "C" ct_status ct_backproject_static(const ct_geometry* g, const float* d_
         e = ct::launch_backproject(g->d_views, g->grid, g->tiling, d_sino, acc, stream);
     if (e == cudaSuccess) e = from_internal(g, acc, d_volume, stream);
     return from_cuda(e);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Filtered backprojection.
+
+namespace {
+
+struct FbpLayout {
+    size_t views, taps, filtered, total;
+};
+
+FbpLayout fbp_layout(const ct_geometry* g) {
+    FbpLayout L;
+    L.views = 0;
+    L.taps = align_up(sizeof(ct::FbpView) * (size_t)g->info.n_views);
+    L.filtered = L.taps + align_up(sizeof(float) * (size_t)(2 * g->info.n_u - 1));
+    L.total = L.filtered + align_up(sino_bytes(g));
+    return L;
+}
+
+constexpr int32_t kFbpMaxU = 16384;
+
+}  // namespace
+
+extern "C" size_t ct_fbp_workspace_bytes(const ct_geometry* g) {
+    return g == nullptr ? 0 : fbp_layout(g).total;
+}
+
+extern "C" ct_status ct_fbp(const ct_geometry* g, const float* d_sino, float* d_volume,
+                            const float* d_view_weights, const double* isocenter,
+                            ct_fbp_window window, void* d_workspace, size_t workspace_bytes,
+                            cudaStream_t stream) {
+    if (g == nullptr) return CT_ERR_INVALID_ARGUMENT;
+    const int b = g->info.beam;
+    if (b == CT_PARALLEL3D || g->d_offsets != nullptr) return CT_ERR_INVALID_ARGUMENT;
+    if ((int)window < CT_WINDOW_RAM_LAK || (int)window > CT_WINDOW_HANN)
+        return CT_ERR_INVALID_ARGUMENT;
+    if (g->info.n_u > kFbpMaxU) return CT_ERR_INVALID_ARGUMENT;
+    // gather grid limits: 3D (ceil(nz/32), ceil(nx/8), ny), 2D (ceil(nx/32), ceil(ny/8))
+    if (is_2d(b) ? (g->info.ny + 7) / 8 > 65535
+                 : (g->info.nx + 7) / 8 > 65535 || g->info.ny > 65535)
+        return CT_ERR_INVALID_ARGUMENT;
+    double iso[3] = {0.0, 0.0, 0.0};
+    if (isocenter != nullptr) {
+        for (int a = 0; a < (is_2d(b) ? 2 : 3); ++a) {
+            if (!std::isfinite(isocenter[a])) return CT_ERR_INVALID_ARGUMENT;
+            iso[a] = isocenter[a];
+        }
+    }
+    const FbpLayout L = fbp_layout(g);
+    ct_status st = check_call(g, d_sino, sino_bytes(g), d_volume, volume_bytes(g), d_workspace,
+                              workspace_bytes, L.total);
+    if (st != CT_OK) return st;
+    const size_t wbytes = sizeof(float) * (size_t)g->info.n_views;
+    if (d_view_weights != nullptr) {
+        if ((st = check_device_ptr(d_view_weights, g->device)) != CT_OK) return st;
+        if (overlap(d_view_weights, wbytes, d_volume, volume_bytes(g)) ||
+            overlap(d_view_weights, wbytes, d_workspace, L.total))
+            return CT_ERR_ALIASING;
+    }
+    ct::FbpParams P;
+    P.n_views = g->info.n_views;
+    P.n_u = g->info.n_u;
+    P.n_v = g->info.n_v;
+    P.nx = g->info.nx; P.ny = g->info.ny; P.nz = g->info.nz;
+    P.two_d = is_2d(b) ? 1 : 0;
+    P.parallel = is_parallel(b) ? 1 : 0;
+    P.window = (int32_t)window;
+    P.du = g->du;
+    P.dv = g->dv;
+    for (int a = 0; a < 3; ++a) P.iso[a] = iso[a];
+    P.sx = g->grid.sp[0];
+    P.sy = g->grid.sp[1];
+    P.sz = g->grid.sp[2];
+    char* ws = static_cast<char*>(d_workspace);
+    return from_cuda(ct::launch_fbp(P, g->d_raw, d_view_weights,
+                                    reinterpret_cast<ct::FbpView*>(ws + L.views),
+                                    reinterpret_cast<float*>(ws + L.taps), d_sino,
+                                    reinterpret_cast<float*>(ws + L.filtered), d_volume, stream));
 }

@@ -96,4 +96,39 @@ cudaError_t launch_sirt_update(float* x, float* b, const float* c, float relax, 
 cudaError_t launch_transpose(const float* in, float* out, int64_t rows, int64_t cols,
                              int64_t batch, cudaStream_t stream);
 
+// Filtered backprojection (kernels in fbp_kernels.cu).  Physical units, origin at the volume
+// centre (the caller's frame, not the Siddon kernels' voxel frame).
+enum FbpWindow : int32_t {
+    FBP_RAM_LAK = 0,
+    FBP_SHEPP_LOGAN = 1,
+    FBP_COSINE = 2,
+    FBP_HAMMING = 3,
+    FBP_HANN = 4,
+};
+struct FbpParams {
+    int32_t n_views, n_u, n_v;
+    int32_t nx, ny, nz;
+    int32_t two_d, parallel, window;
+    double du, dv;
+    double iso[3];
+    float sx, sy, sz;  // voxel pitches along x, y, z
+};
+// Per-view constants computed on the device by the preparation kernel.
+struct FbpView {
+    float s[3];    // source (fan/cone)
+    float n[3];    // detector normal
+    float eu[3];   // det_u / du
+    float ev[3];   // det_v / dv (cone)
+    float pc[3];   // pixel (0, 0) minus source, for the cosine weights
+    float pdu[3];  // du det_u
+    float pdv[3];  // dv det_v
+    float D;       // (c - s) . n
+    float ku0, kv0;  // additive terms of the fractional pixel indices
+    float wg;      // view weight times the constant part of the distance weight
+};
+// Workspace: views (n_views FbpView), taps (2 n_u - 1 floats), filtered sinogram.
+cudaError_t launch_fbp(const FbpParams& p, const double* raw_views, const float* view_weights,
+                       FbpView* views, float* taps, const float* sino, float* filtered,
+                       float* vol, cudaStream_t stream);
+
 }  // namespace ct

@@ -265,6 +265,54 @@ CT_API ct_status ct_cgls_iterate(const ct_geometry *geom, float *d_x, const floa
 CT_API ct_status ct_backproject_static(const ct_geometry *geom, const float *d_sino,
                                        float *d_volume, struct CUstream_st *stream);
 
+/*
+ * Filtered backprojection: parallel-beam FBP (CT_PARALLEL2D), fan-beam FBP (CT_FAN2D) and
+ * Feldkamp-Davis-Kress cone-beam reconstruction (CT_CONE), on flat detectors.  The pages list the
+ * stages (diffct "Differentiable analytical reconstruction" and the FBP/FDK example pages:
+ * detector cosine weights, a ramp filter with physical sample spacing and an optional window,
+ * angular integration weights and a voxel-driven distance-weighted gather) without formulas;
+ * this is the textbook form:
+ *
+ *   1. fan/cone: p'(u, v) = p(u, v) |(c - s) . n| / |P(u, v) - s|   (s source, c detector
+ *      centre, n detector normal, P the pixel);
+ *   2. Q(u_i, v) = du sum_j h((i - j) du) p'(u_j, v), the band-limited ramp
+ *      h(x) = 2 int_0^{1/(2 du)} f W(f) cos(2 pi f x) df with window W (ct_fbp_window), as a
+ *      linear convolution along u (no wrap-around);
+ *   3. f(X) = sum_k w_k g_k(X) Q_k(u_k(X), v_k(X)): X projected onto view k's detector through
+ *      the source (parallel: along the ray), Q interpolated bilinearly (0 off the detector),
+ *      g = 1 for parallel beams, else g = (D_sd / D_so) / U(X)^2 with
+ *      U(X) = ((X - s) . n) / ((iso - s) . n), D_so = |(iso - s) . n|, D_sd = |(c - s) . n|.
+ *
+ * This is an approximate inverse, not the Siddon adjoint.  Voxel centres as in the frame above
+ * (per-axis pitches of ct_geometry_create_ex are honoured).
+ *
+ * d_sino       device sinogram, read only.
+ * d_volume     device volume, overwritten.
+ * d_view_weights  device, n_views floats, or NULL for the uniform full-scan quadrature
+ *              w_k = pi / n_views (a 180-degree parallel scan, or a 360-degree fan/cone scan with
+ *              the 1/2 redundancy factor).  Short scans pass their own (e.g. Parker) weights.
+ * isocenter    host, 3 doubles (x, y, z; z ignored in 2D), or NULL for the origin: the point
+ *              whose detector-plane distance sets D_so.
+ * Workspace: at least ct_fbp_workspace_bytes(geom) (the filtered sinogram, per-view constants
+ * and the filter taps).
+ * Errors: CT_ERR_INVALID_ARGUMENT for CT_PARALLEL3D, surface detectors, an unknown window, or
+ * n_u > 16384, or a grid beyond the gather launch (3D: ny > 65535 or nx > 524280; 2D:
+ * ny > 524280); otherwise as ct_backproject.
+ */
+typedef enum {
+    CT_WINDOW_RAM_LAK = 0,     /* W(f) = 1                                          */
+    CT_WINDOW_SHEPP_LOGAN = 1, /* W(f) = sin(pi f du) / (pi f du)                   */
+    CT_WINDOW_COSINE = 2,      /* W(f) = cos(pi f du)                               */
+    CT_WINDOW_HAMMING = 3,     /* W(f) = 0.54 + 0.46 cos(2 pi f du)                 */
+    CT_WINDOW_HANN = 4         /* W(f) = 0.5 + 0.5 cos(2 pi f du)                   */
+} ct_fbp_window;
+
+CT_API size_t ct_fbp_workspace_bytes(const ct_geometry *geom);
+CT_API ct_status ct_fbp(const ct_geometry *geom, const float *d_sino, float *d_volume,
+                        const float *d_view_weights, const double *isocenter,
+                        ct_fbp_window window, void *d_workspace, size_t workspace_bytes,
+                        struct CUstream_st *stream);
+
 /* Static, human-readable name of a status code. */
 CT_API const char *ct_status_string(ct_status status);
 

@@ -1,0 +1,176 @@
+"""Filtered backprojection (FBP / FDK) through the C ABI against the float64 oracle (oracle/fbp.py).
+
+Tolerance.  The GPU path filters and gathers in float32; the oracle in float64.  The gather's
+fractional detector index u(X) carries a float32 rounding error of a few ulp of the largest
+coordinate involved (about 1e-6 pixel for these sizes); the ramp-filtered sinogram changes by at
+most ~2 max|Q| per pixel, and the filter's float32 sums of n_u terms add ~n_u eps relative to
+sum|h p|.  Over a whole volume both stay below 1e-4 of the result's L2 norm, so small cases are
+compared at rel L2 <= 2e-4 and max |diff| <= 2e-3 max |f|; sampled voxels of the full-size cone
+case at max |diff| <= 2e-3 max |f|.
+"""
+import math
+
+import numpy as np
+import pytest
+
+from fan_beam_projector_siddon_b300 import workloads as W
+from oracle import fbp as F
+from tests._parity import rel_l2, torch_cuda
+
+pytestmark = pytest.mark.gpu
+
+REL_L2 = 2e-4
+MAX_REL = 2e-3
+
+
+@pytest.fixture(scope="module")
+def ct():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from fan_beam_projector_siddon_b300 import build
+    build.build()
+    import fan_beam_projector_siddon_b300 as ct
+    return ct
+
+
+def _cpu(t):
+    import torch
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+def _oracle(w, sino, **kw):
+    return F.fbp(w.beam, w.views, w.vol_shape, w.voxel_spacing, w.n_u, w.n_v, w.du, w.dv, sino,
+                 **kw)
+
+
+def _check(got, want):
+    err = rel_l2(got, want)
+    mx = float(np.abs(got - want).max()) / max(float(np.abs(want).max()), 1e-30)
+    assert err <= REL_L2 and mx <= MAX_REL, (err, mx)
+
+
+def _phantom_sino(w):
+    """Sinogram of the workload's phantom by the oracle's own Siddon projector (float64)."""
+    import oracle
+    return oracle.Geometry.from_workload(w).project(w.phantom(), threads=8)
+
+
+@pytest.mark.parametrize("n", [1, 2, 3])
+def test_small_phantom_matches_oracle(ct, n):
+    w = W.small_config(n)
+    sino = _phantom_sino(w)
+    g = ct.Geometry.from_workload(w)
+    got = _cpu(g.fbp(torch_cuda(sino.astype(np.float32))))
+    want = _oracle(w, sino.astype(np.float32).astype(np.float64))
+    _check(got, want)
+
+
+@pytest.mark.parametrize("window", ["ram-lak", "shepp-logan", "cosine", "hamming", "hann"])
+@pytest.mark.parametrize("n", [2, 3])
+def test_windows_on_random_sinograms(ct, n, window):
+    w = W.small_config(n)
+    sino = W.random_sinogram(w, 40 + n)
+    g = ct.Geometry.from_workload(w)
+    got = _cpu(g.fbp(torch_cuda(sino), window=window))
+    _check(got, _oracle(w, sino.astype(np.float64), window=window))
+
+
+@pytest.mark.parametrize("n", [2, 3])
+def test_view_weights_and_isocentre(ct, n):
+    w = W.small_config(n)
+    sino = W.random_sinogram(w, 7)
+    wts = np.random.default_rng(8).uniform(0.0, 0.05, size=w.views.shape[0]).astype(np.float32)
+    iso = (1.5, -2.25, 0.75)[: 2 if n == 2 else 3]
+    g = ct.Geometry.from_workload(w)
+    got = _cpu(g.fbp(torch_cuda(sino), window="hann", view_weights=torch_cuda(wts),
+                     isocenter=iso))
+    want = _oracle(w, sino.astype(np.float64), window="hann",
+                   view_weights=wts.astype(np.float64), isocenter=iso)
+    _check(got, want)
+
+
+@pytest.mark.parametrize("kind", ["cone", "fan"])
+def test_anisotropic_voxels(ct, kind):
+    w = W.anisotropic_config(kind)
+    sino = W.random_sinogram(w, 11)
+    g = ct.Geometry.from_workload(w)
+    got = _cpu(g.fbp(torch_cuda(sino)))
+    _check(got, _oracle(w, sino.astype(np.float64)))
+
+
+def test_full_size_cone_sampled_voxels(ct):
+    """The 256^3, 360-view cone workload (the benchmark's), sampled voxels against the oracle."""
+    w = W.config(3)
+    sino = W.random_sinogram(w, 5)
+    g = ct.Geometry.from_workload(w)
+    got = _cpu(g.fbp(torch_cuda(sino)))
+    rng = np.random.default_rng(6)
+    idx = np.stack([rng.integers(0, s, 48) for s in w.vol_shape], axis=1)
+    idx = np.concatenate([idx, [[0, 0, 0], [255, 255, 255], [128, 0, 255]]])
+    want = _oracle(w, sino.astype(np.float64), voxels=idx)
+    scale = float(np.abs(got).max())
+    diff = np.abs(got[idx[:, 0], idx[:, 1], idx[:, 2]] - want)
+    assert diff.max() <= MAX_REL * scale, (diff.max(), scale)
+
+
+def test_batch_dims_and_determinism(ct):
+    w = W.small_config(3)
+    s = np.stack([W.random_sinogram(w, 1), W.random_sinogram(w, 2)])
+    g = ct.Geometry.from_workload(w)
+    st = torch_cuda(s)
+    a = _cpu(g.fbp(st))
+    b = _cpu(g.fbp(st))
+    assert np.array_equal(a, b)
+    one = _cpu(g.fbp(torch_cuda(s[1])))
+    assert np.array_equal(a[1], one)
+
+
+def test_linearity(ct):
+    w = W.small_config(2)
+    a, b = W.random_sinogram(w, 3), W.random_sinogram(w, 4)
+    g = ct.Geometry.from_workload(w)
+    fa, fb = _cpu(g.fbp(torch_cuda(a))), _cpu(g.fbp(torch_cuda(b)))
+    fab = _cpu(g.fbp(torch_cuda(2.0 * a - b)))
+    assert rel_l2(fab, 2.0 * fa - fb) < 1e-5
+
+
+def test_errors(ct):
+    import torch
+    w = W.small_config(3)
+    g = ct.Geometry.from_workload(w)
+    sino = torch.zeros(g.sino_shape, device="cuda")
+    vol = torch.zeros(g.volume_shape, device="cuda")
+    need = ct.ct_fbp_workspace_bytes(g.handle)
+    assert need >= 4 * sino.numel()
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+
+    def call(status, **kw):
+        args = dict(d_sino=sino.data_ptr(), d_volume=vol.data_ptr(), d_view_weights=None,
+                    isocenter=None, window=0, d_workspace=ws.data_ptr(), workspace_bytes=need)
+        args.update(kw)
+        with pytest.raises(ct.CtError) as ei:
+            ct.ct_fbp(g.handle, args["d_sino"], args["d_volume"], args["d_view_weights"],
+                      args["isocenter"], args["window"], args["d_workspace"],
+                      args["workspace_bytes"], s)
+        assert ei.value.status == status
+
+    call(7, workspace_bytes=need - 1)
+    call(1, window=5)
+    call(1, isocenter=(math.nan, 0.0, 0.0))
+    call(4, d_volume=ws.data_ptr())
+    host = np.zeros(4, np.float32)
+    call(3, d_view_weights=host.ctypes.data)
+    # parallel3d and surface detectors have no FBP here
+    p = W.small_config(5)
+    gp = ct.Geometry.from_workload(p)
+    with pytest.raises(ct.CtError) as ei:
+        gp.fbp(torch.zeros(gp.sino_shape, device="cuda"))
+    assert ei.value.status == 1
+    c = W.curved_config("cone")
+    gc = ct.Geometry.from_workload(c)
+    with pytest.raises(ct.CtError) as ei:
+        gc.fbp(torch.zeros(gc.sino_shape, device="cuda"))
+    assert ei.value.status == 1
