@@ -755,15 +755,20 @@ extern "C" ct_status ct_backproject_static(const ct_geometry* g, const float* d_
 namespace {
 
 struct FbpLayout {
-    size_t views, taps, filtered, total;
+    int32_t rows, cols;  // padded filtered sinogram of one view
+    size_t views, cosines, taps, filtered, total;
 };
 
 FbpLayout fbp_layout(const ct_geometry* g) {
     FbpLayout L;
+    const size_t nv = (size_t)g->info.n_views;
+    L.rows = g->info.n_u + 3;
+    L.cols = is_2d(g->info.beam) ? 1 : g->info.n_v + 3;
     L.views = 0;
-    L.taps = align_up(sizeof(ct::FbpView) * (size_t)g->info.n_views);
+    L.cosines = align_up(sizeof(ct::FbpView) * nv);
+    L.taps = L.cosines + align_up(sizeof(ct::FbpCosine) * nv);
     L.filtered = L.taps + align_up(sizeof(float) * (size_t)(2 * g->info.n_u - 1));
-    L.total = L.filtered + align_up(sino_bytes(g));
+    L.total = L.filtered + align_up(sizeof(float) * nv * (size_t)L.rows * (size_t)L.cols);
     return L;
 }
 
@@ -815,6 +820,8 @@ extern "C" ct_status ct_fbp(const ct_geometry* g, const float* d_sino, float* d_
     P.two_d = is_2d(b) ? 1 : 0;
     P.parallel = is_parallel(b) ? 1 : 0;
     P.window = (int32_t)window;
+    P.rows = L.rows;
+    P.cols = L.cols;
     P.du = g->du;
     P.dv = g->dv;
     for (int a = 0; a < 3; ++a) P.iso[a] = iso[a];
@@ -824,6 +831,7 @@ extern "C" ct_status ct_fbp(const ct_geometry* g, const float* d_sino, float* d_
     char* ws = static_cast<char*>(d_workspace);
     return from_cuda(ct::launch_fbp(P, g->d_raw, d_view_weights,
                                     reinterpret_cast<ct::FbpView*>(ws + L.views),
+                                    reinterpret_cast<ct::FbpCosine*>(ws + L.cosines),
                                     reinterpret_cast<float*>(ws + L.taps), d_sino,
                                     reinterpret_cast<float*>(ws + L.filtered), d_volume, stream));
 }

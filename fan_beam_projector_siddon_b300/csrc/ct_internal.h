@@ -109,26 +109,40 @@ struct FbpParams {
     int32_t n_views, n_u, n_v;
     int32_t nx, ny, nz;
     int32_t two_d, parallel, window;
+    int32_t rows, cols;  // padded filtered sinogram per view: rows = n_u + 3, cols = n_v + 3 (2D: 1)
     double du, dv;
     double iso[3];
     float sx, sy, sz;  // voxel pitches along x, y, z
 };
-// Per-view constants computed on the device by the preparation kernel.
+// Per-view constants of the gather (64 bytes, read as four float4).
 struct FbpView {
-    float s[3];    // source (fan/cone)
-    float n[3];    // detector normal
-    float eu[3];   // det_u / du
-    float ev[3];   // det_v / dv (cone)
-    float pc[3];   // pixel (0, 0) minus source, for the cosine weights
+    float s[3];      // source (fan/cone)
+    float n[3];      // detector normal
+    float eu[3];     // det_u / du
+    float ev[3];     // det_v / dv (cone)
+    float D;         // (c - s) . n
+    float ku0, kv0;  // additive terms of the fractional pixel indices
+    float wg;        // view weight times the constant part of the distance weight
+};
+static_assert(sizeof(FbpView) == 64, "FbpView layout");
+// Per-view constants of the cosine pre-weights (48 bytes).
+struct FbpCosine {
+    float pc[3];   // pixel (0, 0) minus source
     float pdu[3];  // du det_u
     float pdv[3];  // dv det_v
-    float D;       // (c - s) . n
-    float ku0, kv0;  // additive terms of the fractional pixel indices
-    float wg;      // view weight times the constant part of the distance weight
+    float D;       // |(c - s) . n|
+    float pad[2];
 };
-// Workspace: views (n_views FbpView), taps (2 n_u - 1 floats), filtered sinogram.
+static_assert(sizeof(FbpCosine) == 48, "FbpCosine layout");
+// Filtered sinogram layout: view k, pixel (u, v) at
+//     filtered[(k * rows + u + 1) * cols + v + 1]            (3D)
+//     filtered[k * rows + u + 1]                             (2D)
+// with zero pads one pixel before and two after each axis, so that a bilinear read at any index
+// clamped to [-1, n] stays in bounds and reads 0 off the detector.
+// Scratch: views (n_views FbpView), cosine records (n_views FbpCosine), taps (2 n_u - 1 floats),
+// filtered sinogram (n_views * rows * cols floats).
 cudaError_t launch_fbp(const FbpParams& p, const double* raw_views, const float* view_weights,
-                       FbpView* views, float* taps, const float* sino, float* filtered,
-                       float* vol, cudaStream_t stream);
+                       FbpView* views, FbpCosine* cosines, float* taps, const float* sino,
+                       float* filtered, float* vol, cudaStream_t stream);
 
 }  // namespace ct

@@ -7,10 +7,15 @@
 //   2. filter taps of the band-limited ramp with the chosen window, closed forms in float64
 //      (same kernel);
 //   3. per detector column: cosine pre-weight and linear convolution along u with the taps,
-//      columns staged in shared memory (fbp_filter_kernel);
+//      columns staged in shared memory, written into a zero-padded filtered sinogram
+//      (fbp_filter_blocked_kernel: 32 columns a block, 16 outputs a thread held in registers;
+//      fbp_filter_kernel for 2D and very wide detectors);
 //   4. voxel-driven gather: project each voxel centre onto every view's detector, interpolate
-//      the filtered sinogram bilinearly (0 outside), apply the distance weight and the view
-//      weight, sum over views (fbp_gather_kernel).
+//      the filtered sinogram bilinearly (0 outside, read from the pads without branches), apply
+//      the distance weight and the view weight, sum over views (fdk_gather_kernel,
+//      fbp2d_gather_kernel).  Per-view constants are staged in shared memory; each thread keeps
+//      several voxels along one axis so that the constants and the voxel-independent parts of
+//      the projection are loaded and computed once per view.
 // This operator is not the Siddon adjoint; it is a separate, approximate inverse.
 #include "ct_internal.h"
 
@@ -51,10 +56,22 @@ __device__ double ramp_tap(int window, double x, double tau) {
     }
 }
 
-// One thread per view (its FbpView) and one thread per filter tap, over one flat grid.
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ int64_t qrow(const FbpParams& p, int view, int u) {
+    return ((int64_t)view * p.rows + u + 1) * p.cols;
+}
+
+// One thread per view (its FbpView and FbpCosine) and one thread per filter tap, over one flat
+// grid.
 __global__ void fbp_prepare_kernel(FbpParams p, const double* __restrict__ raw,
                                    const float* __restrict__ user_weights,
-                                   FbpView* __restrict__ out_views, float* __restrict__ taps) {
+                                   FbpView* __restrict__ out_views,
+                                   FbpCosine* __restrict__ out_cos, float* __restrict__ taps) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     const int n_taps = 2 * p.n_u - 1;
     if (i < n_taps) {
@@ -71,14 +88,18 @@ __global__ void fbp_prepare_kernel(FbpParams p, const double* __restrict__ raw,
         v[0] = 0.0; v[1] = 0.0; v[2] = 1.0;
         n[0] = u[1]; n[1] = -u[0]; n[2] = 0.0;
     } else {
-        for (int a = 0; a < 3; ++a) { s[a] = r[a]; c[a] = r[3 + a]; u[a] = r[6 + a]; v[a] = r[9 + a]; }
+        for (int a = 0; a < 3; ++a) {
+            s[a] = r[a]; c[a] = r[3 + a]; u[a] = r[6 + a]; v[a] = r[9 + a];
+        }
         n[0] = u[1] * v[2] - u[2] * v[1];
         n[1] = u[2] * v[0] - u[0] * v[2];
         n[2] = u[0] * v[1] - u[1] * v[0];
     }
     const double w = user_weights ? (double)user_weights[i] : 3.14159265358979323846 / p.n_views;
     const double cu = 0.5 * (p.n_u - 1), cv = p.two_d ? 0.0 : 0.5 * (p.n_v - 1);
+    const double dvv = p.two_d ? 0.0 : p.dv;
     FbpView V;
+    FbpCosine C;
     double D = 0.0, Dso = 0.0, scu = 0.0, scv = 0.0, ccu = 0.0;
     for (int a = 0; a < 3; ++a) {
         D += (c[a] - s[a]) * n[a];
@@ -92,30 +113,73 @@ __global__ void fbp_prepare_kernel(FbpParams p, const double* __restrict__ raw,
         V.n[a] = (float)n[a];
         V.eu[a] = (float)(u[a] / p.du);
         V.ev[a] = p.two_d ? 0.0f : (float)(v[a] / p.dv);
-        // pixel (iu, iv) = pc + iu * pdu + iv * pdv   (for the cosine weights)
-        V.pc[a] = (float)(c[a] - cu * p.du * u[a] - cv * (p.two_d ? 0.0 : p.dv * v[a]) - s[a]);
-        V.pdu[a] = (float)(p.du * u[a]);
-        V.pdv[a] = p.two_d ? 0.0f : (float)(p.dv * v[a]);
+        // pixel (iu, iv) minus the source = pc + iu * pdu + iv * pdv
+        C.pc[a] = (float)(c[a] - cu * p.du * u[a] - cv * dvv * v[a] - s[a]);
+        C.pdu[a] = (float)(p.du * u[a]);
+        C.pdv[a] = (float)(dvv * v[a]);
     }
     V.D = (float)D;
+    C.D = (float)fabs(D);
+    C.pad[0] = C.pad[1] = 0.0f;
     if (p.parallel) {
-        // u(X) = X . eu - c . eu / du + cu
+        // u(X) = X . det_u / du - c . det_u / du + cu
         V.ku0 = (float)(cu - ccu / p.du);
         V.kv0 = 0.0f;
         V.wg = (float)w;
     } else {
+        // u(X) = ku0 + D ((X - s) . det_u / du) / ((X - s) . n), likewise v
         V.ku0 = (float)(scu / p.du + cu);
         V.kv0 = (float)(p.two_d ? 0.0 : scv / p.dv + cv);
-        // weight w * (D_sd / D_so) / U^2 with U = den / D_so  ->  w * |D| * |D_so| / den^2
+        // w (D_sd / D_so) / U^2 with U = den / D_so  =  w |D| |D_so| / den^2
         V.wg = (float)(w * fabs(D) * fabs(Dso));
     }
     out_views[i] = V;
+    out_cos[i] = C;
+}
+
+// Cosine weight |(c - s) . n| / |P(iu, iv) - s| of one pixel.
+__device__ __forceinline__ float cosine_weight(const FbpCosine& C, int iu, int iv) {
+    const float fu = (float)iu, fv = (float)iv;
+    float d2 = 0.0f;
+#pragma unroll
+    for (int a = 0; a < 3; ++a) {
+        const float d = fmaf(fv, C.pdv[a], fmaf(fu, C.pdu[a], C.pc[a]));
+        d2 = fmaf(d, d, d2);
+    }
+    return C.D * rsqrtf(d2);
+}
+
+// Zero pads of the filtered sinogram that belong to columns [v0, v0 + nv) of one view (rows -1,
+// n_u, n_u + 1), plus the pad columns -1 and V, V + 1 over all rows when the tile touches them.
+__device__ void write_pads(const FbpParams& p, int view, int v0, int nv, float* out) {
+    const int V = p.two_d ? 1 : p.n_v;
+    if (p.two_d) {
+        if (threadIdx.x < 3) {
+            const int u = threadIdx.x == 0 ? -1 : p.n_u + (int)threadIdx.x - 1;
+            out[qrow(p, view, u)] = 0.0f;
+        }
+        return;
+    }
+    for (int i = threadIdx.x; i < 3 * nv; i += blockDim.x) {
+        const int rr = i / nv, j = i - rr * nv;
+        const int u = rr == 0 ? -1 : p.n_u + rr - 1;
+        out[qrow(p, view, u) + v0 + j + 1] = 0.0f;
+    }
+    if (v0 == 0)
+        for (int u = (int)threadIdx.x - 1; u < p.n_u + 2; u += blockDim.x)
+            out[qrow(p, view, u)] = 0.0f;
+    if (v0 + nv == V)
+        for (int u = (int)threadIdx.x - 1; u < p.n_u + 2; u += blockDim.x) {
+            out[qrow(p, view, u) + V + 1] = 0.0f;
+            out[qrow(p, view, u) + V + 2] = 0.0f;
+        }
 }
 
 // Cosine pre-weight and linear convolution along u for one view and a tile of tv detector
-// columns (v values).  Shared memory: the pre-weighted tile [n_u][tv] and the taps.
+// columns (v values); one output per thread and step.  Shared memory: the pre-weighted tile
+// [n_u][tv] and the taps.  Used for 2D sinograms (one column a view) and wide detectors.
 __global__ void __launch_bounds__(256) fbp_filter_kernel(FbpParams p,
-                                                        const FbpView* __restrict__ views,
+                                                        const FbpCosine* __restrict__ cosines,
                                                         const float* __restrict__ taps,
                                                         const float* __restrict__ sino,
                                                         float* __restrict__ out, int tv,
@@ -127,161 +191,296 @@ __global__ void __launch_bounds__(256) fbp_filter_kernel(FbpParams p,
     const int view = blockIdx.x / v_blocks;
     const int v0 = (blockIdx.x - view * v_blocks) * tv;
     const int nv = min(tv, V - v0);
-    const FbpView& W = views[view];
+    const FbpCosine C = cosines[view];
     for (int i = threadIdx.x; i < 2 * n_u - 1; i += blockDim.x) stap[i] = taps[i];
     for (int i = threadIdx.x; i < n_u * tv; i += blockDim.x) {
         const int iu = i / tv, j = i - iu * tv;
         float val = 0.0f;
         if (j < nv) {
             val = sino[((int64_t)view * n_u + iu) * V + v0 + j];
-            if (!p.parallel) {  // |(c - s) . n| / |pixel - s|
-                const float fu = (float)iu, fv = (float)(v0 + j);
-                float d2 = 0.0f;
-#pragma unroll
-                for (int a = 0; a < 3; ++a) {
-                    const float d = fmaf(fv, W.pdv[a], fmaf(fu, W.pdu[a], W.pc[a]));
-                    d2 = fmaf(d, d, d2);
-                }
-                val *= fabsf(W.D) * rsqrtf(d2);
-            }
+            if (!p.parallel) val *= cosine_weight(C, iu, v0 + j);
         }
         tile[i] = val;
     }
     __syncthreads();
+    const int vo = p.two_d ? 0 : 1;
     for (int i = threadIdx.x; i < n_u * tv; i += blockDim.x) {
         const int iu = i / tv, j = i - iu * tv;
         if (j >= nv) continue;
         float acc = 0.0f;
         const float* h = stap + (iu + n_u - 1);  // h[iu - k] = stap[iu - k + n_u - 1]
         for (int k = 0; k < n_u; ++k) acc = fmaf(h[-k], tile[k * tv + j], acc);
-        out[((int64_t)view * n_u + iu) * V + v0 + j] = acc;
+        out[qrow(p, view, iu) + v0 + j + vo] = acc;
     }
+    write_pads(p, view, v0, nv, out);
 }
 
-// Voxel-driven gather.  Block: 32 lanes along the volume's fastest gathered axis (z for 3D, x for
-// 2D) x 8 along x (3D) or y (2D); views staged in shared memory in chunks.
-template <int MODE>  // 0 parallel 2D, 1 fan 2D, 2 cone
-__global__ void __launch_bounds__(256) fbp_gather_kernel(FbpParams p,
+// The same filter for 3D sinograms, 32 columns a block (one per lane) and R consecutive outputs
+// a thread: each step loads R tile values and 2R - 1 taps (broadcast) for R * R FMAs.  The tile
+// has n_pad >= n_u rows (multiple of R, zero beyond n_u); taps are stored so that
+// stap[m] = h(m - (n_pad - 1)), zero outside the filter's support.
+template <int R>
+__global__ void __launch_bounds__(256) fbp_filter_blocked_kernel(
+    FbpParams p, const FbpCosine* __restrict__ cosines, const float* __restrict__ taps,
+    const float* __restrict__ sino, float* __restrict__ out, int n_pad, int v_blocks) {
+    extern __shared__ float sm[];
+    float* tile = sm;                     // [n_pad][32]
+    float* stap = sm + (int64_t)n_pad * 32;  // [2 n_pad]
+    const int n_u = p.n_u, V = p.n_v;
+    const int view = blockIdx.x / v_blocks;
+    const int v0 = (blockIdx.x - view * v_blocks) * 32;
+    const int nv = min(32, V - v0);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int shift = n_pad - n_u;
+    for (int m = threadIdx.x; m < 2 * n_pad; m += blockDim.x) {
+        const int g = m - shift;
+        stap[m] = (g >= 0 && g < 2 * n_u - 1) ? taps[g] : 0.0f;
+    }
+    const FbpCosine C = cosines[view];
+    for (int i = threadIdx.x; i < n_pad * 32; i += blockDim.x) {
+        const int k = i >> 5, j = i & 31;
+        float val = 0.0f;
+        if (k < n_u && j < nv) {
+            val = sino[((int64_t)view * n_u + k) * V + v0 + j];
+            if (!p.parallel) val *= cosine_weight(C, k, v0 + j);
+        }
+        tile[i] = val;
+    }
+    __syncthreads();
+    for (int r0 = warp * R; r0 < n_u; r0 += 8 * R) {
+        float acc[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) acc[r] = 0.0f;
+        for (int k0 = 0; k0 < n_pad; k0 += R) {
+            float t[R], hh[2 * R - 1];
+#pragma unroll
+            for (int i = 0; i < R; ++i) t[i] = tile[(k0 + i) * 32 + lane];
+            const float* hp = stap + (r0 - k0 - (R - 1) + n_pad - 1);
+#pragma unroll
+            for (int d = 0; d < 2 * R - 1; ++d) hh[d] = hp[d];
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int i = 0; i < R; ++i) acc[r] = fmaf(hh[r - i + R - 1], t[i], acc[r]);
+        }
+        if (lane < nv) {
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+                if (r0 + r < n_u) out[qrow(p, view, r0 + r) + v0 + lane + 1] = acc[r];
+        }
+    }
+    write_pads(p, view, v0, nv, out);
+}
+
+// Cone-beam (FDK) gather.  Block: 8 warps, one x each; lane l of a warp takes the NZ voxels
+// z0 + l + 32 m (m < NZ) at that x and at y = blockIdx.z, so a warp's 32 lanes read 32
+// neighbouring v of the same detector rows.  Views are staged in shared memory in chunks.
+template <int NZ>
+__global__ void __launch_bounds__(256) fdk_gather_kernel(FbpParams p,
                                                         const FbpView* __restrict__ views,
                                                         const float* __restrict__ q,
                                                         float* __restrict__ vol) {
-    constexpr int kChunk = 32;
-    __shared__ FbpView sv[kChunk];
-    __shared__ float st[8][33];
-    const int lane = threadIdx.x & 31, row = threadIdx.x >> 5;
-    int ix, iy, iz;
-    if (MODE == 2) {  // blocks: (z tiles of 32) x (x tiles of 8) x y
-        iz = blockIdx.x * 32 + lane;
-        ix = blockIdx.y * 8 + row;
-        iy = blockIdx.z;
-    } else {          // blocks: (x tiles of 32) x (y tiles of 8)
-        ix = blockIdx.x * 32 + lane;
-        iy = blockIdx.y * 8 + row;
-        iz = 0;
-    }
-    const bool inside = ix < p.nx && iy < p.ny && iz < p.nz;
+    constexpr int kChunk = 64;
+    __shared__ float4 sv[kChunk * 4];
+    __shared__ float st[8][NZ * 32 + 1];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int z0 = blockIdx.x * (32 * NZ);
+    const int ix = blockIdx.y * 8 + warp;
+    const int iy = blockIdx.z;
     const float X = ((float)ix + 0.5f - 0.5f * p.nx) * p.sx;
     const float Y = ((float)iy + 0.5f - 0.5f * p.ny) * p.sy;
-    const float Z = MODE == 2 ? ((float)iz + 0.5f - 0.5f * p.nz) * p.sz : 0.0f;
-    const int n_u = p.n_u, V = MODE == 2 ? p.n_v : 1;
-    float acc = 0.0f;
+    float Z[NZ], acc[NZ];
+#pragma unroll
+    for (int m = 0; m < NZ; ++m) {
+        Z[m] = ((float)(z0 + lane + 32 * m) + 0.5f - 0.5f * p.nz) * p.sz;
+        acc[m] = 0.0f;
+    }
+    const int cols = p.cols;
+    const int64_t view_stride = (int64_t)p.rows * cols;
+    const float umax = (float)p.n_u, vmax = (float)p.n_v;
     for (int k0 = 0; k0 < p.n_views; k0 += kChunk) {
         __syncthreads();
         const int nk = min(kChunk, p.n_views - k0);
-        constexpr int kWords = (int)(sizeof(FbpView) / sizeof(float));
-        for (int i = threadIdx.x; i < nk * kWords; i += blockDim.x)
-            reinterpret_cast<float*>(sv)[i] = reinterpret_cast<const float*>(views + k0)[i];
+        for (int i = threadIdx.x; i < nk * 4; i += blockDim.x)
+            sv[i] = reinterpret_cast<const float4*>(views + k0)[i];
         __syncthreads();
-        if (!inside) continue;
-        for (int k = 0; k < nk; ++k) {
-            const FbpView& W = sv[k];
-            float up, vp = 0.0f, g;
-            if (MODE == 0) {
-                up = fmaf(Y, W.eu[1], fmaf(X, W.eu[0], W.ku0));
-                g = W.wg;
-            } else {
-                const float ax = X - W.s[0], ay = Y - W.s[1], az = Z - W.s[2];
-                const float den = fmaf(az, W.n[2], fmaf(ay, W.n[1], ax * W.n[0]));
-                const float inv = 1.0f / den;
-                const float t = W.D * inv;
-                up = fmaf(t, fmaf(az, W.eu[2], fmaf(ay, W.eu[1], ax * W.eu[0])), W.ku0);
-                if (MODE == 2) vp = fmaf(t, fmaf(az, W.ev[2], fmaf(ay, W.ev[1], ax * W.ev[0])), W.kv0);
-                g = W.wg * inv * inv;
+        const float* base = q + (int64_t)k0 * view_stride;
+        for (int k = 0; k < nk; ++k, base += view_stride) {
+            // A = (s, n.x), B = (n.y, n.z, eu.x, eu.y), C = (eu.z, ev), E = (D, ku0, kv0, wg)
+            const float4 A = sv[4 * k], B = sv[4 * k + 1], C = sv[4 * k + 2], E = sv[4 * k + 3];
+            const float ax = X - A.x, ay = Y - A.y;
+            const float den_xy = fmaf(ay, B.x, ax * A.w);
+            const float au_xy = fmaf(ay, B.w, ax * B.z);
+            const float av_xy = fmaf(ay, C.z, ax * C.y);
+#pragma unroll
+            for (int m = 0; m < NZ; ++m) {
+                const float az = Z[m] - A.z;
+                const float den = fmaf(az, B.y, den_xy);
+                const float au = fmaf(az, C.x, au_xy);
+                const float av = fmaf(az, C.w, av_xy);
+                const float inv = rcp_approx(den);
+                const float t = E.x * inv;
+                const float up = fminf(fmaxf(fmaf(t, au, E.y), -1.0f), umax);
+                const float vp = fminf(fmaxf(fmaf(t, av, E.z), -1.0f), vmax);
+                const float fu0 = floorf(up), fv0 = floorf(vp);
+                const float fu = up - fu0, fv = vp - fv0;
+                const float* pq = base + ((int)fu0 + 1) * cols + (int)fv0 + 1;
+                const float s00 = __ldg(pq), s01 = __ldg(pq + 1);
+                const float s10 = __ldg(pq + cols), s11 = __ldg(pq + cols + 1);
+                const float a0 = fmaf(fv, s01 - s00, s00);
+                const float a1 = fmaf(fv, s11 - s10, s10);
+                const float val = fmaf(fu, a1 - a0, a0);
+                acc[m] = fmaf(E.w * inv * inv, val, acc[m]);
             }
-            // keep the indices in int range (a voxel in the source's plane gives inf or NaN,
-            // which lands off the detector and contributes 0)
-            up = fminf(fmaxf(up, -2.0f), (float)n_u + 1.0f);
-            vp = fminf(fmaxf(vp, -2.0f), (float)V + 1.0f);
-            const float fu0 = floorf(up), fv0 = floorf(vp);
-            const int u0 = (int)fu0, v0 = (int)fv0;
-            const float fu = up - fu0, fv = vp - fv0;
-            const float* base = q + (int64_t)(k0 + k) * n_u * V;
-            float s00 = 0.f, s10 = 0.f, s01 = 0.f, s11 = 0.f;
-            const bool u0ok = u0 >= 0 && u0 < n_u, u1ok = u0 + 1 >= 0 && u0 + 1 < n_u;
-            const bool v0ok = v0 >= 0 && v0 < V, v1ok = v0 + 1 >= 0 && v0 + 1 < V;
-            if (u0ok && v0ok) s00 = __ldg(base + (int64_t)u0 * V + v0);
-            if (u1ok && v0ok) s10 = __ldg(base + (int64_t)(u0 + 1) * V + v0);
-            if (MODE == 2) {
-                if (u0ok && v1ok) s01 = __ldg(base + (int64_t)u0 * V + v0 + 1);
-                if (u1ok && v1ok) s11 = __ldg(base + (int64_t)(u0 + 1) * V + v0 + 1);
-            }
-            const float a0 = fmaf(fu, s10 - s00, s00);
-            const float val = MODE == 2 ? fmaf(fv, fmaf(fu, s11 - s01, s01) - a0, a0) : a0;
-            acc = fmaf(g, val, acc);
         }
     }
-    if (MODE == 2) {  // transpose through shared memory so that the stores run along x
-        __syncthreads();
-        st[row][lane] = acc;
-        __syncthreads();
-        // 256 threads store the 8 (x) x 32 (z) tile: thread -> (z = t / 8, x = t % 8)
-        const int t = threadIdx.x, zz = t >> 3, xx = t & 7;
-        const int oz = blockIdx.x * 32 + zz, ox = blockIdx.y * 8 + xx;
-        if (oz < p.nz && ox < p.nx)
-            vol[((int64_t)oz * p.ny + iy) * p.nx + ox] = st[xx][zz];
-    } else if (inside) {
-        vol[(int64_t)iy * p.nx + ix] = acc;
+    // transpose through shared memory so that the stores run along x
+    __syncthreads();
+#pragma unroll
+    for (int m = 0; m < NZ; ++m) st[warp][lane + 32 * m] = acc[m];
+    __syncthreads();
+    const int x0 = blockIdx.y * 8;
+    for (int i = threadIdx.x; i < 8 * 32 * NZ; i += blockDim.x) {
+        const int zz = i >> 3, xx = i & 7;
+        const int oz = z0 + zz, ox = x0 + xx;
+        if (oz < p.nz && ox < p.nx) vol[((int64_t)oz * p.ny + iy) * p.nx + ox] = st[xx][zz];
     }
 }
+
+// 2D gather (parallel or fan).  Block: lane = x (32 consecutive), warp w takes the NY rows
+// y0 + w + 8 m.
+template <bool PAR, int NY>
+__global__ void __launch_bounds__(256) fbp2d_gather_kernel(FbpParams p,
+                                                          const FbpView* __restrict__ views,
+                                                          const float* __restrict__ q,
+                                                          float* __restrict__ vol) {
+    constexpr int kChunk = 64;
+    __shared__ float4 sv[kChunk * 4];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int ix = blockIdx.x * 32 + lane;
+    const int y0 = blockIdx.y * (8 * NY) + warp;
+    const float X = ((float)ix + 0.5f - 0.5f * p.nx) * p.sx;
+    float Y[NY], acc[NY];
+#pragma unroll
+    for (int m = 0; m < NY; ++m) {
+        Y[m] = ((float)(y0 + 8 * m) + 0.5f - 0.5f * p.ny) * p.sy;
+        acc[m] = 0.0f;
+    }
+    const int rows = p.rows;
+    const float umax = (float)p.n_u;
+    for (int k0 = 0; k0 < p.n_views; k0 += kChunk) {
+        __syncthreads();
+        const int nk = min(kChunk, p.n_views - k0);
+        for (int i = threadIdx.x; i < nk * 4; i += blockDim.x)
+            sv[i] = reinterpret_cast<const float4*>(views + k0)[i];
+        __syncthreads();
+        const float* base = q + (int64_t)k0 * rows + 1;
+        for (int k = 0; k < nk; ++k, base += rows) {
+            const float4 A = sv[4 * k], B = sv[4 * k + 1], E = sv[4 * k + 3];
+            if (PAR) {
+                const float ux = fmaf(X, B.z, E.y);
+#pragma unroll
+                for (int m = 0; m < NY; ++m) {
+                    const float up = fminf(fmaxf(fmaf(Y[m], B.w, ux), -1.0f), umax);
+                    const float fu0 = floorf(up), fu = up - fu0;
+                    const float* pq = base + (int)fu0;
+                    const float s0 = __ldg(pq), s1 = __ldg(pq + 1);
+                    acc[m] = fmaf(E.w, fmaf(fu, s1 - s0, s0), acc[m]);
+                }
+            } else {
+                const float ax = X - A.x;
+                const float den_x = ax * A.w, au_x = ax * B.z;
+#pragma unroll
+                for (int m = 0; m < NY; ++m) {
+                    const float ay = Y[m] - A.y;
+                    const float den = fmaf(ay, B.x, den_x);
+                    const float au = fmaf(ay, B.w, au_x);
+                    const float inv = rcp_approx(den);
+                    const float up = fminf(fmaxf(fmaf(E.x * inv, au, E.y), -1.0f), umax);
+                    const float fu0 = floorf(up), fu = up - fu0;
+                    const float* pq = base + (int)fu0;
+                    const float s0 = __ldg(pq), s1 = __ldg(pq + 1);
+                    acc[m] = fmaf(E.w * inv * inv, fmaf(fu, s1 - s0, s0), acc[m]);
+                }
+            }
+        }
+    }
+    if (ix < p.nx) {
+#pragma unroll
+        for (int m = 0; m < NY; ++m)
+            if (y0 + 8 * m < p.ny) vol[(int64_t)(y0 + 8 * m) * p.nx + ix] = acc[m];
+    }
+}
+
+constexpr int kFilterR = 16;
+constexpr size_t kSmemBudget = 200u * 1024u;
 
 }  // namespace
 
 cudaError_t launch_fbp(const FbpParams& p, const double* raw, const float* user_weights,
-                       FbpView* views, float* taps, const float* sino, float* filtered,
-                       float* vol, cudaStream_t stream) {
+                       FbpView* views, FbpCosine* cosines, float* taps, const float* sino,
+                       float* filtered, float* vol, cudaStream_t stream) {
     const int n_prep = p.n_views > 2 * p.n_u - 1 ? p.n_views : 2 * p.n_u - 1;
     fbp_prepare_kernel<<<(n_prep + 255) / 256, 256, 0, stream>>>(p, raw, user_weights, views,
-                                                                 taps);
+                                                                 cosines, taps);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int V = p.two_d ? 1 : p.n_v;
-    // columns per filter block: as many (up to 32) as fit in shared memory with the taps
-    const size_t tap_bytes = sizeof(float) * (size_t)(2 * p.n_u - 1);
-    const size_t budget = 200u * 1024u;
-    int tv = 32;
-    while (tv > 1 && (size_t)tv * p.n_u * sizeof(float) + tap_bytes > budget) tv >>= 1;
-    if (tv > V) tv = V;
-    const size_t smem = (size_t)tv * p.n_u * sizeof(float) + tap_bytes;
-    if (smem > budget) return cudaErrorInvalidValue;
-    e = cudaFuncSetAttribute(fbp_filter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
-    if (e != cudaSuccess) return e;
-    const int v_blocks = (V + tv - 1) / tv;
-    if ((int64_t)v_blocks * p.n_views > (int64_t)INT32_MAX) return cudaErrorInvalidValue;
-    fbp_filter_kernel<<<v_blocks * p.n_views, 256, smem, stream>>>(p, views, taps, sino, filtered,
-                                                                  tv, v_blocks);
+    const int n_pad = (p.n_u + kFilterR - 1) / kFilterR * kFilterR;
+    const size_t blocked_smem = sizeof(float) * ((size_t)n_pad * 32 + 2 * (size_t)n_pad);
+    if (!p.two_d && blocked_smem <= kSmemBudget) {
+        e = cudaFuncSetAttribute(fbp_filter_blocked_kernel<kFilterR>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)blocked_smem);
+        if (e != cudaSuccess) return e;
+        const int v_blocks = (V + 31) / 32;
+        if ((int64_t)v_blocks * p.n_views > (int64_t)INT32_MAX) return cudaErrorInvalidValue;
+        fbp_filter_blocked_kernel<kFilterR><<<v_blocks * p.n_views, 256, blocked_smem, stream>>>(
+            p, cosines, taps, sino, filtered, n_pad, v_blocks);
+    } else {
+        // columns per block: as many (up to 32) as fit in shared memory with the taps
+        const size_t tap_bytes = sizeof(float) * (size_t)(2 * p.n_u - 1);
+        int tv = 32;
+        while (tv > 1 && (size_t)tv * p.n_u * sizeof(float) + tap_bytes > kSmemBudget) tv >>= 1;
+        if (tv > V) tv = V;
+        const size_t smem = (size_t)tv * p.n_u * sizeof(float) + tap_bytes;
+        if (smem > kSmemBudget) return cudaErrorInvalidValue;
+        e = cudaFuncSetAttribute(fbp_filter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+        if (e != cudaSuccess) return e;
+        const int v_blocks = (V + tv - 1) / tv;
+        if ((int64_t)v_blocks * p.n_views > (int64_t)INT32_MAX) return cudaErrorInvalidValue;
+        fbp_filter_kernel<<<v_blocks * p.n_views, 256, smem, stream>>>(p, cosines, taps, sino,
+                                                                      filtered, tv, v_blocks);
+    }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (p.two_d) {
-        if ((p.ny + 7) / 8 > 65535) return cudaErrorInvalidValue;
-        dim3 g((p.nx + 31) / 32, (p.ny + 7) / 8);
-        if (p.parallel)
-            fbp_gather_kernel<0><<<g, 256, 0, stream>>>(p, views, filtered, vol);
-        else
-            fbp_gather_kernel<1><<<g, 256, 0, stream>>>(p, views, filtered, vol);
+        const int ny_blocks_4 = (p.ny + 31) / 32, ny_blocks_1 = (p.ny + 7) / 8;
+        if (p.ny >= 128) {
+            if (ny_blocks_4 > 65535) return cudaErrorInvalidValue;
+            dim3 g((p.nx + 31) / 32, ny_blocks_4);
+            if (p.parallel)
+                fbp2d_gather_kernel<true, 4><<<g, 256, 0, stream>>>(p, views, filtered, vol);
+            else
+                fbp2d_gather_kernel<false, 4><<<g, 256, 0, stream>>>(p, views, filtered, vol);
+        } else {
+            dim3 g((p.nx + 31) / 32, ny_blocks_1);
+            if (p.parallel)
+                fbp2d_gather_kernel<true, 1><<<g, 256, 0, stream>>>(p, views, filtered, vol);
+            else
+                fbp2d_gather_kernel<false, 1><<<g, 256, 0, stream>>>(p, views, filtered, vol);
+        }
     } else {
         if ((p.nx + 7) / 8 > 65535 || p.ny > 65535) return cudaErrorInvalidValue;
-        dim3 g((p.nz + 31) / 32, (p.nx + 7) / 8, p.ny);
-        fbp_gather_kernel<2><<<g, 256, 0, stream>>>(p, views, filtered, vol);
+        if (p.nz >= 96) {
+            dim3 g((p.nz + 127) / 128, (p.nx + 7) / 8, p.ny);
+            fdk_gather_kernel<4><<<g, 256, 0, stream>>>(p, views, filtered, vol);
+        } else if (p.nz >= 48) {
+            dim3 g((p.nz + 63) / 64, (p.nx + 7) / 8, p.ny);
+            fdk_gather_kernel<2><<<g, 256, 0, stream>>>(p, views, filtered, vol);
+        } else {
+            dim3 g((p.nz + 31) / 32, (p.nx + 7) / 8, p.ny);
+            fdk_gather_kernel<1><<<g, 256, 0, stream>>>(p, views, filtered, vol);
+        }
     }
     return cudaGetLastError();
 }

@@ -5,8 +5,8 @@ fractional detector index u(X) carries a float32 rounding error of a few ulp of 
 coordinate involved (about 1e-6 pixel for these sizes); the ramp-filtered sinogram changes by at
 most ~2 max|Q| per pixel, and the filter's float32 sums of n_u terms add ~n_u eps relative to
 sum|h p|.  Over a whole volume both stay below 1e-4 of the result's L2 norm, so small cases are
-compared at rel L2 <= 2e-4 and max |diff| <= 2e-3 max |f|; sampled voxels of the full-size cone
-case at max |diff| <= 2e-3 max |f|.
+compared at rel L2 <= 2e-4 and max |diff| <= 2e-3 max |f|, both scaled by n_u / 400 for wider
+detectors; sampled voxels of the full-size cone case at max |diff| <= 2e-3 max |f|.
 """
 import math
 
@@ -45,10 +45,12 @@ def _oracle(w, sino, **kw):
                  **kw)
 
 
-def _check(got, want):
+def _check(got, want, n_u=0):
+    # the filter's float32 sums of n_u terms: the bound grows linearly with n_u (above 400)
+    grow = max(1.0, n_u / 400.0)
     err = rel_l2(got, want)
     mx = float(np.abs(got - want).max()) / max(float(np.abs(want).max()), 1e-30)
-    assert err <= REL_L2 and mx <= MAX_REL, (err, mx)
+    assert err <= REL_L2 * grow and mx <= MAX_REL * grow, (err, mx)
 
 
 def _phantom_sino(w):
@@ -97,7 +99,7 @@ def test_anisotropic_voxels(ct, kind):
     sino = W.random_sinogram(w, 11)
     g = ct.Geometry.from_workload(w)
     got = _cpu(g.fbp(torch_cuda(sino)))
-    _check(got, _oracle(w, sino.astype(np.float64)))
+    _check(got, _oracle(w, sino.astype(np.float64)), n_u=w.n_u)
 
 
 def test_full_size_cone_sampled_voxels(ct):
@@ -174,3 +176,28 @@ def test_errors(ct):
     with pytest.raises(ct.CtError) as ei:
         gc.fbp(torch.zeros(gc.sino_shape, device="cuda"))
     assert ei.value.status == 1
+
+
+@pytest.mark.parametrize("n,shape", [(3, (50, 21, 19)), (3, (101, 13, 17)), (2, (1, 130, 41)),
+                                     (1, (1, 131, 37))])
+def test_gather_variants(ct, n, shape):
+    """Volumes that select the other gather shapes (2 and 4 voxels a thread along z; 4 rows a
+    thread in 2D), with ragged tails."""
+    import dataclasses
+    w = dataclasses.replace(W.small_config(n), vol_shape=shape)
+    sino = W.random_sinogram(w, 21)
+    g = ct.Geometry.from_workload(w)
+    got = _cpu(g.fbp(torch_cuda(sino), window="shepp-logan"))
+    _check(got, _oracle(w, sino.astype(np.float64), window="shepp-logan"))
+
+
+def test_wide_detector_uses_the_plain_filter(ct):
+    """n_u = 1601 exceeds the blocked filter's shared memory; the per-output filter runs."""
+    import dataclasses
+    base = W.small_config(3)
+    w = dataclasses.replace(base, n_u=1601, n_v=5, du=0.05, views=base.views[:4],
+                            vol_shape=(4, 9, 11))
+    sino = W.random_sinogram(w, 22)
+    g = ct.Geometry.from_workload(w)
+    got = _cpu(g.fbp(torch_cuda(sino)))
+    _check(got, _oracle(w, sino.astype(np.float64)), n_u=w.n_u)
