@@ -19,6 +19,8 @@
 // This operator is not the Siddon adjoint; it is a separate, approximate inverse.
 #include "ct_internal.h"
 
+#include <algorithm>
+
 #include <cuda_runtime.h>
 
 namespace ct {
@@ -279,7 +281,8 @@ template <int NZ>
 __global__ void __launch_bounds__(256) fdk_gather_kernel(FbpParams p,
                                                         const FbpView* __restrict__ views,
                                                         const float* __restrict__ q,
-                                                        float* __restrict__ vol) {
+                                                        float* __restrict__ vol, int k_begin,
+                                                        int k_end) {
     constexpr int kChunk = 64;
     __shared__ float4 sv[kChunk * 4];
     __shared__ float st[8][NZ * 32 + 1];
@@ -298,9 +301,9 @@ __global__ void __launch_bounds__(256) fdk_gather_kernel(FbpParams p,
     const int cols = p.cols;
     const int64_t view_stride = (int64_t)p.rows * cols;
     const float umax = (float)p.n_u, vmax = (float)p.n_v;
-    for (int k0 = 0; k0 < p.n_views; k0 += kChunk) {
+    for (int k0 = k_begin; k0 < k_end; k0 += kChunk) {
         __syncthreads();
-        const int nk = min(kChunk, p.n_views - k0);
+        const int nk = min(kChunk, k_end - k0);
         for (int i = threadIdx.x; i < nk * 4; i += blockDim.x)
             sv[i] = reinterpret_cast<const float4*>(views + k0)[i];
         __syncthreads();
@@ -312,6 +315,31 @@ __global__ void __launch_bounds__(256) fdk_gather_kernel(FbpParams p,
             const float den_xy = fmaf(ay, B.x, ax * A.w);
             const float au_xy = fmaf(ay, B.w, ax * B.z);
             const float av_xy = fmaf(ay, C.z, ax * C.y);
+            if (B.y == 0.0f && C.x == 0.0f) {
+                // n.z = 0 and det_u.z = 0 (a detector whose v axis is the z axis, as on circular
+                // and helical orbits): den, u and the weight do not depend on z.  The same
+                // operations as below with the z terms exactly zero, so the results are the
+                // general path's bit for bit.
+                const float inv = rcp_approx(den_xy);
+                const float t = E.x * inv;
+                const float up = fminf(fmaxf(fmaf(t, au_xy, E.y), -1.0f), umax);
+                const float fu0 = floorf(up), fu = up - fu0;
+                const float g = E.w * inv * inv;
+                const float* prow = base + ((int)fu0 + 1) * cols + 1;
+#pragma unroll
+                for (int m = 0; m < NZ; ++m) {
+                    const float av = fmaf(Z[m] - A.z, C.w, av_xy);
+                    const float vp = fminf(fmaxf(fmaf(t, av, E.z), -1.0f), vmax);
+                    const float fv0 = floorf(vp), fv = vp - fv0;
+                    const float* pq = prow + (int)fv0;
+                    const float s00 = __ldg(pq), s01 = __ldg(pq + 1);
+                    const float s10 = __ldg(pq + cols), s11 = __ldg(pq + cols + 1);
+                    const float a0 = fmaf(fv, s01 - s00, s00);
+                    const float a1 = fmaf(fv, s11 - s10, s10);
+                    acc[m] = fmaf(g, fmaf(fu, a1 - a0, a0), acc[m]);
+                }
+                continue;
+            }
 #pragma unroll
             for (int m = 0; m < NZ; ++m) {
                 const float az = Z[m] - A.z;
@@ -329,8 +357,8 @@ __global__ void __launch_bounds__(256) fdk_gather_kernel(FbpParams p,
                 const float s10 = __ldg(pq + cols), s11 = __ldg(pq + cols + 1);
                 const float a0 = fmaf(fv, s01 - s00, s00);
                 const float a1 = fmaf(fv, s11 - s10, s10);
-                const float val = fmaf(fu, a1 - a0, a0);
-                acc[m] = fmaf(E.w * inv * inv, val, acc[m]);
+                const float g = E.w * inv * inv;
+                acc[m] = fmaf(g, fmaf(fu, a1 - a0, a0), acc[m]);
             }
         }
     }
@@ -343,7 +371,10 @@ __global__ void __launch_bounds__(256) fdk_gather_kernel(FbpParams p,
     for (int i = threadIdx.x; i < 8 * 32 * NZ; i += blockDim.x) {
         const int zz = i >> 3, xx = i & 7;
         const int oz = z0 + zz, ox = x0 + xx;
-        if (oz < p.nz && ox < p.nx) vol[((int64_t)oz * p.ny + iy) * p.nx + ox] = st[xx][zz];
+        if (oz < p.nz && ox < p.nx) {
+            float* o = vol + ((int64_t)oz * p.ny + iy) * p.nx + ox;
+            *o = k_begin == 0 ? st[xx][zz] : *o + st[xx][zz];
+        }
     }
 }
 
@@ -471,15 +502,27 @@ cudaError_t launch_fbp(const FbpParams& p, const double* raw, const float* user_
         }
     } else {
         if ((p.nx + 7) / 8 > 65535 || p.ny > 65535) return cudaErrorInvalidValue;
-        if (p.nz >= 96) {
-            dim3 g((p.nz + 127) / 128, (p.nx + 7) / 8, p.ny);
-            fdk_gather_kernel<4><<<g, 256, 0, stream>>>(p, views, filtered, vol);
-        } else if (p.nz >= 48) {
-            dim3 g((p.nz + 63) / 64, (p.nx + 7) / 8, p.ny);
-            fdk_gather_kernel<2><<<g, 256, 0, stream>>>(p, views, filtered, vol);
-        } else {
-            dim3 g((p.nz + 31) / 32, (p.nx + 7) / 8, p.ny);
-            fdk_gather_kernel<1><<<g, 256, 0, stream>>>(p, views, filtered, vol);
+        // Views in passes whose filtered slices fit in L2 together (about 48 MB), so that all
+        // resident blocks read the same views; later passes add to the volume.
+        const size_t slice = sizeof(float) * (size_t)p.rows * (size_t)p.cols;
+        int per_pass = (int)std::min<size_t>((size_t)p.n_views, (48u << 20) / slice);
+        per_pass = per_pass < 16 ? 16 : per_pass / 16 * 16;
+        for (int k = 0; k < p.n_views; k += per_pass) {
+            const int k_end = std::min(p.n_views, k + per_pass);
+            if (p.nz >= 192) {
+                dim3 g((p.nz + 255) / 256, (p.nx + 7) / 8, p.ny);
+                fdk_gather_kernel<8><<<g, 256, 0, stream>>>(p, views, filtered, vol, k, k_end);
+            } else if (p.nz >= 96) {
+                dim3 g((p.nz + 127) / 128, (p.nx + 7) / 8, p.ny);
+                fdk_gather_kernel<4><<<g, 256, 0, stream>>>(p, views, filtered, vol, k, k_end);
+            } else if (p.nz >= 48) {
+                dim3 g((p.nz + 63) / 64, (p.nx + 7) / 8, p.ny);
+                fdk_gather_kernel<2><<<g, 256, 0, stream>>>(p, views, filtered, vol, k, k_end);
+            } else {
+                dim3 g((p.nz + 31) / 32, (p.nx + 7) / 8, p.ny);
+                fdk_gather_kernel<1><<<g, 256, 0, stream>>>(p, views, filtered, vol, k, k_end);
+            }
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
         }
     }
     return cudaGetLastError();

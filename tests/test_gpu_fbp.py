@@ -178,11 +178,13 @@ def test_errors(ct):
     assert ei.value.status == 1
 
 
-@pytest.mark.parametrize("n,shape", [(3, (50, 21, 19)), (3, (101, 13, 17)), (2, (1, 130, 41)),
-                                     (1, (1, 131, 37))])
+@pytest.mark.parametrize("n,shape", [(3, (50, 21, 19)), (3, (101, 13, 17)), (3, (200, 7, 9)),
+                                     (4, (50, 9, 11)), (4, (101, 5, 7)), (4, (200, 7, 9)),
+                                     (2, (1, 130, 41)), (1, (1, 131, 37))])
 def test_gather_variants(ct, n, shape):
-    """Volumes that select the other gather shapes (2 and 4 voxels a thread along z; 4 rows a
-    thread in 2D), with ragged tails."""
+    """Volumes that select the other gather shapes (2, 4 and 8 voxels a thread along z; 4 rows a
+    thread in 2D), with ragged tails; the circular orbit (workload 3) takes the z-independent
+    path, the jittered helix (workload 4, tilted detectors) the general one."""
     import dataclasses
     w = dataclasses.replace(W.small_config(n), vol_shape=shape)
     sino = W.random_sinogram(w, 21)
