@@ -153,3 +153,78 @@ def _bilinear(Q: np.ndarray, up: np.ndarray, vp: np.ndarray) -> np.ndarray:
             vals[ok] = Q[iu[ok], iv[ok]]
             res += wu * wv * vals
     return res
+
+
+def fbp_transpose(beam: int, views: np.ndarray, vol_shape, spacing, n_u: int, n_v: int,
+                  du: float, dv: float, vol: np.ndarray, window: str = "ram-lak",
+                  view_weights=None, isocenter=None):
+    """The transpose of `fbp` as a linear map from sinograms to volumes: volume -> sinogram.
+
+    The pages state that the analytical operator's backward pass scatters the same interpolation
+    coefficients, distance weights and normalisation (diffct "Differentiable analytical
+    reconstruction"; "Analytical Reconstruction Helpers": dedicated transpose kernels).  Written
+    as the transposes of the three stages in reverse order: the gather's bilinear coefficients
+    times w_k g_k(X) scattered onto each view's detector, the filter (its matrix
+    tau h((i - j) tau) is symmetric because h is even), then the cosine weights (diagonal).
+    """
+    assert beam in (0, 1, 2), "parallel (2D), fan (2D) and cone beams"
+    two_d = beam in (0, 1)
+    nz, ny, nx = vol_shape
+    n_views = views.shape[0]
+    V = 1 if two_d else n_v
+    f = np.asarray(vol, dtype=np.float64).reshape(1 if two_d else nz, ny, nx)
+    w = (np.full(n_views, math.pi / n_views) if view_weights is None
+         else np.asarray(view_weights, dtype=np.float64))
+    iso = np.zeros(3) if isocenter is None else np.r_[np.asarray(isocenter, float), [0.0] * (3 - len(isocenter))]
+    cu, cv = (n_u - 1) / 2.0, (V - 1) / 2.0
+    uu = (np.arange(n_u) - cu) * du
+    vv = (np.arange(V) - cv) * dv if not two_d else np.zeros(1)
+    taps = ramp_taps(n_u, du, window)
+    sp = np.broadcast_to(np.asarray(spacing, dtype=np.float64), (2 if two_d else 3,))
+    sz, sy, sx = (1.0, sp[0], sp[1]) if two_d else (sp[0], sp[1], sp[2])
+    zs = (np.arange(nz) + 0.5 - nz / 2.0) * sz if not two_d else np.zeros(1)
+    ys = (np.arange(ny) + 0.5 - ny / 2.0) * sy
+    xs = (np.arange(nx) + 0.5 - nx / 2.0) * sx
+    Z, Y, X = np.meshgrid(zs, ys, xs, indexing="ij")
+    P = np.stack([X, Y, Z], axis=-1)
+    out = np.zeros((n_views, n_u, V))
+    for k in range(n_views):
+        first, ctr, u, v, n = _frames(beam, views[k])
+        if beam == 0:
+            upix = ((P - ctr) @ u) / du + cu
+            vpix = np.zeros_like(upix)
+            g = np.ones_like(upix)
+        else:
+            a = P - first
+            den = a @ n
+            D = (ctr - first) @ n
+            upix = ((first - ctr) @ u + D * (a @ u) / den) / du + cu
+            vpix = (((first - ctr) @ v + D * (a @ v) / den) / dv + cv) if not two_d else np.zeros_like(upix)
+            Uw = den / ((iso - first) @ n)
+            g = (abs(D) / abs((iso - first) @ n)) / (Uw * Uw)
+        # transpose of the gather: scatter w g f with the bilinear coefficients
+        Q = _bilinear_transpose(w[k] * g * f, upix, vpix, n_u, V)
+        # transpose of the filter (symmetric), then of the cosine weights
+        q = np.empty_like(Q)
+        for j in range(V):
+            q[:, j] = du * np.convolve(Q[:, j], taps, mode="full")[n_u - 1:2 * n_u - 1]
+        if beam != 0:
+            pix = ctr[None, None, :] + uu[:, None, None] * u + vv[None, :, None] * v
+            q *= abs((ctr - first) @ n) / np.linalg.norm(pix - first, axis=-1)
+        out[k] = q
+    return out[:, :, 0] if two_d else out
+
+
+def _bilinear_transpose(vals: np.ndarray, up: np.ndarray, vp: np.ndarray, nU: int, nV: int):
+    """Adds vals at fractional pixel indices into an (nU, nV) grid with the bilinear
+    coefficients of `_bilinear` (contributions off the grid are dropped)."""
+    u0 = np.floor(up).astype(np.int64)
+    v0 = np.floor(vp).astype(np.int64)
+    fu, fv = up - u0, vp - v0
+    res = np.zeros((nU, nV))
+    for du_, wu in ((0, 1 - fu), (1, fu)):
+        for dv_, wv in ((0, 1 - fv), (1, fv)):
+            iu, iv = u0 + du_, v0 + dv_
+            ok = (iu >= 0) & (iu < nU) & (iv >= 0) & (iv < nV)
+            np.add.at(res, (iu[ok], iv[ok]), (wu * wv * vals)[ok])
+    return res

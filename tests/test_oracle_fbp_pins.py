@@ -157,3 +157,21 @@ def test_voxel_subset_equals_the_grid():
     sub = F.fbp(w.beam, w.views, w.vol_shape, w.voxel_spacing, w.n_u, w.n_v, w.du, w.dv, sino,
                 voxels=idx)
     np.testing.assert_allclose(sub, full[idx[:, 0], idx[:, 1], idx[:, 2]], rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("n", [1, 2, 3])
+def test_transpose_satisfies_the_adjoint_identity(n):
+    """<F y, x> = <y, F^T x> for random y, x: pins fbp_transpose to fbp (already pinned by the
+    reconstructions above) in every stage (scatter coefficients, weights, filter, cosines)."""
+    w = W.small_config(n)
+    rng = np.random.default_rng(50 + n)
+    y = rng.standard_normal(w.sino_shape)
+    vol_shape = (w.vol_shape[1], w.vol_shape[2]) if w.beam in (0, 1) else w.vol_shape
+    x = rng.standard_normal(vol_shape)
+    kw = dict(window="hann", view_weights=rng.uniform(0.01, 0.1, w.views.shape[0]),
+              isocenter=(0.7, -1.1, 0.4)[: 2 if w.beam in (0, 1) else 3])
+    Fy = F.fbp(w.beam, w.views, w.vol_shape, w.voxel_spacing, w.n_u, w.n_v, w.du, w.dv, y, **kw)
+    Ftx = F.fbp_transpose(w.beam, w.views, w.vol_shape, w.voxel_spacing, w.n_u, w.n_v, w.du,
+                          w.dv, x, **kw)
+    lhs, rhs = float(np.sum(Fy * x)), float(np.sum(y * Ftx))
+    assert abs(lhs - rhs) <= 1e-11 * np.linalg.norm(Fy) * np.linalg.norm(x), (lhs, rhs)
