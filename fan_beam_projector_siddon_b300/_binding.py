@@ -94,6 +94,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.ct_fbp_workspace_bytes.restype = sz
     L.ct_fbp.argtypes = [vp, vp, vp, vp, ctypes.POINTER(f64), i32, vp, sz, vp]
     L.ct_fbp.restype = i32
+    L.ct_fbp_transpose.argtypes = [vp, vp, vp, vp, ctypes.POINTER(f64), i32, vp, sz, vp]
+    L.ct_fbp_transpose.restype = i32
     L.ct_status_string.argtypes = [i32]
     L.ct_status_string.restype = ctypes.c_char_p
     _lib = L
@@ -231,19 +233,38 @@ def ct_fbp_workspace_bytes(handle: int) -> int:
     return int(load_library().ct_fbp_workspace_bytes(handle))
 
 
-def ct_fbp(handle: int, d_sino: int, d_volume: int, d_view_weights: int | None, isocenter,
-           window, d_workspace: int, workspace_bytes: int, stream: int | None) -> None:
-    """Filtered backprojection; ``window`` is a name of ``FBP_WINDOWS`` or its code and
-    ``isocenter`` a host 3-vector or None."""
+def _fbp_args(isocenter, window):
     code = FBP_WINDOWS[window] if isinstance(window, str) else int(window)
     iso = None
     if isocenter is not None:
         arr = np.zeros(3, dtype=np.float64)
         vals = np.asarray(isocenter, dtype=np.float64).ravel()
         arr[:len(vals)] = vals
-        iso = arr.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
-    _check(load_library().ct_fbp(handle, d_sino, d_volume, d_view_weights, iso, code,
+        iso = arr
+    return code, iso
+
+
+def _dptr(arr):
+    return None if arr is None else arr.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def ct_fbp(handle: int, d_sino: int, d_volume: int, d_view_weights: int | None, isocenter,
+           window, d_workspace: int, workspace_bytes: int, stream: int | None) -> None:
+    """Filtered backprojection; ``window`` is a name of ``FBP_WINDOWS`` or its code and
+    ``isocenter`` a host 3-vector or None."""
+    code, iso = _fbp_args(isocenter, window)
+    _check(load_library().ct_fbp(handle, d_sino, d_volume, d_view_weights, _dptr(iso), code,
                                  d_workspace, workspace_bytes, stream), "ct_fbp")
+
+
+def ct_fbp_transpose(handle: int, d_volume: int, d_sino: int, d_view_weights: int | None,
+                     isocenter, window, d_workspace: int, workspace_bytes: int,
+                     stream: int | None) -> None:
+    """Transpose of ``ct_fbp`` (volume -> sinogram), same arguments."""
+    code, iso = _fbp_args(isocenter, window)
+    _check(load_library().ct_fbp_transpose(handle, d_volume, d_sino, d_view_weights, _dptr(iso),
+                                           code, d_workspace, workspace_bytes, stream),
+           "ct_fbp_transpose")
 
 
 def ct_status_string(status: int) -> str:
@@ -402,31 +423,41 @@ class Geometry:
                         initialised, self._stream(stream))
         return x
 
-    def fbp(self, sino, out=None, window="ram-lak", view_weights=None, isocenter=None,
-            workspace=None, stream=None):
-        """Filtered backprojection (FBP / FDK) of a sinogram; leading dimensions are kept and
-        reconstructed one after another with the same workspace."""
+    def _fbp_call(self, fn, src, src_shape, dst_shape, out, window, view_weights, isocenter,
+                  workspace, stream):
         import torch
-        assert sino.is_cuda and sino.dtype == torch.float32 and sino.is_contiguous()
-        nd = len(self.sino_shape)
-        assert tuple(sino.shape[sino.dim() - nd:]) == tuple(self.sino_shape)
-        lead = tuple(sino.shape[:sino.dim() - nd])
+        assert src.is_cuda and src.dtype == torch.float32 and src.is_contiguous()
+        nd = len(src_shape)
+        assert tuple(src.shape[src.dim() - nd:]) == tuple(src_shape)
+        lead = tuple(src.shape[:src.dim() - nd])
         if out is None:
-            out = torch.empty(lead + tuple(self.volume_shape), dtype=torch.float32,
-                              device=sino.device)
+            out = torch.empty(lead + tuple(dst_shape), dtype=torch.float32, device=src.device)
         need = ct_fbp_workspace_bytes(self.handle)
         if workspace is None:
-            workspace = torch.empty(need, dtype=torch.uint8, device=sino.device)
+            workspace = torch.empty(need, dtype=torch.uint8, device=src.device)
         ws, wsb = workspace.data_ptr(), workspace.numel() * workspace.element_size()
         wptr = None
         if view_weights is not None:
             view_weights = torch.as_tensor(view_weights, dtype=torch.float32,
-                                           device=sino.device).contiguous()
+                                           device=src.device).contiguous()
             assert view_weights.numel() == self.info.n_views
             wptr = view_weights.data_ptr()
-        s2 = sino.reshape((-1,) + tuple(self.sino_shape))
-        o2 = out.view((-1,) + tuple(self.volume_shape))
+        s2 = src.reshape((-1,) + tuple(src_shape))
+        o2 = out.view((-1,) + tuple(dst_shape))
         for b in range(s2.shape[0]):
-            ct_fbp(self.handle, s2[b].data_ptr(), o2[b].data_ptr(), wptr, isocenter, window,
-                   ws, wsb, self._stream(stream))
+            fn(self.handle, s2[b].data_ptr(), o2[b].data_ptr(), wptr, isocenter, window, ws, wsb,
+               self._stream(stream))
         return out
+
+    def fbp(self, sino, out=None, window="ram-lak", view_weights=None, isocenter=None,
+            workspace=None, stream=None):
+        """Filtered backprojection (FBP / FDK) of a sinogram; leading dimensions are kept and
+        reconstructed one after another with the same workspace."""
+        return self._fbp_call(ct_fbp, sino, self.sino_shape, self.volume_shape, out, window,
+                              view_weights, isocenter, workspace, stream)
+
+    def fbp_transpose(self, volume, out=None, window="ram-lak", view_weights=None,
+                      isocenter=None, workspace=None, stream=None):
+        """Transpose of ``fbp`` (volume -> sinogram); leading dimensions are kept."""
+        return self._fbp_call(ct_fbp_transpose, volume, self.volume_shape, self.sino_shape, out,
+                              window, view_weights, isocenter, workspace, stream)

@@ -780,10 +780,13 @@ extern "C" size_t ct_fbp_workspace_bytes(const ct_geometry* g) {
     return g == nullptr ? 0 : fbp_layout(g).total;
 }
 
-extern "C" ct_status ct_fbp(const ct_geometry* g, const float* d_sino, float* d_volume,
-                            const float* d_view_weights, const double* isocenter,
-                            ct_fbp_window window, void* d_workspace, size_t workspace_bytes,
-                            cudaStream_t stream) {
+namespace {
+
+// Argument checks shared by ct_fbp and ct_fbp_transpose; fills the kernel parameters.
+ct_status fbp_setup(const ct_geometry* g, const void* in, size_t in_bytes, const void* out,
+                    size_t out_bytes, const float* d_view_weights, const double* isocenter,
+                    ct_fbp_window window, const void* d_workspace, size_t workspace_bytes,
+                    ct::FbpParams* P, FbpLayout* L) {
     if (g == nullptr) return CT_ERR_INVALID_ARGUMENT;
     const int b = g->info.beam;
     if (b == CT_PARALLEL3D || g->d_offsets != nullptr) return CT_ERR_INVALID_ARGUMENT;
@@ -801,37 +804,71 @@ extern "C" ct_status ct_fbp(const ct_geometry* g, const float* d_sino, float* d_
             iso[a] = isocenter[a];
         }
     }
-    const FbpLayout L = fbp_layout(g);
-    ct_status st = check_call(g, d_sino, sino_bytes(g), d_volume, volume_bytes(g), d_workspace,
-                              workspace_bytes, L.total);
+    *L = fbp_layout(g);
+    ct_status st = check_call(g, in, in_bytes, out, out_bytes, d_workspace, workspace_bytes,
+                              L->total);
     if (st != CT_OK) return st;
     const size_t wbytes = sizeof(float) * (size_t)g->info.n_views;
     if (d_view_weights != nullptr) {
         if ((st = check_device_ptr(d_view_weights, g->device)) != CT_OK) return st;
-        if (overlap(d_view_weights, wbytes, d_volume, volume_bytes(g)) ||
-            overlap(d_view_weights, wbytes, d_workspace, L.total))
+        if (overlap(d_view_weights, wbytes, out, out_bytes) ||
+            overlap(d_view_weights, wbytes, d_workspace, L->total))
             return CT_ERR_ALIASING;
     }
+    ct::FbpParams& p = *P;
+    p.n_views = g->info.n_views;
+    p.n_u = g->info.n_u;
+    p.n_v = g->info.n_v;
+    p.nx = g->info.nx; p.ny = g->info.ny; p.nz = g->info.nz;
+    p.two_d = is_2d(b) ? 1 : 0;
+    p.parallel = is_parallel(b) ? 1 : 0;
+    p.window = (int32_t)window;
+    p.rows = L->rows;
+    p.cols = L->cols;
+    p.du = g->du;
+    p.dv = g->dv;
+    for (int a = 0; a < 3; ++a) p.iso[a] = iso[a];
+    p.sx = g->grid.sp[0];
+    p.sy = g->grid.sp[1];
+    p.sz = g->grid.sp[2];
+    return CT_OK;
+}
+
+}  // namespace
+
+extern "C" ct_status ct_fbp(const ct_geometry* g, const float* d_sino, float* d_volume,
+                            const float* d_view_weights, const double* isocenter,
+                            ct_fbp_window window, void* d_workspace, size_t workspace_bytes,
+                            cudaStream_t stream) {
     ct::FbpParams P;
-    P.n_views = g->info.n_views;
-    P.n_u = g->info.n_u;
-    P.n_v = g->info.n_v;
-    P.nx = g->info.nx; P.ny = g->info.ny; P.nz = g->info.nz;
-    P.two_d = is_2d(b) ? 1 : 0;
-    P.parallel = is_parallel(b) ? 1 : 0;
-    P.window = (int32_t)window;
-    P.rows = L.rows;
-    P.cols = L.cols;
-    P.du = g->du;
-    P.dv = g->dv;
-    for (int a = 0; a < 3; ++a) P.iso[a] = iso[a];
-    P.sx = g->grid.sp[0];
-    P.sy = g->grid.sp[1];
-    P.sz = g->grid.sp[2];
+    FbpLayout L;
+    if (g == nullptr) return CT_ERR_INVALID_ARGUMENT;
+    const ct_status st = fbp_setup(g, d_sino, sino_bytes(g), d_volume, volume_bytes(g),
+                                   d_view_weights, isocenter, window, d_workspace,
+                                   workspace_bytes, &P, &L);
+    if (st != CT_OK) return st;
     char* ws = static_cast<char*>(d_workspace);
     return from_cuda(ct::launch_fbp(P, g->d_raw, d_view_weights,
                                     reinterpret_cast<ct::FbpView*>(ws + L.views),
                                     reinterpret_cast<ct::FbpCosine*>(ws + L.cosines),
                                     reinterpret_cast<float*>(ws + L.taps), d_sino,
                                     reinterpret_cast<float*>(ws + L.filtered), d_volume, stream));
+}
+
+extern "C" ct_status ct_fbp_transpose(const ct_geometry* g, const float* d_volume, float* d_sino,
+                                      const float* d_view_weights, const double* isocenter,
+                                      ct_fbp_window window, void* d_workspace,
+                                      size_t workspace_bytes, cudaStream_t stream) {
+    ct::FbpParams P;
+    FbpLayout L;
+    if (g == nullptr) return CT_ERR_INVALID_ARGUMENT;
+    const ct_status st = fbp_setup(g, d_volume, volume_bytes(g), d_sino, sino_bytes(g),
+                                   d_view_weights, isocenter, window, d_workspace,
+                                   workspace_bytes, &P, &L);
+    if (st != CT_OK) return st;
+    char* ws = static_cast<char*>(d_workspace);
+    return from_cuda(ct::launch_fbp_transpose(
+        P, g->d_raw, d_view_weights, reinterpret_cast<ct::FbpView*>(ws + L.views),
+        reinterpret_cast<ct::FbpCosine*>(ws + L.cosines), reinterpret_cast<float*>(ws + L.taps),
+        d_volume, reinterpret_cast<float*>(ws + L.filtered), d_sino, stream));
 }

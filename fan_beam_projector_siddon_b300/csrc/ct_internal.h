@@ -144,5 +144,11 @@ static_assert(sizeof(FbpCosine) == 48, "FbpCosine layout");
 cudaError_t launch_fbp(const FbpParams& p, const double* raw_views, const float* view_weights,
                        FbpView* views, FbpCosine* cosines, float* taps, const float* sino,
                        float* filtered, float* vol, cudaStream_t stream);
+// Transpose of the same operator: volume -> sinogram.  `scattered` is the padded array (the
+// filtered-sinogram slot of the scratch); it is cleared on the stream first.
+cudaError_t launch_fbp_transpose(const FbpParams& p, const double* raw_views,
+                                 const float* view_weights, FbpView* views, FbpCosine* cosines,
+                                 float* taps, const float* vol, float* scattered, float* sino,
+                                 cudaStream_t stream);
 
 }  // namespace ct

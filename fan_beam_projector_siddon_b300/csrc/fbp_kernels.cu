@@ -180,10 +180,13 @@ __device__ void write_pads(const FbpParams& p, int view, int v0, int nv, float* 
 // Cosine pre-weight and linear convolution along u for one view and a tile of tv detector
 // columns (v values); one output per thread and step.  Shared memory: the pre-weighted tile
 // [n_u][tv] and the taps.  Used for 2D sinograms (one column a view) and wide detectors.
+// ADJ (the transpose): the input is the padded array (interior only), the convolution is the same
+// (its matrix is symmetric) and the cosine weight multiplies the output instead.
+template <bool ADJ>
 __global__ void __launch_bounds__(256) fbp_filter_kernel(FbpParams p,
                                                         const FbpCosine* __restrict__ cosines,
                                                         const float* __restrict__ taps,
-                                                        const float* __restrict__ sino,
+                                                        const float* __restrict__ in,
                                                         float* __restrict__ out, int tv,
                                                         int v_blocks) {
     extern __shared__ float sm[];
@@ -193,38 +196,47 @@ __global__ void __launch_bounds__(256) fbp_filter_kernel(FbpParams p,
     const int view = blockIdx.x / v_blocks;
     const int v0 = (blockIdx.x - view * v_blocks) * tv;
     const int nv = min(tv, V - v0);
+    const int vo = p.two_d ? 0 : 1;
     const FbpCosine C = cosines[view];
     for (int i = threadIdx.x; i < 2 * n_u - 1; i += blockDim.x) stap[i] = taps[i];
     for (int i = threadIdx.x; i < n_u * tv; i += blockDim.x) {
         const int iu = i / tv, j = i - iu * tv;
         float val = 0.0f;
         if (j < nv) {
-            val = sino[((int64_t)view * n_u + iu) * V + v0 + j];
-            if (!p.parallel) val *= cosine_weight(C, iu, v0 + j);
+            if (ADJ) {
+                val = in[qrow(p, view, iu) + v0 + j + vo];
+            } else {
+                val = in[((int64_t)view * n_u + iu) * V + v0 + j];
+                if (!p.parallel) val *= cosine_weight(C, iu, v0 + j);
+            }
         }
         tile[i] = val;
     }
     __syncthreads();
-    const int vo = p.two_d ? 0 : 1;
     for (int i = threadIdx.x; i < n_u * tv; i += blockDim.x) {
         const int iu = i / tv, j = i - iu * tv;
         if (j >= nv) continue;
         float acc = 0.0f;
         const float* h = stap + (iu + n_u - 1);  // h[iu - k] = stap[iu - k + n_u - 1]
         for (int k = 0; k < n_u; ++k) acc = fmaf(h[-k], tile[k * tv + j], acc);
-        out[qrow(p, view, iu) + v0 + j + vo] = acc;
+        if (ADJ) {
+            if (!p.parallel) acc *= cosine_weight(C, iu, v0 + j);
+            out[((int64_t)view * n_u + iu) * V + v0 + j] = acc;
+        } else {
+            out[qrow(p, view, iu) + v0 + j + vo] = acc;
+        }
     }
-    write_pads(p, view, v0, nv, out);
+    if (!ADJ) write_pads(p, view, v0, nv, out);
 }
 
 // The same filter for 3D sinograms, 32 columns a block (one per lane) and R consecutive outputs
 // a thread: each step loads R tile values and 2R - 1 taps (broadcast) for R * R FMAs.  The tile
 // has n_pad >= n_u rows (multiple of R, zero beyond n_u); taps are stored so that
 // stap[m] = h(m - (n_pad - 1)), zero outside the filter's support.
-template <int R>
+template <int R, bool ADJ>
 __global__ void __launch_bounds__(256) fbp_filter_blocked_kernel(
     FbpParams p, const FbpCosine* __restrict__ cosines, const float* __restrict__ taps,
-    const float* __restrict__ sino, float* __restrict__ out, int n_pad, int v_blocks) {
+    const float* __restrict__ in, float* __restrict__ out, int n_pad, int v_blocks) {
     extern __shared__ float sm[];
     float* tile = sm;                     // [n_pad][32]
     float* stap = sm + (int64_t)n_pad * 32;  // [2 n_pad]
@@ -243,8 +255,12 @@ __global__ void __launch_bounds__(256) fbp_filter_blocked_kernel(
         const int k = i >> 5, j = i & 31;
         float val = 0.0f;
         if (k < n_u && j < nv) {
-            val = sino[((int64_t)view * n_u + k) * V + v0 + j];
-            if (!p.parallel) val *= cosine_weight(C, k, v0 + j);
+            if (ADJ) {
+                val = in[qrow(p, view, k) + v0 + j + 1];
+            } else {
+                val = in[((int64_t)view * n_u + k) * V + v0 + j];
+                if (!p.parallel) val *= cosine_weight(C, k, v0 + j);
+            }
         }
         tile[i] = val;
     }
@@ -267,11 +283,19 @@ __global__ void __launch_bounds__(256) fbp_filter_blocked_kernel(
         }
         if (lane < nv) {
 #pragma unroll
-            for (int r = 0; r < R; ++r)
-                if (r0 + r < n_u) out[qrow(p, view, r0 + r) + v0 + lane + 1] = acc[r];
+            for (int r = 0; r < R; ++r) {
+                if (r0 + r >= n_u) continue;
+                if (ADJ) {
+                    const float a = p.parallel ? acc[r]
+                                               : acc[r] * cosine_weight(C, r0 + r, v0 + lane);
+                    out[((int64_t)view * n_u + r0 + r) * V + v0 + lane] = a;
+                } else {
+                    out[qrow(p, view, r0 + r) + v0 + lane + 1] = acc[r];
+                }
+            }
         }
     }
-    write_pads(p, view, v0, nv, out);
+    if (!ADJ) write_pads(p, view, v0, nv, out);
 }
 
 // Cone-beam (FDK) gather.  Block: 8 warps, one x each; lane l of a warp takes the NZ voxels
@@ -443,89 +467,308 @@ __global__ void __launch_bounds__(256) fbp2d_gather_kernel(FbpParams p,
     }
 }
 
+// Transpose of the cone-beam gather: every voxel adds w g f(X) times its four bilinear
+// coefficients to the padded filtered-sinogram array (contributions that land in the pads are
+// discarded later).  Same block shape, view passes and z-independent path as the gather.
+template <int NZ>
+__global__ void __launch_bounds__(256) fdk_scatter_kernel(FbpParams p,
+                                                         const FbpView* __restrict__ views,
+                                                         const float* __restrict__ vol,
+                                                         float* __restrict__ q, int k_begin,
+                                                         int k_end) {
+    constexpr int kChunk = 64;
+    __shared__ float4 sv[kChunk * 4];
+    __shared__ float st[8][NZ * 32 + 1];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int z0 = blockIdx.x * (32 * NZ);
+    const int x0 = blockIdx.y * 8;
+    const int ix = x0 + warp;
+    const int iy = blockIdx.z;
+    // voxel values, loaded along x and transposed through shared memory
+    for (int i = threadIdx.x; i < 8 * 32 * NZ; i += blockDim.x) {
+        const int zz = i >> 3, xx = i & 7;
+        const int oz = z0 + zz, ox = x0 + xx;
+        st[xx][zz] = (oz < p.nz && ox < p.nx) ? vol[((int64_t)oz * p.ny + iy) * p.nx + ox] : 0.0f;
+    }
+    __syncthreads();
+    const float X = ((float)ix + 0.5f - 0.5f * p.nx) * p.sx;
+    const float Y = ((float)iy + 0.5f - 0.5f * p.ny) * p.sy;
+    float Z[NZ], f[NZ];
+#pragma unroll
+    for (int m = 0; m < NZ; ++m) {
+        Z[m] = ((float)(z0 + lane + 32 * m) + 0.5f - 0.5f * p.nz) * p.sz;
+        f[m] = st[warp][lane + 32 * m];
+    }
+    const int cols = p.cols;
+    const int64_t view_stride = (int64_t)p.rows * cols;
+    const float umax = (float)p.n_u, vmax = (float)p.n_v;
+    for (int k0 = k_begin; k0 < k_end; k0 += kChunk) {
+        __syncthreads();
+        const int nk = min(kChunk, k_end - k0);
+        for (int i = threadIdx.x; i < nk * 4; i += blockDim.x)
+            sv[i] = reinterpret_cast<const float4*>(views + k0)[i];
+        __syncthreads();
+        float* base = q + (int64_t)k0 * view_stride;
+        for (int k = 0; k < nk; ++k, base += view_stride) {
+            const float4 A = sv[4 * k], B = sv[4 * k + 1], C = sv[4 * k + 2], E = sv[4 * k + 3];
+            const float ax = X - A.x, ay = Y - A.y;
+            const float den_xy = fmaf(ay, B.x, ax * A.w);
+            const float au_xy = fmaf(ay, B.w, ax * B.z);
+            const float av_xy = fmaf(ay, C.z, ax * C.y);
+            if (B.y == 0.0f && C.x == 0.0f) {  // z-independent u and weight (see the gather)
+                const float inv = rcp_approx(den_xy);
+                const float t = E.x * inv;
+                const float up = fminf(fmaxf(fmaf(t, au_xy, E.y), -1.0f), umax);
+                const float fu0 = floorf(up), fu = up - fu0;
+                const float g = E.w * inv * inv;
+                float* prow = base + ((int)fu0 + 1) * cols + 1;
+#pragma unroll
+                for (int m = 0; m < NZ; ++m) {
+                    const float av = fmaf(Z[m] - A.z, C.w, av_xy);
+                    const float vp = fminf(fmaxf(fmaf(t, av, E.z), -1.0f), vmax);
+                    const float fv0 = floorf(vp), fv = vp - fv0;
+                    float* pq = prow + (int)fv0;
+                    const float c = g * f[m];
+                    const float c1 = c * fu, c0 = c - c1;
+                    const float c01 = c0 * fv, c11 = c1 * fv;
+                    atomicAdd(pq, c0 - c01);
+                    atomicAdd(pq + 1, c01);
+                    atomicAdd(pq + cols, c1 - c11);
+                    atomicAdd(pq + cols + 1, c11);
+                }
+                continue;
+            }
+#pragma unroll
+            for (int m = 0; m < NZ; ++m) {
+                const float az = Z[m] - A.z;
+                const float den = fmaf(az, B.y, den_xy);
+                const float au = fmaf(az, C.x, au_xy);
+                const float av = fmaf(az, C.w, av_xy);
+                const float inv = rcp_approx(den);
+                const float t = E.x * inv;
+                const float up = fminf(fmaxf(fmaf(t, au, E.y), -1.0f), umax);
+                const float vp = fminf(fmaxf(fmaf(t, av, E.z), -1.0f), vmax);
+                const float fu0 = floorf(up), fv0 = floorf(vp);
+                const float fu = up - fu0, fv = vp - fv0;
+                float* pq = base + ((int)fu0 + 1) * cols + (int)fv0 + 1;
+                const float c = E.w * inv * inv * f[m];
+                const float c1 = c * fu, c0 = c - c1;
+                const float c01 = c0 * fv, c11 = c1 * fv;
+                atomicAdd(pq, c0 - c01);
+                atomicAdd(pq + 1, c01);
+                atomicAdd(pq + cols, c1 - c11);
+                atomicAdd(pq + cols + 1, c11);
+            }
+        }
+    }
+}
+
+// Transpose of the 2D gather (parallel or fan), same block shape as fbp2d_gather_kernel.
+template <bool PAR, int NY>
+__global__ void __launch_bounds__(256) fbp2d_scatter_kernel(FbpParams p,
+                                                           const FbpView* __restrict__ views,
+                                                           const float* __restrict__ vol,
+                                                           float* __restrict__ q) {
+    constexpr int kChunk = 64;
+    __shared__ float4 sv[kChunk * 4];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int ix = blockIdx.x * 32 + lane;
+    const int y0 = blockIdx.y * (8 * NY) + warp;
+    const float X = ((float)ix + 0.5f - 0.5f * p.nx) * p.sx;
+    float Y[NY], f[NY];
+#pragma unroll
+    for (int m = 0; m < NY; ++m) {
+        const int iy = y0 + 8 * m;
+        Y[m] = ((float)iy + 0.5f - 0.5f * p.ny) * p.sy;
+        f[m] = (ix < p.nx && iy < p.ny) ? vol[(int64_t)iy * p.nx + ix] : 0.0f;
+    }
+    const int rows = p.rows;
+    const float umax = (float)p.n_u;
+    for (int k0 = 0; k0 < p.n_views; k0 += kChunk) {
+        __syncthreads();
+        const int nk = min(kChunk, p.n_views - k0);
+        for (int i = threadIdx.x; i < nk * 4; i += blockDim.x)
+            sv[i] = reinterpret_cast<const float4*>(views + k0)[i];
+        __syncthreads();
+        float* base = q + (int64_t)k0 * rows + 1;
+        for (int k = 0; k < nk; ++k, base += rows) {
+            const float4 A = sv[4 * k], B = sv[4 * k + 1], E = sv[4 * k + 3];
+            const float ax = X - A.x;
+            const float den_x = ax * A.w, au_x = ax * B.z;
+            const float ux = fmaf(X, B.z, E.y);
+#pragma unroll
+            for (int m = 0; m < NY; ++m) {
+                float up, c;
+                if (PAR) {
+                    up = fminf(fmaxf(fmaf(Y[m], B.w, ux), -1.0f), umax);
+                    c = E.w * f[m];
+                } else {
+                    const float ay = Y[m] - A.y;
+                    const float den = fmaf(ay, B.x, den_x);
+                    const float au = fmaf(ay, B.w, au_x);
+                    const float inv = rcp_approx(den);
+                    up = fminf(fmaxf(fmaf(E.x * inv, au, E.y), -1.0f), umax);
+                    c = E.w * inv * inv * f[m];
+                }
+                const float fu0 = floorf(up), fu = up - fu0;
+                float* pq = base + (int)fu0;
+                const float c1 = c * fu;
+                atomicAdd(pq, c - c1);
+                atomicAdd(pq + 1, c1);
+            }
+        }
+    }
+}
+
 constexpr int kFilterR = 16;
 constexpr size_t kSmemBudget = 200u * 1024u;
+
+// Filter stage (forward: sinogram -> padded array; ADJ: padded array -> sinogram).
+template <bool ADJ>
+cudaError_t launch_filter(const FbpParams& p, const FbpCosine* cosines, const float* taps,
+                          const float* in, float* out, cudaStream_t stream) {
+    cudaError_t e;
+    const int V = p.two_d ? 1 : p.n_v;
+    const int n_pad = (p.n_u + kFilterR - 1) / kFilterR * kFilterR;
+    const size_t blocked_smem = sizeof(float) * ((size_t)n_pad * 32 + 2 * (size_t)n_pad);
+    if (!p.two_d && blocked_smem <= kSmemBudget) {
+        e = cudaFuncSetAttribute(fbp_filter_blocked_kernel<kFilterR, ADJ>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)blocked_smem);
+        if (e != cudaSuccess) return e;
+        const int v_blocks = (V + 31) / 32;
+        if ((int64_t)v_blocks * p.n_views > (int64_t)INT32_MAX) return cudaErrorInvalidValue;
+        fbp_filter_blocked_kernel<kFilterR, ADJ>
+            <<<v_blocks * p.n_views, 256, blocked_smem, stream>>>(p, cosines, taps, in, out, n_pad,
+                                                                  v_blocks);
+        return cudaGetLastError();
+    }
+    // columns per block: as many (up to 32) as fit in shared memory with the taps
+    const size_t tap_bytes = sizeof(float) * (size_t)(2 * p.n_u - 1);
+    int tv = 32;
+    while (tv > 1 && (size_t)tv * p.n_u * sizeof(float) + tap_bytes > kSmemBudget) tv >>= 1;
+    if (tv > V) tv = V;
+    const size_t smem = (size_t)tv * p.n_u * sizeof(float) + tap_bytes;
+    if (smem > kSmemBudget) return cudaErrorInvalidValue;
+    e = cudaFuncSetAttribute(fbp_filter_kernel<ADJ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e != cudaSuccess) return e;
+    const int v_blocks = (V + tv - 1) / tv;
+    if ((int64_t)v_blocks * p.n_views > (int64_t)INT32_MAX) return cudaErrorInvalidValue;
+    fbp_filter_kernel<ADJ><<<v_blocks * p.n_views, 256, smem, stream>>>(p, cosines, taps, in, out,
+                                                                       tv, v_blocks);
+    return cudaGetLastError();
+}
+
+// Views per gather/scatter pass: the pass's filtered slices fit in L2 together (about 48 MB),
+// so that all resident blocks touch the same views.
+int views_per_pass(const FbpParams& p) {
+    const size_t slice = sizeof(float) * (size_t)p.rows * (size_t)p.cols;
+    int per_pass = (int)std::min<size_t>((size_t)p.n_views, (48u << 20) / slice);
+    return per_pass < 16 ? 16 : per_pass / 16 * 16;
+}
+
+cudaError_t launch_prepare(const FbpParams& p, const double* raw, const float* user_weights,
+                           FbpView* views, FbpCosine* cosines, float* taps, cudaStream_t stream) {
+    const int n_prep = p.n_views > 2 * p.n_u - 1 ? p.n_views : 2 * p.n_u - 1;
+    fbp_prepare_kernel<<<(n_prep + 255) / 256, 256, 0, stream>>>(p, raw, user_weights, views,
+                                                                 cosines, taps);
+    return cudaGetLastError();
+}
 
 }  // namespace
 
 cudaError_t launch_fbp(const FbpParams& p, const double* raw, const float* user_weights,
                        FbpView* views, FbpCosine* cosines, float* taps, const float* sino,
                        float* filtered, float* vol, cudaStream_t stream) {
-    const int n_prep = p.n_views > 2 * p.n_u - 1 ? p.n_views : 2 * p.n_u - 1;
-    fbp_prepare_kernel<<<(n_prep + 255) / 256, 256, 0, stream>>>(p, raw, user_weights, views,
-                                                                 cosines, taps);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_prepare(p, raw, user_weights, views, cosines, taps, stream);
     if (e != cudaSuccess) return e;
-    const int V = p.two_d ? 1 : p.n_v;
-    const int n_pad = (p.n_u + kFilterR - 1) / kFilterR * kFilterR;
-    const size_t blocked_smem = sizeof(float) * ((size_t)n_pad * 32 + 2 * (size_t)n_pad);
-    if (!p.two_d && blocked_smem <= kSmemBudget) {
-        e = cudaFuncSetAttribute(fbp_filter_blocked_kernel<kFilterR>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)blocked_smem);
-        if (e != cudaSuccess) return e;
-        const int v_blocks = (V + 31) / 32;
-        if ((int64_t)v_blocks * p.n_views > (int64_t)INT32_MAX) return cudaErrorInvalidValue;
-        fbp_filter_blocked_kernel<kFilterR><<<v_blocks * p.n_views, 256, blocked_smem, stream>>>(
-            p, cosines, taps, sino, filtered, n_pad, v_blocks);
-    } else {
-        // columns per block: as many (up to 32) as fit in shared memory with the taps
-        const size_t tap_bytes = sizeof(float) * (size_t)(2 * p.n_u - 1);
-        int tv = 32;
-        while (tv > 1 && (size_t)tv * p.n_u * sizeof(float) + tap_bytes > kSmemBudget) tv >>= 1;
-        if (tv > V) tv = V;
-        const size_t smem = (size_t)tv * p.n_u * sizeof(float) + tap_bytes;
-        if (smem > kSmemBudget) return cudaErrorInvalidValue;
-        e = cudaFuncSetAttribute(fbp_filter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
-        if (e != cudaSuccess) return e;
-        const int v_blocks = (V + tv - 1) / tv;
-        if ((int64_t)v_blocks * p.n_views > (int64_t)INT32_MAX) return cudaErrorInvalidValue;
-        fbp_filter_kernel<<<v_blocks * p.n_views, 256, smem, stream>>>(p, cosines, taps, sino,
-                                                                      filtered, tv, v_blocks);
-    }
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_filter<false>(p, cosines, taps, sino, filtered, stream)) != cudaSuccess)
+        return e;
     if (p.two_d) {
-        const int ny_blocks_4 = (p.ny + 31) / 32, ny_blocks_1 = (p.ny + 7) / 8;
         if (p.ny >= 128) {
-            if (ny_blocks_4 > 65535) return cudaErrorInvalidValue;
-            dim3 g((p.nx + 31) / 32, ny_blocks_4);
+            if ((p.ny + 31) / 32 > 65535) return cudaErrorInvalidValue;
+            dim3 g((p.nx + 31) / 32, (p.ny + 31) / 32);
             if (p.parallel)
                 fbp2d_gather_kernel<true, 4><<<g, 256, 0, stream>>>(p, views, filtered, vol);
             else
                 fbp2d_gather_kernel<false, 4><<<g, 256, 0, stream>>>(p, views, filtered, vol);
         } else {
-            dim3 g((p.nx + 31) / 32, ny_blocks_1);
+            dim3 g((p.nx + 31) / 32, (p.ny + 7) / 8);
             if (p.parallel)
                 fbp2d_gather_kernel<true, 1><<<g, 256, 0, stream>>>(p, views, filtered, vol);
             else
                 fbp2d_gather_kernel<false, 1><<<g, 256, 0, stream>>>(p, views, filtered, vol);
         }
+        return cudaGetLastError();
+    }
+    if ((p.nx + 7) / 8 > 65535 || p.ny > 65535) return cudaErrorInvalidValue;
+    const int per_pass = views_per_pass(p);
+    for (int k = 0; k < p.n_views; k += per_pass) {
+        const int k_end = std::min(p.n_views, k + per_pass);
+        if (p.nz >= 192) {
+            dim3 g((p.nz + 255) / 256, (p.nx + 7) / 8, p.ny);
+            fdk_gather_kernel<8><<<g, 256, 0, stream>>>(p, views, filtered, vol, k, k_end);
+        } else if (p.nz >= 96) {
+            dim3 g((p.nz + 127) / 128, (p.nx + 7) / 8, p.ny);
+            fdk_gather_kernel<4><<<g, 256, 0, stream>>>(p, views, filtered, vol, k, k_end);
+        } else if (p.nz >= 48) {
+            dim3 g((p.nz + 63) / 64, (p.nx + 7) / 8, p.ny);
+            fdk_gather_kernel<2><<<g, 256, 0, stream>>>(p, views, filtered, vol, k, k_end);
+        } else {
+            dim3 g((p.nz + 31) / 32, (p.nx + 7) / 8, p.ny);
+            fdk_gather_kernel<1><<<g, 256, 0, stream>>>(p, views, filtered, vol, k, k_end);
+        }
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t launch_fbp_transpose(const FbpParams& p, const double* raw, const float* user_weights,
+                                 FbpView* views, FbpCosine* cosines, float* taps,
+                                 const float* vol, float* scattered, float* sino,
+                                 cudaStream_t stream) {
+    cudaError_t e = launch_prepare(p, raw, user_weights, views, cosines, taps, stream);
+    if (e != cudaSuccess) return e;
+    const size_t qbytes = sizeof(float) * (size_t)p.n_views * (size_t)p.rows * (size_t)p.cols;
+    if ((e = cudaMemsetAsync(scattered, 0, qbytes, stream)) != cudaSuccess) return e;
+    if (p.two_d) {
+        if (p.ny >= 128) {
+            if ((p.ny + 31) / 32 > 65535) return cudaErrorInvalidValue;
+            dim3 g((p.nx + 31) / 32, (p.ny + 31) / 32);
+            if (p.parallel)
+                fbp2d_scatter_kernel<true, 4><<<g, 256, 0, stream>>>(p, views, vol, scattered);
+            else
+                fbp2d_scatter_kernel<false, 4><<<g, 256, 0, stream>>>(p, views, vol, scattered);
+        } else {
+            dim3 g((p.nx + 31) / 32, (p.ny + 7) / 8);
+            if (p.parallel)
+                fbp2d_scatter_kernel<true, 1><<<g, 256, 0, stream>>>(p, views, vol, scattered);
+            else
+                fbp2d_scatter_kernel<false, 1><<<g, 256, 0, stream>>>(p, views, vol, scattered);
+        }
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
     } else {
         if ((p.nx + 7) / 8 > 65535 || p.ny > 65535) return cudaErrorInvalidValue;
-        // Views in passes whose filtered slices fit in L2 together (about 48 MB), so that all
-        // resident blocks read the same views; later passes add to the volume.
-        const size_t slice = sizeof(float) * (size_t)p.rows * (size_t)p.cols;
-        int per_pass = (int)std::min<size_t>((size_t)p.n_views, (48u << 20) / slice);
-        per_pass = per_pass < 16 ? 16 : per_pass / 16 * 16;
+        const int per_pass = views_per_pass(p);
         for (int k = 0; k < p.n_views; k += per_pass) {
             const int k_end = std::min(p.n_views, k + per_pass);
             if (p.nz >= 192) {
                 dim3 g((p.nz + 255) / 256, (p.nx + 7) / 8, p.ny);
-                fdk_gather_kernel<8><<<g, 256, 0, stream>>>(p, views, filtered, vol, k, k_end);
+                fdk_scatter_kernel<8><<<g, 256, 0, stream>>>(p, views, vol, scattered, k, k_end);
             } else if (p.nz >= 96) {
                 dim3 g((p.nz + 127) / 128, (p.nx + 7) / 8, p.ny);
-                fdk_gather_kernel<4><<<g, 256, 0, stream>>>(p, views, filtered, vol, k, k_end);
+                fdk_scatter_kernel<4><<<g, 256, 0, stream>>>(p, views, vol, scattered, k, k_end);
             } else if (p.nz >= 48) {
                 dim3 g((p.nz + 63) / 64, (p.nx + 7) / 8, p.ny);
-                fdk_gather_kernel<2><<<g, 256, 0, stream>>>(p, views, filtered, vol, k, k_end);
+                fdk_scatter_kernel<2><<<g, 256, 0, stream>>>(p, views, vol, scattered, k, k_end);
             } else {
                 dim3 g((p.nz + 31) / 32, (p.nx + 7) / 8, p.ny);
-                fdk_gather_kernel<1><<<g, 256, 0, stream>>>(p, views, filtered, vol, k, k_end);
+                fdk_scatter_kernel<1><<<g, 256, 0, stream>>>(p, views, vol, scattered, k, k_end);
             }
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
         }
     }
-    return cudaGetLastError();
+    return launch_filter<true>(p, cosines, taps, scattered, sino, stream);
 }
 
 }  // namespace ct

@@ -313,6 +313,23 @@ CT_API ct_status ct_fbp(const ct_geometry *geom, const float *d_sino, float *d_v
                         ct_fbp_window window, void *d_workspace, size_t workspace_bytes,
                         struct CUstream_st *stream);
 
+/*
+ * Transpose of ct_fbp as a linear map (sinogram -> volume), for gradients with respect to the
+ * sinogram: d_sino = F^T d_volume, so that <F y, x> = <y, F^T x>.  The pages state that the
+ * analytical operator's backward pass scatters the same interpolation coefficients, distance
+ * weights and normalisation, with dedicated transpose kernels (diffct "Differentiable analytical
+ * reconstruction"; "Analytical Reconstruction Helpers").  Steps: every voxel adds
+ * w_k g_k(X) f(X) times its four bilinear coefficients onto view k's detector (atomic adds;
+ * contributions off the detector are dropped), the same filter (its matrix du h((i - j) du) is
+ * symmetric), then the cosine weights.  Arguments, workspace and errors as for ct_fbp, with
+ * d_volume read and d_sino overwritten.  The atomic adds make the float32 result depend on
+ * the order in which they land (run-to-run differences of a few ulp).
+ */
+CT_API ct_status ct_fbp_transpose(const ct_geometry *geom, const float *d_volume, float *d_sino,
+                                  const float *d_view_weights, const double *isocenter,
+                                  ct_fbp_window window, void *d_workspace,
+                                  size_t workspace_bytes, struct CUstream_st *stream);
+
 /* Static, human-readable name of a status code. */
 CT_API const char *ct_status_string(ct_status status);
 

@@ -92,6 +92,7 @@ def test_null_arguments_are_rejected(lib):
     assert L.ct_sirt_workspace_bytes(None) == 0
     assert L.ct_fbp(None, None, None, None, None, 0, None, 0, None) == 1
     assert L.ct_fbp_workspace_bytes(None) == 0
+    assert L.ct_fbp_transpose(None, None, None, None, None, 0, None, 0, None) == 1
 
 
 def test_surface_admission_before_touching_the_gpu(lib):

@@ -203,3 +203,54 @@ def test_wide_detector_uses_the_plain_filter(ct):
     g = ct.Geometry.from_workload(w)
     got = _cpu(g.fbp(torch_cuda(sino)))
     _check(got, _oracle(w, sino.astype(np.float64)), n_u=w.n_u)
+
+
+# ---------------------------------------------------------------------------------------------
+# transpose (volume -> sinogram)
+# ---------------------------------------------------------------------------------------------
+
+def _oracle_t(w, vol, **kw):
+    return F.fbp_transpose(w.beam, w.views, w.vol_shape, w.voxel_spacing, w.n_u, w.n_v, w.du,
+                           w.dv, vol, **kw)
+
+
+def _vol(w, seed):
+    return W.random_volume(w, seed)
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4])
+def test_transpose_matches_oracle(ct, n):
+    w = W.small_config(n)
+    x = _vol(w, 60 + n)
+    g = ct.Geometry.from_workload(w)
+    got = _cpu(g.fbp_transpose(torch_cuda(x), window="cosine"))
+    _check(got, _oracle_t(w, x.astype(np.float64), window="cosine"))
+
+
+@pytest.mark.parametrize("n,shape", [(3, (50, 21, 19)), (3, (101, 13, 17)), (3, (200, 7, 9)),
+                                     (4, (200, 7, 9)), (2, (1, 130, 41)), (1, (1, 131, 37))])
+def test_transpose_variants(ct, n, shape):
+    import dataclasses
+    w = dataclasses.replace(W.small_config(n), vol_shape=shape)
+    x = _vol(w, 23)
+    wts = np.random.default_rng(9).uniform(0.0, 0.05, size=w.views.shape[0]).astype(np.float32)
+    iso = (0.5, 1.25, -0.75)[: 2 if w.beam in (0, 1) else 3]
+    g = ct.Geometry.from_workload(w)
+    got = _cpu(g.fbp_transpose(torch_cuda(x), view_weights=torch_cuda(wts), isocenter=iso))
+    _check(got, _oracle_t(w, x.astype(np.float64), view_weights=wts.astype(np.float64),
+                          isocenter=iso))
+
+
+@pytest.mark.parametrize("full", [False, True])
+def test_adjoint_identity_on_the_gpu(ct, full):
+    """<F y, x> = <y, F^T x> with both sides computed by the CUDA path; at full size (the cone
+    256^3 x 360 workload) this is the transpose's check, the oracle being too slow there."""
+    w = W.config(3) if full else W.small_config(3)
+    g = ct.Geometry.from_workload(w)
+    y = W.random_sinogram(w, 31)
+    x = _vol(w, 32)
+    Fy = _cpu(g.fbp(torch_cuda(y), window="hamming")).astype(np.float64)
+    Ftx = _cpu(g.fbp_transpose(torch_cuda(x), window="hamming")).astype(np.float64)
+    lhs, rhs = float(np.sum(Fy * x)), float(np.sum(y * Ftx))
+    scale = np.linalg.norm(Fy) * np.linalg.norm(x)
+    assert abs(lhs - rhs) <= 1e-5 * scale, (lhs, rhs, scale)
