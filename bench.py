@@ -335,6 +335,69 @@ def batch_leg(ct, torch, w, U, nb: int = 4, reps: int = 3):
             "pair_updates_per_s": 2 * nb * U / ((fp + bp) * 1e-3)}
 
 
+FDK_FLOPS_PER_VOXEL_VIEW = 38   # projection 23, distance weight 2, bilinear 11, accumulate 2
+FP32_LANES_PER_SM, N_SMS, SM_MAX_GHZ = 128, 148, 2.032
+
+
+def fdk_leg(ct, torch, w, reps: int = 5, cpu_baseline: bool = True):
+    """Filtered backprojection (FDK, Ram-Lak window) of the metric workload's geometry and its
+    transpose, CUDA events around each C-ABI call, L2 flushed before each.  Rate in voxel-view
+    updates per second; the roofline is the float32 ALU one (the gather kernel is issue-bound):
+    38 algorithmic flops per voxel-view against 148 SMs x 128 lanes x 2 flops x 2.032 GHz."""
+    g = ct.Geometry.from_workload(w)
+    sino = torch.from_numpy(W.random_sinogram(w, 11)).cuda()
+    vol = torch.empty(g.volume_shape, device="cuda")
+    ws = torch.empty(ct.ct_fbp_workspace_bytes(g.handle), dtype=torch.uint8, device="cuda")
+    out_t = torch.empty_like(sino)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    fw, tr = [], []
+    for k in range(reps + 2):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        flush.zero_()
+        e[0].record(stream)
+        g.fbp(sino, out=vol, workspace=ws)
+        e[1].record(stream)
+        flush.zero_()
+        e[2].record(stream)
+        g.fbp_transpose(vol, out=out_t, workspace=ws)
+        e[3].record(stream)
+        torch.cuda.synchronize()
+        if k >= 2:
+            fw.append(e[0].elapsed_time(e[1]))
+            tr.append(e[2].elapsed_time(e[3]))
+    fms, tms = statistics.median(fw), statistics.median(tr)
+    vv = w.n_voxels * w.n_views
+    peak = N_SMS * FP32_LANES_PER_SM * 2 * SM_MAX_GHZ * 1e9 / 1e12
+    achieved = FDK_FLOPS_PER_VOXEL_VIEW * vv / (fms * 1e-3) / 1e12
+    out = {"workload": w.name, "window": "ram-lak", "fdk_ms": fms, "transpose_ms": tms,
+           "voxel_views": vv, "voxel_views_per_s": vv / (fms * 1e-3),
+           "transpose_voxel_views_per_s": vv / (tms * 1e-3),
+           "roofline": {"bound": "alu", "kernel": "ct_fbp (gather ~87% of it)",
+                        "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                        "frac": achieved / peak,
+                        "peak_source": "derived: 148 SMs x 128 fp32 lanes x 2 x 2.032 GHz",
+                        "flops_model": "38 flops per voxel-view"}}
+    del sino, vol, ws, out_t, flush
+    torch.cuda.empty_cache()
+    if cpu_baseline:
+        from oracle import fbp as F
+        n_views, n_vox = 16, 4096
+        idx_views = np.linspace(0, w.n_views - 1, n_views).round().astype(int)
+        rng = np.random.default_rng(12)
+        vox = np.stack([rng.integers(0, s, n_vox) for s in w.vol_shape], axis=1)
+        sino_h = W.random_sinogram(w, 11)[idx_views].astype(np.float64)
+        t0 = time.perf_counter()
+        F.fbp(w.beam, w.views[idx_views], w.vol_shape, w.voxel_spacing, w.n_u, w.n_v, w.du, w.dv,
+              sino_h, voxels=vox)
+        dt = time.perf_counter() - t0
+        out["cpu_baseline"] = {"value": n_views * n_vox / dt, "unit": "voxel-views/s",
+                               "cores": 1, "kind": "oracle",
+                               "sample": f"{n_vox} voxels x {n_views} views (filtering of the "
+                                         f"{n_views} views included), {dt:.1f} s"}
+    return out
+
+
 def context_leg(ct, torch):
     """The pages' performance-table workload shape (512^3 volume, circular cone, 360 views,
     1024x768 detector at pitch 1.25; sid/sdd are not printed, 1000/1500 is this build's
@@ -531,6 +594,8 @@ def run_ours(args, rank, world):
         "clocks": clocks,
     }
     line["batch4"] = batch_leg(ct, torch, w, U)
+    if not args.no_fdk:
+        line["fdk"] = fdk_leg(ct, torch, w, cpu_baseline=world == 1 and not args.no_cpu_baseline)
     if not args.no_sirt:
         line["sirt"], line["cgls"] = sirt_leg(ct, torch)
     if args.context:
@@ -554,6 +619,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sirt", action="store_true", help="skip the SIRT/CGLS leg")
+    ap.add_argument("--no-fdk", action="store_true", help="skip the FBP/FDK leg")
     ap.add_argument("--context", action="store_true",
                     help="also time the pages' performance-table workload shape")
     ap.add_argument("--sample-views", type=int, default=None,
