@@ -229,17 +229,17 @@ def sample_views(w: W.Workload, requested: int | None) -> int:
     return int(max(1, min(w.n_views, n)))
 
 
-def profiled_traffic(kernel: str):
+def profiled_traffic(kernel: str, source: str = "siddon_kernels.cu"):
     """DRAM bytes per launch of `kernel` from its committed ncu summary, or None when the kernel
     source changed since that capture (the summary records the source's sha256 prefix)."""
     import hashlib
     import glob
-    src = os.path.join(ROOT, "fan_beam_projector_siddon_b300", "csrc", "siddon_kernels.cu")
+    src = os.path.join(ROOT, "fan_beam_projector_siddon_b300", "csrc", source)
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     for path in glob.glob(os.path.join(ROOT, "profiles", f"{kernel}_cone256_360v.md")):
         text = open(path).read()
-        m_sha = re.search(r"sha256 \(first 16 hex digits of `csrc/siddon_kernels.cu`\): ([0-9a-f]{16})",
-                          text)
+        m_sha = re.search(r"sha256 \(first 16 hex digits of `csrc/" + re.escape(source) +
+                          r"`\): ([0-9a-f]{16})", text)
         m_tr = re.search(r"traffic_bytes_per_launch: (\d+)", text)
         if m_sha and m_tr and m_sha.group(1) == sha:
             return int(m_tr.group(1)), os.path.relpath(path, ROOT)
@@ -378,6 +378,9 @@ def fdk_leg(ct, torch, w, reps: int = 5, cpu_baseline: bool = True):
                         "frac": achieved / peak,
                         "peak_source": "derived: 148 SMs x 128 fp32 lanes x 2 x 2.032 GHz",
                         "flops_model": "38 flops per voxel-view"}}
+    traffic, src = profiled_traffic("fdk_gather_kernel", "fbp_kernels.cu")
+    out["roofline"]["traffic"] = traffic
+    out["roofline"]["traffic_source"] = src
     del sino, vol, ws, out_t, flush
     torch.cuda.empty_cache()
     if cpu_baseline:
