@@ -254,3 +254,48 @@ def test_adjoint_identity_on_the_gpu(ct, full):
     lhs, rhs = float(np.sum(Fy * x)), float(np.sum(y * Ftx))
     scale = np.linalg.norm(Fy) * np.linalg.norm(x)
     assert abs(lhs - rhs) <= 1e-5 * scale, (lhs, rhs, scale)
+
+
+# ---------------------------------------------------------------------------------------------
+# edge cases
+# ---------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("case", ["one_view", "one_row", "one_voxel", "one_column"])
+def test_degenerate_shapes(ct, case):
+    import dataclasses
+    base = W.small_config(3)
+    if case == "one_view":
+        w = dataclasses.replace(base, views=base.views[:1])
+    elif case == "one_row":
+        w = dataclasses.replace(base, n_v=1, vol_shape=(5, 21, 23))
+    elif case == "one_voxel":
+        w = dataclasses.replace(base, vol_shape=(1, 1, 1), voxel_spacing=3.0)
+    else:
+        w = dataclasses.replace(base, n_u=1, vol_shape=(9, 4, 5))
+    y = W.random_sinogram(w, 3)
+    x = W.random_volume(w, 4)
+    g = ct.Geometry.from_workload(w)
+    got = _cpu(g.fbp(torch_cuda(y), window="hann"))
+    want = _oracle(w, y.astype(np.float64), window="hann")
+    if np.abs(want).max() > 0:
+        _check(got, want)
+    else:
+        assert np.abs(got).max() == 0
+    got_t = _cpu(g.fbp_transpose(torch_cuda(x), window="hann"))
+    want_t = _oracle_t(w, x.astype(np.float64), window="hann")
+    if np.abs(want_t).max() > 0:
+        _check(got_t, want_t)
+    else:
+        assert np.abs(got_t).max() == 0
+
+
+def test_zero_weights_and_empty_batch(ct):
+    import torch
+    w = W.small_config(2)
+    g = ct.Geometry.from_workload(w)
+    y = torch_cuda(W.random_sinogram(w, 5))
+    zero = torch.zeros(w.views.shape[0], device="cuda")
+    assert _cpu(g.fbp(y, view_weights=zero)).max() == 0
+    assert _cpu(g.fbp_transpose(torch_cuda(W.random_volume(w, 6)), view_weights=zero)).max() == 0
+    empty = torch.zeros((0,) + tuple(g.sino_shape), device="cuda")
+    assert g.fbp(empty).shape == (0,) + tuple(g.volume_shape)
