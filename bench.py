@@ -246,6 +246,25 @@ def profiled_traffic(kernel: str, source: str = "siddon_kernels.cu"):
     return None, None
 
 
+def profiled_sol(kernel: str, source: str = "siddon_kernels.cu"):
+    """ncu speed-of-light figures of `kernel` from its committed summary (percent of ncu's own
+    peaks: memory SOL = max over L1/L2/DRAM, L2 and DRAM throughput), or None when the kernel
+    source changed since the capture."""
+    traffic, path = profiled_traffic(kernel, source)
+    if path is None:
+        return None
+    text = open(os.path.join(ROOT, path)).read()
+    out = {"source": path}
+    for key, label in (("memory_sol_pct", "memory throughput (ncu SOL"),
+                       ("l2_pct", "L2 throughput"), ("dram_pct", "DRAM throughput"),
+                       ("issue_pct", "issue slots busy")):
+        m = re.search(r"\| " + re.escape(label) + r"[^|]*\| ([0-9.]+) %", text)
+        out[key] = float(m.group(1)) if m else None
+    m = re.search(r"\| duration \(sum over captured launches, serialised\) \| ([0-9.]+) ms", text)
+    out["ms"] = float(m.group(1)) if m else None
+    return out
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -337,6 +356,19 @@ def batch_leg(ct, torch, w, U, nb: int = 4, reps: int = 3):
 
 FDK_FLOPS_PER_VOXEL_VIEW = 38   # projection 23, distance weight 2, bilinear 11, accumulate 2
 FP32_LANES_PER_SM, N_SMS, SM_MAX_GHZ = 128, 148, 2.032
+
+
+def ncu_sol():
+    """The pair's ncu-achieved memory fraction (max over L1/L2/DRAM of each walk kernel, weighted
+    by the kernels' durations in the same captures), from the committed profiles."""
+    fp, bp = profiled_sol("project_kernel"), profiled_sol("backproject_kernel")
+    if not fp or not bp or None in (fp["ms"], bp["ms"], fp["memory_sol_pct"],
+                                    bp["memory_sol_pct"]):
+        return None
+    pair = (fp["memory_sol_pct"] * fp["ms"] + bp["memory_sol_pct"] * bp["ms"]) / (fp["ms"] + bp["ms"])
+    return {"project_kernel": fp, "backproject_kernel": bp,
+            "pair_memory_sol_pct": pair,
+            "note": "percent of ncu's own peaks; both walks are issue-bound (see profiles/)"}
 
 
 def fdk_leg(ct, torch, w, reps: int = 5, cpu_baseline: bool = True):
@@ -593,6 +625,7 @@ def run_ours(args, rank, world):
         "e2e": {"value": world * 2 * U / (e2e_ms * 1e-3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "timing": "host wall clock around the steps, copies overlapped on a 2nd stream"},
+        "ncu_sol": ncu_sol(),
         "gpu_launches": 4 * args.steps,
         "clocks": clocks,
     }

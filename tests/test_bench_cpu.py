@@ -90,3 +90,25 @@ def test_reference_arm_non_zero_rank_exits_quietly():
     r = _run_reference({"RANK": "1", "WORLD_SIZE": "2"})
     assert r.returncode == 0, r.stderr
     assert r.stdout.strip() == ""
+
+
+def test_profile_figures_parse_or_are_withheld():
+    """Traffic and ncu speed-of-light figures come from the committed profiles only while the
+    kernel source matches the capture; otherwise they are None (never stale numbers)."""
+    import bench
+    for kern, src in (("project_kernel", "siddon_kernels.cu"),
+                      ("backproject_kernel", "siddon_kernels.cu"),
+                      ("fdk_gather_kernel", "fbp_kernels.cu")):
+        traffic, path = bench.profiled_traffic(kern, src)
+        sol = bench.profiled_sol(kern, src)
+        if path is None:
+            assert traffic is None and sol is None
+            continue
+        assert traffic > 0
+        assert 0 < sol["memory_sol_pct"] <= 100 and 0 < sol["issue_pct"] <= 100
+        assert sol["ms"] > 0
+    pair = bench.ncu_sol()
+    if pair is not None:
+        lo = min(pair["project_kernel"]["memory_sol_pct"], pair["backproject_kernel"]["memory_sol_pct"])
+        hi = max(pair["project_kernel"]["memory_sol_pct"], pair["backproject_kernel"]["memory_sol_pct"])
+        assert lo <= pair["pair_memory_sol_pct"] <= hi
