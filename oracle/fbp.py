@@ -13,6 +13,9 @@ cosine, hamming, hann), angular integration weights, and a voxel-driven distance
   quadrature (scipy.integrate.quad) -- not by closed forms;
 * view weight w_k (default pi / n_views: a uniformly sampled full scan, i.e. pi for parallel
   beams over 180 degrees, and 2 pi with the 1/2 redundancy factor for fan/cone over 360);
+* isocentre (fan/cone): the caller's point, else estimated from the detector normals (the pages'
+  default) as the least-squares point nearest the lines {c_k + s n_k}, with a 1e-9 ridge so that
+  rank-deficient sets (one view, parallel normals) give the minimum-norm point;
 * gather: f(X) = sum_k w_k g_k(X) Q_k(u_k(X), v_k(X)) with bilinear interpolation (0 outside the
   detector), g = 1 for parallel beams and, for fan/cone, g = (D_sd / D_so) / U(X)^2 with
   U(X) = ((X - s) . n) / ((iso - s) . n), D_so = |(iso - s) . n|, D_sd = |(c - s) . n|
@@ -64,6 +67,24 @@ def ramp_taps(n_u: int, tau: float, window: str) -> np.ndarray:
     return taps
 
 
+def estimate_isocenter(beam: int, views: np.ndarray) -> np.ndarray:
+    """Least-squares point nearest the lines through each detector centre along its normal:
+    (sum_k P_k + eps I) x = sum_k P_k c_k with P_k = I - n_k n_k^T (unit n_k) and
+    eps = 1e-9 * trace(sum_k P_k) / dim; 2D geometries solve in the plane (z = 0)."""
+    dim = 2 if beam in (0, 1) else 3
+    M = np.zeros((dim, dim))
+    b = np.zeros(dim)
+    for rec in views:
+        _, ctr, _, _, n = _frames(beam, rec)
+        n = n[:dim] / np.linalg.norm(n[:dim])
+        P = np.eye(dim) - np.outer(n, n)
+        M += P
+        b += P @ ctr[:dim]
+    M += 1e-9 * np.trace(M) / dim * np.eye(dim)
+    x = np.linalg.solve(M, b)
+    return np.r_[x, [0.0] * (3 - dim)]
+
+
 def _frames(beam: int, rec: np.ndarray):
     if beam in (0, 1):
         first, ctr, u = np.r_[rec[0:2], 0.0], np.r_[rec[2:4], 0.0], np.r_[rec[4:6], 0.0]
@@ -91,7 +112,8 @@ def fbp(beam: int, views: np.ndarray, vol_shape, spacing, n_u: int, n_v: int, du
     V = p.shape[2]
     w = (np.full(n_views, math.pi / n_views) if view_weights is None
          else np.asarray(view_weights, dtype=np.float64))
-    iso = np.zeros(3) if isocenter is None else np.r_[np.asarray(isocenter, float), [0.0] * (3 - len(isocenter))]
+    iso = (estimate_isocenter(beam, views) if isocenter is None else
+           np.r_[np.asarray(isocenter, float), [0.0] * (3 - len(isocenter))])
     cu, cv = (n_u - 1) / 2.0, (V - 1) / 2.0
     uu = (np.arange(n_u) - cu) * du
     vv = (np.arange(V) - cv) * dv if not two_d else np.zeros(1)
@@ -175,7 +197,8 @@ def fbp_transpose(beam: int, views: np.ndarray, vol_shape, spacing, n_u: int, n_
     f = np.asarray(vol, dtype=np.float64).reshape(1 if two_d else nz, ny, nx)
     w = (np.full(n_views, math.pi / n_views) if view_weights is None
          else np.asarray(view_weights, dtype=np.float64))
-    iso = np.zeros(3) if isocenter is None else np.r_[np.asarray(isocenter, float), [0.0] * (3 - len(isocenter))]
+    iso = (estimate_isocenter(beam, views) if isocenter is None else
+           np.r_[np.asarray(isocenter, float), [0.0] * (3 - len(isocenter))])
     cu, cv = (n_u - 1) / 2.0, (V - 1) / 2.0
     uu = (np.arange(n_u) - cu) * du
     vv = (np.arange(V) - cv) * dv if not two_d else np.zeros(1)

@@ -175,3 +175,37 @@ def test_transpose_satisfies_the_adjoint_identity(n):
                           w.dv, x, **kw)
     lhs, rhs = float(np.sum(Fy * x)), float(np.sum(y * Ftx))
     assert abs(lhs - rhs) <= 1e-11 * np.linalg.norm(Fy) * np.linalg.norm(x), (lhs, rhs)
+
+
+def test_isocenter_estimate_from_detector_normals():
+    """Circular orbits about the origin give the origin; an orbit about c0 gives c0 (2D and 3D);
+    a single view gives the point of its normal line nearest the origin (minimum norm)."""
+    v2 = W.circular_fan_2d(90, 160.0, 256.0)
+    np.testing.assert_allclose(F.estimate_isocenter(1, v2), 0.0, atol=1e-9)
+    c0 = np.array([3.0, -2.0])
+    s2 = v2.copy(); s2[:, 0:2] += c0; s2[:, 2:4] += c0
+    np.testing.assert_allclose(F.estimate_isocenter(1, s2)[:2], c0, atol=1e-6)
+    v3 = W.circular_cone(60, 120.0, 200.0)
+    c3 = np.array([1.5, 2.0, -4.0])
+    s3 = v3.copy(); s3[:, 0:3] += c3; s3[:, 3:6] += c3
+    np.testing.assert_allclose(F.estimate_isocenter(2, s3), c3, atol=1e-6)
+    one = v2[:1]                       # line through det_center (-96, 0) along x: nearest (0, 0)
+    np.testing.assert_allclose(F.estimate_isocenter(1, one)[:2], [0.0, 0.0], atol=1e-6)
+    one_off = one.copy(); one_off[0, 1] += 5.0; one_off[0, 3] += 5.0   # line y = 5
+    np.testing.assert_allclose(F.estimate_isocenter(1, one_off)[:2], [0.0, 5.0], atol=1e-6)
+
+
+def test_fan_fbp_about_a_shifted_centre_with_the_estimated_isocentre():
+    """The shifted-orbit disk reconstructs without passing the isocentre."""
+    n, R, sid, sdd = 64, 14.0, 160.0, 256.0
+    c0 = np.array([3.0, -2.0])
+    views = W.circular_fan_2d(240, sid, sdd)
+    views[:, 0:2] += c0
+    views[:, 2:4] += c0
+    n_u, du = 161, 0.8
+    sino = _fan_disk_sino(views, n_u, du, R, c0)
+    img = F.fbp(1, views, (1, n, n), 1.0, n_u, 1, du, 1.0, sino)
+    c = _radius_grid(n, 1.0)
+    Y, X = np.meshgrid(c, c, indexing="ij")
+    r = np.hypot(X - c0[0], Y - c0[1])
+    assert abs(np.median(img[r < 0.8 * R]) - 1.0) < 0.01
