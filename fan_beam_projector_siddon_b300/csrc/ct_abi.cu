@@ -3,6 +3,7 @@
 #include <cmath>
 #include <cstdint>
 #include <algorithm>
+#include <utility>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -782,6 +783,63 @@ extern "C" size_t ct_fbp_workspace_bytes(const ct_geometry* g) {
 
 namespace {
 
+// Isocentre estimated from the detector normals ("Analytical Reconstruction Helpers": the default
+// isocentre is estimated from the detector normals): the least-squares point nearest the lines
+// {c_k + s n_k} through each detector centre along its unit normal,
+// (sum_k P_k + eps I) x = sum_k P_k c_k with P_k = I - n_k n_k^T and
+// eps = 1e-9 trace(sum_k P_k) / dim, so that rank-deficient sets (one view, parallel normals) give
+// the minimum-norm point.  2D geometries solve in the plane.  Float64, Gaussian elimination with
+// partial pivoting on the symmetric positive definite system.
+void estimate_isocenter(const ct_geometry* g, double* iso) {
+    const int b = g->info.beam;
+    const int dim = is_2d(b) ? 2 : 3;
+    const int w = is_2d(b) ? 6 : 12;
+    double M[3][3] = {}, rhs[3] = {};
+    for (int k = 0; k < g->info.n_views; ++k) {
+        double first[3], ctr[3], u[3], v[3], n[3];
+        unpack(b, g->host_views.data() + (int64_t)k * w, first, ctr, u, v);
+        if (is_2d(b)) {
+            n[0] = u[1]; n[1] = -u[0]; n[2] = 0.0;
+        } else {
+            cross3(u, v, n);
+        }
+        double nn = 0.0;
+        for (int a = 0; a < dim; ++a) nn += n[a] * n[a];
+        nn = std::sqrt(nn);
+        for (int a = 0; a < dim; ++a) n[a] /= nn;
+        for (int r = 0; r < dim; ++r) {
+            for (int c = 0; c < dim; ++c) {
+                const double P = (r == c ? 1.0 : 0.0) - n[r] * n[c];
+                M[r][c] += P;
+                rhs[r] += P * ctr[c];
+            }
+        }
+    }
+    double tr = 0.0;
+    for (int a = 0; a < dim; ++a) tr += M[a][a];
+    for (int a = 0; a < dim; ++a) M[a][a] += 1e-9 * tr / dim;
+    for (int col = 0; col < dim; ++col) {
+        int piv = col;
+        for (int r = col + 1; r < dim; ++r)
+            if (std::fabs(M[r][col]) > std::fabs(M[piv][col])) piv = r;
+        if (piv != col) {
+            for (int c = 0; c < dim; ++c) std::swap(M[col][c], M[piv][c]);
+            std::swap(rhs[col], rhs[piv]);
+        }
+        for (int r = col + 1; r < dim; ++r) {
+            const double f = M[r][col] / M[col][col];
+            for (int c = col; c < dim; ++c) M[r][c] -= f * M[col][c];
+            rhs[r] -= f * rhs[col];
+        }
+    }
+    for (int r = dim - 1; r >= 0; --r) {
+        double acc = rhs[r];
+        for (int c = r + 1; c < dim; ++c) acc -= M[r][c] * iso[c];
+        iso[r] = acc / M[r][r];
+    }
+    if (dim == 2) iso[2] = 0.0;
+}
+
 // Argument checks shared by ct_fbp and ct_fbp_transpose; fills the kernel parameters.
 ct_status fbp_setup(const ct_geometry* g, const void* in, size_t in_bytes, const void* out,
                     size_t out_bytes, const float* d_view_weights, const double* isocenter,
@@ -803,6 +861,8 @@ ct_status fbp_setup(const ct_geometry* g, const void* in, size_t in_bytes, const
             if (!std::isfinite(isocenter[a])) return CT_ERR_INVALID_ARGUMENT;
             iso[a] = isocenter[a];
         }
+    } else if (!is_parallel(b)) {
+        estimate_isocenter(g, iso);
     }
     *L = fbp_layout(g);
     ct_status st = check_call(g, in, in_bytes, out, out_bytes, d_workspace, workspace_bytes,

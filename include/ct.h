@@ -291,8 +291,13 @@ CT_API ct_status ct_backproject_static(const ct_geometry *geom, const float *d_s
  * d_view_weights  device, n_views floats, or NULL for the uniform full-scan quadrature
  *              w_k = pi / n_views (a 180-degree parallel scan, or a 360-degree fan/cone scan with
  *              the 1/2 redundancy factor).  Short scans pass their own (e.g. Parker) weights.
- * isocenter    host, 3 doubles (x, y, z; z ignored in 2D), or NULL for the origin: the point
- *              whose detector-plane distance sets D_so.
+ * isocenter    host, 3 doubles (x, y, z; z ignored in 2D), or NULL: the point whose
+ *              detector-plane distance sets D_so (fan/cone; unused for parallel beams).  NULL
+ *              estimates it from the detector normals, as the pages' default does: the
+ *              least-squares point nearest the lines through each detector centre along its
+ *              normal (the origin for circular orbits about it); one view, or views whose
+ *              normals are all parallel, give that set's minimum-norm point, so pass the
+ *              isocentre explicitly for such geometries.
  * Workspace: at least ct_fbp_workspace_bytes(geom) (the filtered sinogram, per-view constants
  * and the filter taps).
  * Errors: CT_ERR_INVALID_ARGUMENT for CT_PARALLEL3D, surface detectors, an unknown window, or

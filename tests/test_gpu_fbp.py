@@ -299,3 +299,24 @@ def test_zero_weights_and_empty_batch(ct):
     assert _cpu(g.fbp_transpose(torch_cuda(W.random_volume(w, 6)), view_weights=zero)).max() == 0
     empty = torch.zeros((0,) + tuple(g.sino_shape), device="cuda")
     assert g.fbp(empty).shape == (0,) + tuple(g.volume_shape)
+
+
+@pytest.mark.parametrize("n", [2, 3])
+def test_estimated_isocentre_matches_oracle(ct, n):
+    """Without an isocentre both sides estimate it from the detector normals; a shifted orbit
+    makes the estimate matter (the distance weights depend on it)."""
+    import dataclasses
+    base = W.small_config(n)
+    views = base.views.copy()
+    shift = np.array([2.5, -1.5, 0.75])[: 2 if n == 2 else 3]
+    d = len(shift)
+    views[:, 0:d] += shift
+    views[:, d:2 * d] += shift
+    w = dataclasses.replace(base, views=views)
+    y = W.random_sinogram(w, 8)
+    g = ct.Geometry.from_workload(w)
+    got = _cpu(g.fbp(torch_cuda(y)))
+    _check(got, _oracle(w, y.astype(np.float64)))
+    x = W.random_volume(w, 9)
+    got_t = _cpu(g.fbp_transpose(torch_cuda(x)))
+    _check(got_t, _oracle_t(w, x.astype(np.float64)))
