@@ -380,6 +380,8 @@ def fdk_leg(ct, torch, w, reps: int = 5, cpu_baseline: bool = True):
     sino = torch.from_numpy(W.random_sinogram(w, 11)).cuda()
     vol = torch.empty(g.volume_shape, device="cuda")
     ws = torch.empty(ct.ct_fbp_workspace_bytes(g.handle), dtype=torch.uint8, device="cuda")
+    ws_t = torch.empty(ct.ct_fbp_transpose_workspace_bytes(g.handle), dtype=torch.uint8,
+                       device="cuda")
     out_t = torch.empty_like(sino)
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
@@ -392,7 +394,7 @@ def fdk_leg(ct, torch, w, reps: int = 5, cpu_baseline: bool = True):
         e[1].record(stream)
         flush.zero_()
         e[2].record(stream)
-        g.fbp_transpose(vol, out=out_t, workspace=ws)
+        g.fbp_transpose(vol, out=out_t, workspace=ws_t)
         e[3].record(stream)
         torch.cuda.synchronize()
         if k >= 2:
@@ -413,7 +415,7 @@ def fdk_leg(ct, torch, w, reps: int = 5, cpu_baseline: bool = True):
     traffic, src = profiled_traffic("fdk_gather_kernel", "fbp_kernels.cu")
     out["roofline"]["traffic"] = traffic
     out["roofline"]["traffic_source"] = src
-    del sino, vol, ws, out_t, flush
+    del sino, vol, ws, ws_t, out_t, flush
     torch.cuda.empty_cache()
     if cpu_baseline:
         from oracle import fbp as F

@@ -8,7 +8,7 @@ from ._binding import (CT_CONE, CT_FAN2D, CT_PARALLEL2D, CT_PARALLEL3D, FBP_WIND
                        Geometry, GeometryInfo, ct_backproject, ct_backproject_batch,
                        ct_backproject_static, ct_batch_workspace_bytes, ct_cgls_iterate,
                        ct_cgls_workspace_bytes, ct_fbp, ct_fbp_transpose,
-                       ct_fbp_workspace_bytes,
+                       ct_fbp_transpose_workspace_bytes, ct_fbp_workspace_bytes,
                        ct_geometry_create, ct_geometry_create_surface, ct_geometry_destroy,
                        ct_geometry_get_info, ct_project, ct_project_batch, ct_sirt_iterate,
                        ct_sirt_workspace_bytes, ct_status_string, load_library)
@@ -16,7 +16,8 @@ from ._binding import (CT_CONE, CT_FAN2D, CT_PARALLEL2D, CT_PARALLEL3D, FBP_WIND
 __all__ = ["CT_CONE", "CT_FAN2D", "CT_PARALLEL2D", "CT_PARALLEL3D", "FBP_WINDOWS", "CtError",
            "Geometry", "GeometryInfo", "ct_backproject", "ct_backproject_batch",
            "ct_backproject_static", "ct_batch_workspace_bytes", "ct_cgls_iterate",
-           "ct_cgls_workspace_bytes", "ct_fbp", "ct_fbp_transpose", "ct_fbp_workspace_bytes",
+           "ct_cgls_workspace_bytes", "ct_fbp", "ct_fbp_transpose",
+           "ct_fbp_transpose_workspace_bytes", "ct_fbp_workspace_bytes",
            "ct_geometry_create",
            "ct_geometry_create_surface", "ct_geometry_destroy", "ct_geometry_get_info",
            "ct_project", "ct_project_batch", "ct_sirt_iterate", "ct_sirt_workspace_bytes",

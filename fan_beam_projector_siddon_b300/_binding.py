@@ -94,6 +94,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.ct_fbp_workspace_bytes.restype = sz
     L.ct_fbp.argtypes = [vp, vp, vp, vp, ctypes.POINTER(f64), i32, vp, sz, vp]
     L.ct_fbp.restype = i32
+    L.ct_fbp_transpose_workspace_bytes.argtypes = [vp]
+    L.ct_fbp_transpose_workspace_bytes.restype = sz
     L.ct_fbp_transpose.argtypes = [vp, vp, vp, vp, ctypes.POINTER(f64), i32, vp, sz, vp]
     L.ct_fbp_transpose.restype = i32
     L.ct_status_string.argtypes = [i32]
@@ -255,6 +257,10 @@ def ct_fbp(handle: int, d_sino: int, d_volume: int, d_view_weights: int | None, 
     code, iso = _fbp_args(isocenter, window)
     _check(load_library().ct_fbp(handle, d_sino, d_volume, d_view_weights, _dptr(iso), code,
                                  d_workspace, workspace_bytes, stream), "ct_fbp")
+
+
+def ct_fbp_transpose_workspace_bytes(handle: int) -> int:
+    return int(load_library().ct_fbp_transpose_workspace_bytes(handle))
 
 
 def ct_fbp_transpose(handle: int, d_volume: int, d_sino: int, d_view_weights: int | None,
@@ -423,8 +429,8 @@ class Geometry:
                         initialised, self._stream(stream))
         return x
 
-    def _fbp_call(self, fn, src, src_shape, dst_shape, out, window, view_weights, isocenter,
-                  workspace, stream):
+    def _fbp_call(self, fn, need, src, src_shape, dst_shape, out, window, view_weights,
+                  isocenter, workspace, stream):
         import torch
         assert src.is_cuda and src.dtype == torch.float32 and src.is_contiguous()
         nd = len(src_shape)
@@ -432,7 +438,6 @@ class Geometry:
         lead = tuple(src.shape[:src.dim() - nd])
         if out is None:
             out = torch.empty(lead + tuple(dst_shape), dtype=torch.float32, device=src.device)
-        need = ct_fbp_workspace_bytes(self.handle)
         if workspace is None:
             workspace = torch.empty(need, dtype=torch.uint8, device=src.device)
         ws, wsb = workspace.data_ptr(), workspace.numel() * workspace.element_size()
@@ -453,11 +458,13 @@ class Geometry:
             workspace=None, stream=None):
         """Filtered backprojection (FBP / FDK) of a sinogram; leading dimensions are kept and
         reconstructed one after another with the same workspace."""
-        return self._fbp_call(ct_fbp, sino, self.sino_shape, self.volume_shape, out, window,
-                              view_weights, isocenter, workspace, stream)
+        return self._fbp_call(ct_fbp, ct_fbp_workspace_bytes(self.handle), sino,
+                              self.sino_shape, self.volume_shape, out, window, view_weights,
+                              isocenter, workspace, stream)
 
     def fbp_transpose(self, volume, out=None, window="ram-lak", view_weights=None,
                       isocenter=None, workspace=None, stream=None):
         """Transpose of ``fbp`` (volume -> sinogram); leading dimensions are kept."""
-        return self._fbp_call(ct_fbp_transpose, volume, self.volume_shape, self.sino_shape, out,
-                              window, view_weights, isocenter, workspace, stream)
+        return self._fbp_call(ct_fbp_transpose, ct_fbp_transpose_workspace_bytes(self.handle),
+                              volume, self.volume_shape, self.sino_shape, out, window,
+                              view_weights, isocenter, workspace, stream)

@@ -757,19 +757,30 @@ namespace {
 
 struct FbpLayout {
     int32_t rows, cols;  // padded filtered sinogram of one view
+    int32_t bu, bv;      // transpose: 2 x 2 blocks (2D: pairs) per view and parity copy
     size_t views, cosines, taps, filtered, total;
 };
 
-FbpLayout fbp_layout(const ct_geometry* g) {
+// Scratch of ct_fbp (transpose = 0: the padded filtered sinogram) or of ct_fbp_transpose
+// (transpose = 1: the parity copies of the padded detector, 4 copies of 2 x 2 blocks; 2D 2 copies
+// of pairs).
+FbpLayout fbp_layout(const ct_geometry* g, bool transpose) {
     FbpLayout L;
     const size_t nv = (size_t)g->info.n_views;
+    const bool two_d = is_2d(g->info.beam);
     L.rows = g->info.n_u + 3;
-    L.cols = is_2d(g->info.beam) ? 1 : g->info.n_v + 3;
+    L.cols = two_d ? 1 : g->info.n_v + 3;
+    L.bu = (g->info.n_u + 2) / 2 + 1;
+    L.bv = two_d ? 1 : (g->info.n_v + 2) / 2 + 1;
     L.views = 0;
     L.cosines = align_up(sizeof(ct::FbpView) * nv);
     L.taps = L.cosines + align_up(sizeof(ct::FbpCosine) * nv);
     L.filtered = L.taps + align_up(sizeof(float) * (size_t)(2 * g->info.n_u - 1));
-    L.total = L.filtered + align_up(sizeof(float) * nv * (size_t)L.rows * (size_t)L.cols);
+    const size_t slot = transpose
+        ? (two_d ? sizeof(float) * 4 * nv * (size_t)L.bu
+                 : sizeof(float) * 16 * nv * (size_t)L.bu * (size_t)L.bv)
+        : sizeof(float) * nv * (size_t)L.rows * (size_t)L.cols;
+    L.total = L.filtered + align_up(slot);
     return L;
 }
 
@@ -778,7 +789,11 @@ constexpr int32_t kFbpMaxU = 16384;
 }  // namespace
 
 extern "C" size_t ct_fbp_workspace_bytes(const ct_geometry* g) {
-    return g == nullptr ? 0 : fbp_layout(g).total;
+    return g == nullptr ? 0 : fbp_layout(g, false).total;
+}
+
+extern "C" size_t ct_fbp_transpose_workspace_bytes(const ct_geometry* g) {
+    return g == nullptr ? 0 : fbp_layout(g, true).total;
 }
 
 namespace {
@@ -844,7 +859,7 @@ void estimate_isocenter(const ct_geometry* g, double* iso) {
 ct_status fbp_setup(const ct_geometry* g, const void* in, size_t in_bytes, const void* out,
                     size_t out_bytes, const float* d_view_weights, const double* isocenter,
                     ct_fbp_window window, const void* d_workspace, size_t workspace_bytes,
-                    ct::FbpParams* P, FbpLayout* L) {
+                    bool transpose, ct::FbpParams* P, FbpLayout* L) {
     if (g == nullptr) return CT_ERR_INVALID_ARGUMENT;
     const int b = g->info.beam;
     if (b == CT_PARALLEL3D || g->d_offsets != nullptr) return CT_ERR_INVALID_ARGUMENT;
@@ -864,7 +879,7 @@ ct_status fbp_setup(const ct_geometry* g, const void* in, size_t in_bytes, const
     } else if (!is_parallel(b)) {
         estimate_isocenter(g, iso);
     }
-    *L = fbp_layout(g);
+    *L = fbp_layout(g, transpose);
     ct_status st = check_call(g, in, in_bytes, out, out_bytes, d_workspace, workspace_bytes,
                               L->total);
     if (st != CT_OK) return st;
@@ -885,6 +900,8 @@ ct_status fbp_setup(const ct_geometry* g, const void* in, size_t in_bytes, const
     p.window = (int32_t)window;
     p.rows = L->rows;
     p.cols = L->cols;
+    p.bu = L->bu;
+    p.bv = L->bv;
     p.du = g->du;
     p.dv = g->dv;
     for (int a = 0; a < 3; ++a) p.iso[a] = iso[a];
@@ -905,7 +922,7 @@ extern "C" ct_status ct_fbp(const ct_geometry* g, const float* d_sino, float* d_
     if (g == nullptr) return CT_ERR_INVALID_ARGUMENT;
     const ct_status st = fbp_setup(g, d_sino, sino_bytes(g), d_volume, volume_bytes(g),
                                    d_view_weights, isocenter, window, d_workspace,
-                                   workspace_bytes, &P, &L);
+                                   workspace_bytes, false, &P, &L);
     if (st != CT_OK) return st;
     char* ws = static_cast<char*>(d_workspace);
     return from_cuda(ct::launch_fbp(P, g->d_raw, d_view_weights,
@@ -924,7 +941,7 @@ extern "C" ct_status ct_fbp_transpose(const ct_geometry* g, const float* d_volum
     if (g == nullptr) return CT_ERR_INVALID_ARGUMENT;
     const ct_status st = fbp_setup(g, d_volume, volume_bytes(g), d_sino, sino_bytes(g),
                                    d_view_weights, isocenter, window, d_workspace,
-                                   workspace_bytes, &P, &L);
+                                   workspace_bytes, true, &P, &L);
     if (st != CT_OK) return st;
     char* ws = static_cast<char*>(d_workspace);
     return from_cuda(ct::launch_fbp_transpose(

@@ -110,6 +110,7 @@ struct FbpParams {
     int32_t nx, ny, nz;
     int32_t two_d, parallel, window;
     int32_t rows, cols;  // padded filtered sinogram per view: rows = n_u + 3, cols = n_v + 3 (2D: 1)
+    int32_t bu, bv;      // transpose: 2 x 2 blocks per view and copy along u, v (2D: pairs, bv = 1)
     double du, dv;
     double iso[3];
     float sx, sy, sz;  // voxel pitches along x, y, z
@@ -144,8 +145,10 @@ static_assert(sizeof(FbpCosine) == 48, "FbpCosine layout");
 cudaError_t launch_fbp(const FbpParams& p, const double* raw_views, const float* view_weights,
                        FbpView* views, FbpCosine* cosines, float* taps, const float* sino,
                        float* filtered, float* vol, cudaStream_t stream);
-// Transpose of the same operator: volume -> sinogram.  `scattered` is the padded array (the
-// filtered-sinogram slot of the scratch); it is cleared on the stream first.
+// Transpose of the same operator: volume -> sinogram.  `scattered` holds the parity copies of
+// the padded detector (layout in fbp_kernels.cu, fbp_copies_floats floats); it is cleared on the
+// stream first.
+size_t fbp_copies_floats(const FbpParams& p);
 cudaError_t launch_fbp_transpose(const FbpParams& p, const double* raw_views,
                                  const float* view_weights, FbpView* views, FbpCosine* cosines,
                                  float* taps, const float* vol, float* scattered, float* sino,

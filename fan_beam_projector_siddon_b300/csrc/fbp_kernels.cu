@@ -68,6 +68,56 @@ __device__ __forceinline__ int64_t qrow(const FbpParams& p, int view, int u) {
     return ((int64_t)view * p.rows + u + 1) * p.cols;
 }
 
+// Transpose scatter target: parity copies of the padded detector.  With padded indices
+// U = u + 1 in [0, n_u + 2] and V = v + 1 in [0, n_v + 2], copy (pu, pv) in {0,1}^2 stores pixel
+// (U, V) in the 2 x 2 block ((U + pu) / 2, (V + pv) / 2), slot ((U + pu) & 1) * 2 + ((V + pv) & 1),
+// blocks of 4 floats in [copy][view][bu][bv] order.  A bilinear footprint (U0..U0+1, V0..V0+1)
+// is then one aligned float4 of copy (U0 & 1, V0 & 1), added with one vector reduction; the
+// pixel's value is the sum over the four copies.  2D: copies pu in {0,1} of pairs (U + pu) / 2,
+// slot (U + pu) & 1, in [copy][view][bu] order (float2 reductions).
+__device__ __forceinline__ float4* copy_block(const FbpParams& p, float* q, int view, int U0,
+                                              int V0) {
+    const int pu = U0 & 1, pv = V0 & 1;
+    const int64_t blk = (((int64_t)(pu * 2 + pv) * p.n_views + view) * p.bu + ((U0 + pu) >> 1)) *
+                            p.bv + ((V0 + pv) >> 1);
+    return reinterpret_cast<float4*>(q) + blk;
+}
+__device__ __forceinline__ float2* copy_pair(const FbpParams& p, float* q, int view, int U0) {
+    const int pu = U0 & 1;
+    const int64_t blk = ((int64_t)pu * p.n_views + view) * p.bu + ((U0 + pu) >> 1);
+    return reinterpret_cast<float2*>(q) + blk;
+}
+__device__ __forceinline__ void red_add4(float4* a, float x, float y, float z, float w) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(a), "f"(x), "f"(y),
+                 "f"(z), "f"(w)
+                 : "memory");
+}
+__device__ __forceinline__ void red_add2(float2* a, float x, float y) {
+    asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(a), "f"(x), "f"(y) : "memory");
+}
+// Sum of the copies at padded pixel (U, V) (2D: V ignored).
+__device__ __forceinline__ float copies_at(const FbpParams& p, const float* q, int view, int U,
+                                           int V) {
+    if (p.two_d) {
+        float s = 0.0f;
+#pragma unroll
+        for (int pu = 0; pu < 2; ++pu) {
+            const int64_t blk = ((int64_t)pu * p.n_views + view) * p.bu + ((U + pu) >> 1);
+            s += q[blk * 2 + ((U + pu) & 1)];
+        }
+        return s;
+    }
+    float s = 0.0f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const int pu = c >> 1, pv = c & 1;
+        const int64_t blk = (((int64_t)c * p.n_views + view) * p.bu + ((U + pu) >> 1)) * p.bv +
+                            ((V + pv) >> 1);
+        s += q[blk * 4 + ((U + pu) & 1) * 2 + ((V + pv) & 1)];
+    }
+    return s;
+}
+
 // One thread per view (its FbpView and FbpCosine) and one thread per filter tap, over one flat
 // grid.
 __global__ void fbp_prepare_kernel(FbpParams p, const double* __restrict__ raw,
@@ -204,7 +254,7 @@ __global__ void __launch_bounds__(256) fbp_filter_kernel(FbpParams p,
         float val = 0.0f;
         if (j < nv) {
             if (ADJ) {
-                val = in[qrow(p, view, iu) + v0 + j + vo];
+                val = copies_at(p, in, view, iu + 1, v0 + j + 1);
             } else {
                 val = in[((int64_t)view * n_u + iu) * V + v0 + j];
                 if (!p.parallel) val *= cosine_weight(C, iu, v0 + j);
@@ -256,7 +306,7 @@ __global__ void __launch_bounds__(256) fbp_filter_blocked_kernel(
         float val = 0.0f;
         if (k < n_u && j < nv) {
             if (ADJ) {
-                val = in[qrow(p, view, k) + v0 + j + 1];
+                val = copies_at(p, in, view, k + 1, v0 + j + 1);
             } else {
                 val = in[((int64_t)view * n_u + k) * V + v0 + j];
                 if (!p.parallel) val *= cosine_weight(C, k, v0 + j);
@@ -468,8 +518,9 @@ __global__ void __launch_bounds__(256) fbp2d_gather_kernel(FbpParams p,
 }
 
 // Transpose of the cone-beam gather: every voxel adds w g f(X) times its four bilinear
-// coefficients to the padded filtered-sinogram array (contributions that land in the pads are
-// discarded later).  Same block shape, view passes and z-independent path as the gather.
+// coefficients, as one float4 reduction, to the parity copies of the padded detector
+// (contributions that land in the pads are discarded later).  Same block shape, view passes and
+// z-independent path as the gather.
 template <int NZ>
 __global__ void __launch_bounds__(256) fdk_scatter_kernel(FbpParams p,
                                                          const FbpView* __restrict__ views,
@@ -499,8 +550,6 @@ __global__ void __launch_bounds__(256) fdk_scatter_kernel(FbpParams p,
         Z[m] = ((float)(z0 + lane + 32 * m) + 0.5f - 0.5f * p.nz) * p.sz;
         f[m] = st[warp][lane + 32 * m];
     }
-    const int cols = p.cols;
-    const int64_t view_stride = (int64_t)p.rows * cols;
     const float umax = (float)p.n_u, vmax = (float)p.n_v;
     for (int k0 = k_begin; k0 < k_end; k0 += kChunk) {
         __syncthreads();
@@ -508,8 +557,8 @@ __global__ void __launch_bounds__(256) fdk_scatter_kernel(FbpParams p,
         for (int i = threadIdx.x; i < nk * 4; i += blockDim.x)
             sv[i] = reinterpret_cast<const float4*>(views + k0)[i];
         __syncthreads();
-        float* base = q + (int64_t)k0 * view_stride;
-        for (int k = 0; k < nk; ++k, base += view_stride) {
+        for (int k = 0; k < nk; ++k) {
+            const int view = k0 + k;
             const float4 A = sv[4 * k], B = sv[4 * k + 1], C = sv[4 * k + 2], E = sv[4 * k + 3];
             const float ax = X - A.x, ay = Y - A.y;
             const float den_xy = fmaf(ay, B.x, ax * A.w);
@@ -521,20 +570,17 @@ __global__ void __launch_bounds__(256) fdk_scatter_kernel(FbpParams p,
                 const float up = fminf(fmaxf(fmaf(t, au_xy, E.y), -1.0f), umax);
                 const float fu0 = floorf(up), fu = up - fu0;
                 const float g = E.w * inv * inv;
-                float* prow = base + ((int)fu0 + 1) * cols + 1;
+                const int U0 = (int)fu0 + 1;
 #pragma unroll
                 for (int m = 0; m < NZ; ++m) {
                     const float av = fmaf(Z[m] - A.z, C.w, av_xy);
                     const float vp = fminf(fmaxf(fmaf(t, av, E.z), -1.0f), vmax);
                     const float fv0 = floorf(vp), fv = vp - fv0;
-                    float* pq = prow + (int)fv0;
                     const float c = g * f[m];
                     const float c1 = c * fu, c0 = c - c1;
                     const float c01 = c0 * fv, c11 = c1 * fv;
-                    atomicAdd(pq, c0 - c01);
-                    atomicAdd(pq + 1, c01);
-                    atomicAdd(pq + cols, c1 - c11);
-                    atomicAdd(pq + cols + 1, c11);
+                    red_add4(copy_block(p, q, view, U0, (int)fv0 + 1), c0 - c01, c01, c1 - c11,
+                             c11);
                 }
                 continue;
             }
@@ -550,14 +596,11 @@ __global__ void __launch_bounds__(256) fdk_scatter_kernel(FbpParams p,
                 const float vp = fminf(fmaxf(fmaf(t, av, E.z), -1.0f), vmax);
                 const float fu0 = floorf(up), fv0 = floorf(vp);
                 const float fu = up - fu0, fv = vp - fv0;
-                float* pq = base + ((int)fu0 + 1) * cols + (int)fv0 + 1;
                 const float c = E.w * inv * inv * f[m];
                 const float c1 = c * fu, c0 = c - c1;
                 const float c01 = c0 * fv, c11 = c1 * fv;
-                atomicAdd(pq, c0 - c01);
-                atomicAdd(pq + 1, c01);
-                atomicAdd(pq + cols, c1 - c11);
-                atomicAdd(pq + cols + 1, c11);
+                red_add4(copy_block(p, q, view, (int)fu0 + 1, (int)fv0 + 1), c0 - c01, c01,
+                         c1 - c11, c11);
             }
         }
     }
@@ -582,7 +625,6 @@ __global__ void __launch_bounds__(256) fbp2d_scatter_kernel(FbpParams p,
         Y[m] = ((float)iy + 0.5f - 0.5f * p.ny) * p.sy;
         f[m] = (ix < p.nx && iy < p.ny) ? vol[(int64_t)iy * p.nx + ix] : 0.0f;
     }
-    const int rows = p.rows;
     const float umax = (float)p.n_u;
     for (int k0 = 0; k0 < p.n_views; k0 += kChunk) {
         __syncthreads();
@@ -590,8 +632,8 @@ __global__ void __launch_bounds__(256) fbp2d_scatter_kernel(FbpParams p,
         for (int i = threadIdx.x; i < nk * 4; i += blockDim.x)
             sv[i] = reinterpret_cast<const float4*>(views + k0)[i];
         __syncthreads();
-        float* base = q + (int64_t)k0 * rows + 1;
-        for (int k = 0; k < nk; ++k, base += rows) {
+        for (int k = 0; k < nk; ++k) {
+            const int view = k0 + k;
             const float4 A = sv[4 * k], B = sv[4 * k + 1], E = sv[4 * k + 3];
             const float ax = X - A.x;
             const float den_x = ax * A.w, au_x = ax * B.z;
@@ -611,10 +653,8 @@ __global__ void __launch_bounds__(256) fbp2d_scatter_kernel(FbpParams p,
                     c = E.w * inv * inv * f[m];
                 }
                 const float fu0 = floorf(up), fu = up - fu0;
-                float* pq = base + (int)fu0;
                 const float c1 = c * fu;
-                atomicAdd(pq, c - c1);
-                atomicAdd(pq + 1, c1);
+                red_add2(copy_pair(p, q, view, (int)fu0 + 1), c - c1, c1);
             }
         }
     }
@@ -723,14 +763,20 @@ cudaError_t launch_fbp(const FbpParams& p, const double* raw, const float* user_
     return cudaSuccess;
 }
 
+size_t fbp_copies_floats(const FbpParams& p) {
+    return p.two_d ? 2 * 2 * (size_t)p.n_views * (size_t)p.bu
+                   : 4 * 4 * (size_t)p.n_views * (size_t)p.bu * (size_t)p.bv;
+}
+
 cudaError_t launch_fbp_transpose(const FbpParams& p, const double* raw, const float* user_weights,
                                  FbpView* views, FbpCosine* cosines, float* taps,
                                  const float* vol, float* scattered, float* sino,
                                  cudaStream_t stream) {
     cudaError_t e = launch_prepare(p, raw, user_weights, views, cosines, taps, stream);
     if (e != cudaSuccess) return e;
-    const size_t qbytes = sizeof(float) * (size_t)p.n_views * (size_t)p.rows * (size_t)p.cols;
-    if ((e = cudaMemsetAsync(scattered, 0, qbytes, stream)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(scattered, 0, sizeof(float) * fbp_copies_floats(p), stream)) !=
+        cudaSuccess)
+        return e;
     if (p.two_d) {
         if (p.ny >= 128) {
             if ((p.ny + 31) / 32 > 65535) return cudaErrorInvalidValue;

@@ -326,10 +326,13 @@ CT_API ct_status ct_fbp(const ct_geometry *geom, const float *d_sino, float *d_v
  * reconstruction"; "Analytical Reconstruction Helpers").  Steps: every voxel adds
  * w_k g_k(X) f(X) times its four bilinear coefficients onto view k's detector (atomic adds;
  * contributions off the detector are dropped), the same filter (its matrix du h((i - j) du) is
- * symmetric), then the cosine weights.  Arguments, workspace and errors as for ct_fbp, with
- * d_volume read and d_sino overwritten.  The atomic adds make the float32 result depend on
- * the order in which they land (run-to-run differences of a few ulp).
+ * symmetric), then the cosine weights.  Arguments and errors as for ct_fbp, with d_volume read
+ * and d_sino overwritten; the workspace is at least ct_fbp_transpose_workspace_bytes(geom) (per
+ * view and detector pixel 4 floats for cone beams, 2 for 2D, plus the per-view constants and
+ * taps).  The atomic adds make the float32 result depend on the order in which they land
+ * (run-to-run differences of a few ulp).
  */
+CT_API size_t ct_fbp_transpose_workspace_bytes(const ct_geometry *geom);
 CT_API ct_status ct_fbp_transpose(const ct_geometry *geom, const float *d_volume, float *d_sino,
                                   const float *d_view_weights, const double *isocenter,
                                   ct_fbp_window window, void *d_workspace,

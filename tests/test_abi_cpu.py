@@ -93,6 +93,7 @@ def test_null_arguments_are_rejected(lib):
     assert L.ct_fbp(None, None, None, None, None, 0, None, 0, None) == 1
     assert L.ct_fbp_workspace_bytes(None) == 0
     assert L.ct_fbp_transpose(None, None, None, None, None, 0, None, 0, None) == 1
+    assert L.ct_fbp_transpose_workspace_bytes(None) == 0
 
 
 def test_surface_admission_before_touching_the_gpu(lib):

@@ -160,6 +160,13 @@ def test_errors(ct):
         assert ei.value.status == status
 
     call(7, workspace_bytes=need - 1)
+    # the transpose needs its own (larger) scratch: the parity copies of the detector
+    need_t = ct.ct_fbp_transpose_workspace_bytes(g.handle)
+    assert need_t > need
+    with pytest.raises(ct.CtError) as ei:
+        ct.ct_fbp_transpose(g.handle, vol.data_ptr(), sino.data_ptr(), None, None, 0,
+                            ws.data_ptr(), need, s)
+    assert ei.value.status == 7
     call(1, window=5)
     call(1, isocenter=(math.nan, 0.0, 0.0))
     call(4, d_volume=ws.data_ptr())
