@@ -16,6 +16,8 @@ cosine, hamming, hann), angular integration weights, and a voxel-driven distance
 * isocentre (fan/cone): the caller's point, else estimated from the detector normals (the pages'
   default) as the least-squares point nearest the lines {c_k + s n_k}, with a 1e-9 ridge so that
   rank-deficient sets (one view, parallel normals) give the minimum-norm point;
+* optional per (view, detector column) weights before filtering, e.g. Parker's short-scan
+  weights (Parker 1982) for circular fan/cone orbits spanning pi + 2 delta;
 * gather: f(X) = sum_k w_k g_k(X) Q_k(u_k(X), v_k(X)) with bilinear interpolation (0 outside the
   detector), g = 1 for parallel beams and, for fan/cone, g = (D_sd / D_so) / U(X)^2 with
   U(X) = ((X - s) . n) / ((iso - s) . n), D_so = |(iso - s) . n|, D_sd = |(c - s) . n|
@@ -85,6 +87,61 @@ def estimate_isocenter(beam: int, views: np.ndarray) -> np.ndarray:
     return np.r_[x, [0.0] * (3 - dim)]
 
 
+def parker_formula(beta, gamma, delta):
+    """Parker's short-scan weight for source angle beta in [0, pi + 2 delta] and fan angle gamma
+    (same rotational sense as beta), half fan angle delta; 0 outside the scan."""
+    beta, gamma = np.broadcast_arrays(np.asarray(beta, float), np.asarray(gamma, float))
+    w = np.zeros(beta.shape)
+    a = delta - gamma
+    b = delta + gamma
+    r1 = (beta >= 0) & (beta < 2 * a)
+    r2 = (beta >= 2 * a) & (beta <= np.pi - 2 * gamma)
+    r3 = (beta > np.pi - 2 * gamma) & (beta <= np.pi + 2 * delta)
+    w[r1] = np.sin(np.pi / 4 * beta[r1] / a[r1]) ** 2
+    w[r2] = 1.0
+    w[r3] = np.sin(np.pi / 4 * (np.pi + 2 * delta - beta[r3]) / b[r3]) ** 2
+    return w
+
+
+def parker_geometry(beam: int, views: np.ndarray, n_u: int, du: float, isocenter=None):
+    """(beta (n_views,), gamma (n_views, n_u), delta, span) of a circular fan or cone orbit in
+    the xy-plane: beta the source angle about the isocentre from the first view, in the sense of
+    rotation; gamma the fan angle of each detector column (the column's centre line) from the
+    central ray (source to isocentre), in the same sense; delta the largest |gamma|; span the last
+    view's beta.  Raises ValueError if the orbit is not a circle about the isocentre."""
+    assert beam in (1, 2), "fan and cone beams"
+    iso = (estimate_isocenter(beam, views) if isocenter is None else
+           np.r_[np.asarray(isocenter, float), [0.0] * (3 - len(isocenter))])
+    src = np.array([_frames(beam, r)[0] for r in views])
+    rel = src[:, :2] - iso[:2]
+    radius = np.hypot(rel[:, 0], rel[:, 1])
+    if np.ptp(radius) > 1e-6 * radius.mean() or (beam == 2 and np.ptp(src[:, 2]) > 1e-6 * radius.mean()):
+        raise ValueError("not a circular orbit in the xy-plane about the isocentre")
+    beta = np.unwrap(np.arctan2(rel[:, 1], rel[:, 0]))
+    sense = 1.0 if beta[-1] >= beta[0] else -1.0
+    beta = (beta - beta[0]) * sense
+    cu = (n_u - 1) / 2.0
+    gamma = np.zeros((views.shape[0], n_u))
+    for k, rec in enumerate(views):
+        first, ctr, u, _, _ = _frames(beam, rec)
+        a = (iso - first)[:2]
+        P = ctr[None, :] + ((np.arange(n_u) - cu) * du)[:, None] * u[None, :]
+        b = (P - first)[:, :2]
+        gamma[k] = sense * np.arctan2(a[0] * b[:, 1] - a[1] * b[:, 0], b @ a)
+    return beta, gamma, float(np.abs(gamma).max()), float(beta[-1])
+
+
+def parker_weights(beam: int, views: np.ndarray, n_u: int, du: float, isocenter=None):
+    """Per (view, column) Parker weights of a circular short scan (pages: short-scan Parker
+    weighting before filtering).  With a span above pi + 2 delta the effective half fan angle is
+    (span - pi) / 2, which keeps conjugate rays' weights summing to 1.  Raises ValueError if the
+    span is shorter than pi + 2 delta."""
+    beta, gamma, delta, span = parker_geometry(beam, views, n_u, du, isocenter)
+    if span < np.pi + 2 * delta - 1e-9:
+        raise ValueError("the scan spans less than pi + 2 delta")
+    return parker_formula(beta[:, None], gamma, (span - np.pi) / 2)
+
+
 def _frames(beam: int, rec: np.ndarray):
     if beam in (0, 1):
         first, ctr, u = np.r_[rec[0:2], 0.0], np.r_[rec[2:4], 0.0], np.r_[rec[4:6], 0.0]
@@ -98,7 +155,7 @@ def _frames(beam: int, rec: np.ndarray):
 
 def fbp(beam: int, views: np.ndarray, vol_shape, spacing, n_u: int, n_v: int, du: float,
         dv: float, sino: np.ndarray, window: str = "ram-lak", view_weights=None, isocenter=None,
-        voxels=None):
+        voxels=None, pixel_weights=None):
     """Filtered backprojection of `sino` ((views, U) or (views, U, V)) onto the volume grid.
 
     `spacing` is one pitch or per-axis pitches in tensor order ((dz, dy, dx), 2D (dy, dx)); voxel
@@ -137,6 +194,8 @@ def fbp(beam: int, views: np.ndarray, vol_shape, spacing, n_u: int, n_v: int, du
         if beam != 0:                                              # cosine pre-weights
             pix = ctr[None, None, :] + uu[:, None, None] * u + vv[None, :, None] * v
             q *= abs((ctr - first) @ n) / np.linalg.norm(pix - first, axis=-1)
+        if pixel_weights is not None:                              # e.g. Parker weights
+            q *= np.asarray(pixel_weights, dtype=np.float64)[k][:, None]
         # filter every detector column along u (linear convolution, no wrap-around)
         Q = np.empty_like(q)
         for j in range(V):
@@ -179,7 +238,7 @@ def _bilinear(Q: np.ndarray, up: np.ndarray, vp: np.ndarray) -> np.ndarray:
 
 def fbp_transpose(beam: int, views: np.ndarray, vol_shape, spacing, n_u: int, n_v: int,
                   du: float, dv: float, vol: np.ndarray, window: str = "ram-lak",
-                  view_weights=None, isocenter=None):
+                  view_weights=None, isocenter=None, pixel_weights=None):
     """The transpose of `fbp` as a linear map from sinograms to volumes: volume -> sinogram.
 
     The pages state that the analytical operator's backward pass scatters the same interpolation
@@ -234,6 +293,8 @@ def fbp_transpose(beam: int, views: np.ndarray, vol_shape, spacing, n_u: int, n_
         if beam != 0:
             pix = ctr[None, None, :] + uu[:, None, None] * u + vv[None, :, None] * v
             q *= abs((ctr - first) @ n) / np.linalg.norm(pix - first, axis=-1)
+        if pixel_weights is not None:
+            q *= np.asarray(pixel_weights, dtype=np.float64)[k][:, None]
         out[k] = q
     return out[:, :, 0] if two_d else out
 

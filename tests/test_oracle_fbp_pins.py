@@ -209,3 +209,93 @@ def test_fan_fbp_about_a_shifted_centre_with_the_estimated_isocentre():
     Y, X = np.meshgrid(c, c, indexing="ij")
     r = np.hypot(X - c0[0], Y - c0[1])
     assert abs(np.median(img[r < 0.8 * R]) - 1.0) < 0.01
+
+
+# ---- Parker short-scan weights ----------------------------------------------------------------
+
+def test_parker_formula_weights_of_conjugate_rays_sum_to_one():
+    """A ray (beta, gamma) and its conjugate (beta + pi + 2 gamma, -gamma) (or beta - pi + 2 gamma)
+    carry weights summing to 1; rays without a conjugate in the scan weigh 1."""
+    rng = np.random.default_rng(1)
+    delta = 0.3
+    beta = rng.uniform(0, np.pi + 2 * delta, 20000)
+    gamma = rng.uniform(-delta, delta, 20000)
+    w = F.parker_formula(beta, gamma, delta)
+    fwd = beta + np.pi + 2 * gamma
+    back = beta - np.pi + 2 * gamma
+    conj = np.where(fwd <= np.pi + 2 * delta, fwd, back)
+    has = (fwd <= np.pi + 2 * delta) | (back >= 0)
+    wc = F.parker_formula(conj, -gamma, delta)
+    np.testing.assert_allclose((w + wc)[has], 1.0, atol=1e-12)
+    np.testing.assert_allclose(w[~has], 1.0, atol=0)
+    assert w.min() >= 0 and w.max() <= 1
+
+
+def _fan_short_scan(n_views, sid, sdd, n_u, du, margin=0.02):
+    """A circular fan scan over pi + 2 delta (+ margin), delta the detector's half fan angle."""
+    half = (n_u - 1) / 2.0 * du
+    delta = np.arctan(half / sdd)
+    span = np.pi + 2 * delta + margin
+    views = W.circular_fan_2d(n_views, sid, sdd, span=span * n_views / (n_views - 1))
+    return views, delta
+
+
+def test_parker_geometry_matches_the_geometric_conjugate_ray():
+    """beta and gamma taken from the records obey the conjugate relation of the actual lines:
+    the second intersection of a ray's line with the source circle sits at beta + pi + 2 gamma,
+    and the ray back from there has fan angle -gamma.  This pins the signs of beta and gamma."""
+    views, _ = _fan_short_scan(360, 160.0, 256.0, 129, 0.8)
+    beta, gamma, delta, span = F.parker_geometry(1, views, 129, 0.8)
+    R = 160.0
+    th0 = np.arctan2(views[0, 1], views[0, 0])
+    for k, j in [(3, 10), (100, 64), (200, 120), (350, 5)]:
+        s = views[k, 0:2]
+        c, u = views[k, 2:4], views[k, 4:6]
+        P = c + (j - 64) * 0.8 * u
+        d = (P - s) / np.linalg.norm(P - s)
+        t = -2 * (s @ d)                       # |s + t d| = R, other root than t = 0
+        s2 = s + t * d
+        assert abs(np.linalg.norm(s2) - R) < 1e-9
+        b2 = (np.arctan2(s2[1], s2[0]) - th0) % (2 * np.pi)
+        want = (beta[k] + np.pi + 2 * gamma[k, j]) % (2 * np.pi)
+        assert abs(np.angle(np.exp(1j * (b2 - want)))) < 1e-9
+        a2, d2 = -s2, s - s2                   # back along the line from s2: central ray vs ray
+        g2 = np.arctan2(a2[0] * d2[1] - a2[1] * d2[0], a2 @ d2)
+        assert abs(g2 + gamma[k, j]) < 1e-9
+    assert delta < span - np.pi
+
+
+def test_short_scan_fan_fbp_of_a_disk_with_parker_weights():
+    n, R, sid, sdd, n_u, du = 64, 20.0, 160.0, 256.0, 161, 0.8
+    views, _ = _fan_short_scan(240, sid, sdd, n_u, du)
+    beta, _, _, span = F.parker_geometry(1, views, n_u, du)
+    pw = F.parker_weights(1, views, n_u, du)
+    sino = np.zeros((views.shape[0], n_u))
+    uu = (np.arange(n_u) - (n_u - 1) / 2.0) * du
+    for k in range(views.shape[0]):
+        src = np.r_[views[k, 0:2], 0.0]
+        pix = np.r_[views[k, 2:4], 0.0][None, :] + uu[:, None] * np.r_[views[k, 4:6], 0.0][None, :]
+        sino[k] = _chord_ball(src[None, :], pix, R)
+    dbeta = span / (views.shape[0] - 1)
+    img = F.fbp(1, views, (1, n, n), 1.0, n_u, 1, du, 1.0, sino,
+                view_weights=np.full(views.shape[0], dbeta), pixel_weights=pw)
+    c = _radius_grid(n, 1.0)
+    r = np.hypot(*np.meshgrid(c, c, indexing="ij"))
+    assert abs(np.median(img[r < 0.8 * R]) - 1.0) < 0.01
+    assert np.abs(img[r < 0.8 * R] - 1.0).max() < 0.05
+    fov = 0.95 * (n_u - 1) / 2 * du * sid / sdd
+    assert np.abs(img[(r > 1.25 * R) & (r < fov)]).max() < 0.05
+    # without the Parker weights the doubly measured wedge shows
+    bad = F.fbp(1, views, (1, n, n), 1.0, n_u, 1, du, 1.0, sino,
+                view_weights=np.full(views.shape[0], dbeta))
+    assert np.abs(bad[r < 0.8 * R] - 1.0).max() > 0.2
+
+
+def test_parker_rejects_short_and_non_circular_scans():
+    views, delta = _fan_short_scan(100, 160.0, 256.0, 161, 0.8, margin=-0.2)
+    with pytest.raises(ValueError):
+        F.parker_weights(1, views, 161, 0.8)
+    bad = W.circular_fan_2d(100, 160.0, 256.0)
+    bad[7, 0:2] *= 1.01
+    with pytest.raises(ValueError):
+        F.parker_weights(1, bad, 161, 0.8)
