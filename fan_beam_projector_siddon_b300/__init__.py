@@ -7,7 +7,7 @@ thin ctypes binding plus the seeded input generators in ``workloads``.
 from ._binding import (CT_CONE, CT_FAN2D, CT_PARALLEL2D, CT_PARALLEL3D, FBP_WINDOWS, CtError,
                        Geometry, GeometryInfo, ct_backproject, ct_backproject_batch,
                        ct_backproject_static, ct_batch_workspace_bytes, ct_cgls_iterate,
-                       ct_cgls_workspace_bytes, ct_fbp, ct_fbp_transpose,
+                       ct_cgls_workspace_bytes, ct_fbp, ct_fbp_parker_weights, ct_fbp_transpose,
                        ct_fbp_transpose_workspace_bytes, ct_fbp_workspace_bytes,
                        ct_geometry_create, ct_geometry_create_surface, ct_geometry_destroy,
                        ct_geometry_get_info, ct_project, ct_project_batch, ct_sirt_iterate,
@@ -16,7 +16,7 @@ from ._binding import (CT_CONE, CT_FAN2D, CT_PARALLEL2D, CT_PARALLEL3D, FBP_WIND
 __all__ = ["CT_CONE", "CT_FAN2D", "CT_PARALLEL2D", "CT_PARALLEL3D", "FBP_WINDOWS", "CtError",
            "Geometry", "GeometryInfo", "ct_backproject", "ct_backproject_batch",
            "ct_backproject_static", "ct_batch_workspace_bytes", "ct_cgls_iterate",
-           "ct_cgls_workspace_bytes", "ct_fbp", "ct_fbp_transpose",
+           "ct_cgls_workspace_bytes", "ct_fbp", "ct_fbp_parker_weights", "ct_fbp_transpose",
            "ct_fbp_transpose_workspace_bytes", "ct_fbp_workspace_bytes",
            "ct_geometry_create",
            "ct_geometry_create_surface", "ct_geometry_destroy", "ct_geometry_get_info",

@@ -92,11 +92,13 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.ct_backproject_static.restype = i32
     L.ct_fbp_workspace_bytes.argtypes = [vp]
     L.ct_fbp_workspace_bytes.restype = sz
-    L.ct_fbp.argtypes = [vp, vp, vp, vp, ctypes.POINTER(f64), i32, vp, sz, vp]
+    L.ct_fbp.argtypes = [vp, vp, vp, vp, vp, ctypes.POINTER(f64), i32, vp, sz, vp]
     L.ct_fbp.restype = i32
     L.ct_fbp_transpose_workspace_bytes.argtypes = [vp]
     L.ct_fbp_transpose_workspace_bytes.restype = sz
-    L.ct_fbp_transpose.argtypes = [vp, vp, vp, vp, ctypes.POINTER(f64), i32, vp, sz, vp]
+    L.ct_fbp_transpose.argtypes = [vp, vp, vp, vp, vp, ctypes.POINTER(f64), i32, vp, sz, vp]
+    L.ct_fbp_parker_weights.argtypes = [vp, ctypes.POINTER(f64), ctypes.POINTER(ctypes.c_float)]
+    L.ct_fbp_parker_weights.restype = i32
     L.ct_fbp_transpose.restype = i32
     L.ct_status_string.argtypes = [i32]
     L.ct_status_string.restype = ctypes.c_char_p
@@ -250,13 +252,15 @@ def _dptr(arr):
     return None if arr is None else arr.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
 
 
-def ct_fbp(handle: int, d_sino: int, d_volume: int, d_view_weights: int | None, isocenter,
-           window, d_workspace: int, workspace_bytes: int, stream: int | None) -> None:
+def ct_fbp(handle: int, d_sino: int, d_volume: int, d_view_weights: int | None,
+           d_pixel_weights: int | None, isocenter, window, d_workspace: int,
+           workspace_bytes: int, stream: int | None) -> None:
     """Filtered backprojection; ``window`` is a name of ``FBP_WINDOWS`` or its code and
     ``isocenter`` a host 3-vector or None."""
     code, iso = _fbp_args(isocenter, window)
-    _check(load_library().ct_fbp(handle, d_sino, d_volume, d_view_weights, _dptr(iso), code,
-                                 d_workspace, workspace_bytes, stream), "ct_fbp")
+    _check(load_library().ct_fbp(handle, d_sino, d_volume, d_view_weights, d_pixel_weights,
+                                 _dptr(iso), code, d_workspace, workspace_bytes, stream),
+           "ct_fbp")
 
 
 def ct_fbp_transpose_workspace_bytes(handle: int) -> int:
@@ -264,13 +268,23 @@ def ct_fbp_transpose_workspace_bytes(handle: int) -> int:
 
 
 def ct_fbp_transpose(handle: int, d_volume: int, d_sino: int, d_view_weights: int | None,
-                     isocenter, window, d_workspace: int, workspace_bytes: int,
-                     stream: int | None) -> None:
+                     d_pixel_weights: int | None, isocenter, window, d_workspace: int,
+                     workspace_bytes: int, stream: int | None) -> None:
     """Transpose of ``ct_fbp`` (volume -> sinogram), same arguments."""
     code, iso = _fbp_args(isocenter, window)
-    _check(load_library().ct_fbp_transpose(handle, d_volume, d_sino, d_view_weights, _dptr(iso),
-                                           code, d_workspace, workspace_bytes, stream),
-           "ct_fbp_transpose")
+    _check(load_library().ct_fbp_transpose(handle, d_volume, d_sino, d_view_weights,
+                                           d_pixel_weights, _dptr(iso), code, d_workspace,
+                                           workspace_bytes, stream), "ct_fbp_transpose")
+
+
+def ct_fbp_parker_weights(handle: int, n_views: int, n_u: int, isocenter=None) -> np.ndarray:
+    """Parker short-scan weights, a host (n_views, n_u) float32 array."""
+    _, iso = _fbp_args(isocenter, 0)
+    out = np.empty((n_views, n_u), dtype=np.float32)
+    _check(load_library().ct_fbp_parker_weights(
+        handle, _dptr(iso), out.ctypes.data_as(ctypes.POINTER(ctypes.c_float))),
+        "ct_fbp_parker_weights")
+    return out
 
 
 def ct_status_string(status: int) -> str:
@@ -430,7 +444,7 @@ class Geometry:
         return x
 
     def _fbp_call(self, fn, need, src, src_shape, dst_shape, out, window, view_weights,
-                  isocenter, workspace, stream):
+                  isocenter, workspace, stream, pixel_weights=None):
         import torch
         assert src.is_cuda and src.dtype == torch.float32 and src.is_contiguous()
         nd = len(src_shape)
@@ -447,24 +461,34 @@ class Geometry:
                                            device=src.device).contiguous()
             assert view_weights.numel() == self.info.n_views
             wptr = view_weights.data_ptr()
+        pptr = None
+        if pixel_weights is not None:
+            pixel_weights = torch.as_tensor(pixel_weights, dtype=torch.float32,
+                                            device=src.device).contiguous()
+            assert pixel_weights.numel() == self.info.n_views * self.info.n_u
+            pptr = pixel_weights.data_ptr()
         s2 = src.reshape((-1,) + tuple(src_shape))
         o2 = out.view((-1,) + tuple(dst_shape))
         for b in range(s2.shape[0]):
-            fn(self.handle, s2[b].data_ptr(), o2[b].data_ptr(), wptr, isocenter, window, ws, wsb,
-               self._stream(stream))
+            fn(self.handle, s2[b].data_ptr(), o2[b].data_ptr(), wptr, pptr, isocenter, window,
+               ws, wsb, self._stream(stream))
         return out
 
     def fbp(self, sino, out=None, window="ram-lak", view_weights=None, isocenter=None,
-            workspace=None, stream=None):
+            workspace=None, stream=None, pixel_weights=None):
         """Filtered backprojection (FBP / FDK) of a sinogram; leading dimensions are kept and
         reconstructed one after another with the same workspace."""
         return self._fbp_call(ct_fbp, ct_fbp_workspace_bytes(self.handle), sino,
                               self.sino_shape, self.volume_shape, out, window, view_weights,
-                              isocenter, workspace, stream)
+                              isocenter, workspace, stream, pixel_weights)
 
     def fbp_transpose(self, volume, out=None, window="ram-lak", view_weights=None,
-                      isocenter=None, workspace=None, stream=None):
+                      isocenter=None, workspace=None, stream=None, pixel_weights=None):
         """Transpose of ``fbp`` (volume -> sinogram); leading dimensions are kept."""
         return self._fbp_call(ct_fbp_transpose, ct_fbp_transpose_workspace_bytes(self.handle),
                               volume, self.volume_shape, self.sino_shape, out, window,
-                              view_weights, isocenter, workspace, stream)
+                              view_weights, isocenter, workspace, stream, pixel_weights)
+
+    def parker_weights(self, isocenter=None) -> np.ndarray:
+        """Parker short-scan weights (n_views, n_u) for ``fbp(..., pixel_weights=)``."""
+        return ct_fbp_parker_weights(self.handle, self.info.n_views, self.info.n_u, isocenter)

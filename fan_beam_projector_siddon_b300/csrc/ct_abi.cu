@@ -543,10 +543,16 @@ size_t ct_batch_workspace_bytes(const ct_geometry* g, int32_t batch) {
     return (size_t)std::min(batch, 4) * align_up(volume_bytes(g));
 }
 
+// The byte sizes of `batch` volumes and sinograms fit in size_t.
+static bool batch_fits(const ct_geometry* g, int32_t batch) {
+    const size_t most = std::max(volume_bytes(g), sino_bytes(g));
+    return most == 0 || (size_t)batch <= SIZE_MAX / most;
+}
+
 ct_status ct_project_batch(const ct_geometry* g, int32_t batch, const float* d_volumes,
                            float* d_sinos, void* d_workspace, size_t workspace_bytes,
                            cudaStream_t stream) {
-    if (g == nullptr || batch <= 0) return CT_ERR_INVALID_ARGUMENT;
+    if (g == nullptr || batch <= 0 || !batch_fits(g, batch)) return CT_ERR_INVALID_ARGUMENT;
     ct_status st = check_call(g, d_volumes, (size_t)batch * volume_bytes(g), d_sinos,
                               (size_t)batch * sino_bytes(g), d_workspace, workspace_bytes,
                               ct_batch_workspace_bytes(g, batch));
@@ -577,7 +583,7 @@ ct_status ct_project_batch(const ct_geometry* g, int32_t batch, const float* d_v
 ct_status ct_backproject_batch(const ct_geometry* g, int32_t batch, const float* d_sinos,
                                float* d_volumes, void* d_workspace, size_t workspace_bytes,
                                cudaStream_t stream) {
-    if (g == nullptr || batch <= 0) return CT_ERR_INVALID_ARGUMENT;
+    if (g == nullptr || batch <= 0 || !batch_fits(g, batch)) return CT_ERR_INVALID_ARGUMENT;
     ct_status st = check_call(g, d_sinos, (size_t)batch * sino_bytes(g), d_volumes,
                               (size_t)batch * volume_bytes(g), d_workspace, workspace_bytes,
                               ct_batch_workspace_bytes(g, batch));
@@ -857,9 +863,9 @@ void estimate_isocenter(const ct_geometry* g, double* iso) {
 
 // Argument checks shared by ct_fbp and ct_fbp_transpose; fills the kernel parameters.
 ct_status fbp_setup(const ct_geometry* g, const void* in, size_t in_bytes, const void* out,
-                    size_t out_bytes, const float* d_view_weights, const double* isocenter,
-                    ct_fbp_window window, const void* d_workspace, size_t workspace_bytes,
-                    bool transpose, ct::FbpParams* P, FbpLayout* L) {
+                    size_t out_bytes, const float* d_view_weights, const float* d_pixel_weights,
+                    const double* isocenter, ct_fbp_window window, const void* d_workspace,
+                    size_t workspace_bytes, bool transpose, ct::FbpParams* P, FbpLayout* L) {
     if (g == nullptr) return CT_ERR_INVALID_ARGUMENT;
     const int b = g->info.beam;
     if (b == CT_PARALLEL3D || g->d_offsets != nullptr) return CT_ERR_INVALID_ARGUMENT;
@@ -890,6 +896,13 @@ ct_status fbp_setup(const ct_geometry* g, const void* in, size_t in_bytes, const
             overlap(d_view_weights, wbytes, d_workspace, L->total))
             return CT_ERR_ALIASING;
     }
+    const size_t pbytes = wbytes * (size_t)g->info.n_u;
+    if (d_pixel_weights != nullptr) {
+        if ((st = check_device_ptr(d_pixel_weights, g->device)) != CT_OK) return st;
+        if (overlap(d_pixel_weights, pbytes, out, out_bytes) ||
+            overlap(d_pixel_weights, pbytes, d_workspace, L->total))
+            return CT_ERR_ALIASING;
+    }
     ct::FbpParams& p = *P;
     p.n_views = g->info.n_views;
     p.n_u = g->info.n_u;
@@ -908,21 +921,22 @@ ct_status fbp_setup(const ct_geometry* g, const void* in, size_t in_bytes, const
     p.sx = g->grid.sp[0];
     p.sy = g->grid.sp[1];
     p.sz = g->grid.sp[2];
+    p.pixel_weights = d_pixel_weights;
     return CT_OK;
 }
 
 }  // namespace
 
 extern "C" ct_status ct_fbp(const ct_geometry* g, const float* d_sino, float* d_volume,
-                            const float* d_view_weights, const double* isocenter,
-                            ct_fbp_window window, void* d_workspace, size_t workspace_bytes,
-                            cudaStream_t stream) {
+                            const float* d_view_weights, const float* d_pixel_weights,
+                            const double* isocenter, ct_fbp_window window, void* d_workspace,
+                            size_t workspace_bytes, cudaStream_t stream) {
     ct::FbpParams P;
     FbpLayout L;
     if (g == nullptr) return CT_ERR_INVALID_ARGUMENT;
     const ct_status st = fbp_setup(g, d_sino, sino_bytes(g), d_volume, volume_bytes(g),
-                                   d_view_weights, isocenter, window, d_workspace,
-                                   workspace_bytes, false, &P, &L);
+                                   d_view_weights, d_pixel_weights, isocenter, window,
+                                   d_workspace, workspace_bytes, false, &P, &L);
     if (st != CT_OK) return st;
     char* ws = static_cast<char*>(d_workspace);
     return from_cuda(ct::launch_fbp(P, g->d_raw, d_view_weights,
@@ -933,19 +947,107 @@ extern "C" ct_status ct_fbp(const ct_geometry* g, const float* d_sino, float* d_
 }
 
 extern "C" ct_status ct_fbp_transpose(const ct_geometry* g, const float* d_volume, float* d_sino,
-                                      const float* d_view_weights, const double* isocenter,
-                                      ct_fbp_window window, void* d_workspace,
-                                      size_t workspace_bytes, cudaStream_t stream) {
+                                      const float* d_view_weights, const float* d_pixel_weights,
+                                      const double* isocenter, ct_fbp_window window,
+                                      void* d_workspace, size_t workspace_bytes,
+                                      cudaStream_t stream) {
     ct::FbpParams P;
     FbpLayout L;
     if (g == nullptr) return CT_ERR_INVALID_ARGUMENT;
     const ct_status st = fbp_setup(g, d_volume, volume_bytes(g), d_sino, sino_bytes(g),
-                                   d_view_weights, isocenter, window, d_workspace,
-                                   workspace_bytes, true, &P, &L);
+                                   d_view_weights, d_pixel_weights, isocenter, window,
+                                   d_workspace, workspace_bytes, true, &P, &L);
     if (st != CT_OK) return st;
     char* ws = static_cast<char*>(d_workspace);
     return from_cuda(ct::launch_fbp_transpose(
         P, g->d_raw, d_view_weights, reinterpret_cast<ct::FbpView*>(ws + L.views),
         reinterpret_cast<ct::FbpCosine*>(ws + L.cosines), reinterpret_cast<float*>(ws + L.taps),
         d_volume, reinterpret_cast<float*>(ws + L.filtered), d_sino, stream));
+}
+
+// ---------------------------------------------------------------------------------------------
+// Parker short-scan weights ("Differentiable analytical reconstruction": short scans add Parker
+// weighting before filtering; Parker 1982).
+
+extern "C" ct_status ct_fbp_parker_weights(const ct_geometry* g, const double* isocenter,
+                                           float* out) {
+    if (g == nullptr || out == nullptr) return CT_ERR_INVALID_ARGUMENT;
+    const int b = g->info.beam;
+    if (b != CT_FAN2D && b != CT_CONE) return CT_ERR_INVALID_ARGUMENT;
+    if (g->d_offsets != nullptr) return CT_ERR_INVALID_ARGUMENT;
+    double iso[3] = {0.0, 0.0, 0.0};
+    if (isocenter != nullptr) {
+        for (int a = 0; a < (is_2d(b) ? 2 : 3); ++a) {
+            if (!std::isfinite(isocenter[a])) return CT_ERR_INVALID_ARGUMENT;
+            iso[a] = isocenter[a];
+        }
+    } else {
+        estimate_isocenter(g, iso);
+    }
+    const int n_views = g->info.n_views, n_u = g->info.n_u;
+    const int w = is_2d(b) ? 6 : 12;
+    const double pi = 3.14159265358979323846;
+    // source angles about the isocentre, unwrapped, in the sense of rotation; the orbit must be a
+    // circle in the xy-plane about the isocentre
+    std::vector<double> beta((size_t)n_views);
+    double rmin = 1e300, rmax = 0.0, zmin = 1e300, zmax = -1e300;
+    for (int k = 0; k < n_views; ++k) {
+        double first[3], ctr[3], u[3], v[3];
+        unpack(b, g->host_views.data() + (int64_t)k * w, first, ctr, u, v);
+        const double rx = first[0] - iso[0], ry = first[1] - iso[1];
+        const double r = std::hypot(rx, ry);
+        rmin = std::min(rmin, r);
+        rmax = std::max(rmax, r);
+        zmin = std::min(zmin, first[2]);
+        zmax = std::max(zmax, first[2]);
+        double a = std::atan2(ry, rx);
+        if (k > 0) {
+            while (a - beta[(size_t)k - 1] > pi) a -= 2.0 * pi;
+            while (a - beta[(size_t)k - 1] < -pi) a += 2.0 * pi;
+        }
+        beta[(size_t)k] = a;
+    }
+    const double rmean = 0.5 * (rmin + rmax);
+    if (!(rmean > 0.0) || rmax - rmin > 1e-6 * rmean || zmax - zmin > 1e-6 * rmean)
+        return CT_ERR_INVALID_GEOMETRY;
+    const double sense = beta[(size_t)n_views - 1] >= beta[0] ? 1.0 : -1.0;
+    const double b0 = beta[0];
+    for (double& x : beta) x = (x - b0) * sense;
+    // fan angle of each detector column's centre line from the central ray, same sense
+    std::vector<double> gamma((size_t)n_views * (size_t)n_u);
+    double delta = 0.0;
+    const double cu = 0.5 * (n_u - 1);
+    for (int k = 0; k < n_views; ++k) {
+        double first[3], ctr[3], u[3], v[3];
+        unpack(b, g->host_views.data() + (int64_t)k * w, first, ctr, u, v);
+        const double ax = iso[0] - first[0], ay = iso[1] - first[1];
+        for (int j = 0; j < n_u; ++j) {
+            const double o = (j - cu) * g->du;
+            const double bx = ctr[0] + o * u[0] - first[0], by = ctr[1] + o * u[1] - first[1];
+            const double gm = sense * std::atan2(ax * by - ay * bx, ax * bx + ay * by);
+            gamma[(size_t)k * n_u + j] = gm;
+            delta = std::max(delta, std::fabs(gm));
+        }
+    }
+    const double span = beta[(size_t)n_views - 1];
+    if (span < pi + 2.0 * delta - 1e-9) return CT_ERR_INVALID_GEOMETRY;
+    const double d = 0.5 * (span - pi);  // effective half fan angle
+    for (int k = 0; k < n_views; ++k) {
+        const double bk = beta[(size_t)k];
+        for (int j = 0; j < n_u; ++j) {
+            const double gm = gamma[(size_t)k * n_u + j];
+            double wt = 0.0;
+            if (bk >= 0.0 && bk < 2.0 * (d - gm)) {
+                const double sn = std::sin(0.25 * pi * bk / (d - gm));
+                wt = sn * sn;
+            } else if (bk >= 2.0 * (d - gm) && bk <= pi - 2.0 * gm) {
+                wt = 1.0;
+            } else if (bk > pi - 2.0 * gm && bk <= pi + 2.0 * d) {
+                const double sn = std::sin(0.25 * pi * (pi + 2.0 * d - bk) / (d + gm));
+                wt = sn * sn;
+            }
+            out[(size_t)k * n_u + j] = (float)wt;
+        }
+    }
+    return CT_OK;
 }

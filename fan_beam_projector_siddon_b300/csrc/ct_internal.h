@@ -114,6 +114,7 @@ struct FbpParams {
     double du, dv;
     double iso[3];
     float sx, sy, sz;  // voxel pitches along x, y, z
+    const float* pixel_weights;  // optional (n_views, n_u) weights before filtering, or nullptr
 };
 // Per-view constants of the gather (64 bytes, read as four float4).
 struct FbpView {

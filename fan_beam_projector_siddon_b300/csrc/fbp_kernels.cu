@@ -258,6 +258,7 @@ __global__ void __launch_bounds__(256) fbp_filter_kernel(FbpParams p,
             } else {
                 val = in[((int64_t)view * n_u + iu) * V + v0 + j];
                 if (!p.parallel) val *= cosine_weight(C, iu, v0 + j);
+                if (p.pixel_weights) val *= p.pixel_weights[(int64_t)view * n_u + iu];
             }
         }
         tile[i] = val;
@@ -271,6 +272,7 @@ __global__ void __launch_bounds__(256) fbp_filter_kernel(FbpParams p,
         for (int k = 0; k < n_u; ++k) acc = fmaf(h[-k], tile[k * tv + j], acc);
         if (ADJ) {
             if (!p.parallel) acc *= cosine_weight(C, iu, v0 + j);
+            if (p.pixel_weights) acc *= p.pixel_weights[(int64_t)view * n_u + iu];
             out[((int64_t)view * n_u + iu) * V + v0 + j] = acc;
         } else {
             out[qrow(p, view, iu) + v0 + j + vo] = acc;
@@ -310,6 +312,7 @@ __global__ void __launch_bounds__(256) fbp_filter_blocked_kernel(
             } else {
                 val = in[((int64_t)view * n_u + k) * V + v0 + j];
                 if (!p.parallel) val *= cosine_weight(C, k, v0 + j);
+                if (p.pixel_weights) val *= p.pixel_weights[(int64_t)view * n_u + k];
             }
         }
         tile[i] = val;
@@ -336,8 +339,8 @@ __global__ void __launch_bounds__(256) fbp_filter_blocked_kernel(
             for (int r = 0; r < R; ++r) {
                 if (r0 + r >= n_u) continue;
                 if (ADJ) {
-                    const float a = p.parallel ? acc[r]
-                                               : acc[r] * cosine_weight(C, r0 + r, v0 + lane);
+                    float a = p.parallel ? acc[r] : acc[r] * cosine_weight(C, r0 + r, v0 + lane);
+                    if (p.pixel_weights) a *= p.pixel_weights[(int64_t)view * n_u + r0 + r];
                     out[((int64_t)view * n_u + r0 + r) * V + v0 + lane] = a;
                 } else {
                     out[qrow(p, view, r0 + r) + v0 + lane + 1] = acc[r];

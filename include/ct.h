@@ -290,7 +290,10 @@ CT_API ct_status ct_backproject_static(const ct_geometry *geom, const float *d_s
  * d_volume     device volume, overwritten.
  * d_view_weights  device, n_views floats, or NULL for the uniform full-scan quadrature
  *              w_k = pi / n_views (a 180-degree parallel scan, or a 360-degree fan/cone scan with
- *              the 1/2 redundancy factor).  Short scans pass their own (e.g. Parker) weights.
+ *              the 1/2 redundancy factor).  Short scans pass the angular step instead.
+ * d_pixel_weights device, n_views x n_u floats, or NULL: weights per view and detector column
+ *              applied with the cosine weights before filtering, e.g. Parker's short-scan
+ *              weights from ct_fbp_parker_weights.
  * isocenter    host, 3 doubles (x, y, z; z ignored in 2D), or NULL: the point whose
  *              detector-plane distance sets D_so (fan/cone; unused for parallel beams).  NULL
  *              estimates it from the detector normals, as the pages' default does: the
@@ -314,9 +317,9 @@ typedef enum {
 
 CT_API size_t ct_fbp_workspace_bytes(const ct_geometry *geom);
 CT_API ct_status ct_fbp(const ct_geometry *geom, const float *d_sino, float *d_volume,
-                        const float *d_view_weights, const double *isocenter,
-                        ct_fbp_window window, void *d_workspace, size_t workspace_bytes,
-                        struct CUstream_st *stream);
+                        const float *d_view_weights, const float *d_pixel_weights,
+                        const double *isocenter, ct_fbp_window window, void *d_workspace,
+                        size_t workspace_bytes, struct CUstream_st *stream);
 
 /*
  * Transpose of ct_fbp as a linear map (sinogram -> volume), for gradients with respect to the
@@ -334,9 +337,32 @@ CT_API ct_status ct_fbp(const ct_geometry *geom, const float *d_sino, float *d_v
  */
 CT_API size_t ct_fbp_transpose_workspace_bytes(const ct_geometry *geom);
 CT_API ct_status ct_fbp_transpose(const ct_geometry *geom, const float *d_volume, float *d_sino,
-                                  const float *d_view_weights, const double *isocenter,
-                                  ct_fbp_window window, void *d_workspace,
-                                  size_t workspace_bytes, struct CUstream_st *stream);
+                                  const float *d_view_weights, const float *d_pixel_weights,
+                                  const double *isocenter, ct_fbp_window window,
+                                  void *d_workspace, size_t workspace_bytes,
+                                  struct CUstream_st *stream);
+
+/*
+ * Parker's short-scan weights (Parker 1982) for a circular fan or cone scan, host-computed in
+ * float64: the pages add them before filtering for short scans ("Differentiable analytical
+ * reconstruction": short_scan).  beta = source angle about the isocentre from the first view,
+ * in the sense of rotation; gamma = fan angle of detector column u (its centre line) from the
+ * central ray, in the same sense; delta = max |gamma|.  With the last view at beta = span
+ * >= pi + 2 delta the weights use the effective half fan angle d = (span - pi) / 2:
+ *     w = sin^2(pi/4 * beta / (d - gamma))                0 <= beta < 2 (d - gamma)
+ *       = 1                                                up to beta = pi - 2 gamma
+ *       = sin^2(pi/4 * (pi + 2 d - beta) / (d + gamma))    up to beta = pi + 2 d
+ * so that the two measurements of every line weigh 1 together.  Use them as ct_fbp's
+ * d_pixel_weights with view weights equal to the angular step (no 1/2 factor).
+ *
+ * isocenter  host, 3 doubles, or NULL to estimate it as ct_fbp does.
+ * out        HOST, n_views x n_u floats (view-major), written on CT_OK.
+ * Errors: CT_ERR_INVALID_ARGUMENT for parallel beams, surface detectors or NULL pointers;
+ * CT_ERR_INVALID_GEOMETRY if the sources are not on a circle in the xy-plane about the
+ * isocentre (relative tolerance 1e-6) or the scan spans less than pi + 2 delta.
+ */
+CT_API ct_status ct_fbp_parker_weights(const ct_geometry *geom, const double *isocenter,
+                                       float *out);
 
 /* Static, human-readable name of a status code. */
 CT_API const char *ct_status_string(ct_status status);

@@ -151,12 +151,13 @@ def test_errors(ct):
 
     def call(status, **kw):
         args = dict(d_sino=sino.data_ptr(), d_volume=vol.data_ptr(), d_view_weights=None,
-                    isocenter=None, window=0, d_workspace=ws.data_ptr(), workspace_bytes=need)
+                    d_pixel_weights=None, isocenter=None, window=0, d_workspace=ws.data_ptr(),
+                    workspace_bytes=need)
         args.update(kw)
         with pytest.raises(ct.CtError) as ei:
             ct.ct_fbp(g.handle, args["d_sino"], args["d_volume"], args["d_view_weights"],
-                      args["isocenter"], args["window"], args["d_workspace"],
-                      args["workspace_bytes"], s)
+                      args["d_pixel_weights"], args["isocenter"], args["window"],
+                      args["d_workspace"], args["workspace_bytes"], s)
         assert ei.value.status == status
 
     call(7, workspace_bytes=need - 1)
@@ -164,7 +165,7 @@ def test_errors(ct):
     need_t = ct.ct_fbp_transpose_workspace_bytes(g.handle)
     assert need_t > need
     with pytest.raises(ct.CtError) as ei:
-        ct.ct_fbp_transpose(g.handle, vol.data_ptr(), sino.data_ptr(), None, None, 0,
+        ct.ct_fbp_transpose(g.handle, vol.data_ptr(), sino.data_ptr(), None, None, None, 0,
                             ws.data_ptr(), need, s)
     assert ei.value.status == 7
     call(1, window=5)
@@ -172,6 +173,12 @@ def test_errors(ct):
     call(4, d_volume=ws.data_ptr())
     host = np.zeros(4, np.float32)
     call(3, d_view_weights=host.ctypes.data)
+    call(3, d_pixel_weights=host.ctypes.data)
+    call(4, d_pixel_weights=vol.data_ptr())
+    # Parker weights: parallel beams have none
+    with pytest.raises(ct.CtError) as ei:
+        ct.Geometry.from_workload(W.small_config(1)).parker_weights()
+    assert ei.value.status == 1
     # parallel3d and surface detectors have no FBP here
     p = W.small_config(5)
     gp = ct.Geometry.from_workload(p)
@@ -327,3 +334,66 @@ def test_estimated_isocentre_matches_oracle(ct, n):
     x = W.random_volume(w, 9)
     got_t = _cpu(g.fbp_transpose(torch_cuda(x)))
     _check(got_t, _oracle_t(w, x.astype(np.float64)))
+
+
+
+# ---------------------------------------------------------------------------------------------
+# short scans with Parker weights
+# ---------------------------------------------------------------------------------------------
+
+def _short_scan(n, margin=0.03):
+    """Workload n (2: fan, 3: cone) on a circular orbit spanning pi + 2 delta + margin."""
+    import dataclasses
+    base = W.small_config(n)
+    src = base.views[0, 0:2] if n == 2 else base.views[0, 0:3]
+    d = 2 if n == 2 else 3
+    sid = float(np.linalg.norm(base.views[0, 0:2]))
+    sdd = sid + float(np.linalg.norm(base.views[0, d:d + 2]))
+    delta = np.arctan(((base.n_u - 1) / 2.0 * base.du) / sdd)
+    span = np.pi + 2 * delta + margin
+    nv = base.views.shape[0]
+    full = span * nv / (nv - 1)
+    views = (W.circular_fan_2d(nv, sid, sdd, span=full) if n == 2 else
+             W.circular_cone(nv, sid, sdd, span=full))
+    return dataclasses.replace(base, views=views), span
+
+
+@pytest.mark.parametrize("n", [2, 3])
+def test_parker_weights_match_oracle(ct, n):
+    w, _ = _short_scan(n)
+    g = ct.Geometry.from_workload(w)
+    got = g.parker_weights()
+    want = F.parker_weights(w.beam, w.views, w.n_u, w.du)
+    np.testing.assert_allclose(got, want, atol=2e-6)
+    assert got.min() >= 0 and got.max() <= 1 and (got < 0.5).any()
+
+
+@pytest.mark.parametrize("n", [2, 3])
+def test_short_scan_fbp_and_transpose_with_parker_weights(ct, n):
+    w, span = _short_scan(n)
+    g = ct.Geometry.from_workload(w)
+    pw = g.parker_weights()
+    vw = np.full(w.views.shape[0], span / (w.views.shape[0] - 1), dtype=np.float32)
+    y = W.random_sinogram(w, 12)
+    got = _cpu(g.fbp(torch_cuda(y), view_weights=torch_cuda(vw), pixel_weights=torch_cuda(pw)))
+    _check(got, _oracle(w, y.astype(np.float64), view_weights=vw.astype(np.float64),
+                        pixel_weights=pw.astype(np.float64)))
+    x = W.random_volume(w, 13)
+    got_t = _cpu(g.fbp_transpose(torch_cuda(x), view_weights=torch_cuda(vw),
+                                 pixel_weights=torch_cuda(pw)))
+    _check(got_t, _oracle_t(w, x.astype(np.float64), view_weights=vw.astype(np.float64),
+                            pixel_weights=pw.astype(np.float64)))
+
+
+def test_parker_rejects_short_and_non_circular_scans(ct):
+    import dataclasses
+    w, _ = _short_scan(2, margin=-0.3)
+    with pytest.raises(ct.CtError) as ei:
+        ct.Geometry.from_workload(w).parker_weights()
+    assert ei.value.status == 2
+    base = W.small_config(2)
+    bad = base.views.copy()
+    bad[3, 0:2] *= 1.01
+    with pytest.raises(ct.CtError) as ei:
+        ct.Geometry.from_workload(dataclasses.replace(base, views=bad)).parker_weights()
+    assert ei.value.status == 2
