@@ -115,3 +115,35 @@ def test_surface_admission_before_touching_the_gpu(lib):
     c = W.anisotropic_config("cone")
     _expect(lib, 1, lib.ct_geometry_create, c.beam, c.views, c.vol_shape, (1.0, 0.0, 1.0),
             c.n_u, c.n_v, c.du, c.dv)
+
+
+def test_header_is_strict_c99(tmp_path):
+    """include/ct.h is a C header: it compiles alone under gcc -std=c99 -pedantic -Werror."""
+    import subprocess
+    src = tmp_path / "hdr.c"
+    src.write_text('#include "ct.h"\nint main(void) { return (int)sizeof(ct_geometry_info) == 0; }\n')
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-c",
+                        "-I", os.path.join(ROOT, "include"), str(src), "-o",
+                        str(tmp_path / "hdr.o")], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
+def build_c_check(out_dir):
+    """Compile and link tests/c/abi_check.c against libctproj.so and the CUDA runtime."""
+    import subprocess
+    ct_build.build()
+    cuda = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+    exe = os.path.join(str(out_dir), "abi_check")
+    pkg = os.path.dirname(ct_build.LIB)
+    cmd = ["gcc", "-std=c11", "-Wall", "-Wextra", "-Werror", "-O1",
+           os.path.join(ROOT, "tests", "c", "abi_check.c"), "-I", os.path.join(ROOT, "include"),
+           "-I", os.path.join(cuda, "include"), "-L", pkg, "-lctproj",
+           "-L", os.path.join(cuda, "lib64"), "-lcudart", "-lm", "-Wl,-rpath," + pkg,
+           "-Wl,-rpath," + os.path.join(cuda, "lib64"), "-o", exe]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    return exe
+
+
+def test_c_program_links_against_the_library(tmp_path):
+    assert os.path.exists(build_c_check(tmp_path))
