@@ -26,7 +26,9 @@
  *
  * Threading and streams: a geometry handle is immutable after creation; calls on different
  * streams may share a handle, but not a workspace.  Every compute call is asynchronous on the
- * given stream (NULL = legacy default stream), allocates nothing and never synchronises.
+ * given stream (NULL = legacy default stream), allocates nothing and never synchronises, so the
+ * projector, SIRT, CGLS and FBP calls can be recorded into a CUDA graph by stream capture
+ * (thread-local capture mode) and replayed; a replay reads the buffers' current contents.
  * Asynchronous CUDA errors surface as CT_ERR_CUDA on a later call.  No call aborts the process.
  */
 #ifndef CT_H
