@@ -1051,3 +1051,20 @@ extern "C" ct_status ct_fbp_parker_weights(const ct_geometry* g, const double* i
     }
     return CT_OK;
 }
+
+// ---------------------------------------------------------------------------------------------
+// Bounds-checking builds.
+
+extern "C" ct_status ct_debug_bounds_violations(uint64_t* count) {
+    if (count == nullptr) return CT_ERR_INVALID_ARGUMENT;
+    *count = 0;
+#ifdef CT_DEBUG_BOUNDS
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return from_cuda(e);
+    *count = ct::siddon_bounds_violations(true) + ct::fbp_bounds_violations(true);
+    e = cudaGetLastError();
+    return from_cuda(e);
+#else
+    return CT_ERR_INVALID_ARGUMENT;
+#endif
+}

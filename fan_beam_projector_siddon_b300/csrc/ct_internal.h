@@ -8,6 +8,13 @@
 
 namespace ct {
 
+// Bounds-checking builds (compiled with -DCT_DEBUG_BOUNDS): every data-dependent voxel or detector
+// index the kernels form is checked before use; an index outside its array skips the access and
+// increments a per-file device counter (no trap).  Release builds compile the checks away.
+// Counters of the kernel files, read and reset from the host (0 in release builds).
+uint64_t siddon_bounds_violations(bool reset);
+uint64_t fbp_bounds_violations(bool reset);
+
 // Internal volume orders (the kernels' memory layout of the volume).
 enum Layout : int32_t {
     LAYOUT_ZYX = 0,  // caller's order, x fastest

@@ -26,6 +26,24 @@
 namespace ct {
 namespace {
 
+#ifdef CT_DEBUG_BOUNDS
+__device__ unsigned long long g_bounds_violations = 0;
+#endif
+
+// True when 0 <= i < n; in bounds-checking builds a miss is counted (the caller skips the access).
+__device__ __forceinline__ bool in_bounds(int64_t i, int64_t n) {
+#ifdef CT_DEBUG_BOUNDS
+    if ((uint64_t)i >= (uint64_t)n) {
+        atomicAdd(&g_bounds_violations, 1ull);
+        return false;
+    }
+#else
+    (void)i;
+    (void)n;
+#endif
+    return true;
+}
+
 // I(x) = int_0^F f cos(2 pi f x) df  and  J(c) = int_0^F sin(2 pi f c) df.
 __device__ double ramp_I(double x, double F) {
     if (x == 0.0) return 0.5 * F * F;
@@ -80,19 +98,27 @@ __device__ __forceinline__ float4* copy_block(const FbpParams& p, float* q, int 
     const int pu = U0 & 1, pv = V0 & 1;
     const int64_t blk = (((int64_t)(pu * 2 + pv) * p.n_views + view) * p.bu + ((U0 + pu) >> 1)) *
                             p.bv + ((V0 + pv) >> 1);
+    if (!in_bounds(blk, 4 * (int64_t)p.n_views * p.bu * p.bv)) return nullptr;
     return reinterpret_cast<float4*>(q) + blk;
 }
 __device__ __forceinline__ float2* copy_pair(const FbpParams& p, float* q, int view, int U0) {
     const int pu = U0 & 1;
     const int64_t blk = ((int64_t)pu * p.n_views + view) * p.bu + ((U0 + pu) >> 1);
+    if (!in_bounds(blk, 2 * (int64_t)p.n_views * p.bu)) return nullptr;
     return reinterpret_cast<float2*>(q) + blk;
 }
 __device__ __forceinline__ void red_add4(float4* a, float x, float y, float z, float w) {
+#ifdef CT_DEBUG_BOUNDS
+    if (a == nullptr) return;
+#endif
     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(a), "f"(x), "f"(y),
                  "f"(z), "f"(w)
                  : "memory");
 }
 __device__ __forceinline__ void red_add2(float2* a, float x, float y) {
+#ifdef CT_DEBUG_BOUNDS
+    if (a == nullptr) return;
+#endif
     asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(a), "f"(x), "f"(y) : "memory");
 }
 // Sum of the copies at padded pixel (U, V) (2D: V ignored).
@@ -409,6 +435,9 @@ __global__ void __launch_bounds__(256) fdk_gather_kernel(FbpParams p,
                     const float vp = fminf(fmaxf(fmaf(t, av, E.z), -1.0f), vmax);
                     const float fv0 = floorf(vp), fv = vp - fv0;
                     const float* pq = prow + (int)fv0;
+#ifdef CT_DEBUG_BOUNDS
+                    if (!in_bounds(pq - q, (int64_t)p.n_views * p.rows * cols - cols - 1)) continue;
+#endif
                     const float s00 = __ldg(pq), s01 = __ldg(pq + 1);
                     const float s10 = __ldg(pq + cols), s11 = __ldg(pq + cols + 1);
                     const float a0 = fmaf(fv, s01 - s00, s00);
@@ -430,6 +459,9 @@ __global__ void __launch_bounds__(256) fdk_gather_kernel(FbpParams p,
                 const float fu0 = floorf(up), fv0 = floorf(vp);
                 const float fu = up - fu0, fv = vp - fv0;
                 const float* pq = base + ((int)fu0 + 1) * cols + (int)fv0 + 1;
+#ifdef CT_DEBUG_BOUNDS
+                if (!in_bounds(pq - q, (int64_t)p.n_views * p.rows * cols - cols - 1)) continue;
+#endif
                 const float s00 = __ldg(pq), s01 = __ldg(pq + 1);
                 const float s10 = __ldg(pq + cols), s11 = __ldg(pq + cols + 1);
                 const float a0 = fmaf(fv, s01 - s00, s00);
@@ -492,6 +524,9 @@ __global__ void __launch_bounds__(256) fbp2d_gather_kernel(FbpParams p,
                     const float up = fminf(fmaxf(fmaf(Y[m], B.w, ux), -1.0f), umax);
                     const float fu0 = floorf(up), fu = up - fu0;
                     const float* pq = base + (int)fu0;
+#ifdef CT_DEBUG_BOUNDS
+                    if (!in_bounds(pq - q, (int64_t)p.n_views * rows - 1)) continue;
+#endif
                     const float s0 = __ldg(pq), s1 = __ldg(pq + 1);
                     acc[m] = fmaf(E.w, fmaf(fu, s1 - s0, s0), acc[m]);
                 }
@@ -507,6 +542,9 @@ __global__ void __launch_bounds__(256) fbp2d_gather_kernel(FbpParams p,
                     const float up = fminf(fmaxf(fmaf(E.x * inv, au, E.y), -1.0f), umax);
                     const float fu0 = floorf(up), fu = up - fu0;
                     const float* pq = base + (int)fu0;
+#ifdef CT_DEBUG_BOUNDS
+                    if (!in_bounds(pq - q, (int64_t)p.n_views * rows - 1)) continue;
+#endif
                     const float s0 = __ldg(pq), s1 = __ldg(pq + 1);
                     acc[m] = fmaf(E.w * inv * inv, fmaf(fu, s1 - s0, s0), acc[m]);
                 }
@@ -764,6 +802,21 @@ cudaError_t launch_fbp(const FbpParams& p, const double* raw, const float* user_
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;
+}
+
+uint64_t fbp_bounds_violations(bool reset) {
+#ifdef CT_DEBUG_BOUNDS
+    unsigned long long v = 0;
+    cudaMemcpyFromSymbol(&v, g_bounds_violations, sizeof(v));
+    if (reset) {
+        const unsigned long long zero = 0;
+        cudaMemcpyToSymbol(g_bounds_violations, &zero, sizeof(zero));
+    }
+    return v;
+#else
+    (void)reset;
+    return 0;
+#endif
 }
 
 size_t fbp_copies_floats(const FbpParams& p) {

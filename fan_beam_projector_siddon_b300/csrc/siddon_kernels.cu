@@ -22,6 +22,19 @@
 namespace ct {
 namespace {
 
+#ifdef CT_DEBUG_BOUNDS
+__device__ unsigned long long g_bounds_violations = 0;
+
+// True when 0 <= i < n; otherwise the miss is counted and the caller skips the access.
+__device__ __forceinline__ bool in_bounds(int64_t i, int64_t n) {
+    if ((uint64_t)i >= (uint64_t)n) {
+        atomicAdd(&g_bounds_violations, 1ull);
+        return false;
+    }
+    return true;
+}
+#endif
+
 constexpr int kThreads = 256;  // 8 warps
 constexpr int kRows = 4;       // 3D tiles: 8 warps x 4 rows = 32 pixels along the warp axis
 constexpr int kTile = 32;      // 3D tiles are 32 x 32 pixels
@@ -49,6 +62,9 @@ struct Ray {
     int idx;       // entry voxel, linear index in the internal layout
     float tend;    // chord length inside the box (voxel units)
     float scale;   // physical length per unit of voxel-space length along this ray
+#ifdef CT_DEBUG_BOUNDS
+    int64_t nvox;  // voxels of one volume (bounds-checking builds)
+#endif
 };
 
 // Ray set-up for pixel (u, v).  Returns false when the ray misses the volume.  F is the inner
@@ -166,6 +182,9 @@ __device__ __forceinline__ bool setup_ray(const ViewRec& vr, const Grid& g, int 
         idx += i0 * g.stride[a];
     }
     r.idx = idx;
+#ifdef CT_DEBUG_BOUNDS
+    r.nvox = (int64_t)g.n[0] * g.n[1] * g.n[2];
+#endif
     return true;
 }
 
@@ -201,10 +220,20 @@ __device__ __forceinline__ void walk(const Ray& r, const float* __restrict__ vin
     for (int b = 0; b < NB; ++b) acc[b] = 0.0f;
     // segment [.., .. + seg) in voxel idx: gather from / scatter into every volume of the batch
     auto scatter = [&](int i, float seg) {
+#ifdef CT_DEBUG_BOUNDS
+        if (!in_bounds(i, r.nvox)) return;
+#endif
 #pragma unroll
         for (int b = 0; b < NB; ++b) atomicAdd(vout + b * vstride + i, __fmul_rn(val[b], seg));
     };
     auto load = [&](int i, float (&v)[NB]) {
+#ifdef CT_DEBUG_BOUNDS
+        if (!in_bounds(i, r.nvox)) {
+#pragma unroll
+            for (int b = 0; b < NB; ++b) v[b] = 0.0f;
+            return;
+        }
+#endif
 #pragma unroll
         for (int b = 0; b < NB; ++b) v[b] = __ldg(vin + b * vstride + i);
     };
@@ -679,6 +708,25 @@ __global__ void __launch_bounds__(256) transpose_kernel(const float* __restrict_
         if (r < rows && cc < cols) out[base + cc * rows + r] = tile[tx][ty + k];
     }
 }
+
+}  // namespace
+
+uint64_t siddon_bounds_violations(bool reset) {
+#ifdef CT_DEBUG_BOUNDS
+    unsigned long long v = 0;
+    cudaMemcpyFromSymbol(&v, g_bounds_violations, sizeof(v));
+    if (reset) {
+        const unsigned long long zero = 0;
+        cudaMemcpyToSymbol(g_bounds_violations, &zero, sizeof(zero));
+    }
+    return v;
+#else
+    (void)reset;
+    return 0;
+#endif
+}
+
+namespace {
 
 int64_t grid_for(const Tiling& t) {
     return (int64_t)t.tiles_v * t.n_views * t.tiles_u;

@@ -366,6 +366,16 @@ CT_API ct_status ct_fbp_transpose(const ct_geometry *geom, const float *d_volume
 CT_API ct_status ct_fbp_parker_weights(const ct_geometry *geom, const double *isocenter,
                                        float *out);
 
+/*
+ * Bounds-checking builds (the library compiled with -DCT_DEBUG_BOUNDS; the package's build
+ * script does that with debug_bounds=True): every data-dependent voxel or detector index the
+ * kernels form is checked before use, and an index outside its array skips the access and is
+ * counted on the device instead of faulting.  This call synchronises the device and returns the
+ * count since the previous call (then resets it).  Release builds return CT_ERR_INVALID_ARGUMENT
+ * with *count = 0.  The pages have no counterpart; it stands in for a memory checker.
+ */
+CT_API ct_status ct_debug_bounds_violations(uint64_t *count);
+
 /* Static, human-readable name of a status code. */
 CT_API const char *ct_status_string(ct_status status);
 
