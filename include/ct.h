@@ -1,6 +1,8 @@
 /*
  * ct.h -- C ABI of libctproj: the cell-constant Siddon CT forward projector A, its matched
- * adjoint A^T and a SIRT iteration built on the pair, for one NVIDIA B300 (sm_103a).
+ * adjoint A^T, SIRT and CGLS built on the pair, batched volumes, per-axis voxel pitches,
+ * parameterised detector surfaces, and filtered backprojection (FBP/FDK, short scans) with its
+ * transpose, for one NVIDIA B300 (sm_103a).
  *
  * Operator (diffct documentation, "Differentiable analytical reconstruction", first paragraph:
  * "cell-constant Siddon forward operator and its matched adjoint"; "Trajectories and Geometry",
