@@ -69,7 +69,9 @@ def test_cgls_matches_oracle_small(ct, n):
     g.cgls(x, y, 5, ws, initialised=True)
     torch.cuda.synchronize()
     sens, res32 = _float32_storage_sensitivity(go, y_or, x_or, 8)
-    assert rel_l2(x.cpu().numpy(), x_or) <= max(CGLS_RTOL, 10.0 * sens)
+    # (the same two-realisation argument as for the residual below: 2 x 10 times the
+    # float32-storage change)
+    assert rel_l2(x.cpu().numpy(), x_or) <= max(CGLS_RTOL, 20.0 * sens)
     # the residual of the GPU iterate matches the oracle's after 8 steps, within 1 % or twenty
     # times what float32 storage alone does to it: the float32-storage run is one realisation of
     # float32 rounding, the GPU (whose atomic backprojections also change their summation order
