@@ -18,6 +18,8 @@ cosine, hamming, hann), angular integration weights, and a voxel-driven distance
   rank-deficient sets (one view, parallel normals) give the minimum-norm point;
 * optional per (view, detector column) weights before filtering, e.g. Parker's short-scan
   weights (Parker 1982) for circular fan/cone orbits spanning pi + 2 delta;
+* optional caller filter kernel replacing the windowed ramp (a learned filter), and the
+  gradients of a loss with respect to that kernel and to the view weights (`fbp_gradients`);
 * gather: f(X) = sum_k w_k g_k(X) Q_k(u_k(X), v_k(X)) with bilinear interpolation (0 outside the
   detector), g = 1 for parallel beams and, for fan/cone, g = (D_sd / D_so) / U(X)^2 with
   U(X) = ((X - s) . n) / ((iso - s) . n), D_so = |(iso - s) . n|, D_sd = |(c - s) . n|
@@ -153,9 +155,20 @@ def _frames(beam: int, rec: np.ndarray):
     return first, ctr, u, v, n
 
 
+def filter_kernel(n_u: int, du: float, window: str = "ram-lak", kernel=None) -> np.ndarray:
+    """The discrete filter applied along u: Q_i = sum_j kernel[i - j + n_u - 1] p_j.  Default:
+    du * h((i - j) du), the band-limited windowed ramp; a caller's kernel (2 n_u - 1 values, e.g.
+    a learned filter) replaces it."""
+    if kernel is not None:
+        k = np.asarray(kernel, dtype=np.float64).reshape(-1)
+        assert k.size == 2 * n_u - 1
+        return k
+    return du * ramp_taps(n_u, du, window)
+
+
 def fbp(beam: int, views: np.ndarray, vol_shape, spacing, n_u: int, n_v: int, du: float,
         dv: float, sino: np.ndarray, window: str = "ram-lak", view_weights=None, isocenter=None,
-        voxels=None, pixel_weights=None):
+        voxels=None, pixel_weights=None, kernel=None):
     """Filtered backprojection of `sino` ((views, U) or (views, U, V)) onto the volume grid.
 
     `spacing` is one pitch or per-axis pitches in tensor order ((dz, dy, dx), 2D (dy, dx)); voxel
@@ -174,7 +187,7 @@ def fbp(beam: int, views: np.ndarray, vol_shape, spacing, n_u: int, n_v: int, du
     cu, cv = (n_u - 1) / 2.0, (V - 1) / 2.0
     uu = (np.arange(n_u) - cu) * du
     vv = (np.arange(V) - cv) * dv if not two_d else np.zeros(1)
-    taps = ramp_taps(n_u, du, window)
+    kern = filter_kernel(n_u, du, window, kernel)
     sp = np.broadcast_to(np.asarray(spacing, dtype=np.float64), (2 if two_d else 3,))
     sz, sy, sx = (1.0, sp[0], sp[1]) if two_d else (sp[0], sp[1], sp[2])
     # voxel centres
@@ -199,7 +212,7 @@ def fbp(beam: int, views: np.ndarray, vol_shape, spacing, n_u: int, n_v: int, du
         # filter every detector column along u (linear convolution, no wrap-around)
         Q = np.empty_like(q)
         for j in range(V):
-            Q[:, j] = du * np.convolve(q[:, j], taps, mode="full")[n_u - 1:2 * n_u - 1]
+            Q[:, j] = np.convolve(q[:, j], kern, mode="full")[n_u - 1:2 * n_u - 1]
         # gather
         if beam == 0:
             upix = ((P - ctr) @ u) / du + cu
@@ -238,7 +251,7 @@ def _bilinear(Q: np.ndarray, up: np.ndarray, vp: np.ndarray) -> np.ndarray:
 
 def fbp_transpose(beam: int, views: np.ndarray, vol_shape, spacing, n_u: int, n_v: int,
                   du: float, dv: float, vol: np.ndarray, window: str = "ram-lak",
-                  view_weights=None, isocenter=None, pixel_weights=None):
+                  view_weights=None, isocenter=None, pixel_weights=None, kernel=None):
     """The transpose of `fbp` as a linear map from sinograms to volumes: volume -> sinogram.
 
     The pages state that the analytical operator's backward pass scatters the same interpolation
@@ -261,7 +274,7 @@ def fbp_transpose(beam: int, views: np.ndarray, vol_shape, spacing, n_u: int, n_
     cu, cv = (n_u - 1) / 2.0, (V - 1) / 2.0
     uu = (np.arange(n_u) - cu) * du
     vv = (np.arange(V) - cv) * dv if not two_d else np.zeros(1)
-    taps = ramp_taps(n_u, du, window)
+    kern = filter_kernel(n_u, du, window, kernel)
     sp = np.broadcast_to(np.asarray(spacing, dtype=np.float64), (2 if two_d else 3,))
     sz, sy, sx = (1.0, sp[0], sp[1]) if two_d else (sp[0], sp[1], sp[2])
     zs = (np.arange(nz) + 0.5 - nz / 2.0) * sz if not two_d else np.zeros(1)
@@ -286,10 +299,11 @@ def fbp_transpose(beam: int, views: np.ndarray, vol_shape, spacing, n_u: int, n_
             g = (abs(D) / abs((iso - first) @ n)) / (Uw * Uw)
         # transpose of the gather: scatter w g f with the bilinear coefficients
         Q = _bilinear_transpose(w[k] * g * f, upix, vpix, n_u, V)
-        # transpose of the filter (symmetric), then of the cosine weights
+        # transpose of the filter (the kernel reversed; the windowed ramps are symmetric), then of
+        # the cosine weights
         q = np.empty_like(Q)
         for j in range(V):
-            q[:, j] = du * np.convolve(Q[:, j], taps, mode="full")[n_u - 1:2 * n_u - 1]
+            q[:, j] = np.convolve(Q[:, j], kern[::-1], mode="full")[n_u - 1:2 * n_u - 1]
         if beam != 0:
             pix = ctr[None, None, :] + uu[:, None, None] * u + vv[None, :, None] * v
             q *= abs((ctr - first) @ n) / np.linalg.norm(pix - first, axis=-1)
@@ -312,3 +326,59 @@ def _bilinear_transpose(vals: np.ndarray, up: np.ndarray, vp: np.ndarray, nU: in
             ok = (iu >= 0) & (iu < nU) & (iv >= 0) & (iv < nV)
             np.add.at(res, (iu[ok], iv[ok]), (wu * wv * vals)[ok])
     return res
+
+
+def fbp_gradients(beam: int, views: np.ndarray, vol_shape, spacing, n_u: int, n_v: int,
+                  du: float, dv: float, sino: np.ndarray, grad_vol: np.ndarray,
+                  window: str = "ram-lak", view_weights=None, isocenter=None,
+                  pixel_weights=None, kernel=None):
+    """Gradients of L(f) with f = fbp(sino, ...) with respect to the filter kernel and the view
+    weights, given dL/df = grad_vol (the pages: filter and explicit weight gradients propagate
+    through the analytical pipeline).  f is linear in both: with q_k the pre-weighted sinogram,
+    Q_k = H q_k the filtered one and G_k the view's gather without its weight,
+    dL/dw_k = <G_k^T grad, Q_k> and dL/dkernel[d + n_u - 1] = sum_k w_k sum_i (G_k^T grad)_i
+    q_k[i - d].  Returns (grad_kernel (2 n_u - 1,), grad_view_weights (n_views,))."""
+    assert beam in (0, 1, 2)
+    two_d = beam in (0, 1)
+    n_views = views.shape[0]
+    V = 1 if two_d else n_v
+    w = (np.full(n_views, math.pi / n_views) if view_weights is None
+         else np.asarray(view_weights, dtype=np.float64))
+    ones = np.ones(n_views)
+    # G_k^T grad for every view (unit view weights) through the transpose with an identity filter
+    # and no cosine or pixel weights
+    ident = np.zeros(2 * n_u - 1)
+    ident[n_u - 1] = 1.0
+    gq = np.asarray(fbp_transpose(beam, views, vol_shape, spacing, n_u, n_v, du, dv, grad_vol,
+                                  view_weights=ones, isocenter=isocenter, kernel=ident,
+                                  pixel_weights=None), dtype=np.float64)
+    gq = gq.reshape(n_views, n_u, V)
+    if beam != 0:  # undo the cosine weights the transpose applied
+        for k in range(n_views):
+            first, ctr, u, v, n = _frames(beam, views[k])
+            cu, cv = (n_u - 1) / 2.0, (V - 1) / 2.0
+            uu = (np.arange(n_u) - cu) * du
+            vv = (np.arange(V) - cv) * dv if not two_d else np.zeros(1)
+            pix = ctr[None, None, :] + uu[:, None, None] * u + vv[None, :, None] * v
+            gq[k] /= abs((ctr - first) @ n) / np.linalg.norm(pix - first, axis=-1)
+    kern = filter_kernel(n_u, du, window, kernel)
+    p = np.asarray(sino, dtype=np.float64).reshape(n_views, n_u, V)
+    g_kern = np.zeros(2 * n_u - 1)
+    g_w = np.zeros(n_views)
+    for k in range(n_views):
+        first, ctr, u, v, n = _frames(beam, views[k])
+        q = p[k].copy()
+        if beam != 0:
+            cu, cv = (n_u - 1) / 2.0, (V - 1) / 2.0
+            uu = (np.arange(n_u) - cu) * du
+            vv = (np.arange(V) - cv) * dv if not two_d else np.zeros(1)
+            pix = ctr[None, None, :] + uu[:, None, None] * u + vv[None, :, None] * v
+            q *= abs((ctr - first) @ n) / np.linalg.norm(pix - first, axis=-1)
+        if pixel_weights is not None:
+            q *= np.asarray(pixel_weights, dtype=np.float64)[k][:, None]
+        for j in range(V):
+            Qj = np.convolve(q[:, j], kern, mode="full")[n_u - 1:2 * n_u - 1]
+            g_w[k] += gq[k][:, j] @ Qj
+            # sum_i gq_i q_{i-d} for d = -(n_u-1) .. n_u-1
+            g_kern += w[k] * np.correlate(gq[k][:, j], q[:, j], mode="full")
+    return g_kern, g_w

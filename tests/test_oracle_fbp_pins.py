@@ -299,3 +299,62 @@ def test_parker_rejects_short_and_non_circular_scans():
     bad[7, 0:2] *= 1.01
     with pytest.raises(ValueError):
         F.parker_weights(1, bad, 161, 0.8)
+
+
+# ---- caller filter kernels and gradients ---------------------------------------------------------
+
+def test_default_kernel_is_the_scaled_window_taps():
+    w = W.small_config(2)
+    y = W.random_sinogram(w, 1).astype(np.float64)
+    a = F.fbp(w.beam, w.views, w.vol_shape, w.voxel_spacing, w.n_u, w.n_v, w.du, w.dv, y,
+              window="cosine")
+    k = w.du * F.ramp_taps(w.n_u, w.du, "cosine")
+    b = F.fbp(w.beam, w.views, w.vol_shape, w.voxel_spacing, w.n_u, w.n_v, w.du, w.dv, y,
+              kernel=k)
+    np.testing.assert_allclose(a, b, rtol=0, atol=1e-12 * np.abs(a).max())
+
+
+@pytest.mark.parametrize("n", [1, 2, 3])
+def test_transpose_with_an_asymmetric_kernel_satisfies_the_adjoint_identity(n):
+    w = W.small_config(n)
+    rng = np.random.default_rng(70 + n)
+    y = rng.standard_normal(w.sino_shape)
+    vol_shape = (w.vol_shape[1], w.vol_shape[2]) if w.beam in (0, 1) else w.vol_shape
+    x = rng.standard_normal(vol_shape)
+    kern = rng.standard_normal(2 * w.n_u - 1)
+    Fy = F.fbp(w.beam, w.views, w.vol_shape, w.voxel_spacing, w.n_u, w.n_v, w.du, w.dv, y,
+               kernel=kern)
+    Ftx = F.fbp_transpose(w.beam, w.views, w.vol_shape, w.voxel_spacing, w.n_u, w.n_v, w.du,
+                          w.dv, x, kernel=kern)
+    lhs, rhs = float(np.sum(Fy * x)), float(np.sum(y * Ftx))
+    assert abs(lhs - rhs) <= 1e-11 * np.linalg.norm(Fy) * np.linalg.norm(x)
+
+
+@pytest.mark.parametrize("n", [1, 2, 3])
+def test_gradients_equal_linear_probes(n):
+    """f is linear in the kernel and in the view weights, so dL/dkernel[t] = <grad, f(kernel=e_t)>
+    and dL/dw_k = <grad, f(view_weights=e_k)> exactly; checked on sampled t and k with pixel
+    weights and an isocentre in play."""
+    w = W.small_config(n)
+    rng = np.random.default_rng(80 + n)
+    y = W.random_sinogram(w, 2).astype(np.float64)
+    vol_shape = (w.vol_shape[1], w.vol_shape[2]) if w.beam in (0, 1) else w.vol_shape
+    grad = rng.standard_normal(vol_shape)
+    nviews = w.views.shape[0]
+    wts = rng.uniform(0.01, 0.05, nviews)
+    pw = rng.uniform(0.5, 1.5, (nviews, w.n_u))
+    iso = (0.4, -0.3, 0.2)[: 2 if w.beam in (0, 1) else 3]
+    kern = F.filter_kernel(w.n_u, w.du, "hamming")
+    kw = dict(view_weights=wts, isocenter=iso, pixel_weights=pw)
+    gk, gw = F.fbp_gradients(w.beam, w.views, w.vol_shape, w.voxel_spacing, w.n_u, w.n_v, w.du,
+                             w.dv, y, grad, kernel=kern, **kw)
+    args = (w.beam, w.views, w.vol_shape, w.voxel_spacing, w.n_u, w.n_v, w.du, w.dv, y)
+    for t in (0, w.n_u - 1, w.n_u + 2, 2 * w.n_u - 2):
+        e = np.zeros_like(kern); e[t] = 1.0
+        want = float(np.sum(F.fbp(*args, kernel=e, **kw) * grad))
+        assert abs(gk[t] - want) <= 1e-10 * (abs(want) + np.abs(gk).max())
+    for k in (0, nviews // 2, nviews - 1):
+        e = np.zeros(nviews); e[k] = 1.0
+        want = float(np.sum(F.fbp(*args, kernel=kern, view_weights=e, isocenter=iso,
+                                  pixel_weights=pw) * grad))
+        assert abs(gw[k] - want) <= 1e-10 * (abs(want) + np.abs(gw).max())
