@@ -5,6 +5,7 @@ The compute path is the C-ABI library ``libctproj.so`` (CUDA, sm_103a); this pac
 thin ctypes binding plus the seeded input generators in ``workloads``.
 """
 from ._binding import (CT_CONE, CT_FAN2D, CT_PARALLEL2D, CT_PARALLEL3D, FBP_WINDOWS, CtError,
+                       FbpOptions, ct_fbp_gradients, ct_fbp_gradients_workspace_bytes, fbp_options,
                        Geometry, GeometryInfo, ct_backproject, ct_backproject_batch,
                        ct_backproject_static, ct_batch_workspace_bytes, ct_cgls_iterate,
                        ct_cgls_workspace_bytes, ct_fbp, ct_fbp_parker_weights, ct_fbp_transpose,
@@ -14,6 +15,7 @@ from ._binding import (CT_CONE, CT_FAN2D, CT_PARALLEL2D, CT_PARALLEL3D, FBP_WIND
                        ct_sirt_workspace_bytes, ct_status_string, load_library)
 
 __all__ = ["CT_CONE", "CT_FAN2D", "CT_PARALLEL2D", "CT_PARALLEL3D", "FBP_WINDOWS", "CtError",
+           "FbpOptions", "ct_fbp_gradients", "ct_fbp_gradients_workspace_bytes", "fbp_options",
            "Geometry", "GeometryInfo", "ct_backproject", "ct_backproject_batch",
            "ct_backproject_static", "ct_batch_workspace_bytes", "ct_cgls_iterate",
            "ct_cgls_workspace_bytes", "ct_fbp", "ct_fbp_parker_weights", "ct_fbp_transpose",

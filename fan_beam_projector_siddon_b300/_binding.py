@@ -32,6 +32,13 @@ class CtError(RuntimeError):
         super().__init__(f"{call} failed: {name}")
 
 
+class FbpOptions(ctypes.Structure):
+    """``ct_fbp_options``: window code, device pointers (or None) and a host isocentre."""
+    _fields_ = [("window", ctypes.c_int32), ("d_view_weights", ctypes.c_void_p),
+                ("d_pixel_weights", ctypes.c_void_p), ("d_kernel", ctypes.c_void_p),
+                ("isocenter", ctypes.POINTER(ctypes.c_double))]
+
+
 class GeometryInfo(ctypes.Structure):
     _fields_ = [("beam", ctypes.c_int32), ("n_views", ctypes.c_int32),
                 ("nz", ctypes.c_int32), ("ny", ctypes.c_int32), ("nx", ctypes.c_int32),
@@ -92,11 +99,16 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.ct_backproject_static.restype = i32
     L.ct_fbp_workspace_bytes.argtypes = [vp]
     L.ct_fbp_workspace_bytes.restype = sz
-    L.ct_fbp.argtypes = [vp, vp, vp, vp, vp, ctypes.POINTER(f64), i32, vp, sz, vp]
+    opt = ctypes.POINTER(FbpOptions)
+    L.ct_fbp.argtypes = [vp, vp, vp, opt, vp, sz, vp]
     L.ct_fbp.restype = i32
     L.ct_fbp_transpose_workspace_bytes.argtypes = [vp]
     L.ct_fbp_transpose_workspace_bytes.restype = sz
-    L.ct_fbp_transpose.argtypes = [vp, vp, vp, vp, vp, ctypes.POINTER(f64), i32, vp, sz, vp]
+    L.ct_fbp_transpose.argtypes = [vp, vp, vp, opt, vp, sz, vp]
+    L.ct_fbp_gradients_workspace_bytes.argtypes = [vp]
+    L.ct_fbp_gradients_workspace_bytes.restype = sz
+    L.ct_fbp_gradients.argtypes = [vp, vp, vp, opt, vp, vp, vp, sz, vp]
+    L.ct_fbp_gradients.restype = i32
     L.ct_fbp_parker_weights.argtypes = [vp, ctypes.POINTER(f64), ctypes.POINTER(ctypes.c_float)]
     L.ct_fbp_parker_weights.restype = i32
     L.ct_fbp_transpose.restype = i32
@@ -252,29 +264,50 @@ def _dptr(arr):
     return None if arr is None else arr.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
 
 
-def ct_fbp(handle: int, d_sino: int, d_volume: int, d_view_weights: int | None,
-           d_pixel_weights: int | None, isocenter, window, d_workspace: int,
-           workspace_bytes: int, stream: int | None) -> None:
-    """Filtered backprojection; ``window`` is a name of ``FBP_WINDOWS`` or its code and
-    ``isocenter`` a host 3-vector or None."""
+def fbp_options(window="ram-lak", d_view_weights: int | None = None,
+                d_pixel_weights: int | None = None, d_kernel: int | None = None,
+                isocenter=None):
+    """(FbpOptions, keep-alive) for the FBP calls; keep the second item alive during the call."""
     code, iso = _fbp_args(isocenter, window)
-    _check(load_library().ct_fbp(handle, d_sino, d_volume, d_view_weights, d_pixel_weights,
-                                 _dptr(iso), code, d_workspace, workspace_bytes, stream),
-           "ct_fbp")
+    o = FbpOptions(code, d_view_weights, d_pixel_weights, d_kernel, _dptr(iso))
+    return o, iso
+
+
+def ct_fbp(handle: int, d_sino: int, d_volume: int, options: "FbpOptions | None",
+           d_workspace: int, workspace_bytes: int, stream: int | None) -> None:
+    """Filtered backprojection with ``options`` (``fbp_options(...)[0]``, or None for the
+    defaults)."""
+    _check(load_library().ct_fbp(handle, d_sino, d_volume,
+                                 None if options is None else ctypes.byref(options),
+                                 d_workspace, workspace_bytes, stream), "ct_fbp")
 
 
 def ct_fbp_transpose_workspace_bytes(handle: int) -> int:
     return int(load_library().ct_fbp_transpose_workspace_bytes(handle))
 
 
-def ct_fbp_transpose(handle: int, d_volume: int, d_sino: int, d_view_weights: int | None,
-                     d_pixel_weights: int | None, isocenter, window, d_workspace: int,
-                     workspace_bytes: int, stream: int | None) -> None:
-    """Transpose of ``ct_fbp`` (volume -> sinogram), same arguments."""
-    code, iso = _fbp_args(isocenter, window)
-    _check(load_library().ct_fbp_transpose(handle, d_volume, d_sino, d_view_weights,
-                                           d_pixel_weights, _dptr(iso), code, d_workspace,
-                                           workspace_bytes, stream), "ct_fbp_transpose")
+def ct_fbp_transpose(handle: int, d_volume: int, d_sino: int, options: "FbpOptions | None",
+                     d_workspace: int, workspace_bytes: int, stream: int | None) -> None:
+    """Transpose of ``ct_fbp`` (volume -> sinogram), same options."""
+    _check(load_library().ct_fbp_transpose(handle, d_volume, d_sino,
+                                           None if options is None else ctypes.byref(options),
+                                           d_workspace, workspace_bytes, stream),
+           "ct_fbp_transpose")
+
+
+def ct_fbp_gradients_workspace_bytes(handle: int) -> int:
+    return int(load_library().ct_fbp_gradients_workspace_bytes(handle))
+
+
+def ct_fbp_gradients(handle: int, d_sino: int, d_grad_volume: int,
+                     options: "FbpOptions | None", d_grad_kernel: int | None,
+                     d_grad_view_weights: int | None, d_workspace: int, workspace_bytes: int,
+                     stream: int | None) -> None:
+    """dL/dkernel and dL/dview_weights of the FBP of ``d_sino`` given dL/df = ``d_grad_volume``."""
+    _check(load_library().ct_fbp_gradients(handle, d_sino, d_grad_volume,
+                                           None if options is None else ctypes.byref(options),
+                                           d_grad_kernel, d_grad_view_weights, d_workspace,
+                                           workspace_bytes, stream), "ct_fbp_gradients")
 
 
 def ct_fbp_parker_weights(handle: int, n_views: int, n_u: int, isocenter=None) -> np.ndarray:
@@ -443,8 +476,21 @@ class Geometry:
                         initialised, self._stream(stream))
         return x
 
+    def _fbp_inputs(self, device, view_weights, pixel_weights, kernel):
+        """Device float32 tensors (or None) for the optional FBP inputs, checked for size."""
+        import torch
+        out = []
+        for t, n in ((view_weights, self.info.n_views),
+                     (pixel_weights, self.info.n_views * self.info.n_u),
+                     (kernel, 2 * self.info.n_u - 1)):
+            if t is not None:
+                t = torch.as_tensor(t, dtype=torch.float32, device=device).contiguous()
+                assert t.numel() == n
+            out.append(t)
+        return out
+
     def _fbp_call(self, fn, need, src, src_shape, dst_shape, out, window, view_weights,
-                  isocenter, workspace, stream, pixel_weights=None):
+                  isocenter, workspace, stream, pixel_weights=None, kernel=None):
         import torch
         assert src.is_cuda and src.dtype == torch.float32 and src.is_contiguous()
         nd = len(src_shape)
@@ -455,39 +501,60 @@ class Geometry:
         if workspace is None:
             workspace = torch.empty(need, dtype=torch.uint8, device=src.device)
         ws, wsb = workspace.data_ptr(), workspace.numel() * workspace.element_size()
-        wptr = None
-        if view_weights is not None:
-            view_weights = torch.as_tensor(view_weights, dtype=torch.float32,
-                                           device=src.device).contiguous()
-            assert view_weights.numel() == self.info.n_views
-            wptr = view_weights.data_ptr()
-        pptr = None
-        if pixel_weights is not None:
-            pixel_weights = torch.as_tensor(pixel_weights, dtype=torch.float32,
-                                            device=src.device).contiguous()
-            assert pixel_weights.numel() == self.info.n_views * self.info.n_u
-            pptr = pixel_weights.data_ptr()
+        vw, pw, kn = self._fbp_inputs(src.device, view_weights, pixel_weights, kernel)
+        opts, keep = fbp_options(window, None if vw is None else vw.data_ptr(),
+                                 None if pw is None else pw.data_ptr(),
+                                 None if kn is None else kn.data_ptr(), isocenter)
         s2 = src.reshape((-1,) + tuple(src_shape))
         o2 = out.view((-1,) + tuple(dst_shape))
         for b in range(s2.shape[0]):
-            fn(self.handle, s2[b].data_ptr(), o2[b].data_ptr(), wptr, pptr, isocenter, window,
-               ws, wsb, self._stream(stream))
+            fn(self.handle, s2[b].data_ptr(), o2[b].data_ptr(), opts, ws, wsb,
+               self._stream(stream))
+        del keep
         return out
 
     def fbp(self, sino, out=None, window="ram-lak", view_weights=None, isocenter=None,
-            workspace=None, stream=None, pixel_weights=None):
+            workspace=None, stream=None, pixel_weights=None, kernel=None):
         """Filtered backprojection (FBP / FDK) of a sinogram; leading dimensions are kept and
-        reconstructed one after another with the same workspace."""
+        reconstructed one after another with the same workspace.  ``kernel`` (2 n_u - 1 values)
+        replaces the windowed ramp."""
         return self._fbp_call(ct_fbp, ct_fbp_workspace_bytes(self.handle), sino,
                               self.sino_shape, self.volume_shape, out, window, view_weights,
-                              isocenter, workspace, stream, pixel_weights)
+                              isocenter, workspace, stream, pixel_weights, kernel)
 
     def fbp_transpose(self, volume, out=None, window="ram-lak", view_weights=None,
-                      isocenter=None, workspace=None, stream=None, pixel_weights=None):
+                      isocenter=None, workspace=None, stream=None, pixel_weights=None,
+                      kernel=None):
         """Transpose of ``fbp`` (volume -> sinogram); leading dimensions are kept."""
         return self._fbp_call(ct_fbp_transpose, ct_fbp_transpose_workspace_bytes(self.handle),
                               volume, self.volume_shape, self.sino_shape, out, window,
-                              view_weights, isocenter, workspace, stream, pixel_weights)
+                              view_weights, isocenter, workspace, stream, pixel_weights, kernel)
+
+    def fbp_gradients(self, sino, grad_volume, window="ram-lak", view_weights=None,
+                      isocenter=None, pixel_weights=None, kernel=None, want_kernel=True,
+                      want_view_weights=True, workspace=None, stream=None):
+        """(dL/dkernel, dL/dview_weights) of ``fbp(sino, ...)`` given dL/df = ``grad_volume``;
+        an entry is None when not wanted."""
+        import torch
+        for t, shape in ((sino, self.sino_shape), (grad_volume, self.volume_shape)):
+            assert t.is_cuda and t.dtype == torch.float32 and t.is_contiguous()
+            assert tuple(t.shape) == tuple(shape)
+        dev = sino.device
+        if workspace is None:
+            workspace = torch.empty(ct_fbp_gradients_workspace_bytes(self.handle),
+                                    dtype=torch.uint8, device=dev)
+        vw, pw, kn = self._fbp_inputs(dev, view_weights, pixel_weights, kernel)
+        opts, keep = fbp_options(window, None if vw is None else vw.data_ptr(),
+                                 None if pw is None else pw.data_ptr(),
+                                 None if kn is None else kn.data_ptr(), isocenter)
+        gk = torch.empty(2 * self.info.n_u - 1, device=dev) if want_kernel else None
+        gw = torch.empty(self.info.n_views, device=dev) if want_view_weights else None
+        ct_fbp_gradients(self.handle, sino.data_ptr(), grad_volume.data_ptr(), opts,
+                         None if gk is None else gk.data_ptr(),
+                         None if gw is None else gw.data_ptr(), workspace.data_ptr(),
+                         workspace.numel(), self._stream(stream))
+        del keep
+        return gk, gw
 
     def parker_weights(self, isocenter=None) -> np.ndarray:
         """Parker short-scan weights (n_views, n_u) for ``fbp(..., pixel_weights=)``."""

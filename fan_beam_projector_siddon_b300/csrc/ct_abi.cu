@@ -761,16 +761,18 @@ extern "C" ct_status ct_backproject_static(const ct_geometry* g, const float* d_
 
 namespace {
 
+enum FbpMode { kFbpForward = 0, kFbpTranspose = 1, kFbpGradients = 2 };
+
 struct FbpLayout {
     int32_t rows, cols;  // padded filtered sinogram of one view
-    int32_t bu, bv;      // transpose: 2 x 2 blocks (2D: pairs) per view and parity copy
-    size_t views, cosines, taps, filtered, total;
+    int32_t bu, bv;      // 2 x 2 blocks (2D: pairs) per view and parity copy
+    size_t views, cosines, taps, filtered, copies, acc, total;
 };
 
-// Scratch of ct_fbp (transpose = 0: the padded filtered sinogram) or of ct_fbp_transpose
-// (transpose = 1: the parity copies of the padded detector, 4 copies of 2 x 2 blocks; 2D 2 copies
-// of pairs).
-FbpLayout fbp_layout(const ct_geometry* g, bool transpose) {
+// Scratch: per-view constants and taps, then (forward) the padded filtered sinogram, (transpose)
+// the parity copies of the padded detector (4 copies of 2 x 2 blocks; 2D 2 copies of pairs), or
+// (gradients) both plus 2 n_u - 1 doubles.
+FbpLayout fbp_layout(const ct_geometry* g, FbpMode mode) {
     FbpLayout L;
     const size_t nv = (size_t)g->info.n_views;
     const bool two_d = is_2d(g->info.beam);
@@ -781,12 +783,24 @@ FbpLayout fbp_layout(const ct_geometry* g, bool transpose) {
     L.views = 0;
     L.cosines = align_up(sizeof(ct::FbpView) * nv);
     L.taps = L.cosines + align_up(sizeof(ct::FbpCosine) * nv);
-    L.filtered = L.taps + align_up(sizeof(float) * (size_t)(2 * g->info.n_u - 1));
-    const size_t slot = transpose
-        ? (two_d ? sizeof(float) * 4 * nv * (size_t)L.bu
-                 : sizeof(float) * 16 * nv * (size_t)L.bu * (size_t)L.bv)
-        : sizeof(float) * nv * (size_t)L.rows * (size_t)L.cols;
-    L.total = L.filtered + align_up(slot);
+    size_t off = L.taps + align_up(sizeof(float) * (size_t)(2 * g->info.n_u - 1));
+    const size_t padded = sizeof(float) * nv * (size_t)L.rows * (size_t)L.cols;
+    const size_t copies = two_d ? sizeof(float) * 4 * nv * (size_t)L.bu
+                                : sizeof(float) * 16 * nv * (size_t)L.bu * (size_t)L.bv;
+    L.filtered = L.copies = L.acc = off;
+    if (mode != kFbpTranspose) {
+        L.filtered = off;
+        off += align_up(padded);
+    }
+    if (mode != kFbpForward) {
+        L.copies = off;
+        off += align_up(copies);
+    }
+    if (mode == kFbpGradients) {
+        L.acc = off;
+        off += align_up(sizeof(double) * (size_t)(2 * g->info.n_u - 1));
+    }
+    L.total = off;
     return L;
 }
 
@@ -795,11 +809,15 @@ constexpr int32_t kFbpMaxU = 16384;
 }  // namespace
 
 extern "C" size_t ct_fbp_workspace_bytes(const ct_geometry* g) {
-    return g == nullptr ? 0 : fbp_layout(g, false).total;
+    return g == nullptr ? 0 : fbp_layout(g, kFbpForward).total;
 }
 
 extern "C" size_t ct_fbp_transpose_workspace_bytes(const ct_geometry* g) {
-    return g == nullptr ? 0 : fbp_layout(g, true).total;
+    return g == nullptr ? 0 : fbp_layout(g, kFbpTranspose).total;
+}
+
+extern "C" size_t ct_fbp_gradients_workspace_bytes(const ct_geometry* g) {
+    return g == nullptr ? 0 : fbp_layout(g, kFbpGradients).total;
 }
 
 namespace {
@@ -861,15 +879,32 @@ void estimate_isocenter(const ct_geometry* g, double* iso) {
     if (dim == 2) iso[2] = 0.0;
 }
 
-// Argument checks shared by ct_fbp and ct_fbp_transpose; fills the kernel parameters.
+// Device buffer of `bytes` given by the caller: device memory of the handle's device, not
+// overlapping `out` or the workspace.
+ct_status check_input(const ct_geometry* g, const void* ptr, size_t bytes, const void* out,
+                      size_t out_bytes, const void* ws, size_t ws_bytes) {
+    ct_status st = check_device_ptr(ptr, g->device);
+    if (st != CT_OK) return st;
+    if (overlap(ptr, bytes, out, out_bytes) || overlap(ptr, bytes, ws, ws_bytes))
+        return CT_ERR_ALIASING;
+    return CT_OK;
+}
+
+// Argument checks shared by the FBP entry points; fills the kernel parameters.
 ct_status fbp_setup(const ct_geometry* g, const void* in, size_t in_bytes, const void* out,
-                    size_t out_bytes, const float* d_view_weights, const float* d_pixel_weights,
-                    const double* isocenter, ct_fbp_window window, const void* d_workspace,
-                    size_t workspace_bytes, bool transpose, ct::FbpParams* P, FbpLayout* L) {
+                    size_t out_bytes, const ct_fbp_options* opt, const void* d_workspace,
+                    size_t workspace_bytes, FbpMode mode, ct::FbpParams* P, FbpLayout* L) {
     if (g == nullptr) return CT_ERR_INVALID_ARGUMENT;
+    ct_fbp_options o;
+    if (opt != nullptr) {
+        o = *opt;
+    } else {
+        std::memset(&o, 0, sizeof(o));
+        o.window = CT_WINDOW_RAM_LAK;
+    }
     const int b = g->info.beam;
     if (b == CT_PARALLEL3D || g->d_offsets != nullptr) return CT_ERR_INVALID_ARGUMENT;
-    if ((int)window < CT_WINDOW_RAM_LAK || (int)window > CT_WINDOW_HANN)
+    if ((int)o.window < CT_WINDOW_RAM_LAK || (int)o.window > CT_WINDOW_HANN)
         return CT_ERR_INVALID_ARGUMENT;
     if (g->info.n_u > kFbpMaxU) return CT_ERR_INVALID_ARGUMENT;
     // gather grid limits: 3D (ceil(nz/32), ceil(nx/8), ny), 2D (ceil(nx/32), ceil(ny/8))
@@ -877,40 +912,41 @@ ct_status fbp_setup(const ct_geometry* g, const void* in, size_t in_bytes, const
                  : (g->info.nx + 7) / 8 > 65535 || g->info.ny > 65535)
         return CT_ERR_INVALID_ARGUMENT;
     double iso[3] = {0.0, 0.0, 0.0};
-    if (isocenter != nullptr) {
+    if (o.isocenter != nullptr) {
         for (int a = 0; a < (is_2d(b) ? 2 : 3); ++a) {
-            if (!std::isfinite(isocenter[a])) return CT_ERR_INVALID_ARGUMENT;
-            iso[a] = isocenter[a];
+            if (!std::isfinite(o.isocenter[a])) return CT_ERR_INVALID_ARGUMENT;
+            iso[a] = o.isocenter[a];
         }
     } else if (!is_parallel(b)) {
         estimate_isocenter(g, iso);
     }
-    *L = fbp_layout(g, transpose);
+    *L = fbp_layout(g, mode);
     ct_status st = check_call(g, in, in_bytes, out, out_bytes, d_workspace, workspace_bytes,
                               L->total);
     if (st != CT_OK) return st;
     const size_t wbytes = sizeof(float) * (size_t)g->info.n_views;
-    if (d_view_weights != nullptr) {
-        if ((st = check_device_ptr(d_view_weights, g->device)) != CT_OK) return st;
-        if (overlap(d_view_weights, wbytes, out, out_bytes) ||
-            overlap(d_view_weights, wbytes, d_workspace, L->total))
-            return CT_ERR_ALIASING;
-    }
     const size_t pbytes = wbytes * (size_t)g->info.n_u;
-    if (d_pixel_weights != nullptr) {
-        if ((st = check_device_ptr(d_pixel_weights, g->device)) != CT_OK) return st;
-        if (overlap(d_pixel_weights, pbytes, out, out_bytes) ||
-            overlap(d_pixel_weights, pbytes, d_workspace, L->total))
-            return CT_ERR_ALIASING;
-    }
+    const size_t kbytes = sizeof(float) * (size_t)(2 * g->info.n_u - 1);
+    if (o.d_view_weights != nullptr &&
+        (st = check_input(g, o.d_view_weights, wbytes, out, out_bytes, d_workspace, L->total)) !=
+            CT_OK)
+        return st;
+    if (o.d_pixel_weights != nullptr &&
+        (st = check_input(g, o.d_pixel_weights, pbytes, out, out_bytes, d_workspace,
+                          L->total)) != CT_OK)
+        return st;
+    if (o.d_kernel != nullptr &&
+        (st = check_input(g, o.d_kernel, kbytes, out, out_bytes, d_workspace, L->total)) != CT_OK)
+        return st;
     ct::FbpParams& p = *P;
+    std::memset(&p, 0, sizeof(p));
     p.n_views = g->info.n_views;
     p.n_u = g->info.n_u;
     p.n_v = g->info.n_v;
     p.nx = g->info.nx; p.ny = g->info.ny; p.nz = g->info.nz;
     p.two_d = is_2d(b) ? 1 : 0;
     p.parallel = is_parallel(b) ? 1 : 0;
-    p.window = (int32_t)window;
+    p.window = (int32_t)o.window;
     p.rows = L->rows;
     p.cols = L->cols;
     p.bu = L->bu;
@@ -921,25 +957,28 @@ ct_status fbp_setup(const ct_geometry* g, const void* in, size_t in_bytes, const
     p.sx = g->grid.sp[0];
     p.sy = g->grid.sp[1];
     p.sz = g->grid.sp[2];
-    p.pixel_weights = d_pixel_weights;
+    p.pixel_weights = o.d_pixel_weights;
+    p.kernel = o.d_kernel;
     return CT_OK;
+}
+
+const float* view_weights_of(const ct_fbp_options* opt) {
+    return opt == nullptr ? nullptr : opt->d_view_weights;
 }
 
 }  // namespace
 
 extern "C" ct_status ct_fbp(const ct_geometry* g, const float* d_sino, float* d_volume,
-                            const float* d_view_weights, const float* d_pixel_weights,
-                            const double* isocenter, ct_fbp_window window, void* d_workspace,
+                            const ct_fbp_options* options, void* d_workspace,
                             size_t workspace_bytes, cudaStream_t stream) {
     ct::FbpParams P;
     FbpLayout L;
     if (g == nullptr) return CT_ERR_INVALID_ARGUMENT;
-    const ct_status st = fbp_setup(g, d_sino, sino_bytes(g), d_volume, volume_bytes(g),
-                                   d_view_weights, d_pixel_weights, isocenter, window,
-                                   d_workspace, workspace_bytes, false, &P, &L);
+    const ct_status st = fbp_setup(g, d_sino, sino_bytes(g), d_volume, volume_bytes(g), options,
+                                   d_workspace, workspace_bytes, kFbpForward, &P, &L);
     if (st != CT_OK) return st;
     char* ws = static_cast<char*>(d_workspace);
-    return from_cuda(ct::launch_fbp(P, g->d_raw, d_view_weights,
+    return from_cuda(ct::launch_fbp(P, g->d_raw, view_weights_of(options),
                                     reinterpret_cast<ct::FbpView*>(ws + L.views),
                                     reinterpret_cast<ct::FbpCosine*>(ws + L.cosines),
                                     reinterpret_cast<float*>(ws + L.taps), d_sino,
@@ -947,22 +986,57 @@ extern "C" ct_status ct_fbp(const ct_geometry* g, const float* d_sino, float* d_
 }
 
 extern "C" ct_status ct_fbp_transpose(const ct_geometry* g, const float* d_volume, float* d_sino,
-                                      const float* d_view_weights, const float* d_pixel_weights,
-                                      const double* isocenter, ct_fbp_window window,
+                                      const ct_fbp_options* options, void* d_workspace,
+                                      size_t workspace_bytes, cudaStream_t stream) {
+    ct::FbpParams P;
+    FbpLayout L;
+    if (g == nullptr) return CT_ERR_INVALID_ARGUMENT;
+    const ct_status st = fbp_setup(g, d_volume, volume_bytes(g), d_sino, sino_bytes(g), options,
+                                   d_workspace, workspace_bytes, kFbpTranspose, &P, &L);
+    if (st != CT_OK) return st;
+    char* ws = static_cast<char*>(d_workspace);
+    return from_cuda(ct::launch_fbp_transpose(
+        P, g->d_raw, view_weights_of(options), reinterpret_cast<ct::FbpView*>(ws + L.views),
+        reinterpret_cast<ct::FbpCosine*>(ws + L.cosines), reinterpret_cast<float*>(ws + L.taps),
+        d_volume, reinterpret_cast<float*>(ws + L.copies), d_sino, stream));
+}
+
+extern "C" ct_status ct_fbp_gradients(const ct_geometry* g, const float* d_sino,
+                                      const float* d_grad_volume, const ct_fbp_options* options,
+                                      float* d_grad_kernel, float* d_grad_view_weights,
                                       void* d_workspace, size_t workspace_bytes,
                                       cudaStream_t stream) {
     ct::FbpParams P;
     FbpLayout L;
-    if (g == nullptr) return CT_ERR_INVALID_ARGUMENT;
-    const ct_status st = fbp_setup(g, d_volume, volume_bytes(g), d_sino, sino_bytes(g),
-                                   d_view_weights, d_pixel_weights, isocenter, window,
-                                   d_workspace, workspace_bytes, true, &P, &L);
+    if (g == nullptr || (d_grad_kernel == nullptr && d_grad_view_weights == nullptr))
+        return CT_ERR_INVALID_ARGUMENT;
+    // the outputs: the kernel gradient and the view-weight gradient, checked like outputs
+    float* first_out = d_grad_kernel ? d_grad_kernel : d_grad_view_weights;
+    const size_t kbytes = sizeof(float) * (size_t)(2 * g->info.n_u - 1);
+    const size_t wbytes = sizeof(float) * (size_t)g->info.n_views;
+    const size_t first_bytes = d_grad_kernel ? kbytes : wbytes;
+    ct_status st = fbp_setup(g, d_sino, sino_bytes(g), first_out, first_bytes, options,
+                             d_workspace, workspace_bytes, kFbpGradients, &P, &L);
     if (st != CT_OK) return st;
+    if ((st = check_device_ptr(d_grad_volume, g->device)) != CT_OK) return st;
+    if (overlap(d_grad_volume, volume_bytes(g), d_workspace, L.total) ||
+        overlap(d_grad_volume, volume_bytes(g), first_out, first_bytes))
+        return CT_ERR_ALIASING;
+    if (d_grad_kernel && d_grad_view_weights) {
+        if ((st = check_device_ptr(d_grad_view_weights, g->device)) != CT_OK) return st;
+        if (overlap(d_grad_view_weights, wbytes, d_grad_kernel, kbytes) ||
+            overlap(d_grad_view_weights, wbytes, d_workspace, L.total) ||
+            overlap(d_grad_view_weights, wbytes, d_sino, sino_bytes(g)) ||
+            overlap(d_grad_view_weights, wbytes, d_grad_volume, volume_bytes(g)))
+            return CT_ERR_ALIASING;
+    }
     char* ws = static_cast<char*>(d_workspace);
-    return from_cuda(ct::launch_fbp_transpose(
-        P, g->d_raw, d_view_weights, reinterpret_cast<ct::FbpView*>(ws + L.views),
+    return from_cuda(ct::launch_fbp_gradients(
+        P, g->d_raw, view_weights_of(options), reinterpret_cast<ct::FbpView*>(ws + L.views),
         reinterpret_cast<ct::FbpCosine*>(ws + L.cosines), reinterpret_cast<float*>(ws + L.taps),
-        d_volume, reinterpret_cast<float*>(ws + L.filtered), d_sino, stream));
+        d_sino, d_grad_volume, reinterpret_cast<float*>(ws + L.copies),
+        reinterpret_cast<float*>(ws + L.filtered), reinterpret_cast<double*>(ws + L.acc),
+        d_grad_kernel, d_grad_view_weights, stream));
 }
 
 // ---------------------------------------------------------------------------------------------

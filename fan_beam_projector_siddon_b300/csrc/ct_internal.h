@@ -122,6 +122,9 @@ struct FbpParams {
     double iso[3];
     float sx, sy, sz;  // voxel pitches along x, y, z
     const float* pixel_weights;  // optional (n_views, n_u) weights before filtering, or nullptr
+    const float* kernel;  // optional caller filter (2 n_u - 1), replacing the window, or nullptr
+    int32_t reverse_kernel;  // 1: the taps are stored reversed (the transpose's filter)
+    int32_t unit_weights;    // 1: every view weight is 1 (gradient scatter)
 };
 // Per-view constants of the gather (64 bytes, read as four float4).
 struct FbpView {
@@ -157,6 +160,14 @@ cudaError_t launch_fbp(const FbpParams& p, const double* raw_views, const float*
 // the padded detector (layout in fbp_kernels.cu, fbp_copies_floats floats); it is cleared on the
 // stream first.
 size_t fbp_copies_floats(const FbpParams& p);
+// Gradients of a loss L(f), f = the FBP of `sino`, given dL/df = grad_vol: dL/dkernel (2 n_u - 1
+// floats, or nullptr) and dL/dview_weights (n_views floats, or nullptr).  Scratch: the transpose's
+// (copies) plus the padded filtered sinogram (`filtered`) and 2 n_u - 1 doubles (`acc`).
+cudaError_t launch_fbp_gradients(const FbpParams& p, const double* raw_views,
+                                 const float* view_weights, FbpView* views, FbpCosine* cosines,
+                                 float* taps, const float* sino, const float* grad_vol,
+                                 float* copies, float* filtered, double* acc, float* grad_kernel,
+                                 float* grad_view_weights, cudaStream_t stream);
 cudaError_t launch_fbp_transpose(const FbpParams& p, const double* raw_views,
                                  const float* view_weights, FbpView* views, FbpCosine* cosines,
                                  float* taps, const float* vol, float* scattered, float* sino,

@@ -153,8 +153,11 @@ __global__ void fbp_prepare_kernel(FbpParams p, const double* __restrict__ raw,
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     const int n_taps = 2 * p.n_u - 1;
     if (i < n_taps) {
-        const int n = i - (p.n_u - 1);
-        taps[i] = (float)(ramp_tap(p.window, n * p.du, p.du) * p.du);  // tau * h(n tau)
+        // the transpose's filter is the forward's with the taps reversed
+        const int src = p.reverse_kernel ? n_taps - 1 - i : i;
+        const int n = src - (p.n_u - 1);
+        taps[i] = p.kernel ? p.kernel[src]
+                           : (float)(ramp_tap(p.window, n * p.du, p.du) * p.du);  // tau h(n tau)
     }
     if (i >= p.n_views) return;
     const double* r = raw + (int64_t)i * (p.two_d ? 6 : 12);
@@ -173,7 +176,9 @@ __global__ void fbp_prepare_kernel(FbpParams p, const double* __restrict__ raw,
         n[1] = u[2] * v[0] - u[0] * v[2];
         n[2] = u[0] * v[1] - u[1] * v[0];
     }
-    const double w = user_weights ? (double)user_weights[i] : 3.14159265358979323846 / p.n_views;
+    const double w = p.unit_weights ? 1.0
+                     : user_weights ? (double)user_weights[i]
+                                    : 3.14159265358979323846 / p.n_views;
     const double cu = 0.5 * (p.n_u - 1), cv = p.two_d ? 0.0 : 0.5 * (p.n_v - 1);
     const double dvv = p.two_d ? 0.0 : p.dv;
     FbpView V;
@@ -819,15 +824,99 @@ uint64_t fbp_bounds_violations(bool reset) {
 #endif
 }
 
+namespace {
+
+// dL/dw_k = sum over the detector of (G_k^T grad) * Q_k (unit-weight scatter times the filtered
+// sinogram), one block per view, float64 sums in a fixed order (deterministic).
+__global__ void __launch_bounds__(256) fbp_weight_grad_kernel(FbpParams p,
+                                                             const float* __restrict__ copies,
+                                                             const float* __restrict__ filtered,
+                                                             float* __restrict__ grad_w) {
+    __shared__ double part[256];
+    const int view = blockIdx.x;
+    const int V = p.two_d ? 1 : p.n_v;
+    const int vo = p.two_d ? 0 : 1;
+    double s = 0.0;
+    for (int i = threadIdx.x; i < p.n_u * V; i += blockDim.x) {
+        const int iu = i / V, iv = i - iu * V;
+        const float g = copies_at(p, copies, view, iu + 1, iv + 1);
+        const float q = filtered[((int64_t)view * p.rows + iu + 1) * p.cols + iv + vo];
+        s += (double)g * (double)q;
+    }
+    part[threadIdx.x] = s;
+    __syncthreads();
+    for (int h = 128; h > 0; h >>= 1) {
+        if ((int)threadIdx.x < h) part[threadIdx.x] += part[threadIdx.x + h];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) grad_w[view] = (float)part[0];
+}
+
+// dL/dkernel[d + n_u - 1] = sum_k w_k sum_v sum_i (G_k^T grad)[i][v] q_k[i - d][v], q the
+// pre-weighted sinogram.  One block per (view, tile of tv columns): the tile's scatter values and
+// pre-weighted columns (zero-padded by n_u - 1 on both sides) in shared memory, one tap offset d
+// per thread and step, float64 block sums added to `acc`.
+__global__ void __launch_bounds__(256) fbp_kernel_grad_kernel(
+    FbpParams p, const FbpView* __restrict__ views, const FbpCosine* __restrict__ cosines,
+    const float* __restrict__ view_weights, const float* __restrict__ sino,
+    const float* __restrict__ copies, int tv, int v_blocks, double* __restrict__ acc) {
+    extern __shared__ float sm2[];
+    const int n_u = p.n_u, V = p.two_d ? 1 : p.n_v;
+    const int wpad = 3 * n_u - 2;        // padded column length
+    float* G = sm2;                      // [tv][n_u]
+    float* P = sm2 + (int64_t)tv * n_u;  // [tv][3 n_u - 2], P[j][x] = q[x - (n_u - 1)]
+    const int view = blockIdx.x / v_blocks;
+    const int v0 = (blockIdx.x - view * v_blocks) * tv;
+    const int nv = min(tv, V - v0);
+    const FbpCosine C = cosines[view];
+    for (int i = threadIdx.x; i < tv * n_u; i += blockDim.x) {
+        const int j = i / n_u, iu = i - j * n_u;
+        G[i] = j < nv ? copies_at(p, copies, view, iu + 1, v0 + j + 1) : 0.0f;
+    }
+    for (int i = threadIdx.x; i < tv * wpad; i += blockDim.x) {
+        const int j = i / wpad, x = i - j * wpad, iu = x - (n_u - 1);
+        float val = 0.0f;
+        if (j < nv && iu >= 0 && iu < n_u) {
+            val = sino[((int64_t)view * n_u + iu) * V + v0 + j];
+            if (!p.parallel) val *= cosine_weight(C, iu, v0 + j);
+            if (p.pixel_weights) val *= p.pixel_weights[(int64_t)view * n_u + iu];
+        }
+        P[i] = val;
+    }
+    __syncthreads();
+    const double w = view_weights ? (double)view_weights[view]
+                                  : 3.14159265358979323846 / p.n_views;
+    for (int t = threadIdx.x; t < 2 * n_u - 1; t += blockDim.x) {
+        const int d = t - (n_u - 1);
+        float s = 0.0f;
+        for (int j = 0; j < nv; ++j) {
+            const float* g = G + j * n_u;
+            const float* q = P + j * wpad + (n_u - 1) - d;  // q[i] = column value at i - d
+            for (int i = 0; i < n_u; ++i) s = fmaf(g[i], q[i], s);
+        }
+        atomicAdd(acc + t, w * (double)s);
+    }
+}
+
+__global__ void fbp_finish_kernel_grad(const double* __restrict__ acc, float* __restrict__ out,
+                                       int n) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) out[i] = (float)acc[i];
+}
+
+}  // namespace
+
 size_t fbp_copies_floats(const FbpParams& p) {
     return p.two_d ? 2 * 2 * (size_t)p.n_views * (size_t)p.bu
                    : 4 * 4 * (size_t)p.n_views * (size_t)p.bu * (size_t)p.bv;
 }
 
-cudaError_t launch_fbp_transpose(const FbpParams& p, const double* raw, const float* user_weights,
-                                 FbpView* views, FbpCosine* cosines, float* taps,
-                                 const float* vol, float* scattered, float* sino,
+cudaError_t launch_fbp_transpose(const FbpParams& p_in, const double* raw,
+                                 const float* user_weights, FbpView* views, FbpCosine* cosines,
+                                 float* taps, const float* vol, float* scattered, float* sino,
                                  cudaStream_t stream) {
+    FbpParams p = p_in;
+    p.reverse_kernel = 1;  // the filter's transpose: the kernel reversed
     cudaError_t e = launch_prepare(p, raw, user_weights, views, cosines, taps, stream);
     if (e != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(scattered, 0, sizeof(float) * fbp_copies_floats(p), stream)) !=
@@ -871,6 +960,70 @@ cudaError_t launch_fbp_transpose(const FbpParams& p, const double* raw, const fl
         }
     }
     return launch_filter<true>(p, cosines, taps, scattered, sino, stream);
+}
+
+cudaError_t launch_fbp_gradients(const FbpParams& p_in, const double* raw,
+                                 const float* user_weights, FbpView* views, FbpCosine* cosines,
+                                 float* taps, const float* sino, const float* grad_vol,
+                                 float* copies, float* filtered, double* acc, float* grad_kernel,
+                                 float* grad_view_weights, cudaStream_t stream) {
+    cudaError_t e;
+    // (1) the scatter of dL/df with unit view weights: G_k^T grad in the parity copies
+    FbpParams pu = p_in;
+    pu.unit_weights = 1;
+    pu.reverse_kernel = 0;
+    if ((e = launch_prepare(pu, raw, user_weights, views, cosines, taps, stream)) != cudaSuccess)
+        return e;
+    if ((e = cudaMemsetAsync(copies, 0, sizeof(float) * fbp_copies_floats(pu), stream)) !=
+        cudaSuccess)
+        return e;
+    if (pu.two_d) {
+        if ((pu.ny + 31) / 32 > 65535) return cudaErrorInvalidValue;
+        dim3 g((pu.nx + 31) / 32, (pu.ny + 7) / 8);
+        if (pu.parallel)
+            fbp2d_scatter_kernel<true, 1><<<g, 256, 0, stream>>>(pu, views, grad_vol, copies);
+        else
+            fbp2d_scatter_kernel<false, 1><<<g, 256, 0, stream>>>(pu, views, grad_vol, copies);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    } else {
+        if ((pu.nx + 7) / 8 > 65535 || pu.ny > 65535) return cudaErrorInvalidValue;
+        dim3 g((pu.nz + 31) / 32, (pu.nx + 7) / 8, pu.ny);
+        fdk_scatter_kernel<1><<<g, 256, 0, stream>>>(pu, views, grad_vol, copies, 0, pu.n_views);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    // (2) dL/dw: the filtered sinogram (forward filter) against the scatter
+    if (grad_view_weights != nullptr) {
+        if ((e = launch_filter<false>(pu, cosines, taps, sino, filtered, stream)) != cudaSuccess)
+            return e;
+        fbp_weight_grad_kernel<<<pu.n_views, 256, 0, stream>>>(pu, copies, filtered,
+                                                                grad_view_weights);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    // (3) dL/dkernel: correlation of the scatter with the pre-weighted sinogram
+    if (grad_kernel != nullptr) {
+        const int n_u = pu.n_u, V = pu.two_d ? 1 : pu.n_v;
+        const size_t per_col = sizeof(float) * ((size_t)n_u + 3 * (size_t)n_u - 2);
+        int tv = 32;
+        while (tv > 1 && tv * per_col > kSmemBudget) tv >>= 1;
+        if (tv > V) tv = V;
+        if (tv * per_col > kSmemBudget) return cudaErrorInvalidValue;
+        const size_t smem = tv * per_col;
+        e = cudaFuncSetAttribute(fbp_kernel_grad_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        const int v_blocks = (V + tv - 1) / tv;
+        if ((int64_t)v_blocks * pu.n_views > (int64_t)INT32_MAX) return cudaErrorInvalidValue;
+        if ((e = cudaMemsetAsync(acc, 0, sizeof(double) * (size_t)(2 * n_u - 1), stream)) !=
+            cudaSuccess)
+            return e;
+        fbp_kernel_grad_kernel<<<v_blocks * pu.n_views, 256, smem, stream>>>(
+            pu, views, cosines, user_weights, sino, copies, tv, v_blocks, acc);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        fbp_finish_kernel_grad<<<(2 * n_u - 1 + 255) / 256, 256, 0, stream>>>(acc, grad_kernel,
+                                                                              2 * n_u - 1);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace ct

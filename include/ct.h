@@ -279,9 +279,10 @@ CT_API ct_status ct_backproject_static(const ct_geometry *geom, const float *d_s
  *
  *   1. fan/cone: p'(u, v) = p(u, v) |(c - s) . n| / |P(u, v) - s|   (s source, c detector
  *      centre, n detector normal, P the pixel);
- *   2. Q(u_i, v) = du sum_j h((i - j) du) p'(u_j, v), the band-limited ramp
- *      h(x) = 2 int_0^{1/(2 du)} f W(f) cos(2 pi f x) df with window W (ct_fbp_window), as a
- *      linear convolution along u (no wrap-around);
+ *   2. Q(u_i, v) = sum_j k[i - j + n_u - 1] p'(u_j, v), a linear convolution along u (no
+ *      wrap-around) with the discrete kernel k[m] = du h((m - n_u + 1) du), h the band-limited
+ *      ramp h(x) = 2 int_0^{1/(2 du)} f W(f) cos(2 pi f x) df with window W (ct_fbp_window), or
+ *      the caller's kernel (e.g. a learned filter);
  *   3. f(X) = sum_k w_k g_k(X) Q_k(u_k(X), v_k(X)): X projected onto view k's detector through
  *      the source (parallel: along the ray), Q interpolated bilinearly (0 off the detector),
  *      g = 1 for parallel beams, else g = (D_sd / D_so) / U(X)^2 with
@@ -292,19 +293,23 @@ CT_API ct_status ct_backproject_static(const ct_geometry *geom, const float *d_s
  *
  * d_sino       device sinogram, read only.
  * d_volume     device volume, overwritten.
- * d_view_weights  device, n_views floats, or NULL for the uniform full-scan quadrature
- *              w_k = pi / n_views (a 180-degree parallel scan, or a 360-degree fan/cone scan with
- *              the 1/2 redundancy factor).  Short scans pass the angular step instead.
- * d_pixel_weights device, n_views x n_u floats, or NULL: weights per view and detector column
- *              applied with the cosine weights before filtering, e.g. Parker's short-scan
- *              weights from ct_fbp_parker_weights.
- * isocenter    host, 3 doubles (x, y, z; z ignored in 2D), or NULL: the point whose
- *              detector-plane distance sets D_so (fan/cone; unused for parallel beams).  NULL
- *              estimates it from the detector normals, as the pages' default does: the
- *              least-squares point nearest the lines through each detector centre along its
- *              normal (the origin for circular orbits about it); one view, or views whose
- *              normals are all parallel, give that set's minimum-norm point, so pass the
- *              isocentre explicitly for such geometries.
+ * options      NULL for the defaults, or (fields):
+ *   window          ct_fbp_window of the ramp (used when d_kernel is NULL).
+ *   d_view_weights  device, n_views floats, or NULL for the uniform full-scan quadrature
+ *                   w_k = pi / n_views (a 180-degree parallel scan, or a 360-degree fan/cone scan
+ *                   with the 1/2 redundancy factor).  Short scans pass the angular step instead.
+ *   d_pixel_weights device, n_views x n_u floats, or NULL: weights per view and detector column
+ *                   applied with the cosine weights before filtering, e.g. Parker's short-scan
+ *                   weights from ct_fbp_parker_weights.
+ *   d_kernel        device, 2 n_u - 1 floats, or NULL: the discrete filter k above (offset
+ *                   m - n_u + 1 at index m), replacing the windowed ramp.
+ *   isocenter       host, 3 doubles (x, y, z; z ignored in 2D), or NULL: the point whose
+ *                   detector-plane distance sets D_so (fan/cone; unused for parallel beams).
+ *                   NULL estimates it from the detector normals, as the pages' default does: the
+ *                   least-squares point nearest the lines through each detector centre along its
+ *                   normal (the origin for circular orbits about it); one view, or views whose
+ *                   normals are all parallel, give that set's minimum-norm point, so pass the
+ *                   isocentre explicitly for such geometries.
  * Workspace: at least ct_fbp_workspace_bytes(geom) (the filtered sinogram, per-view constants
  * and the filter taps).
  * Errors: CT_ERR_INVALID_ARGUMENT for CT_PARALLEL3D, surface detectors, an unknown window, or
@@ -319,11 +324,18 @@ typedef enum {
     CT_WINDOW_HANN = 4         /* W(f) = 0.5 + 0.5 cos(2 pi f du)                   */
 } ct_fbp_window;
 
+typedef struct {
+    ct_fbp_window window;
+    const float *d_view_weights;
+    const float *d_pixel_weights;
+    const float *d_kernel;
+    const double *isocenter;
+} ct_fbp_options;
+
 CT_API size_t ct_fbp_workspace_bytes(const ct_geometry *geom);
 CT_API ct_status ct_fbp(const ct_geometry *geom, const float *d_sino, float *d_volume,
-                        const float *d_view_weights, const float *d_pixel_weights,
-                        const double *isocenter, ct_fbp_window window, void *d_workspace,
-                        size_t workspace_bytes, struct CUstream_st *stream);
+                        const ct_fbp_options *options, void *d_workspace, size_t workspace_bytes,
+                        struct CUstream_st *stream);
 
 /*
  * Transpose of ct_fbp as a linear map (sinogram -> volume), for gradients with respect to the
@@ -332,17 +344,35 @@ CT_API ct_status ct_fbp(const ct_geometry *geom, const float *d_sino, float *d_v
  * weights and normalisation, with dedicated transpose kernels (diffct "Differentiable analytical
  * reconstruction"; "Analytical Reconstruction Helpers").  Steps: every voxel adds
  * w_k g_k(X) f(X) times its four bilinear coefficients onto view k's detector (atomic adds;
- * contributions off the detector are dropped), the same filter (its matrix du h((i - j) du) is
- * symmetric), then the cosine weights.  Arguments and errors as for ct_fbp, with d_volume read
- * and d_sino overwritten; the workspace is at least ct_fbp_transpose_workspace_bytes(geom) (per
- * view and detector pixel 4 floats for cone beams, 2 for 2D, plus the per-view constants and
- * taps).  The atomic adds make the float32 result depend on the order in which they land
- * (run-to-run differences of a few ulp).
+ * contributions off the detector are dropped), the filter with its kernel reversed (the
+ * windowed ramps are symmetric), then the cosine and pixel weights.  Arguments and errors as for
+ * ct_fbp, with d_volume read and d_sino overwritten; the workspace is at least
+ * ct_fbp_transpose_workspace_bytes(geom) (per view and detector pixel 4 floats for cone beams, 2
+ * for 2D, plus the per-view constants and taps).  The atomic adds make the float32 result depend
+ * on the order in which they land (run-to-run differences of a few ulp).
  */
 CT_API size_t ct_fbp_transpose_workspace_bytes(const ct_geometry *geom);
 CT_API ct_status ct_fbp_transpose(const ct_geometry *geom, const float *d_volume, float *d_sino,
-                                  const float *d_view_weights, const float *d_pixel_weights,
-                                  const double *isocenter, ct_fbp_window window,
+                                  const ct_fbp_options *options, void *d_workspace,
+                                  size_t workspace_bytes, struct CUstream_st *stream);
+
+/*
+ * Gradients of a loss L(f), f = ct_fbp(d_sino, options), with respect to the filter kernel and
+ * the view weights, given dL/df = d_grad_volume (the pages: filter and explicit weight gradients
+ * propagate through the analytical pipeline, "Differentiable analytical reconstruction").  f is
+ * linear in both: with q_k the cosine- and pixel-weighted sinogram of view k, Q_k its filtered
+ * columns and G_k the view's gather without its weight,
+ *     dL/dw_k = <G_k^T grad, Q_k>,
+ *     dL/dk[d + n_u - 1] = sum_k w_k sum_v sum_i (G_k^T grad)(u_i, v) q_k(u_{i - d}, v).
+ * d_grad_kernel (device, 2 n_u - 1 floats) and d_grad_view_weights (device, n_views floats) are
+ * overwritten; either may be NULL, not both.  Workspace: ct_fbp_gradients_workspace_bytes(geom).
+ * Float64 sums; the kernel gradient adds per-block float64 partial sums atomically (run-to-run
+ * differences in the last bits).  Errors as for ct_fbp.
+ */
+CT_API size_t ct_fbp_gradients_workspace_bytes(const ct_geometry *geom);
+CT_API ct_status ct_fbp_gradients(const ct_geometry *geom, const float *d_sino,
+                                  const float *d_grad_volume, const ct_fbp_options *options,
+                                  float *d_grad_kernel, float *d_grad_view_weights,
                                   void *d_workspace, size_t workspace_bytes,
                                   struct CUstream_st *stream);
 

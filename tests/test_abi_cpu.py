@@ -90,9 +90,11 @@ def test_null_arguments_are_rejected(lib):
     assert L.ct_sirt_iterate(None, None, None, None, 0, 1, 1.0, 0, None) == 1
     assert L.ct_geometry_destroy(None) == 0
     assert L.ct_sirt_workspace_bytes(None) == 0
-    assert L.ct_fbp(None, None, None, None, None, None, 0, None, 0, None) == 1
+    assert L.ct_fbp(None, None, None, None, None, 0, None) == 1
     assert L.ct_fbp_workspace_bytes(None) == 0
-    assert L.ct_fbp_transpose(None, None, None, None, None, None, 0, None, 0, None) == 1
+    assert L.ct_fbp_transpose(None, None, None, None, None, 0, None) == 1
+    assert L.ct_fbp_gradients(None, None, None, None, None, None, None, 0, None) == 1
+    assert L.ct_fbp_gradients_workspace_bytes(None) == 0
     assert L.ct_fbp_parker_weights(None, None, None) == 1
     assert L.ct_fbp_transpose_workspace_bytes(None) == 0
 

@@ -109,6 +109,7 @@ def test_fbp_indices_stay_in_bounds(pair, n):
     x = torch_cuda(W.random_volume(w, 4))
     f, fd = g.fbp(y, window="shepp-logan"), gd.fbp(y, window="shepp-logan")
     gd.fbp_transpose(x)
+    gd.fbp_gradients(y, x)
     # a voxel grid much larger than the field of view: most projections land off the detector
     import dataclasses
     big = dataclasses.replace(w, vol_shape=(w.vol_shape[0], 3 * w.vol_shape[1], 3 * w.vol_shape[2]),

@@ -151,13 +151,14 @@ def test_errors(ct):
 
     def call(status, **kw):
         args = dict(d_sino=sino.data_ptr(), d_volume=vol.data_ptr(), d_view_weights=None,
-                    d_pixel_weights=None, isocenter=None, window=0, d_workspace=ws.data_ptr(),
-                    workspace_bytes=need)
+                    d_pixel_weights=None, d_kernel=None, isocenter=None, window=0,
+                    d_workspace=ws.data_ptr(), workspace_bytes=need)
         args.update(kw)
+        opts, keep = ct.fbp_options(args["window"], args["d_view_weights"],
+                                    args["d_pixel_weights"], args["d_kernel"], args["isocenter"])
         with pytest.raises(ct.CtError) as ei:
-            ct.ct_fbp(g.handle, args["d_sino"], args["d_volume"], args["d_view_weights"],
-                      args["d_pixel_weights"], args["isocenter"], args["window"],
-                      args["d_workspace"], args["workspace_bytes"], s)
+            ct.ct_fbp(g.handle, args["d_sino"], args["d_volume"], opts, args["d_workspace"],
+                      args["workspace_bytes"], s)
         assert ei.value.status == status
 
     call(7, workspace_bytes=need - 1)
@@ -165,8 +166,8 @@ def test_errors(ct):
     need_t = ct.ct_fbp_transpose_workspace_bytes(g.handle)
     assert need_t > need
     with pytest.raises(ct.CtError) as ei:
-        ct.ct_fbp_transpose(g.handle, vol.data_ptr(), sino.data_ptr(), None, None, None, 0,
-                            ws.data_ptr(), need, s)
+        ct.ct_fbp_transpose(g.handle, vol.data_ptr(), sino.data_ptr(), None, ws.data_ptr(),
+                            need, s)
     assert ei.value.status == 7
     call(1, window=5)
     call(1, isocenter=(math.nan, 0.0, 0.0))
@@ -175,6 +176,18 @@ def test_errors(ct):
     call(3, d_view_weights=host.ctypes.data)
     call(3, d_pixel_weights=host.ctypes.data)
     call(4, d_pixel_weights=vol.data_ptr())
+    call(3, d_kernel=host.ctypes.data)
+    call(4, d_kernel=ws.data_ptr())
+    # gradients: at least one output; their own (larger) scratch
+    need_g = ct.ct_fbp_gradients_workspace_bytes(g.handle)
+    wsg = torch.empty(need_g, dtype=torch.uint8, device="cuda")
+    gk = torch.empty(2 * w.n_u - 1, device="cuda")
+    for args, status in (((None, None, wsg.data_ptr(), need_g), 1),
+                         ((gk.data_ptr(), None, wsg.data_ptr(), need_g - 1), 7),
+                         ((gk.data_ptr(), gk.data_ptr(), wsg.data_ptr(), need_g), 4)):
+        with pytest.raises(ct.CtError) as ei:
+            ct.ct_fbp_gradients(g.handle, sino.data_ptr(), vol.data_ptr(), None, *args, s)
+        assert ei.value.status == status
     # Parker weights: parallel beams have none
     with pytest.raises(ct.CtError) as ei:
         ct.Geometry.from_workload(W.small_config(1)).parker_weights()
@@ -397,3 +410,52 @@ def test_parker_rejects_short_and_non_circular_scans(ct):
     with pytest.raises(ct.CtError) as ei:
         ct.Geometry.from_workload(dataclasses.replace(base, views=bad)).parker_weights()
     assert ei.value.status == 2
+
+
+
+# ---------------------------------------------------------------------------------------------
+# caller filter kernels and gradients
+# ---------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("n", [1, 2, 3])
+def test_caller_kernel_forward_and_transpose(ct, n):
+    """An asymmetric caller kernel: the forward filter uses it as given, the transpose reversed."""
+    w = W.small_config(n)
+    rng = np.random.default_rng(90 + n)
+    kern = (rng.standard_normal(2 * w.n_u - 1) / w.n_u).astype(np.float32)
+    y = W.random_sinogram(w, 5)
+    x = W.random_volume(w, 6)
+    g = ct.Geometry.from_workload(w)
+    got = _cpu(g.fbp(torch_cuda(y), kernel=torch_cuda(kern)))
+    _check(got, _oracle(w, y.astype(np.float64), kernel=kern.astype(np.float64)))
+    got_t = _cpu(g.fbp_transpose(torch_cuda(x), kernel=torch_cuda(kern)))
+    _check(got_t, _oracle_t(w, x.astype(np.float64), kernel=kern.astype(np.float64)))
+
+
+@pytest.mark.parametrize("n", [1, 2, 3])
+def test_gradients_match_oracle(ct, n):
+    w = W.small_config(n)
+    rng = np.random.default_rng(100 + n)
+    nv = w.views.shape[0]
+    y = W.random_sinogram(w, 7)
+    grad = W.random_volume(w, 8)
+    wts = rng.uniform(0.01, 0.05, nv).astype(np.float32)
+    pw = rng.uniform(0.5, 1.5, (nv, w.n_u)).astype(np.float32)
+    kern = (w.du * F.ramp_taps(w.n_u, w.du, "hann")).astype(np.float32)
+    iso = (0.4, -0.3, 0.2)[: 2 if n < 3 else 3]
+    g = ct.Geometry.from_workload(w)
+    gk, gw = g.fbp_gradients(torch_cuda(y), torch_cuda(grad), view_weights=torch_cuda(wts),
+                             pixel_weights=torch_cuda(pw), kernel=torch_cuda(kern),
+                             isocenter=iso)
+    want_k, want_w = F.fbp_gradients(w.beam, w.views, w.vol_shape, w.voxel_spacing, w.n_u,
+                                     w.n_v, w.du, w.dv, y.astype(np.float64),
+                                     grad.astype(np.float64), kernel=kern.astype(np.float64),
+                                     view_weights=wts.astype(np.float64), isocenter=iso,
+                                     pixel_weights=pw.astype(np.float64))
+    assert rel_l2(_cpu(gk), want_k) < 1e-4
+    assert rel_l2(_cpu(gw), want_w) < 1e-4
+    # one output at a time gives the same values
+    gk2, none = g.fbp_gradients(torch_cuda(y), torch_cuda(grad), view_weights=torch_cuda(wts),
+                                pixel_weights=torch_cuda(pw), kernel=torch_cuda(kern),
+                                isocenter=iso, want_view_weights=False)
+    assert none is None and rel_l2(_cpu(gk2), _cpu(gk)) < 1e-6
