@@ -204,10 +204,16 @@ __device__ __forceinline__ bool setup_ray(const ViewRec& vr, const Grid& g, int 
 // (the voxel after the outer crossing, and the one after a pending inner crossing) one step
 // ahead.  The tail phase takes the remaining events with per-axis exhaustion checks.  Both
 // phases visit the same events in the same order with the same arithmetic.
-template <bool SCATTER, int NB>
+//
+// ISIGN: 0, or the inner-axis step (+1 / -1, the inner axis has unit stride) when every ray of
+// the warp that crosses inner planes moves that way.  SINGLE: every ray of the warp has at most
+// one inner crossing between two outer ones (see walk_dispatch), so the main phase needs no loop
+// for a second one.  The specialisations change no arithmetic.
+template <bool SCATTER, int NB, int ISIGN, bool SINGLE>
 __device__ __forceinline__ void walk(const Ray& r, const float* __restrict__ vin,
                                      float* __restrict__ vout, int64_t vstride,
                                      const float (&val)[NB], float (&acc)[NB]) {
+    const int s2 = ISIGN != 0 ? ISIGN : r.step[2];
     const float INF = f_inf();
     const float na = (float)r.n[0], nb = (float)r.n[1], nf = (float)r.n[2];
     float ta = r.n[0] > 0 ? r.t0[0] : INF;
@@ -252,7 +258,7 @@ __device__ __forceinline__ void walk(const Ray& r, const float* __restrict__ vin
     float v0[NB], v1[NB];  // gather: values of the current voxel and of the next one inward
     if (!SCATTER) {
         load(idx, v0);
-        if (p) load(idx + r.step[2], v1);
+        if (p) load(idx + s2, v1);
     }
 #pragma unroll 1
     while (tstop < lim) {
@@ -262,19 +268,19 @@ __device__ __forceinline__ void walk(const Ray& r, const float* __restrict__ vin
         else
             gather(v0, seg0);
         if (p) {
-            idx += r.step[2];
+            idx += s2;
             t = tf;
             kf += 1.0f;
             tf = kf < nf ? __fmaf_rn(kf, r.dt[2], r.t0[2]) : INF;
 #pragma unroll 1
-            while (tf < tstop) {  // a second inner crossing before this outer one (rare)
+            while (!SINGLE && tf < tstop) {  // a second inner crossing before this outer one (rare)
                 const float seg = __fsub_rn(tf, t);
                 if (SCATTER) {
                     scatter(idx, seg);
-                    idx += r.step[2];
+                    idx += s2;
                 } else {
                     gather(v1, seg);
-                    idx += r.step[2];
+                    idx += s2;
                     load(idx, v1);
                 }
                 t = tf;
@@ -301,7 +307,7 @@ __device__ __forceinline__ void walk(const Ray& r, const float* __restrict__ vin
         p = tf < tstop;
         if (!SCATTER) {
             load(idx, v0);
-            if (p) load(idx + r.step[2], v1);
+            if (p) load(idx + s2, v1);
         }
     }
     // Tail: the remaining events with the per-axis checks.  v0 holds the current voxel's values.
@@ -313,9 +319,9 @@ __device__ __forceinline__ void walk(const Ray& r, const float* __restrict__ vin
             const float seg = __fsub_rn(tf, t);
             if (SCATTER) {
                 scatter(idx, seg);
-                idx += r.step[2];
+                idx += s2;
             } else {
-                idx += r.step[2];
+                idx += s2;
                 float vn[NB];
                 load(idx, vn);
                 gather(v0, seg);
@@ -351,9 +357,9 @@ __device__ __forceinline__ void walk(const Ray& r, const float* __restrict__ vin
         const float seg = __fsub_rn(tf, t);
         if (SCATTER) {
             scatter(idx, seg);
-            idx += r.step[2];
+            idx += s2;
         } else {
-            idx += r.step[2];
+            idx += s2;
             float vn[NB];
             load(idx, vn);
             gather(v0, seg);
@@ -371,17 +377,38 @@ __device__ __forceinline__ void walk(const Ray& r, const float* __restrict__ vin
         gather(v0, seg);
 }
 
+// Picks the walk's specialisation for the lanes that walk together.  At most one inner crossing
+// fits between two outer ones when the inner pitch exceeds every gap between successive outer
+// crossings.  Such a gap is at most min(dt_a, dt_b) plus the rounding of two crossing values, and
+// successive inner crossings are at least dt_f minus that rounding apart; each crossing value is
+// one fmaf below tend, so the margin 1e-5 tend (about 80 ulps of tend) covers it.
+template <bool SCATTER, int NB>
+__device__ __forceinline__ void walk_dispatch(const Ray& r, const float* __restrict__ vin,
+                                              float* __restrict__ vout, int64_t vstride,
+                                              const float (&val)[NB], float (&acc)[NB]) {
+    const unsigned m = __activemask();
+    const bool none = r.n[2] == 0;
+    const bool single =
+        none || r.dt[2] > fminf(r.dt[0], r.dt[1]) + __fmaf_rn(r.tend, 1e-5f, 1e-6f);
+    if (__all_sync(m, single && (none || r.step[2] == 1)))
+        walk<SCATTER, NB, 1, true>(r, vin, vout, vstride, val, acc);
+    else if (__all_sync(m, single && (none || r.step[2] == -1)))
+        walk<SCATTER, NB, -1, true>(r, vin, vout, vstride, val, acc);
+    else
+        walk<SCATTER, NB, 0, false>(r, vin, vout, vstride, val, acc);
+}
+
 // Single-volume forms.
 __device__ __forceinline__ float walk_gather(const Ray& r, const float* __restrict__ vin) {
     const float none[1] = {0.0f};
     float acc[1];
-    walk<false, 1>(r, vin, nullptr, 0, none, acc);
+    walk_dispatch<false, 1>(r, vin, nullptr, 0, none, acc);
     return acc[0];
 }
 __device__ __forceinline__ void walk_scatter(const Ray& r, float* __restrict__ vout, float val) {
     const float v[1] = {val};
     float acc[1];
-    walk<true, 1>(r, nullptr, vout, 0, v, acc);
+    walk_dispatch<true, 1>(r, nullptr, vout, 0, v, acc);
 }
 
 // Block -> (view, pixel tile).  Tiles are ordered detector-v band first, then view, then u tile,
@@ -455,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, BatchBlocks<NB>::value)
             } else {
                 const float none[NB] = {};
                 float acc[NB];
-                walk<false, NB>(ray, vol, nullptr, vstride, none, acc);
+                walk_dispatch<false, NB>(ray, vol, nullptr, vstride, none, acc);
 #pragma unroll
                 for (int b = 0; b < NB; ++b) sino[b * sstride + k] = __fmul_rn(acc[b], ray.scale);
             }
@@ -498,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, BatchBlocks<NB>::value)
             float val[NB], unused[NB];
 #pragma unroll
             for (int b = 0; b < NB; ++b) val[b] = __fmul_rn(y[b], ray.scale);
-            walk<true, NB>(ray, nullptr, vol, vstride, val, unused);
+            walk_dispatch<true, NB>(ray, nullptr, vol, vstride, val, unused);
         }
     }
 }
