@@ -207,8 +207,9 @@ __device__ __forceinline__ bool setup_ray(const ViewRec& vr, const Grid& g, int 
 //
 // ISIGN: 0, or the inner-axis step (+1 / -1, the inner axis has unit stride) when every ray of
 // the warp that crosses inner planes moves that way.  SINGLE: every ray of the warp has at most
-// one inner crossing between two outer ones (see walk_dispatch), so the main phase needs no loop
-// for a second one.  The specialisations change no arithmetic.
+// one inner crossing between two outer ones, and none can run out of inner crossings in the main
+// phase (see walk_dispatch), so the main phase needs neither a loop for a second inner crossing
+// nor the exhaustion check.  The specialisations change no arithmetic.
 template <bool SCATTER, int NB, int ISIGN, bool SINGLE>
 __device__ __forceinline__ void walk(const Ray& r, const float* __restrict__ vin,
                                      float* __restrict__ vout, int64_t vstride,
@@ -271,7 +272,7 @@ __device__ __forceinline__ void walk(const Ray& r, const float* __restrict__ vin
             idx += s2;
             t = tf;
             kf += 1.0f;
-            tf = kf < nf ? __fmaf_rn(kf, r.dt[2], r.t0[2]) : INF;
+            tf = (SINGLE || kf < nf) ? __fmaf_rn(kf, r.dt[2], r.t0[2]) : INF;
 #pragma unroll 1
             while (!SINGLE && tf < tstop) {  // a second inner crossing before this outer one (rare)
                 const float seg = __fsub_rn(tf, t);
@@ -310,6 +311,9 @@ __device__ __forceinline__ void walk(const Ray& r, const float* __restrict__ vin
             if (p) load(idx + s2, v1);
         }
     }
+    // (SINGLE computed the crossing after the last inner one instead of +inf: restore +inf, since
+    // the tail may reach past it.)
+    if (SINGLE && !(kf < nf)) tf = INF;
     // Tail: the remaining events with the per-axis checks.  v0 holds the current voxel's values.
 #pragma unroll 1
     for (int outer = (int)(na - ka) + (int)(nb - kb); outer > 0; --outer) {
@@ -387,9 +391,16 @@ __device__ __forceinline__ void walk_dispatch(const Ray& r, const float* __restr
                                               float* __restrict__ vout, int64_t vstride,
                                               const float (&val)[NB], float (&acc)[NB]) {
     const unsigned m = __activemask();
+    const float INF = f_inf();
     const bool none = r.n[2] == 0;
+    // the crossing after the last inner one, as the walk would compute it, is not before the end
+    // of the main phase (the earlier of the two outer axes' last crossings), so the main phase
+    // never takes it
+    const float la = r.n[0] > 0 ? __fmaf_rn((float)r.n[0] - 1.0f, r.dt[0], r.t0[0]) : INF;
+    const float lb = r.n[1] > 0 ? __fmaf_rn((float)r.n[1] - 1.0f, r.dt[1], r.t0[1]) : INF;
     const bool single =
-        none || r.dt[2] > fminf(r.dt[0], r.dt[1]) + __fmaf_rn(r.tend, 1e-5f, 1e-6f);
+        none || (r.dt[2] > fminf(r.dt[0], r.dt[1]) + __fmaf_rn(r.tend, 1e-5f, 1e-6f) &&
+                 __fmaf_rn((float)r.n[2], r.dt[2], r.t0[2]) >= fminf(la, lb));
     if (__all_sync(m, single && (none || r.step[2] == 1)))
         walk<SCATTER, NB, 1, true>(r, vin, vout, vstride, val, acc);
     else if (__all_sync(m, single && (none || r.step[2] == -1)))
