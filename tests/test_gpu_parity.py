@@ -384,3 +384,37 @@ def test_flat_offsets_surface_equals_flat_detector(ct):
     x = torch_cuda(w.phantom())
     a, b = _cpu(flat.project(x)), _cpu(surf.project(x))
     np.testing.assert_allclose(b, a, rtol=1e-5, atol=1e-5 * float(np.abs(a).max()))
+
+
+def test_walk_specialisation_boundary(ct):
+    """Parallel rays whose inner-axis crossing pitch is just above, at and just below the largest
+    gap between outer-axis crossings: the warps on either side take the specialised or the
+    general walk, and every ray still matches the oracle (both inner directions)."""
+    nz, ny, nx = 24, 20, 28
+    theta = math.radians(30.0)          # azimuth of the rays' xy direction
+    m = max(math.cos(theta), math.sin(theta))
+    phi_b = math.atan(m)                # tan(phi) = m: inner pitch equals the outer gap bound
+    phis = [math.radians(10.0), math.radians(80.0)]
+    # -1e-3 .. -1.4e-4: the pitch difference is a few times down to ~1.3x the walk's rounding
+    # margin (1e-5 of the chord); -1e-6 .. 1e-3: at or below the bound
+    for d in (-1e-3, -2e-4, -1.4e-4, -1e-6, 0.0, 1e-6, 1e-3):
+        phis += [phi_b + d, -(phi_b + d)]
+    views = []
+    for phi in phis:
+        r = [math.cos(theta) * math.cos(phi), math.sin(theta) * math.cos(phi), math.sin(phi)]
+        du_vec = [-math.sin(theta), math.cos(theta), 0.0]
+        views.append(r + [0.1, -0.2, 0.3] + du_vec + [0.0, 0.0, 1.0])
+    views = np.array(views)
+    args = (W.PARALLEL3D, views, (nz, ny, nx), 1.0, 40, 48, 0.7, 0.9)
+    g, go = ct.Geometry(*args), oracle.Geometry(*args)
+    assert g.info.volume_layout == 1  # z fastest: z is the walk's inner axis here
+    rng = np.random.default_rng(11)
+    x = rng.uniform(0.1, 1.0, size=(nz, ny, nx)).astype(np.float32)
+    y_gpu = _cpu(g.project(torch_cuda(x)))
+    y_or = go.project(x)
+    L, _ = go.ray_lengths()
+    assert (L > 0).mean() > 0.5
+    bad = fp_violations(y_gpu, y_or, L, float(x.max()))
+    assert bad.size == 0, bad[:10]
+    yy = rng.uniform(0.1, 1.0, size=go.sino_shape).astype(np.float32)
+    assert rel_l2(_cpu(g.backproject(torch_cuda(yy))), go.backproject(yy)) <= BP_RTOL
