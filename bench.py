@@ -256,8 +256,8 @@ def profiled_sol(kernel: str, source: str = "siddon_kernels.cu"):
     text = open(os.path.join(ROOT, path)).read()
     out = {"source": path}
     for key, label in (("memory_sol_pct", "memory throughput (ncu SOL"),
-                       ("l2_pct", "L2 throughput"), ("dram_pct", "DRAM throughput"),
-                       ("issue_pct", "issue slots busy")):
+                       ("l1tex_pct", "L1TEX throughput"), ("l2_pct", "L2 throughput"),
+                       ("dram_pct", "DRAM throughput"), ("issue_pct", "issue slots busy")):
         m = re.search(r"\| " + re.escape(label) + r"[^|]*\| ([0-9.]+) %", text)
         out[key] = float(m.group(1)) if m else None
     m = re.search(r"\| duration \(sum over captured launches, serialised\) \| ([0-9.]+) ms", text)
@@ -368,14 +368,17 @@ def ncu_sol():
     pair = (fp["memory_sol_pct"] * fp["ms"] + bp["memory_sol_pct"] * bp["ms"]) / (fp["ms"] + bp["ms"])
     return {"project_kernel": fp, "backproject_kernel": bp,
             "pair_memory_sol_pct": pair,
-            "note": "percent of ncu's own peaks; both walks are issue-bound (see profiles/)"}
+            "note": "percent of ncu's own peaks; the forward walk is latency-bound (long "
+                    "scoreboard), the backprojection L1TEX-bound (see profiles/)"}
 
 
 def fdk_leg(ct, torch, w, reps: int = 5, cpu_baseline: bool = True):
     """Filtered backprojection (FDK, Ram-Lak window) of the metric workload's geometry and its
     transpose, CUDA events around each C-ABI call, L2 flushed before each.  Rate in voxel-view
-    updates per second; the roofline is the float32 ALU one (the gather kernel is issue-bound):
-    38 algorithmic flops per voxel-view against 148 SMs x 128 lanes x 2 flops x 2.032 GHz."""
+    updates per second.  The roofline reported is the float32 ALU one: 38 algorithmic flops per
+    voxel-view against 148 SMs x 128 lanes x 2 flops x 2.032 GHz.  The gather kernel's binding
+    limit is L1TEX throughput (its bilinear sinogram reads); `ncu` carries those figures from the
+    committed profile."""
     g = ct.Geometry.from_workload(w)
     sino = torch.from_numpy(W.random_sinogram(w, 11)).cuda()
     vol = torch.empty(g.volume_shape, device="cuda")
@@ -415,6 +418,7 @@ def fdk_leg(ct, torch, w, reps: int = 5, cpu_baseline: bool = True):
     traffic, src = profiled_traffic("fdk_gather_kernel", "fbp_kernels.cu")
     out["roofline"]["traffic"] = traffic
     out["roofline"]["traffic_source"] = src
+    out["roofline"]["ncu"] = profiled_sol("fdk_gather_kernel", "fbp_kernels.cu")
     del sino, vol, ws, ws_t, out_t, flush
     torch.cuda.empty_cache()
     if cpu_baseline:
