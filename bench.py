@@ -626,8 +626,8 @@ def run_ours(args, rank, world):
                      "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                      "traffic_source": traffic_src, "peak_source": peak_kind,
                      "bytes_model": "4 B per ray-voxel update + 4 B per ray + volume once "
-                                    "(gathers/atomics are served by L1/L2; the walk is "
-                                    "issue-bound, see profiles/)"},
+                                    "(gathers/atomics are served by L1/L2; the binding "
+                                    "limits are in profiles/)"},
         "e2e": {"value": world * 2 * U / (e2e_ms * 1e-3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "timing": "host wall clock around the steps, copies overlapped on a 2nd stream"},

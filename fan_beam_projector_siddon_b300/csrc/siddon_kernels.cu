@@ -261,7 +261,7 @@ __device__ __forceinline__ void walk(const Ray& r, const float* __restrict__ vin
         load(idx, v0);
         if (p) load(idx + s2, v1);
     }
-#pragma unroll 1
+#pragma unroll 2  // two steps per iteration: the loop-carried values are renamed, not copied
     while (tstop < lim) {
         const float seg0 = __fsub_rn(p ? tf : tstop, t);
         if (SCATTER)
