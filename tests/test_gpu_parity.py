@@ -418,3 +418,45 @@ def test_walk_specialisation_boundary(ct):
     assert bad.size == 0, bad[:10]
     yy = rng.uniform(0.1, 1.0, size=go.sino_shape).astype(np.float32)
     assert rel_l2(_cpu(g.backproject(torch_cuda(yy))), go.backproject(yy)) <= BP_RTOL
+
+
+def test_walk_specialisation_changes_no_arithmetic(ct):
+    """The same rays projected once in a warp that takes the specialised walk and once in a
+    warp pushed onto the general walk give bit-identical values.  Rows 32..44 of the small cone
+    all climb in z, so their warps vote for the fast walk; mirroring row 44 below the central
+    row (through the detector-surface offsets, which leave every other ray's arithmetic
+    untouched) gives that warp one descending ray, and the sign vote fails."""
+    w = W.small_config(3)
+    off1 = W.flat_offsets(w.n_u, w.n_v, w.du, w.dv)
+    off2 = off1.copy()
+    moved = w.n_v - 1
+    off2[:, moved, 1] *= -1.0
+    band = np.arange(32, w.n_v)
+    # preconditions (float64, host): the band's flat rays climb and pass the one-crossing test
+    # with room to spare; the moved ray descends and still crosses the volume
+    V = w.views
+    src, ctr, du_v, dv_v = V[:, 0:3], V[:, 3:6], V[:, 6:9], V[:, 9:12]
+
+    def dirs(off):
+        pix = (ctr[:, None, None, :] + off[None, :, :, 0:1] * du_v[:, None, None, :]
+               + off[None, :, :, 1:2] * dv_v[:, None, None, :])
+        return pix - src[:, None, None, :]
+
+    d1, d2 = dirs(off1)[:, :, band], dirs(off2)[:, :, moved]
+    assert np.all(d1[..., 2] > 0) and np.all(d2[..., 2] < 0)
+    assert np.all(np.abs(d1[..., 2]) < 0.9 * np.maximum(np.abs(d1[..., 0]), np.abs(d1[..., 1])))
+    go = oracle.Geometry(w.beam, w.views, w.vol_shape, w.voxel_spacing, w.n_u, w.n_v, w.du, w.dv,
+                         offsets=off2)
+    L, _ = go.ray_lengths()
+    assert (L[:, :, moved] > 0).mean() > 0.5
+    g1 = ct.Geometry(w.beam, w.views, w.vol_shape, w.voxel_spacing, w.n_u, w.n_v, w.du, w.dv,
+                     offsets=off1)
+    g2 = ct.Geometry(w.beam, w.views, w.vol_shape, w.voxel_spacing, w.n_u, w.n_v, w.du, w.dv,
+                     offsets=off2)
+    assert g1.info.volume_layout == 1  # z fastest: z is the walk's inner axis
+    x = torch_cuda(w.phantom())
+    a, b = _cpu(g1.project(x)), _cpu(g2.project(x))
+    keep = np.ones(w.n_v, bool)
+    keep[moved] = False
+    assert np.count_nonzero(a[:, :, band[:-1]]) > 0.3 * a[:, :, band[:-1]].size
+    assert np.array_equal(a[:, :, keep], b[:, :, keep])
