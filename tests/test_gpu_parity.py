@@ -460,3 +460,51 @@ def test_walk_specialisation_changes_no_arithmetic(ct):
     keep[moved] = False
     assert np.count_nonzero(a[:, :, band[:-1]]) > 0.3 * a[:, :, band[:-1]].size
     assert np.array_equal(a[:, :, keep], b[:, :, keep])
+
+
+def _random_frames_2d(rng, n, beam):
+    views = []
+    for _ in range(n):
+        th = rng.uniform(0, 2 * math.pi)
+        u = np.array([-math.sin(th), math.cos(th)])
+        if beam == W.FAN2D:
+            r = rng.uniform(30, 60)
+            src = r * np.array([math.cos(th), math.sin(th)]) + rng.uniform(-2, 2, 2)
+            views.append(np.concatenate([src, -0.5 * src, u]))
+        else:
+            views.append(np.concatenate([[math.cos(th), math.sin(th)], rng.uniform(-1, 1, 2), u]))
+    return np.array(views)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_geometries_against_the_oracle(ct, seed):
+    """Random frames, volume shapes, per-axis pitches and detectors for the four beams: every
+    ray of A against the oracle and A^T in relative L2 (exercises the walk's specialised and
+    general forms in whatever mix the geometry gives)."""
+    rng = np.random.default_rng(1000 + seed)
+    beam = [W.CONE, W.PARALLEL3D, W.FAN2D, W.PARALLEL2D][seed % 4]
+    two_d = beam in (W.FAN2D, W.PARALLEL2D)
+    if two_d:
+        shape = (1, int(rng.integers(5, 40)), int(rng.integers(5, 40)))
+        sp = (float(rng.uniform(0.5, 1.5)), float(rng.uniform(0.5, 1.5)))  # (dy, dx)
+        views = _random_frames_2d(rng, 7, beam)
+        n_u, n_v = int(rng.integers(20, 90)), 1
+        du, dv = float(rng.uniform(0.3, 1.2)), 1.0
+    else:
+        shape = tuple(int(v) for v in rng.integers(4, 28, 3))
+        sp = tuple(float(v) for v in rng.uniform(0.5, 1.5, 3))
+        views = _random_frames(rng, 5, beam) * np.repeat([8.0, 8.0, 1.0, 1.0], 3)
+        n_u, n_v = int(rng.integers(20, 70)), int(rng.integers(20, 70))
+        du, dv = float(rng.uniform(0.2, 0.8)), float(rng.uniform(0.2, 0.8))
+    args = (beam, views, shape, sp, n_u, n_v, du, dv)
+    g, go = ct.Geometry(*args), oracle.Geometry(*args)
+    vol_shape = shape[1:] if two_d else shape
+    x = rng.uniform(0.0, 1.0, size=vol_shape).astype(np.float32)
+    y_gpu = _cpu(g.project(torch_cuda(x)))
+    y_or = go.project(x)
+    L, _ = go.ray_lengths()
+    assert (L > 0).mean() > 0.1
+    bad = fp_violations(y_gpu, y_or, L, float(x.max()))
+    assert bad.size == 0, bad[:10]
+    yy = rng.uniform(-1.0, 1.0, size=go.sino_shape).astype(np.float32)
+    assert rel_l2(_cpu(g.backproject(torch_cuda(yy))), go.backproject(yy)) <= BP_RTOL
