@@ -493,7 +493,10 @@ def test_random_geometries_against_the_oracle(ct, seed):
     else:
         shape = tuple(int(v) for v in rng.integers(4, 28, 3))
         sp = tuple(float(v) for v in rng.uniform(0.5, 1.5, 3))
-        views = _random_frames(rng, 5, beam) * np.repeat([8.0, 8.0, 1.0, 1.0], 3)
+        # positions scaled to the box size (the ray direction of a parallel beam stays a unit
+        # vector)
+        scale = [8.0, 8.0, 1.0, 1.0] if beam == W.CONE else [1.0, 8.0, 1.0, 1.0]
+        views = _random_frames(rng, 5, beam) * np.repeat(scale, 3)
         n_u, n_v = int(rng.integers(20, 70)), int(rng.integers(20, 70))
         du, dv = float(rng.uniform(0.2, 0.8)), float(rng.uniform(0.2, 0.8))
     args = (beam, views, shape, sp, n_u, n_v, du, dv)
