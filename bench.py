@@ -262,6 +262,10 @@ def profiled_sol(kernel: str, source: str = "siddon_kernels.cu"):
         out[key] = float(m.group(1)) if m else None
     m = re.search(r"\| duration \(sum over captured launches, serialised\) \| ([0-9.]+) ms", text)
     out["ms"] = float(m.group(1)) if m else None
+    m = re.search(r"\| L2 sector bandwidth \| ([0-9.]+) GB/s = ([0-9.]+) % of the L2 sector peak "
+                  r"\(([0-9.]+) GB/s\)", text)
+    out["l2_sector_gbs"] = float(m.group(1)) if m else None
+    out["l2_sector_peak_gbs"] = float(m.group(3)) if m else None
     return out
 
 
@@ -358,13 +362,19 @@ FDK_FLOPS_PER_VOXEL_VIEW = 38   # projection 23, distance weight 2, bilinear 11,
 FP32_LANES_PER_SM, N_SMS, SM_MAX_GHZ = 128, 148, 2.032
 
 
-def ncu_sol():
+def ncu_sol(U=None, fp_ms=None, bp_ms=None):
     """The pair's ncu-achieved memory fraction (max over L1/L2/DRAM of each walk kernel, weighted
-    by the kernels' durations in the same captures), from the committed profiles."""
+    by the kernels' durations in the same captures), from the committed profiles.  With the
+    update count U and the live CUDA-event times, also each walk's algorithmic L2 fraction:
+    4 B per ray-voxel update over its time, against ncu's L2 sector peak."""
     fp, bp = profiled_sol("project_kernel"), profiled_sol("backproject_kernel")
     if not fp or not bp or None in (fp["ms"], bp["ms"], fp["memory_sol_pct"],
                                     bp["memory_sol_pct"]):
         return None
+    if U is not None:
+        for d, ms in ((fp, fp_ms), (bp, bp_ms)):
+            if d.get("l2_sector_peak_gbs") and ms:
+                d["algorithmic_l2_frac"] = 4.0 * U / (ms * 1e-3) / 1e9 / d["l2_sector_peak_gbs"]
     pair = (fp["memory_sol_pct"] * fp["ms"] + bp["memory_sol_pct"] * bp["ms"]) / (fp["ms"] + bp["ms"])
     return {"project_kernel": fp, "backproject_kernel": bp,
             "pair_memory_sol_pct": pair,
@@ -631,7 +641,7 @@ def run_ours(args, rank, world):
         "e2e": {"value": world * 2 * U / (e2e_ms * 1e-3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "timing": "host wall clock around the steps, copies overlapped on a 2nd stream"},
-        "ncu_sol": ncu_sol(),
+        "ncu_sol": ncu_sol(U, fp_avg, bp_avg),
         "gpu_launches": 4 * args.steps,
         "clocks": clocks,
     }
