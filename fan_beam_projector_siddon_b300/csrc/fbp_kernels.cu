@@ -745,12 +745,48 @@ cudaError_t launch_filter(const FbpParams& p, const FbpCosine* cosines, const fl
     return cudaGetLastError();
 }
 
-// Views per gather/scatter pass: the pass's filtered slices fit in L2 together (about 48 MB),
-// so that all resident blocks touch the same views.
-int views_per_pass(const FbpParams& p) {
-    const size_t slice = sizeof(float) * (size_t)p.rows * (size_t)p.cols;
-    int per_pass = (int)std::min<size_t>((size_t)p.n_views, (48u << 20) / slice);
-    return per_pass < 16 ? 16 : per_pass / 16 * 16;
+// Views per gather or scatter pass: the pass's detector data (the filtered slices the gather
+// reads, or the parity copies the scatter adds into, four times larger) fit in L2 together
+// (about 48 MB), so that all resident blocks touch the same views and the scatter's reductions
+// stay in L2.  Multiples of `step`, at least `step`.
+int views_per_pass(const FbpParams& p, size_t bytes_per_view, int step) {
+    int per_pass = (int)std::min<size_t>((size_t)p.n_views, (48u << 20) / bytes_per_view);
+    return per_pass < step ? step : per_pass / step * step;
+}
+size_t gather_view_bytes(const FbpParams& p) {
+    return sizeof(float) * (size_t)p.rows * (size_t)p.cols;
+}
+size_t scatter_view_bytes(const FbpParams& p) {
+    return sizeof(float4) * 4 * (size_t)p.bu * (size_t)p.bv;  // four copies of 2 x 2 blocks
+}
+
+// The cone-beam scatter of vol into the parity copies, in view passes whose copies fit in L2.
+// Every pass reads the whole volume again, which is cheap only while the volume stays in L2
+// beside the copies; a larger volume takes passes of at least 16 views.
+cudaError_t launch_scatter_3d(const FbpParams& p, const FbpView* views, const float* vol,
+                              float* copies, cudaStream_t stream) {
+    if ((p.nx + 7) / 8 > 65535 || p.ny > 65535) return cudaErrorInvalidValue;
+    const size_t vol_bytes = sizeof(float) * (size_t)p.nx * (size_t)p.ny * (size_t)p.nz;
+    const int per_pass = views_per_pass(p, scatter_view_bytes(p), vol_bytes > (64u << 20) ? 16 : 4);
+    for (int k = 0; k < p.n_views; k += per_pass) {
+        const int k_end = std::min(p.n_views, k + per_pass);
+        if (p.nz >= 192) {
+            dim3 g((p.nz + 255) / 256, (p.nx + 7) / 8, p.ny);
+            fdk_scatter_kernel<8><<<g, 256, 0, stream>>>(p, views, vol, copies, k, k_end);
+        } else if (p.nz >= 96) {
+            dim3 g((p.nz + 127) / 128, (p.nx + 7) / 8, p.ny);
+            fdk_scatter_kernel<4><<<g, 256, 0, stream>>>(p, views, vol, copies, k, k_end);
+        } else if (p.nz >= 48) {
+            dim3 g((p.nz + 63) / 64, (p.nx + 7) / 8, p.ny);
+            fdk_scatter_kernel<2><<<g, 256, 0, stream>>>(p, views, vol, copies, k, k_end);
+        } else {
+            dim3 g((p.nz + 31) / 32, (p.nx + 7) / 8, p.ny);
+            fdk_scatter_kernel<1><<<g, 256, 0, stream>>>(p, views, vol, copies, k, k_end);
+        }
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t launch_prepare(const FbpParams& p, const double* raw, const float* user_weights,
@@ -788,7 +824,7 @@ cudaError_t launch_fbp(const FbpParams& p, const double* raw, const float* user_
         return cudaGetLastError();
     }
     if ((p.nx + 7) / 8 > 65535 || p.ny > 65535) return cudaErrorInvalidValue;
-    const int per_pass = views_per_pass(p);
+    const int per_pass = views_per_pass(p, gather_view_bytes(p), 16);
     for (int k = 0; k < p.n_views; k += per_pass) {
         const int k_end = std::min(p.n_views, k + per_pass);
         if (p.nz >= 192) {
@@ -938,26 +974,8 @@ cudaError_t launch_fbp_transpose(const FbpParams& p_in, const double* raw,
                 fbp2d_scatter_kernel<false, 1><<<g, 256, 0, stream>>>(p, views, vol, scattered);
         }
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    } else {
-        if ((p.nx + 7) / 8 > 65535 || p.ny > 65535) return cudaErrorInvalidValue;
-        const int per_pass = views_per_pass(p);
-        for (int k = 0; k < p.n_views; k += per_pass) {
-            const int k_end = std::min(p.n_views, k + per_pass);
-            if (p.nz >= 192) {
-                dim3 g((p.nz + 255) / 256, (p.nx + 7) / 8, p.ny);
-                fdk_scatter_kernel<8><<<g, 256, 0, stream>>>(p, views, vol, scattered, k, k_end);
-            } else if (p.nz >= 96) {
-                dim3 g((p.nz + 127) / 128, (p.nx + 7) / 8, p.ny);
-                fdk_scatter_kernel<4><<<g, 256, 0, stream>>>(p, views, vol, scattered, k, k_end);
-            } else if (p.nz >= 48) {
-                dim3 g((p.nz + 63) / 64, (p.nx + 7) / 8, p.ny);
-                fdk_scatter_kernel<2><<<g, 256, 0, stream>>>(p, views, vol, scattered, k, k_end);
-            } else {
-                dim3 g((p.nz + 31) / 32, (p.nx + 7) / 8, p.ny);
-                fdk_scatter_kernel<1><<<g, 256, 0, stream>>>(p, views, vol, scattered, k, k_end);
-            }
-            if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        }
+    } else if ((e = launch_scatter_3d(p, views, vol, scattered, stream)) != cudaSuccess) {
+        return e;
     }
     return launch_filter<true>(p, cosines, taps, scattered, sino, stream);
 }
@@ -985,11 +1003,8 @@ cudaError_t launch_fbp_gradients(const FbpParams& p_in, const double* raw,
         else
             fbp2d_scatter_kernel<false, 1><<<g, 256, 0, stream>>>(pu, views, grad_vol, copies);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    } else {
-        if ((pu.nx + 7) / 8 > 65535 || pu.ny > 65535) return cudaErrorInvalidValue;
-        dim3 g((pu.nz + 31) / 32, (pu.nx + 7) / 8, pu.ny);
-        fdk_scatter_kernel<1><<<g, 256, 0, stream>>>(pu, views, grad_vol, copies, 0, pu.n_views);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    } else if ((e = launch_scatter_3d(pu, views, grad_vol, copies, stream)) != cudaSuccess) {
+        return e;
     }
     // (2) dL/dw: the filtered sinogram (forward filter) against the scatter
     if (grad_view_weights != nullptr) {
