@@ -888,49 +888,98 @@ __global__ void __launch_bounds__(256) fbp_weight_grad_kernel(FbpParams p,
     if (threadIdx.x == 0) grad_w[view] = (float)part[0];
 }
 
-// dL/dkernel[d + n_u - 1] = sum_k w_k sum_v sum_i (G_k^T grad)[i][v] q_k[i - d][v], q the
-// pre-weighted sinogram.  One block per (view, tile of tv columns): the tile's scatter values and
-// pre-weighted columns (zero-padded by n_u - 1 on both sides) in shared memory, one tap offset d
-// per thread and step, float64 block sums added to `acc`.
-__global__ void __launch_bounds__(256) fbp_kernel_grad_kernel(
-    FbpParams p, const FbpView* __restrict__ views, const FbpCosine* __restrict__ cosines,
-    const float* __restrict__ view_weights, const float* __restrict__ sino,
-    const float* __restrict__ copies, int tv, int v_blocks, double* __restrict__ acc) {
-    extern __shared__ float sm2[];
-    const int n_u = p.n_u, V = p.two_d ? 1 : p.n_v;
-    const int wpad = 3 * n_u - 2;        // padded column length
-    float* G = sm2;                      // [tv][n_u]
-    float* P = sm2 + (int64_t)tv * n_u;  // [tv][3 n_u - 2], P[j][x] = q[x - (n_u - 1)]
-    const int view = blockIdx.x / v_blocks;
-    const int v0 = (blockIdx.x - view * v_blocks) * tv;
-    const int nv = min(tv, V - v0);
-    const FbpCosine C = cosines[view];
-    for (int i = threadIdx.x; i < tv * n_u; i += blockDim.x) {
-        const int j = i / n_u, iu = i - j * n_u;
-        G[i] = j < nv ? copies_at(p, copies, view, iu + 1, v0 + j + 1) : 0.0f;
+// Operands of the filter-kernel gradient as row-major arrays over rows r = view * V + v (V = 1 in
+// 2D): G[r][u] = w_view (G_k^T grad)[u][v], the scatter summed over the parity copies and scaled
+// by the view weight; Q[r][u] = the cosine- and pixel-weighted sinogram.  Then
+// dL/dk[d + n_u - 1] = sum_k w_k sum_v sum_i g[i] q[i - d] = sum_{i - j = d} M[i][j] with
+// M = G^T Q: a dense contraction over the rows followed by the diagonal sums of M.
+__global__ void fbp_grad_lhs_kernel(FbpParams p, const float* __restrict__ view_weights,
+                                    const float* __restrict__ copies, float* __restrict__ G) {
+    const int V = p.two_d ? 1 : p.n_v;
+    const int64_t n = (int64_t)p.n_views * V * p.n_u;
+    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < n;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = e / p.n_u;
+        const int u = (int)(e - r * p.n_u);
+        const int view = (int)(r / V), v = (int)(r - (int64_t)view * V);
+        const float w = view_weights ? view_weights[view] : 3.14159265358979323846f / p.n_views;
+        G[e] = w * copies_at(p, copies, view, u + 1, v + 1);
     }
-    for (int i = threadIdx.x; i < tv * wpad; i += blockDim.x) {
-        const int j = i / wpad, x = i - j * wpad, iu = x - (n_u - 1);
-        float val = 0.0f;
-        if (j < nv && iu >= 0 && iu < n_u) {
-            val = sino[((int64_t)view * n_u + iu) * V + v0 + j];
-            if (!p.parallel) val *= cosine_weight(C, iu, v0 + j);
-            if (p.pixel_weights) val *= p.pixel_weights[(int64_t)view * n_u + iu];
+}
+
+__global__ void fbp_grad_rhs_kernel(FbpParams p, const FbpCosine* __restrict__ cosines,
+                                    const float* __restrict__ sino, float* __restrict__ Q) {
+    const int V = p.two_d ? 1 : p.n_v;
+    const int64_t n = (int64_t)p.n_views * V * p.n_u;
+    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < n;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = e / p.n_u;
+        const int u = (int)(e - r * p.n_u);
+        const int view = (int)(r / V), v = (int)(r - (int64_t)view * V);
+        float val = sino[((int64_t)view * p.n_u + u) * V + v];
+        if (!p.parallel) val *= cosine_weight(cosines[view], u, v);
+        if (p.pixel_weights) val *= p.pixel_weights[(int64_t)view * p.n_u + u];
+        Q[e] = val;
+    }
+}
+
+// One 64 x 64 tile (i, j) of M = G^T Q over one chunk of rows: 16-row steps staged in shared
+// memory, 4 x 4 outputs per thread in registers (float32 sums over the chunk), then the tile's
+// 127 diagonals summed in shared memory and added into acc[i - j + n_u - 1] in float64.
+constexpr int kGT = 64, kGK = 16;
+
+__global__ void __launch_bounds__(256) fbp_kernel_grad_gemm_kernel(
+    const float* __restrict__ G, const float* __restrict__ Q, int n_u, int64_t rows,
+    int rows_per_chunk, double* __restrict__ acc) {
+    __shared__ __align__(16) float As[kGK][kGT];
+    __shared__ __align__(16) float Bs[kGK][kGT];
+    __shared__ float diag[2 * kGT - 1];
+    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+    const int i0 = blockIdx.x * kGT, j0 = blockIdx.y * kGT;
+    const int64_t r_begin = (int64_t)blockIdx.z * rows_per_chunk;
+    const int64_t r_end = r_begin + rows_per_chunk < rows ? r_begin + rows_per_chunk : rows;
+    float c[4][4];
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) c[x][y] = 0.0f;
+    for (int64_t r0 = r_begin; r0 < r_end; r0 += kGK) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int idx = tid + 256 * e;
+            const int k = idx >> 6, col = idx & (kGT - 1);
+            const int64_t r = r0 + k;
+            const bool ok = r < r_end;
+            As[k][col] = (ok && i0 + col < n_u) ? __ldg(G + r * n_u + i0 + col) : 0.0f;
+            Bs[k][col] = (ok && j0 + col < n_u) ? __ldg(Q + r * n_u + j0 + col) : 0.0f;
         }
-        P[i] = val;
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < kGK; ++k) {
+            const float4 a = *reinterpret_cast<const float4*>(&As[k][ty * 4]);
+            const float4 b = *reinterpret_cast<const float4*>(&Bs[k][tx * 4]);
+            const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+#pragma unroll
+                for (int y = 0; y < 4; ++y) c[x][y] = fmaf(av[x], bv[y], c[x][y]);
+        }
+        __syncthreads();
     }
+    for (int t = tid; t < 2 * kGT - 1; t += 256) diag[t] = 0.0f;
     __syncthreads();
-    const double w = view_weights ? (double)view_weights[view]
-                                  : 3.14159265358979323846 / p.n_views;
-    for (int t = threadIdx.x; t < 2 * n_u - 1; t += blockDim.x) {
-        const int d = t - (n_u - 1);
-        float s = 0.0f;
-        for (int j = 0; j < nv; ++j) {
-            const float* g = G + j * n_u;
-            const float* q = P + j * wpad + (n_u - 1) - d;  // q[i] = column value at i - d
-            for (int i = 0; i < n_u; ++i) s = fmaf(g[i], q[i], s);
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+            const int li = ty * 4 + x, lj = tx * 4 + y;
+            if (i0 + li < n_u && j0 + lj < n_u) atomicAdd(&diag[li - lj + kGT - 1], c[x][y]);
         }
-        atomicAdd(acc + t, w * (double)s);
+    __syncthreads();
+    for (int t = tid; t < 2 * kGT - 1; t += 256) {
+        const int d = i0 - j0 + t - (kGT - 1);  // i - j
+        if (d > -n_u && d < n_u && diag[t] != 0.0f)
+            atomicAdd(acc + d + n_u - 1, (double)diag[t]);
     }
 }
 
@@ -1014,25 +1063,33 @@ cudaError_t launch_fbp_gradients(const FbpParams& p_in, const double* raw,
                                                                 grad_view_weights);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    // (3) dL/dkernel: correlation of the scatter with the pre-weighted sinogram
+    // (3) dL/dkernel: the diagonal sums of G^T Q.  G goes into the filtered buffer (free after
+    // step 2), Q into the parity copies (free once G is built); same stream, so in order.
     if (grad_kernel != nullptr) {
         const int n_u = pu.n_u, V = pu.two_d ? 1 : pu.n_v;
-        const size_t per_col = sizeof(float) * ((size_t)n_u + 3 * (size_t)n_u - 2);
-        int tv = 32;
-        while (tv > 1 && tv * per_col > kSmemBudget) tv >>= 1;
-        if (tv > V) tv = V;
-        if (tv * per_col > kSmemBudget) return cudaErrorInvalidValue;
-        const size_t smem = tv * per_col;
-        e = cudaFuncSetAttribute(fbp_kernel_grad_kernel,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        const int v_blocks = (V + tv - 1) / tv;
-        if ((int64_t)v_blocks * pu.n_views > (int64_t)INT32_MAX) return cudaErrorInvalidValue;
+        const int64_t rows = (int64_t)pu.n_views * V;
+        float* G = filtered;
+        float* Q = copies;
+        const int64_t n = rows * n_u;
+        const int eb = (int)std::min<int64_t>((n + 255) / 256, 148 * 32);
+        fbp_grad_lhs_kernel<<<eb, 256, 0, stream>>>(pu, user_weights, copies, G);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        fbp_grad_rhs_kernel<<<eb, 256, 0, stream>>>(pu, cosines, sino, Q);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
         if ((e = cudaMemsetAsync(acc, 0, sizeof(double) * (size_t)(2 * n_u - 1), stream)) !=
             cudaSuccess)
             return e;
-        fbp_kernel_grad_kernel<<<v_blocks * pu.n_views, 256, smem, stream>>>(
-            pu, views, cosines, user_weights, sino, copies, tv, v_blocks, acc);
+        // enough row chunks for ~4096 blocks, each at least 256 rows, at most 65535 chunks
+        const int64_t tiles = (int64_t)((n_u + kGT - 1) / kGT) * ((n_u + kGT - 1) / kGT);
+        int64_t chunk = rows * tiles / 4096;
+        chunk = std::max<int64_t>(chunk, 256);
+        chunk = std::max<int64_t>(chunk, (rows + 65534) / 65535);
+        chunk = (chunk + kGK - 1) / kGK * kGK;
+        if (chunk > INT32_MAX) return cudaErrorInvalidValue;
+        const dim3 g((n_u + kGT - 1) / kGT, (n_u + kGT - 1) / kGT,
+                     (unsigned)((rows + chunk - 1) / chunk));
+        if (g.y > 65535) return cudaErrorInvalidValue;
+        fbp_kernel_grad_gemm_kernel<<<g, 256, 0, stream>>>(G, Q, n_u, rows, (int)chunk, acc);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         fbp_finish_kernel_grad<<<(2 * n_u - 1 + 255) / 256, 256, 0, stream>>>(acc, grad_kernel,
                                                                               2 * n_u - 1);
