@@ -112,3 +112,25 @@ def test_profile_figures_parse_or_are_withheld():
         lo = min(pair["project_kernel"]["memory_sol_pct"], pair["backproject_kernel"]["memory_sol_pct"])
         hi = max(pair["project_kernel"]["memory_sol_pct"], pair["backproject_kernel"]["memory_sol_pct"])
         assert lo <= pair["pair_memory_sol_pct"] <= hi
+
+
+def test_l2_figures_of_the_walk_profiles():
+    """The L2 sector bandwidth parsed from the committed walk summaries agrees with the row's
+    own percentage of the L2 sector peak, and the algorithmic L2 fraction is a fraction that
+    halves when the time doubles."""
+    import re
+    import bench
+    U = 18315651008
+    pair = bench.ncu_sol(U, 16.3, 17.5)
+    if pair is None:
+        pytest.skip("walk summaries do not match the current kernel source")
+    for name in ("project_kernel", "backproject_kernel"):
+        d = pair[name]
+        text = open(os.path.join(bench.ROOT, d["source"])).read()
+        pct = float(re.search(r"= ([0-9.]+) % of the L2 sector peak", text).group(1))
+        assert 0 < d["l2_sector_gbs"] < d["l2_sector_peak_gbs"]
+        assert abs(100 * d["l2_sector_gbs"] / d["l2_sector_peak_gbs"] - pct) < 0.1
+        assert 0 < d["algorithmic_l2_frac"] < 1
+    slow = bench.ncu_sol(U, 32.6, 35.0)
+    for name in ("project_kernel", "backproject_kernel"):
+        assert abs(slow[name]["algorithmic_l2_frac"] * 2 - pair[name]["algorithmic_l2_frac"]) < 1e-12
