@@ -366,8 +366,9 @@ CT_API ct_status ct_fbp_transpose(const ct_geometry *geom, const float *d_volume
  *     dL/dk[d + n_u - 1] = sum_k w_k sum_v sum_i (G_k^T grad)(u_i, v) q_k(u_{i - d}, v).
  * d_grad_kernel (device, 2 n_u - 1 floats) and d_grad_view_weights (device, n_views floats) are
  * overwritten; either may be NULL, not both.  Workspace: ct_fbp_gradients_workspace_bytes(geom).
- * Float64 sums; the kernel gradient adds per-block float64 partial sums atomically (run-to-run
- * differences in the last bits).  Errors as for ct_fbp.
+ * The kernel gradient sums float32 partials (one block's tile of the products over a chunk of
+ * views) into float64 with atomic adds, so results differ run to run in the last bits.  Errors
+ * as for ct_fbp.
  */
 CT_API size_t ct_fbp_gradients_workspace_bytes(const ct_geometry *geom);
 CT_API ct_status ct_fbp_gradients(const ct_geometry *geom, const float *d_sino,
