@@ -42,10 +42,8 @@ CONFIG_ID = 3
 # units of work
 # ----------------------------------------------------------------------------------------------
 
-def count_updates(w: W.Workload, views=None) -> int:
-    """Ray-voxel segments walked by one pass: per ray that meets the box, 1 + the number of
-    interior cell planes it crosses (float64, vectorised per view).  Independent of both the
-    CUDA path and the oracle."""
+def _count_view(w: W.Workload, k: int) -> int:
+    """Ray-voxel segments of view k (see count_updates)."""
     nz, ny, nx = w.vol_shape
     s = w.voxel_spacing
     dims = 2 if w.is_2d else 3
@@ -54,47 +52,56 @@ def count_updates(w: W.Workload, views=None) -> int:
     uu = (np.arange(w.n_u) - (w.n_u - 1) / 2.0) * w.du
     vv = (np.arange(w.n_v) - (w.n_v - 1) / 2.0) * w.dv if not w.is_2d else np.zeros(1)
     parallel = w.beam in (W.PARALLEL2D, W.PARALLEL3D)
-    total = 0
-    view_ids = range(w.n_views) if views is None else views
-    for k in view_ids:
-        r = w.views[k]
-        if w.is_2d:
-            first, ctr, du = r[0:2], r[2:4], r[4:6]
-            dv = np.zeros(2)
-        else:
-            first, ctr, du, dv = r[0:3], r[3:6], r[6:9], r[9:12]
-        pix = ctr + uu[:, None, None] * du + vv[None, :, None] * dv      # (U, V, dims)
-        if parallel:
-            e = pix
-            d = np.broadcast_to(first, pix.shape)
-            amin = np.full(pix.shape[:2], -np.inf)
-            amax = np.full(pix.shape[:2], np.inf)
-        else:
-            e = np.broadcast_to(first, pix.shape)
-            d = pix - first
-            amin = np.zeros(pix.shape[:2])
-            amax = np.ones(pix.shape[:2])
-        ok = np.ones(pix.shape[:2], dtype=bool)
-        with np.errstate(divide="ignore", invalid="ignore"):
-            for a in range(dims):
-                da, ea = d[..., a], e[..., a]
-                nzd = da != 0
-                t1 = np.where(nzd, (-half[a] - ea) / np.where(nzd, da, 1), -np.inf)
-                t2 = np.where(nzd, (half[a] - ea) / np.where(nzd, da, 1), np.inf)
-                amin = np.maximum(amin, np.minimum(t1, t2))
-                amax = np.minimum(amax, np.maximum(t1, t2))
-                ok &= nzd | ((ea >= -half[a]) & (ea < half[a]))
-        hit = ok & (amax > amin)
-        segs = np.where(hit, 1, 0).astype(np.int64)
+    r = w.views[k]
+    if w.is_2d:
+        first, ctr, du = r[0:2], r[2:4], r[4:6]
+        dv = np.zeros(2)
+    else:
+        first, ctr, du, dv = r[0:3], r[3:6], r[6:9], r[9:12]
+    pix = ctr + uu[:, None, None] * du + vv[None, :, None] * dv      # (U, V, dims)
+    if parallel:
+        e = pix
+        d = np.broadcast_to(first, pix.shape)
+        amin = np.full(pix.shape[:2], -np.inf)
+        amax = np.full(pix.shape[:2], np.inf)
+    else:
+        e = np.broadcast_to(first, pix.shape)
+        d = pix - first
+        amin = np.zeros(pix.shape[:2])
+        amax = np.ones(pix.shape[:2])
+    ok = np.ones(pix.shape[:2], dtype=bool)
+    with np.errstate(divide="ignore", invalid="ignore"):
         for a in range(dims):
-            ci = (e[..., a] + np.where(hit, amin, 0) * d[..., a] + half[a]) / s
-            co = (e[..., a] + np.where(hit, amax, 0) * d[..., a] + half[a]) / s
-            lo, hi = np.minimum(ci, co), np.maximum(ci, co)
-            first_plane = np.maximum(np.floor(lo) + 1, 1)
-            last_plane = np.minimum(np.ceil(hi) - 1, ncell[a] - 1)
-            segs += np.where(hit, np.maximum(0, last_plane - first_plane + 1), 0).astype(np.int64)
-        total += int(segs.sum())
-    return total
+            da, ea = d[..., a], e[..., a]
+            nzd = da != 0
+            t1 = np.where(nzd, (-half[a] - ea) / np.where(nzd, da, 1), -np.inf)
+            t2 = np.where(nzd, (half[a] - ea) / np.where(nzd, da, 1), np.inf)
+            amin = np.maximum(amin, np.minimum(t1, t2))
+            amax = np.minimum(amax, np.maximum(t1, t2))
+            ok &= nzd | ((ea >= -half[a]) & (ea < half[a]))
+    hit = ok & (amax > amin)
+    segs = np.where(hit, 1, 0).astype(np.int64)
+    for a in range(dims):
+        ci = (e[..., a] + np.where(hit, amin, 0) * d[..., a] + half[a]) / s
+        co = (e[..., a] + np.where(hit, amax, 0) * d[..., a] + half[a]) / s
+        lo, hi = np.minimum(ci, co), np.maximum(ci, co)
+        first_plane = np.maximum(np.floor(lo) + 1, 1)
+        last_plane = np.minimum(np.ceil(hi) - 1, ncell[a] - 1)
+        segs += np.where(hit, np.maximum(0, last_plane - first_plane + 1), 0).astype(np.int64)
+    return int(segs.sum())
+
+
+def count_updates(w: W.Workload, views=None, threads: int | None = None) -> int:
+    """Ray-voxel segments walked by one pass: per ray that meets the box, 1 + the number of
+    interior cell planes it crosses (float64, vectorised per view, views on a thread pool).
+    Independent of both the CUDA path and the oracle."""
+    import concurrent.futures as cf
+    view_ids = list(range(w.n_views) if views is None else views)
+    threads = threads or min(16, os.cpu_count() or 1)
+    if threads <= 1 or len(view_ids) < 4:
+        return sum(_count_view(w, k) for k in view_ids)
+    with cf.ThreadPoolExecutor(threads) as ex:
+        return sum(ex.map(lambda k: _count_view(w, k), view_ids))
 
 
 # ----------------------------------------------------------------------------------------------
@@ -278,6 +285,16 @@ def load_peaks():
     return 6400.0, "fallback"
 
 
+def measured_sm_max_mhz():
+    """The SM clock limit recorded beside the measured peaks, or None."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            v = json.load(f).get("sm_max_mhz")
+        return float(v) if v else None
+    return None
+
+
 def sirt_leg(ct, torch, n_iters: int = 10):
     """SIRT on the dual-axis tilt-series workload (512^3, 280 parallel3d views, 512x512 detector),
     the configuration the pages quote SIRT timings on: n_iters iterations from zero, timed with
@@ -359,36 +376,38 @@ def batch_leg(ct, torch, w, U, nb: int = 4, reps: int = 3):
 
 
 FDK_FLOPS_PER_VOXEL_VIEW = 38   # projection 23, distance weight 2, bilinear 11, accumulate 2
-FP32_LANES_PER_SM, N_SMS, SM_MAX_GHZ = 128, 148, 2.032
+FDK_L1_BYTES_PER_VOXEL_VIEW = 16  # the four bilinear taps of the filtered sinogram (L1-served)
+FP32_LANES_PER_SM = 128
 
 
-def ncu_sol(U=None, fp_ms=None, bp_ms=None):
-    """The pair's ncu-achieved memory fraction (max over L1/L2/DRAM of each walk kernel, weighted
-    by the kernels' durations in the same captures), from the committed profiles.  With the
-    update count U and the live CUDA-event times, also each walk's algorithmic L2 fraction:
-    4 B per ray-voxel update over its time, against ncu's L2 sector peak."""
+def ncu_sol():
+    """Figures COPIED from the committed ncu summaries under profiles/ (hand-kept notes of
+    earlier captures of the same kernel source; not measured in this run): per walk kernel the
+    ncu memory SOL, L1TEX, L2 and DRAM throughput percentages, and the pair's L2-only and
+    memory-SOL fractions weighted by the captured durations.  None when a summary is missing or
+    its recorded source hash differs from the current kernel source."""
     fp, bp = profiled_sol("project_kernel"), profiled_sol("backproject_kernel")
     if not fp or not bp or None in (fp["ms"], bp["ms"], fp["memory_sol_pct"],
-                                    bp["memory_sol_pct"]):
+                                    bp["memory_sol_pct"], fp["l2_pct"], bp["l2_pct"]):
         return None
-    if U is not None:
-        for d, ms in ((fp, fp_ms), (bp, bp_ms)):
-            if d.get("l2_sector_peak_gbs") and ms:
-                d["algorithmic_l2_frac"] = 4.0 * U / (ms * 1e-3) / 1e9 / d["l2_sector_peak_gbs"]
-    pair = (fp["memory_sol_pct"] * fp["ms"] + bp["memory_sol_pct"] * bp["ms"]) / (fp["ms"] + bp["ms"])
-    return {"project_kernel": fp, "backproject_kernel": bp,
-            "pair_memory_sol_pct": pair,
-            "note": "percent of ncu's own peaks; the forward walk is latency-bound (long "
-                    "scoreboard), the backprojection L1TEX-bound (see profiles/)"}
+    tot = fp["ms"] + bp["ms"]
+    return {"source": "copied from committed profiles/*.md (not measured in this run)",
+            "project_kernel": fp, "backproject_kernel": bp,
+            "pair_l2_throughput_pct": (fp["l2_pct"] * fp["ms"] + bp["l2_pct"] * bp["ms"]) / tot,
+            "pair_memory_sol_pct":
+                (fp["memory_sol_pct"] * fp["ms"] + bp["memory_sol_pct"] * bp["ms"]) / tot,
+            "note": "percent of ncu's own peaks; memory SOL is the max over L1TEX/L2/DRAM, "
+                    "the L2-only figure is lts__throughput"}
 
 
-def fdk_leg(ct, torch, w, reps: int = 5, cpu_baseline: bool = True):
+def fdk_leg(ct, torch, w, peaks, sm_mhz, reps: int = 5, cpu_baseline: bool = True):
     """Filtered backprojection (FDK, Ram-Lak window) of the metric workload's geometry and its
     transpose, CUDA events around each C-ABI call, L2 flushed before each.  Rate in voxel-view
-    updates per second.  The roofline reported is the float32 ALU one: 38 algorithmic flops per
-    voxel-view against 148 SMs x 128 lanes x 2 flops x 2.032 GHz.  The gather kernel's binding
-    limit is L1TEX throughput (its bilinear sinogram reads); `ncu` carries those figures from the
-    committed profile."""
+    updates per second.  Roofline: the gather kernel, which dominates the call, is bound by
+    L1TEX throughput (its bilinear reads of the filtered sinogram hit L1), so the call's
+    16 B of bilinear taps per voxel-view are set against the measured L1 read rate; the float32
+    ALU fraction (38 flops per voxel-view against SMs x 128 lanes x 2 flops x the SM clock
+    sampled in this run) is reported beside it."""
     g = ct.Geometry.from_workload(w)
     sino = torch.from_numpy(W.random_sinogram(w, 11)).cuda()
     vol = torch.empty(g.volume_shape, device="cuda")
@@ -415,20 +434,28 @@ def fdk_leg(ct, torch, w, reps: int = 5, cpu_baseline: bool = True):
             tr.append(e[2].elapsed_time(e[3]))
     fms, tms = statistics.median(fw), statistics.median(tr)
     vv = w.n_voxels * w.n_views
-    peak = N_SMS * FP32_LANES_PER_SM * 2 * SM_MAX_GHZ * 1e9 / 1e12
-    achieved = FDK_FLOPS_PER_VOXEL_VIEW * vv / (fms * 1e-3) / 1e12
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    alu_peak = sms * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12 if sm_mhz else float("nan")
+    alu = FDK_FLOPS_PER_VOXEL_VIEW * vv / (fms * 1e-3) / 1e12
+    l1 = FDK_L1_BYTES_PER_VOXEL_VIEW * vv / (fms * 1e-3) / 1e9
     out = {"workload": w.name, "window": "ram-lak", "fdk_ms": fms, "transpose_ms": tms,
            "voxel_views": vv, "voxel_views_per_s": vv / (fms * 1e-3),
            "transpose_voxel_views_per_s": vv / (tms * 1e-3),
-           "roofline": {"bound": "alu", "kernel": "ct_fbp (gather ~87% of it)",
-                        "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                        "frac": achieved / peak,
-                        "peak_source": "derived: 148 SMs x 128 fp32 lanes x 2 x 2.032 GHz",
-                        "flops_model": "38 flops per voxel-view"}}
+           "roofline": {"bound": "l1", "kernel": "ct_fbp (the gather dominates it)",
+                        "achieved": l1, "peak": peaks["l1_read_gbs"], "unit": "GB/s",
+                        "frac": l1 / peaks["l1_read_gbs"],
+                        "peak_source": "measured in this run: L1-hitting 16-B read probe",
+                        "bytes_model": "16 B of bilinear taps per voxel-view",
+                        "alu": {"achieved_tflops": alu, "peak_tflops": alu_peak,
+                                "frac": alu / alu_peak,
+                                "peak_source": f"{sms} SMs x 128 fp32 lanes x 2 x {sm_mhz} MHz "
+                                               "(median SM clock sampled in this run)",
+                                "flops_model": "38 flops per voxel-view"}}}
     traffic, src = profiled_traffic("fdk_gather_kernel", "fbp_kernels.cu")
     out["roofline"]["traffic"] = traffic
     out["roofline"]["traffic_source"] = src
-    out["roofline"]["ncu"] = profiled_sol("fdk_gather_kernel", "fbp_kernels.cu")
+    out["roofline"]["ncu_from_committed_profiles"] = profiled_sol("fdk_gather_kernel",
+                                                                  "fbp_kernels.cu")
     del sino, vol, ws, ws_t, out_t, flush
     torch.cuda.empty_cache()
     if cpu_baseline:
@@ -489,6 +516,125 @@ def context_leg(ct, torch):
             "pages_a100_ms": {"fp": 566.79, "bp": 1060.77, "cgls_iteration": 1753.73},
             "note": "context only: the pages' figures are diffct on one A100 with unstated "
                     "sid/sdd; not the same measurement"}
+
+
+L2_PROBE_BYTES = 64 << 20   # fits the 126 MB L2 (about the cone workload's volume)
+
+
+def l2_peaks(ct, torch, reps: int = 5):
+    """Measured on-chip rates on this GPU with the library's probe kernels (CUDA events on the
+    launching stream, best of `reps` after a warm-up; the 64 MiB buffer stays in L2):
+    16-byte L1-bypassing reads, 16-byte L1-hitting reads (every block re-reading 16 KB), and
+    red.global.add.f32 with 8 and 4 updates per 32-byte sector (warp lanes 1 and 2 floats
+    apart)."""
+    n = L2_PROBE_BYTES // 4
+    buf = torch.zeros(n, dtype=torch.float32, device="cuda")
+    sink = torch.zeros(1, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+
+    def best(fn):
+        fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b) * 1e-3)
+        return min(ts)
+
+    passes_r = 40
+    t = best(lambda: ct.ct_probe_l2_read(buf.data_ptr(), n, passes_r, sink.data_ptr(), sp))
+    read_gbs = 16 * (n // 4) * passes_r / t / 1e9
+    out = {"read_gbs": read_gbs, "buffer_bytes": L2_PROBE_BYTES,
+           "how": "ct_probe_l2_read / ct_probe_l2_reduce on a 64 MiB L2-resident buffer, CUDA "
+                  "events, best of %d" % reps}
+    n1, passes_1 = 4096, 4000         # 16 KB per block, re-read: L1 hits after the first pass
+    t = best(lambda: ct.ct_probe_l1_read(buf.data_ptr(), n1, passes_1, sink.data_ptr(), sp))
+    blocks = 4 * torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    out["l1_read_gbs"] = blocks * 16 * (n1 // 4) * passes_1 / t / 1e9
+    passes_a = 8
+    for stride in (1, 2):
+        t = best(lambda: ct.ct_probe_l2_reduce(buf.data_ptr(), n, passes_a, stride, sp))
+        upd = 32 * (n // (32 * stride)) * passes_a / t
+        out[f"red_stride{stride}_updates_per_s"] = upd
+        out[f"red_stride{stride}_gbs"] = 4 * upd / 1e9
+    del buf, sink
+    torch.cuda.empty_cache()
+    return out
+
+
+def walk_roofline(U, fp_ms, bp_ms, peaks):
+    """Each walk's algorithmic L2 fraction: 4 B per ray-voxel update over its CUDA-event time,
+    against the measured L2 rate of its access pattern (gathers: the read probe; reductions: the
+    red.global.add.f32 probe with full sectors)."""
+    fp_gbs = 4.0 * U / (fp_ms * 1e-3) / 1e9
+    bp_gbs = 4.0 * U / (bp_ms * 1e-3) / 1e9
+    return {"fp": {"achieved_gbs": fp_gbs, "peak_gbs": peaks["read_gbs"],
+                   "frac": fp_gbs / peaks["read_gbs"]},
+            "bp": {"achieved_gbs": bp_gbs, "peak_gbs": peaks["red_stride1_gbs"],
+                   "frac": bp_gbs / peaks["red_stride1_gbs"],
+                   "frac_vs_4_per_sector": bp_gbs / peaks["red_stride2_gbs"]}}
+
+
+def workload_leg(ct, torch, n: int, peaks, cpu_baseline: bool, reps: int = 3):
+    """FP and BP of workload n through the C ABI (CUDA events on the launching stream, L2 flushed
+    before each call, median of `reps` after one warm-up), views/s, ray-voxel updates/s, the
+    algorithmic L2 fractions, and the float64 oracle on the host cores over evenly spaced views
+    (the whole workload when it has at most 16 views' worth of work, else extrapolated)."""
+    w = W.config(n)
+    x_host = w.phantom()
+    U = count_updates(w)
+    g = ct.Geometry.from_workload(w)
+    vol = torch.from_numpy(x_host).cuda()
+    meas = torch.from_numpy(W.random_sinogram(w, 3)).cuda()
+    sino = torch.empty(w.sino_shape, dtype=torch.float32, device="cuda")
+    back = torch.empty(w.volume_shape, dtype=torch.float32, device="cuda")
+    ws = g.new_workspace()
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    fps, bps = [], []
+    for k in range(reps + 1):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        flush.zero_()
+        e[0].record(stream)
+        g.project(vol, out=sino, workspace=ws)
+        e[1].record(stream)
+        flush.zero_()
+        e[2].record(stream)
+        g.backproject(meas, out=back, workspace=ws)
+        e[3].record(stream)
+        torch.cuda.synchronize()
+        if k:
+            fps.append(e[0].elapsed_time(e[1]))
+            bps.append(e[2].elapsed_time(e[3]))
+    fp, bp = statistics.median(fps), statistics.median(bps)
+    del vol, meas, sino, back, ws, flush
+    torch.cuda.empty_cache()
+    out = {"workload": w.name, "volume": list(w.vol_shape), "views": w.n_views,
+           "detector": [w.n_u, w.n_v], "updates_per_pass": U, "fp_ms": fp, "bp_ms": bp,
+           "views_per_s": {"fp": w.n_views / (fp * 1e-3), "bp": w.n_views / (bp * 1e-3)},
+           "fp_updates_per_s": U / (fp * 1e-3), "bp_updates_per_s": U / (bp * 1e-3),
+           "pair_updates_per_s": 2 * U / ((fp + bp) * 1e-3),
+           "l2_roofline": walk_roofline(U, fp, bp, peaks),
+           "volume_bytes": 4 * w.n_voxels,
+           "volume_fits_l2": 4 * w.n_voxels <= L2_PROBE_BYTES * 2}
+    if cpu_baseline:
+        cores = os.cpu_count() or 1
+        n_views = w.n_views if 2 * U <= 4e9 else min(w.n_views, 16)
+        r, dt, nu = oracle_sample_rate(w, x_host, n_views, cores)
+        whole = n_views == w.n_views
+        out["cpu_baseline"] = {
+            "value": r, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": (f"FP+BP of all {w.n_views} views ({nu} updates, {dt:.1f} s)" if whole else
+                       f"FP+BP of {n_views} evenly spaced views of {w.n_views} ({nu} updates, "
+                       f"{dt:.1f} s); whole-workload time extrapolated linearly: "
+                       f"{dt * 2 * U / nu:.0f} s"),
+            "extrapolated": not whole}
+    return out
 
 
 def run_ours(args, rank, world):
@@ -609,16 +755,13 @@ def run_ours(args, rank, world):
 
     if rank != 0:
         return 0
-    # ---- roofline of the dominant kernel -----------------------------------------------------
-    peak, peak_kind = load_peaks()
+    # ---- roofline of the dominant kernel: L2, measured on this GPU ---------------------------
+    peaks = l2_peaks(ct, torch)
+    hbm_peak, hbm_kind = load_peaks()
     fp_avg, bp_avg = sum(fp_ms) / len(fp_ms), sum(bp_ms) / len(bp_ms)
-    nrays, nvox = w.n_rays, w.n_voxels
-    fp_bytes = 4 * U + 4 * nrays + 4 * nvox
-    bp_bytes = 4 * U + 4 * nrays + 8 * nvox
-    dom = ("ct_backproject", bp_bytes, bp_avg) if bp_avg >= fp_avg else ("ct_project", fp_bytes,
-                                                                          fp_avg)
-    achieved = dom[1] / (dom[2] * 1e-3) / 1e9
-    kname = "project_kernel" if dom[0] == "ct_project" else "backproject_kernel"
+    walks = walk_roofline(U, fp_avg, bp_avg, peaks)
+    dom = "bp" if bp_avg >= fp_avg else "fp"
+    kname = "backproject_kernel" if dom == "bp" else "project_kernel"
     traffic, traffic_src = profiled_traffic(kname)
     clocks = clk.summary()
     line = {
@@ -632,22 +775,35 @@ def run_ours(args, rank, world):
         "fp_ms": statistics.mean(fp_ms), "bp_ms": statistics.mean(bp_ms),
         "fp_updates_per_s": U / (fp_avg * 1e-3), "bp_updates_per_s": U / (bp_avg * 1e-3),
         "views_per_s": {"fp": w.n_views / (fp_avg * 1e-3), "bp": w.n_views / (bp_avg * 1e-3)},
-        "roofline": {"bound": "hbm", "kernel": dom[0], "achieved": achieved, "peak": peak,
-                     "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
-                     "traffic_source": traffic_src, "peak_source": peak_kind,
-                     "bytes_model": "4 B per ray-voxel update + 4 B per ray + volume once "
-                                    "(gathers/atomics are served by L1/L2; the binding "
-                                    "limits are in profiles/)"},
+        "roofline": {"bound": "l2", "kernel": "ct_backproject" if dom == "bp" else "ct_project",
+                     "achieved": walks[dom]["achieved_gbs"], "peak": walks[dom]["peak_gbs"],
+                     "unit": "GB/s", "frac": walks[dom]["frac"], "traffic": traffic,
+                     "traffic_source": traffic_src,
+                     "peak_source": "measured in this run: " + (
+                         "red.global.add.f32 probe, 8 updates per 32-B sector" if dom == "bp"
+                         else "L1-bypassing 16-B read probe") + " (l2_peaks)",
+                     "bytes_model": "4 B per ray-voxel update (the L2-served gathers or "
+                                    "reductions); traffic = DRAM bytes per launch from the "
+                                    "committed ncu summary, null when its source is stale",
+                     "walks": walks},
+        "l2_peaks": peaks,
+        "hbm_peak": {"gbs": hbm_peak, "source": hbm_kind + " (MEASURED_PEAKS.json copy)"},
         "e2e": {"value": world * 2 * U / (e2e_ms * 1e-3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "timing": "host wall clock around the steps, copies overlapped on a 2nd stream"},
-        "ncu_sol": ncu_sol(U, fp_avg, bp_avg),
+        "ncu_from_committed_profiles": ncu_sol(),
         "gpu_launches": 4 * args.steps,
         "clocks": clocks,
     }
     line["batch4"] = batch_leg(ct, torch, w, U)
+    if not args.no_workloads:
+        line["workloads"] = {f"config{n}": workload_leg(ct, torch, n, peaks,
+                                                        cpu_baseline=not args.no_cpu_baseline)
+                             for n in (1, 2, 4, 5)}
     if not args.no_fdk:
-        line["fdk"] = fdk_leg(ct, torch, w, cpu_baseline=world == 1 and not args.no_cpu_baseline)
+        line["fdk"] = fdk_leg(ct, torch, w, peaks, clocks["sm_mhz"] or clocks["sm_max_mhz"] or
+                              measured_sm_max_mhz(),
+                              cpu_baseline=world == 1 and not args.no_cpu_baseline)
     if not args.no_sirt:
         line["sirt"], line["cgls"] = sirt_leg(ct, torch)
     if args.context:
@@ -672,6 +828,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sirt", action="store_true", help="skip the SIRT/CGLS leg")
     ap.add_argument("--no-fdk", action="store_true", help="skip the FBP/FDK leg")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the FP/BP legs of the other four workloads")
     ap.add_argument("--context", action="store_true",
                     help="also time the pages' performance-table workload shape")
     ap.add_argument("--sample-views", type=int, default=None,

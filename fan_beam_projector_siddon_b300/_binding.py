@@ -97,6 +97,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.ct_cgls_iterate.restype = i32
     L.ct_backproject_static.argtypes = [vp, vp, vp, vp]
     L.ct_backproject_static.restype = i32
+    L.ct_probe_l2_read.argtypes = [vp, sz, i32, vp, vp]
+    L.ct_probe_l2_read.restype = i32
+    L.ct_probe_l1_read.argtypes = [vp, sz, i32, vp, vp]
+    L.ct_probe_l1_read.restype = i32
+    L.ct_probe_l2_reduce.argtypes = [vp, sz, i32, i32, vp]
+    L.ct_probe_l2_reduce.restype = i32
     L.ct_fbp_workspace_bytes.argtypes = [vp]
     L.ct_fbp_workspace_bytes.restype = sz
     opt = ctypes.POINTER(FbpOptions)
@@ -201,6 +207,27 @@ def ct_backproject_static(handle: int, d_sino: int, d_volume: int, stream: int |
     """Backprojection without allocation or workspace (see ``include/ct.h``)."""
     _check(load_library().ct_backproject_static(handle, d_sino, d_volume, stream),
            "ct_backproject_static")
+
+
+def ct_probe_l2_read(d_buf: int, n_floats: int, passes: int, d_sink: int,
+                     stream: int | None) -> None:
+    """L2 read-bandwidth probe (see ``include/ct.h``)."""
+    _check(load_library().ct_probe_l2_read(d_buf, int(n_floats), int(passes), d_sink, stream),
+           "ct_probe_l2_read")
+
+
+def ct_probe_l1_read(d_buf: int, n_floats: int, passes: int, d_sink: int,
+                     stream: int | None) -> None:
+    """L1 read-bandwidth probe (see ``include/ct.h``)."""
+    _check(load_library().ct_probe_l1_read(d_buf, int(n_floats), int(passes), d_sink, stream),
+           "ct_probe_l1_read")
+
+
+def ct_probe_l2_reduce(d_buf: int, n_floats: int, passes: int, stride: int,
+                       stream: int | None) -> None:
+    """L2 reduction-throughput probe (see ``include/ct.h``)."""
+    _check(load_library().ct_probe_l2_reduce(d_buf, int(n_floats), int(passes), int(stride),
+                                             stream), "ct_probe_l2_reduce")
 
 
 def ct_sirt_workspace_bytes(handle: int) -> int:

@@ -9,6 +9,7 @@
 #include <new>
 #include <vector>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "ct.h"
@@ -19,6 +20,7 @@ struct ct_geometry {
     double spacing;
     double du, dv;
     int device;
+    int sm_count;           // streaming multiprocessors of that device
     ct::Grid grid;          // strides of the internal layout
     ct::Tiling tiling;
     ct::ViewRec* d_views;   // device table, n_views records
@@ -181,6 +183,14 @@ cudaError_t from_internal(const ct_geometry* g, const float* src, float* dst, cu
 ct_status check_call(const ct_geometry* g, const void* in, size_t in_bytes, const void* out,
                      size_t out_bytes, const void* ws, size_t ws_bytes, size_t ws_needed) {
     if (g == nullptr || in == nullptr || out == nullptr) return CT_ERR_INVALID_ARGUMENT;
+    // kernels launch on the current device and read the handle's record table: they must be
+    // the same device (checked before anything is queued)
+    int current = -1;
+    if (cudaGetDevice(&current) != cudaSuccess) {
+        cudaGetLastError();
+        return CT_ERR_CUDA;
+    }
+    if (current != g->device) return CT_ERR_INVALID_ARGUMENT;
     ct_status st;
     if ((st = check_device_ptr(in, g->device)) != CT_OK) return st;
     if ((st = check_device_ptr(out, g->device)) != CT_OK) return st;
@@ -388,6 +398,8 @@ ct_status create_impl(ct_beam beam, int32_t n_views, const double* views, int32_
         R.lanes_along_v = (!is_2d(b) && std::fabs(v[fast]) >= std::fabs(u[fast])) ? 1 : 0;
     }
     cudaError_t e = cudaGetDevice(&g->device);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&g->sm_count, cudaDevAttrMultiProcessorCount, g->device);
     if (e == cudaSuccess) e = cudaMalloc(&g->d_views, sizeof(ct::ViewRec) * (size_t)n_views);
     if (e == cudaSuccess)
         e = cudaMemcpy(g->d_views, recs.data(), sizeof(ct::ViewRec) * (size_t)n_views,
@@ -621,7 +633,8 @@ struct CglsLayout {
 
 static CglsLayout cgls_layout(const ct_geometry* g) {
     const size_t vb = align_up(volume_bytes(g)), sb = align_up(sino_bytes(g));
-    const int64_t parts = std::max<int64_t>(ct::project_blocks(g->tiling), ct::norm_blocks());
+    const int64_t parts =
+        std::max<int64_t>(ct::project_blocks(g->tiling), ct::norm_blocks(g->sm_count));
     CglsLayout L{};
     size_t off = 0;
     const bool native = g->info.volume_layout == ct::LAYOUT_ZYX;
@@ -658,7 +671,8 @@ ct_status ct_cgls_iterate(const ct_geometry* g, float* d_x, const float* d_y, vo
     float* Q = reinterpret_cast<float*>(ws + L.q);
     double* parts = reinterpret_cast<double*>(ws + L.partials);
     double* scal = reinterpret_cast<double*>(ws + L.scal);
-    const int64_t fp_parts = ct::project_blocks(g->tiling), nrm_parts = ct::norm_blocks();
+    const int64_t fp_parts = ct::project_blocks(g->tiling),
+                  nrm_parts = ct::norm_blocks(g->sm_count);
     const ct::ViewRec* V = g->d_views;
     cudaError_t e = cudaSuccess;
     if (!native) e = to_internal(g, d_x, X, stream);
@@ -669,7 +683,7 @@ ct_status ct_cgls_iterate(const ct_geometry* g, float* d_x, const float* d_y, vo
         if (e == cudaSuccess) e = cudaMemsetAsync(S, 0, volume_bytes(g), stream);
         if (e == cudaSuccess) e = ct::launch_backproject(V, g->grid, g->tiling, R, S, stream);
         if (e == cudaSuccess) e = cudaMemsetAsync(P, 0, volume_bytes(g), stream);
-        if (e == cudaSuccess) e = ct::launch_norm_partials(S, nvox, parts, stream);
+        if (e == cudaSuccess) e = ct::launch_norm_partials(S, nvox, parts, g->sm_count, stream);
         if (e == cudaSuccess) e = ct::launch_cgls_scalars(parts, nrm_parts, scal, 2, stream);
         if (e == cudaSuccess) e = ct::launch_cgls_update(X, P, S, scal, nvox, stream);
     }
@@ -681,7 +695,7 @@ ct_status ct_cgls_iterate(const ct_geometry* g, float* d_x, const float* d_y, vo
         if (e == cudaSuccess)
             e = ct::launch_backproject_residual(V, g->grid, g->tiling, R, Q, scal, S, stream);
         // beta = |s|^2 / gamma, gamma = |s|^2
-        if (e == cudaSuccess) e = ct::launch_norm_partials(S, nvox, parts, stream);
+        if (e == cudaSuccess) e = ct::launch_norm_partials(S, nvox, parts, g->sm_count, stream);
         if (e == cudaSuccess) e = ct::launch_cgls_scalars(parts, nrm_parts, scal, 1, stream);
         // x += alpha p, p = s + beta p, s = 0
         if (e == cudaSuccess) e = ct::launch_cgls_update(X, P, S, scal, nvox, stream);
@@ -705,14 +719,52 @@ __device__ __align__(256) float g_ct_static_scratch[CT_STATIC_SCRATCH_VOXELS];
 
 constexpr int kMaxStaticDevices = 64;
 std::mutex g_static_mu;
-float* g_static_scratch_ptr[kMaxStaticDevices];  // device address of the array, per device
+// Device address of the array per device, and the id of the context it was looked up in.  A
+// device reset destroys the context (and with it the module and the address); the next call
+// then runs in a new context with another id and looks the address up again.
+float* g_static_scratch_ptr[kMaxStaticDevices];
+unsigned long long g_static_scratch_ctx[kMaxStaticDevices];
+
+// Driver entry points for the current context's id, fetched through the runtime (the library
+// does not link the driver library itself).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+ct_status current_context_id(unsigned long long* id) {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    if (get_current == nullptr || get_id == nullptr) {
+        void* f1 = nullptr;
+        void* f2 = nullptr;
+        cudaDriverEntryPointQueryResult q1, q2;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault,
+                                             &q1) != cudaSuccess ||
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) !=
+                cudaSuccess ||
+            q1 != cudaDriverEntryPointSuccess || q2 != cudaDriverEntryPointSuccess ||
+            f1 == nullptr || f2 == nullptr) {
+            cudaGetLastError();
+            return CT_ERR_CUDA;
+        }
+        get_current = reinterpret_cast<CtxGetCurrentFn>(f1);
+        get_id = reinterpret_cast<CtxGetIdFn>(f2);
+    }
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return CT_ERR_CUDA;
+    if (get_id(ctx, id) != CUDA_SUCCESS) return CT_ERR_CUDA;
+    return CT_OK;
+}
 
 // Device address of the static array on `device`, which must be the current device.  The
-// first call per device looks the address up (this may load the module on that device).
+// first call per device and context looks the address up (this may load the module on that
+// device); later calls in the same context reuse it.
 ct_status static_scratch_on(int device, float** out) {
     if (device < 0 || device >= kMaxStaticDevices) return CT_ERR_INVALID_ARGUMENT;
     std::lock_guard<std::mutex> lock(g_static_mu);
-    if (g_static_scratch_ptr[device] == nullptr) {
+    unsigned long long ctx = 0;
+    const ct_status st = current_context_id(&ctx);
+    if (st != CT_OK) return st;
+    if (g_static_scratch_ptr[device] == nullptr || g_static_scratch_ctx[device] != ctx) {
         void* p = nullptr;
         const cudaError_t e = cudaGetSymbolAddress(&p, g_ct_static_scratch);
         if (e != cudaSuccess || p == nullptr) {
@@ -720,6 +772,7 @@ ct_status static_scratch_on(int device, float** out) {
             return CT_ERR_CUDA;
         }
         g_static_scratch_ptr[device] = static_cast<float*>(p);
+        g_static_scratch_ctx[device] = ctx;
     }
     *out = g_static_scratch_ptr[device];
     return CT_OK;
@@ -1124,6 +1177,58 @@ extern "C" ct_status ct_fbp_parker_weights(const ct_geometry* g, const double* i
         }
     }
     return CT_OK;
+}
+
+// ---------------------------------------------------------------------------------------------
+// L2 roofline probes.
+
+extern "C" ct_status ct_probe_l2_read(const float* d_buf, size_t n_floats, int32_t passes,
+                                      float* d_sink, cudaStream_t stream) {
+    if (d_buf == nullptr || d_sink == nullptr || passes <= 0 || n_floats < 4 ||
+        n_floats > (size_t)INT64_MAX || ((uintptr_t)d_buf & 15) != 0)
+        return CT_ERR_INVALID_ARGUMENT;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return CT_ERR_CUDA;
+    }
+    ct_status st;
+    if ((st = check_device_ptr(d_buf, dev)) != CT_OK) return st;
+    if ((st = check_device_ptr(d_sink, dev)) != CT_OK) return st;
+    if (overlap(d_buf, n_floats * sizeof(float), d_sink, sizeof(float))) return CT_ERR_ALIASING;
+    return from_cuda(ct::launch_l2_read(d_buf, (int64_t)n_floats, passes, d_sink, stream));
+}
+
+extern "C" ct_status ct_probe_l1_read(const float* d_buf, size_t n_floats, int32_t passes,
+                                      float* d_sink, cudaStream_t stream) {
+    if (d_buf == nullptr || d_sink == nullptr || passes <= 0 || n_floats < 4 ||
+        n_floats > (size_t)16384 || ((uintptr_t)d_buf & 15) != 0)
+        return CT_ERR_INVALID_ARGUMENT;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return CT_ERR_CUDA;
+    }
+    ct_status st;
+    if ((st = check_device_ptr(d_buf, dev)) != CT_OK) return st;
+    if ((st = check_device_ptr(d_sink, dev)) != CT_OK) return st;
+    if (overlap(d_buf, n_floats * sizeof(float), d_sink, sizeof(float))) return CT_ERR_ALIASING;
+    return from_cuda(ct::launch_l1_read(d_buf, (int64_t)n_floats, passes, d_sink, stream));
+}
+
+extern "C" ct_status ct_probe_l2_reduce(float* d_buf, size_t n_floats, int32_t passes,
+                                        int32_t stride, cudaStream_t stream) {
+    if (d_buf == nullptr || passes <= 0 || stride < 1 || stride > 32 ||
+        n_floats < (size_t)32 * (size_t)stride || n_floats > (size_t)INT64_MAX)
+        return CT_ERR_INVALID_ARGUMENT;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return CT_ERR_CUDA;
+    }
+    const ct_status st = check_device_ptr(d_buf, dev);
+    if (st != CT_OK) return st;
+    return from_cuda(ct::launch_l2_reduce(d_buf, (int64_t)n_floats, passes, stride, stream));
 }
 
 // ---------------------------------------------------------------------------------------------

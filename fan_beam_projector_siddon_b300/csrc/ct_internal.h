@@ -15,6 +15,10 @@ namespace ct {
 uint64_t siddon_bounds_violations(bool reset);
 uint64_t fbp_bounds_violations(bool reset);
 
+// Streaming multiprocessors of the current device (queried once per device, then cached); grid
+// sizes of the grid-stride kernels are multiples of it.
+int device_sm_count();
+
 // Internal volume orders (the kernels' memory layout of the volume).
 enum Layout : int32_t {
     LAYOUT_ZYX = 0,  // caller's order, x fastest
@@ -82,14 +86,14 @@ cudaError_t launch_project_residual(const ViewRec* views, const Grid& g, const T
                                     cudaStream_t stream);
 // CGLS pieces.  Scalars (float64, device): [gamma, delta, alpha, beta].
 int64_t project_blocks(const Tiling& t);  // blocks (= partial sums) of one projection launch
-int norm_blocks();                          // blocks (= partial sums) of launch_norm_partials
+int norm_blocks(int sm_count);              // blocks (= partial sums) of launch_norm_partials
 cudaError_t launch_project_norm(const ViewRec* views, const Grid& g, const Tiling& t,
                                 const float* vol, float* sino, double* partials,
                                 cudaStream_t stream);
 cudaError_t launch_backproject_residual(const ViewRec* views, const Grid& g, const Tiling& t,
                                         float* r, const float* q, const double* scal, float* vol,
                                         cudaStream_t stream);
-cudaError_t launch_norm_partials(const float* v, int64_t n, double* partials,
+cudaError_t launch_norm_partials(const float* v, int64_t n, double* partials, int sm_count,
                                  cudaStream_t stream);
 cudaError_t launch_cgls_scalars(const double* partials, int64_t n, double* scal, int which,
                                 cudaStream_t stream);
@@ -102,6 +106,17 @@ cudaError_t launch_sirt_update(float* x, float* b, const float* c, float relax, 
 // out[b][c][r] = in[b][r][c] for b < batch, r < rows, c < cols.
 cudaError_t launch_transpose(const float* in, float* out, int64_t rows, int64_t cols,
                              int64_t batch, cudaStream_t stream);
+
+// L2 roofline probes (kernels in probe_kernels.cu): 16-byte L1-bypassing loads over `buf`
+// (n_floats, 16-byte aligned) `passes` times; red.global.add.f32 of 1.0 over `buf` with the lanes
+// of a warp `stride` floats apart, `passes` sweeps.
+cudaError_t launch_l2_read(const float* buf, int64_t n_floats, int32_t passes, float* sink,
+                           cudaStream_t stream);
+cudaError_t launch_l2_reduce(float* buf, int64_t n_floats, int32_t passes, int32_t stride,
+                             cudaStream_t stream);
+// Every block reads the same first n_floats floats of `buf` (L1-resident) `passes` times.
+cudaError_t launch_l1_read(const float* buf, int64_t n_floats, int32_t passes, float* sink,
+                           cudaStream_t stream);
 
 // Filtered backprojection (kernels in fbp_kernels.cu).  Physical units, origin at the volume
 // centre (the caller's frame, not the Siddon kernels' voxel frame).

@@ -1071,7 +1071,7 @@ cudaError_t launch_fbp_gradients(const FbpParams& p_in, const double* raw,
         float* G = filtered;
         float* Q = copies;
         const int64_t n = rows * n_u;
-        const int eb = (int)std::min<int64_t>((n + 255) / 256, 148 * 32);
+        const int eb = (int)std::min<int64_t>((n + 255) / 256, (int64_t)device_sm_count() * 32);
         fbp_grad_lhs_kernel<<<eb, 256, 0, stream>>>(pu, user_weights, copies, G);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         fbp_grad_rhs_kernel<<<eb, 256, 0, stream>>>(pu, cosines, sino, Q);

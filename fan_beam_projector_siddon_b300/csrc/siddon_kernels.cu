@@ -17,6 +17,8 @@
 // in bounds whatever the float rounding does to the order of near-simultaneous crossings.
 #include "ct_internal.h"
 
+#include <atomic>
+
 #include <cuda_runtime.h>
 
 namespace ct {
@@ -771,11 +773,33 @@ int64_t grid_for(const Tiling& t) {
 }
 
 int elementwise_blocks(int64_t n) {
+    const int64_t most = (int64_t)device_sm_count() * 16;
     int64_t b = (n + 255) / 256;
-    return (int)(b < 148 * 16 ? (b > 0 ? b : 1) : 148 * 16);
+    return (int)(b < most ? (b > 0 ? b : 1) : most);
 }
 
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+
 }  // namespace
+
+int device_sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return 148;  // a B300's count; only reached when the runtime cannot name the device
+    }
+    int n = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (n <= 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            n <= 0) {
+            cudaGetLastError();
+            return 148;
+        }
+        g_sm_count[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
 
 // Instantiation by (2D, inner axis).  2D grids are always walked with x inner.
 #define CT_LAUNCH_BY_AXIS(KERNEL, EXTRA, ...)                                                 \
@@ -861,11 +885,11 @@ cudaError_t launch_backproject_residual(const ViewRec* views, const Grid& g, con
     CT_LAUNCH_BY_AXIS(backproject_residual_kernel, CT_NO_EXTRA, views, g, t, r, q, scal, vol);
 }
 
-int norm_blocks() { return 148 * 8; }
+int norm_blocks(int sm_count) { return sm_count * 8; }
 
-cudaError_t launch_norm_partials(const float* v, int64_t n, double* partials,
+cudaError_t launch_norm_partials(const float* v, int64_t n, double* partials, int sm_count,
                                  cudaStream_t stream) {
-    norm_partials_kernel<<<norm_blocks(), kThreads, 0, stream>>>(v, n, partials);
+    norm_partials_kernel<<<norm_blocks(sm_count), kThreads, 0, stream>>>(v, n, partials);
     return cudaGetLastError();
 }
 

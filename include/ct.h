@@ -31,6 +31,9 @@
  * given stream (NULL = legacy default stream), allocates nothing and never synchronises, so the
  * projector, SIRT, CGLS and FBP calls can be recorded into a CUDA graph by stream capture
  * (thread-local capture mode) and replayed; a replay reads the buffers' current contents.
+ * A handle is bound to the device that was current when it was created: every compute call
+ * must be made with that device current, else it returns CT_ERR_INVALID_ARGUMENT before
+ * queueing anything.
  * Asynchronous CUDA errors surface as CT_ERR_CUDA on a later call.  No call aborts the process.
  */
 #ifndef CT_H
@@ -63,7 +66,9 @@ typedef enum {
 
 typedef enum {
     CT_OK = 0,
-    CT_ERR_INVALID_ARGUMENT = 1,   /* NULL handle/pointer, bad size, bad enum, overflow        */
+    CT_ERR_INVALID_ARGUMENT = 1,   /* NULL handle/pointer, bad size, bad enum, overflow, or a
+                                      compute call with another device current than the
+                                      handle's                                                  */
     CT_ERR_INVALID_GEOMETRY = 2,   /* a view record fails the admission checks below          */
     CT_ERR_NOT_DEVICE_POINTER = 3, /* a buffer is not device (or managed) memory of the
                                       handle's device                                          */
@@ -261,7 +266,9 @@ CT_API ct_status ct_cgls_iterate(const ct_geometry *geom, float *d_x, const floa
  * CT_STATIC_SCRATCH_VOXELS voxels; CT_ERR_INVALID_ARGUMENT if the handle's device is not the
  * current device; otherwise as ct_backproject.
  * The first call on a device looks up the array's device address (cudaGetSymbolAddress, which may
- * load the module on that device); make that first call before any stream capture.  Every call
+ * load the module on that device); make that first call before any stream capture.  The address
+ * is kept per device and CUDA context: after a device reset the next call runs in a new context
+ * and looks it up again (again outside any capture).  Every call
  * shares the one array: it is cleared on the stream at the start of each call, and calls whose
  * work overlaps on the GPU (different streams, or graphs replayed concurrently) race on it.
  */
@@ -411,6 +418,36 @@ CT_API ct_status ct_debug_bounds_violations(uint64_t *count);
 
 /* Static, human-readable name of a status code. */
 CT_API const char *ct_status_string(ct_status status);
+
+/*
+ * Roofline probes.  The pages give no counterpart: these calls exist so that a benchmark
+ * can measure, on the GPU at hand and with CUDA events on `stream`, the rates of the access
+ * patterns the projector's kernels press on, and use them as the denominators of their roofline
+ * fractions.  Use a buffer that fits in L2 (64 MiB on a B300) and warm it once first.
+ *
+ * ct_probe_l2_read:   passes x n_floats/4 sixteen-byte loads that bypass L1 (ld.global.cg),
+ *                     grid-stride over d_buf by every resident thread (a multiple of the SM
+ *                     count).  d_buf: device, n_floats >= 4 floats, 16-byte aligned, read only;
+ *                     d_sink: device, one float, written only if the loaded values sum to -1
+ *                     per thread (never, for non-negative contents).  Traffic per call:
+ *                     16 * floor(n_floats / 4) * passes bytes.
+ * ct_probe_l1_read:   the same loads, but allocating in L1 (ld.global.ca), every block re-reading
+ *                     the same first n_floats (4 <= n_floats <= 16384, 16-byte aligned) floats of
+ *                     d_buf, so that after the first pass every load hits in L1.  Traffic per
+ *                     call: 16 * floor(n_floats / 4) * passes bytes per block, blocks = 4 per SM.
+ * ct_probe_l2_reduce: passes sweeps of red.global.add.f32 (+1.0) over d_buf, each warp
+ *                     instruction updating 32 floats `stride` apart (1 <= stride <= 32;
+ *                     stride 1 puts 8 updates in each 32-byte sector, stride 2 four).  Updates
+ *                     per call: 32 * floor(n_floats / (32 stride)) * passes; d_buf is modified.
+ * Errors: CT_ERR_INVALID_ARGUMENT (NULL, sizes, passes <= 0, alignment, stride),
+ * CT_ERR_NOT_DEVICE_POINTER, CT_ERR_ALIASING, CT_ERR_CUDA.
+ */
+CT_API ct_status ct_probe_l2_read(const float *d_buf, size_t n_floats, int32_t passes,
+                                  float *d_sink, struct CUstream_st *stream);
+CT_API ct_status ct_probe_l1_read(const float *d_buf, size_t n_floats, int32_t passes,
+                                  float *d_sink, struct CUstream_st *stream);
+CT_API ct_status ct_probe_l2_reduce(float *d_buf, size_t n_floats, int32_t passes,
+                                    int32_t stride, struct CUstream_st *stream);
 
 #ifdef __cplusplus
 }

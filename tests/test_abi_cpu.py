@@ -97,6 +97,11 @@ def test_null_arguments_are_rejected(lib):
     assert L.ct_fbp_gradients_workspace_bytes(None) == 0
     assert L.ct_fbp_parker_weights(None, None, None) == 1
     assert L.ct_fbp_transpose_workspace_bytes(None) == 0
+    assert L.ct_probe_l2_read(None, 1024, 1, None, None) == 1
+    assert L.ct_probe_l2_reduce(None, 1024, 1, 1, None) == 1
+    assert L.ct_probe_l2_reduce(16, 1024, 1, 0, None) == 1       # stride out of range
+    assert L.ct_probe_l2_reduce(16, 1024, 0, 1, None) == 1       # no passes
+    assert L.ct_probe_l2_read(8, 1024, 1, 16, None) == 1          # not 16-byte aligned
 
 
 def test_surface_admission_before_touching_the_gpu(lib):

@@ -1,12 +1,16 @@
 """CGLS on the GPU (through ct_cgls_iterate) against the float64 oracle's CGLS.
 
-Parity: GPU CGLS with GPU-made data vs oracle CGLS with oracle-made data, both from zero, after
-8 steps.  The GPU keeps its vectors (x, p, r, s) in float32.  How much float32 storage alone
-moves the 8th iterate depends on the problem: on the cone and tilt-series twins about 1e-7, on
-the underdetermined 2D twin (37 views x 83 pixels for 45 x 61 unknowns, i.i.d. image) about 7e-4.
-The test measures that sensitivity with the oracle itself (same recurrences, the oracle's
-operator, vectors rounded to float32 after every update) and allows
-max(1e-3, 10 x that sensitivity).
+Parity: GPU CGLS with GPU-made data against oracle CGLS with oracle-made data, both from zero,
+after k steps.  The GPU keeps its vectors (x, p, r, s) in float32 and its operator walks in
+float32, so it is a perturbation of the float64 run whose size CGLS amplifies as its search
+directions lose conjugacy.  The tolerance is fixed in advance and is not a function of the run:
+the GPU iterate must lie within 1e-3 relative L2 of the oracle's, and its residual |y - A x|^2
+within 1e-3 relative of the oracle's, on twins and step counts where float32 vector storage alone
+moves the oracle's own iterate by at most 1e-5 (the test measures this with the oracle and
+asserts it, so an ill-conditioned case fails instead of widening the bound).  That precondition
+holds for the cone and tilt-series twins at 8 steps (about 1e-7) and for the 2D twins at 4 steps
+(about 1e-6 and 1e-7); beyond that the 2D twins' 8-step sensitivity reaches 7e-4 (parallel) and
+5e-5 (fan).
 """
 import numpy as np
 import pytest
@@ -17,7 +21,8 @@ from tests._parity import rel_l2, torch_cuda
 
 pytestmark = pytest.mark.gpu
 
-CGLS_RTOL = 1e-3
+CGLS_RTOL = 1e-3          # GPU iterate and residual against the float64 oracle's
+CGLS_MAX_SENSITIVITY = 1e-5  # precondition: float32 storage moves the oracle's iterate <= this
 
 
 def _float32_storage_sensitivity(go, y, x_ref, n_iter):
@@ -53,33 +58,28 @@ def ct():
     return ct
 
 
-@pytest.mark.parametrize("n", [1, 3, 5])
-def test_cgls_matches_oracle_small(ct, n):
+@pytest.mark.parametrize("n,steps", [(1, 4), (2, 4), (3, 8), (5, 8)])
+def test_cgls_matches_oracle_small(ct, n, steps):
     import torch
     w = W.small_config(n)
     g = ct.Geometry.from_workload(w)
     go = oracle.Geometry.from_workload(w)
     x_true = w.phantom()
     y_or = go.project(x_true, threads=8)
-    x_or, res_or = go.cgls(y_or, 8)
+    x_or, res_or = go.cgls(y_or, steps)
+    sens, _ = _float32_storage_sensitivity(go, y_or, x_or, steps)
+    assert sens <= CGLS_MAX_SENSITIVITY, sens
     y = g.project(torch_cuda(x_true))
     x = torch.zeros(w.volume_shape, dtype=torch.float32, device="cuda")
     ws = g.new_workspace(cgls=True)
-    g.cgls(x, y, 3, ws, initialised=False)    # 3 + 5: the state carries over between calls
-    g.cgls(x, y, 5, ws, initialised=True)
+    first = steps // 2 - 1                        # the state carries over between calls
+    g.cgls(x, y, first, ws, initialised=False)
+    g.cgls(x, y, steps - first, ws, initialised=True)
     torch.cuda.synchronize()
-    sens, res32 = _float32_storage_sensitivity(go, y_or, x_or, 8)
-    # (the same two-realisation argument as for the residual below: 2 x 10 times the
-    # float32-storage change)
-    assert rel_l2(x.cpu().numpy(), x_or) <= max(CGLS_RTOL, 20.0 * sens)
-    # the residual of the GPU iterate matches the oracle's after 8 steps, within 1 % or twenty
-    # times what float32 storage alone does to it: the float32-storage run is one realisation of
-    # float32 rounding, the GPU (whose atomic backprojections also change their summation order
-    # from run to run) another, and two realisations can differ by twice either one's distance
-    # from the float64 path; ill-conditioned twins (the underdetermined 2D one) amplify both
+    assert rel_l2(x.cpu().numpy(), x_or) <= CGLS_RTOL
     r = (y - g.project(x)).double()
     res_gpu = float((r * r).sum())
-    assert abs(res_gpu - res_or[-1]) <= max(1e-2 * res_or[-1], 20.0 * abs(res32 - res_or[-1]))
+    assert abs(res_gpu - res_or[-1]) <= CGLS_RTOL * res_or[-1], (res_gpu, res_or[-1])
 
 
 def test_cgls_fixed_point_and_zero_iterations(ct):

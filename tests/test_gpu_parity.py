@@ -269,6 +269,35 @@ def test_bad_pointers_aliasing_and_workspace(ct):
     torch.cuda.synchronize()
 
 
+def test_calls_with_another_device_current_are_refused(ct):
+    """A handle is bound to its creation device: with another device current every compute call
+    returns CT_ERR_INVALID_ARGUMENT before queueing any work (needs two GPUs)."""
+    import torch
+    if torch.cuda.device_count() < 2:
+        pytest.skip("needs a second GPU")
+    w = W.small_config(3)
+    torch.cuda.set_device(0)
+    g = ct.Geometry.from_workload(w)
+    vol = torch_cuda(w.phantom())
+    sino = torch.empty(w.sino_shape, device="cuda:0")
+    ws = g.new_workspace()
+    try:
+        torch.cuda.set_device(1)
+        for call in (lambda: ct.ct_project(g.handle, vol.data_ptr(), sino.data_ptr(),
+                                           ws.data_ptr(), ws.numel(), None),
+                     lambda: ct.ct_backproject(g.handle, sino.data_ptr(), vol.data_ptr(),
+                                               ws.data_ptr(), ws.numel(), None),
+                     lambda: ct.ct_backproject_static(g.handle, sino.data_ptr(), vol.data_ptr(),
+                                                      None)):
+            with pytest.raises(ct.CtError) as e:
+                call()
+            assert e.value.status == 1
+    finally:
+        torch.cuda.set_device(0)
+    g.project(vol, out=sino, workspace=ws)
+    torch.cuda.synchronize()
+
+
 # ---------------------------------------------------------------------------------------------
 # per-axis voxel spacing
 # ---------------------------------------------------------------------------------------------

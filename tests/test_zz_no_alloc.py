@@ -27,11 +27,16 @@ def ct():
     return ct
 
 
-@pytest.mark.parametrize("n", [3, 5, 1])
-def test_static_backprojection_matches_workspace_entry_point(ct, n):
+# (workload, whether its internal volume order differs from the caller's): the cone and spiral
+# twins walk a z-fastest volume, so their sums go through the static array; the tilt-series and
+# 2D twins keep the caller's order and accumulate straight into the output
+@pytest.mark.parametrize("n,uses_array", [(3, True), (4, True), (5, False), (1, False)])
+def test_static_backprojection_matches_workspace_entry_point(ct, n, uses_array):
     import torch
     w = W.small_config(n)
     g = ct.Geometry.from_workload(w)
+    assert (g.info.volume_layout != 0) == uses_array
+    assert g.info.n_voxels <= (1 << 22)
     stream = torch.cuda.current_stream().cuda_stream
     for seed in (11, 12):                        # two calls in a row, different inputs
         y = torch_cuda(W.random_sinogram(w, seed))
