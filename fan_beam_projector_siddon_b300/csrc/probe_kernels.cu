@@ -21,23 +21,27 @@ constexpr int kProbeThreads = 512;
 __global__ void __launch_bounds__(kProbeThreads)
     l2_read_kernel(const float4* __restrict__ buf, int64_t n4, int32_t passes,
                    float* __restrict__ sink) {
-    float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a, c = a, d = a;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     const int64_t first = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     for (int32_t p = 0; p < passes; ++p) {
         int64_t i = first;
-        // two loads in flight per thread and iteration
-        for (; i + stride < n4; i += 2 * stride) {
-            const float4 x = __ldcg(buf + i), y = __ldcg(buf + i + stride);
+        // four loads in flight per thread and iteration
+        for (; i + 3 * stride < n4; i += 4 * stride) {
+            const float4 x = __ldcg(buf + i), y = __ldcg(buf + i + stride),
+                         z = __ldcg(buf + i + 2 * stride), w = __ldcg(buf + i + 3 * stride);
             a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
             b.x += y.x; b.y += y.y; b.z += y.z; b.w += y.w;
+            c.x += z.x; c.y += z.y; c.z += z.z; c.w += z.w;
+            d.x += w.x; d.y += w.y; d.z += w.z; d.w += w.w;
         }
-        if (i < n4) {
+        for (; i < n4; i += stride) {
             const float4 x = __ldcg(buf + i);
             a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
         }
     }
-    const float s = a.x + a.y + a.z + a.w + b.x + b.y + b.z + b.w;
+    const float s = a.x + a.y + a.z + a.w + b.x + b.y + b.z + b.w + c.x + c.y + c.z + c.w + d.x +
+                    d.y + d.z + d.w;
     if (s == -1.0f) sink[0] = s;  // keeps the loads; the caller's buffer holds no such sums
 }
 
@@ -70,9 +74,18 @@ __global__ void __launch_bounds__(kProbeThreads)
     const int64_t warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     const int64_t span = 32 * (int64_t)stride;  // elements one warp instruction covers
     const int64_t groups = n / span;
-    for (int32_t p = 0; p < passes; ++p)
-        for (int64_t gi = warp; gi < groups; gi += warps)
-            atomicAdd(buf + gi * span + (int64_t)lane * stride, 1.0f);
+    float* const base = buf + (int64_t)lane * stride;
+    for (int32_t p = 0; p < passes; ++p) {
+        int64_t gi = warp;
+        // four reductions per warp and iteration, to distant groups
+        for (; gi + 3 * warps < groups; gi += 4 * warps) {
+            atomicAdd(base + gi * span, 1.0f);
+            atomicAdd(base + (gi + warps) * span, 1.0f);
+            atomicAdd(base + (gi + 2 * warps) * span, 1.0f);
+            atomicAdd(base + (gi + 3 * warps) * span, 1.0f);
+        }
+        for (; gi < groups; gi += warps) atomicAdd(base + gi * span, 1.0f);
+    }
 }
 
 }  // namespace
