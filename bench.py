@@ -580,12 +580,16 @@ def walk_roofline(U, fp_ms, bp_ms, peaks):
                    "frac_vs_4_per_sector": bp_gbs / peaks["red_stride2_gbs"]}}
 
 
-def workload_leg(ct, torch, n: int, peaks, cpu_baseline: bool, reps: int = 3):
+def workload_leg(ct, torch, n: int, peaks, cpu_baseline: bool, reps: int = 3,
+                 views: int | None = None):
     """FP and BP of workload n through the C ABI (CUDA events on the launching stream, L2 flushed
     before each call, median of `reps` after one warm-up), views/s, ray-voxel updates/s, the
     algorithmic L2 fractions, and the float64 oracle on the host cores over evenly spaced views
-    (the whole workload when it has at most 16 views' worth of work, else extrapolated)."""
+    (the whole workload when it has at most 16 views' worth of work, else extrapolated).
+    `views` restricts the workload to that many evenly spaced views (for profiling captures)."""
     w = W.config(n)
+    if views:
+        w = w.subset(np.linspace(0, w.n_views, views, endpoint=False).astype(int))
     x_host = w.phantom()
     U = count_updates(w)
     g = ct.Geometry.from_workload(w)
@@ -649,6 +653,15 @@ def run_ours(args, rank, world):
 
     dev = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(dev)
+    if args.workload is not None:
+        # one workload's FP/BP leg alone (profiling and spot checks); not the benchmark line
+        if rank == 0:
+            peaks = l2_peaks(ct, torch)
+            print(json.dumps(workload_leg(ct, torch, args.workload, peaks,
+                                          cpu_baseline=not args.no_cpu_baseline,
+                                          reps=max(1, args.steps), views=args.views)),
+                  flush=True)
+        return 0
     w = W.config(CONFIG_ID)
     x_host = w.phantom()
     U = count_updates(w)
@@ -796,7 +809,7 @@ def run_ours(args, rank, world):
         "clocks": clocks,
     }
     line["batch4"] = batch_leg(ct, torch, w, U)
-    if not args.no_workloads:
+    if not args.no_workloads and args.workload is None:
         line["workloads"] = {f"config{n}": workload_leg(ct, torch, n, peaks,
                                                         cpu_baseline=not args.no_cpu_baseline)
                              for n in (1, 2, 4, 5)}
@@ -830,6 +843,10 @@ def main():
     ap.add_argument("--no-fdk", action="store_true", help="skip the FBP/FDK leg")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the FP/BP legs of the other four workloads")
+    ap.add_argument("--workload", type=int, default=None, choices=[1, 2, 3, 4, 5],
+                    help="time only this workload's FP/BP leg (--steps reps) and print it")
+    ap.add_argument("--views", type=int, default=None,
+                    help="with --workload: that many evenly spaced views of it")
     ap.add_argument("--context", action="store_true",
                     help="also time the pages' performance-table workload shape")
     ap.add_argument("--sample-views", type=int, default=None,

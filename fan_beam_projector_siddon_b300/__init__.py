@@ -11,6 +11,7 @@ from ._binding import (CT_CONE, CT_FAN2D, CT_PARALLEL2D, CT_PARALLEL3D, FBP_WIND
                        ct_cgls_workspace_bytes, ct_fbp, ct_fbp_parker_weights, ct_fbp_transpose,
                        ct_fbp_transpose_workspace_bytes, ct_fbp_workspace_bytes,
                        ct_geometry_create, ct_geometry_create_surface, ct_geometry_destroy,
+                       ct_geometry_set_slabs,
                        ct_geometry_get_info, ct_probe_l1_read, ct_probe_l2_read, ct_probe_l2_reduce, ct_project,
                        ct_project_batch, ct_sirt_iterate,
                        ct_sirt_workspace_bytes, ct_status_string, load_library)
@@ -23,5 +24,6 @@ __all__ = ["CT_CONE", "CT_FAN2D", "CT_PARALLEL2D", "CT_PARALLEL3D", "FBP_WINDOWS
            "ct_fbp_transpose_workspace_bytes", "ct_fbp_workspace_bytes",
            "ct_geometry_create",
            "ct_geometry_create_surface", "ct_geometry_destroy", "ct_geometry_get_info",
+           "ct_geometry_set_slabs",
            "ct_probe_l1_read", "ct_probe_l2_read", "ct_probe_l2_reduce", "ct_project", "ct_project_batch",
            "ct_sirt_iterate", "ct_sirt_workspace_bytes", "ct_status_string", "load_library"]

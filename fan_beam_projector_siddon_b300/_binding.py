@@ -45,7 +45,8 @@ class GeometryInfo(ctypes.Structure):
                 ("n_u", ctypes.c_int32), ("n_v", ctypes.c_int32),
                 ("volume_layout", ctypes.c_int32),
                 ("n_rays", ctypes.c_int64), ("n_voxels", ctypes.c_int64),
-                ("workspace_bytes", ctypes.c_size_t), ("sirt_workspace_bytes", ctypes.c_size_t)]
+                ("workspace_bytes", ctypes.c_size_t), ("sirt_workspace_bytes", ctypes.c_size_t),
+                ("n_slabs", ctypes.c_int32), ("slab_cells", ctypes.c_int32)]
 
 
 _lib = None
@@ -77,6 +78,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.ct_geometry_destroy.restype = i32
     L.ct_geometry_get_info.argtypes = [vp, ctypes.POINTER(GeometryInfo)]
     L.ct_geometry_get_info.restype = i32
+    L.ct_geometry_set_slabs.argtypes = [vp, i32]
+    L.ct_geometry_set_slabs.restype = i32
     L.ct_project.argtypes = [vp, vp, vp, vp, sz, vp]
     L.ct_project.restype = i32
     L.ct_backproject.argtypes = [vp, vp, vp, vp, sz, vp]
@@ -189,6 +192,11 @@ def ct_geometry_get_info(handle: int) -> GeometryInfo:
     _check(load_library().ct_geometry_get_info(handle, ctypes.byref(info)),
            "ct_geometry_get_info")
     return info
+
+
+def ct_geometry_set_slabs(handle: int, slab_cells: int) -> None:
+    """Slab height of the tiled walks, 0 = no tiling (see ``include/ct.h``)."""
+    _check(load_library().ct_geometry_set_slabs(handle, int(slab_cells)), "ct_geometry_set_slabs")
 
 
 def ct_project(handle: int, d_volume: int, d_sino: int, d_workspace: int | None,
@@ -372,6 +380,11 @@ class Geometry:
     def from_workload(cls, w) -> "Geometry":
         return cls(w.beam, w.views, w.vol_shape, w.voxel_spacing, w.n_u, w.n_v, w.du, w.dv,
                    getattr(w, "offsets", None))
+
+    def set_slabs(self, slab_cells: int) -> None:
+        """Override the slab tiling of the walks (0 = off); refreshes ``info``."""
+        ct_geometry_set_slabs(self.handle, slab_cells)
+        self.info = ct_geometry_get_info(self.handle)
 
     def close(self) -> None:
         if getattr(self, "handle", None):

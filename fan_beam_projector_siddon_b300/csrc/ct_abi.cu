@@ -26,7 +26,10 @@ struct ct_geometry {
     ct::ViewRec* d_views;   // device table, n_views records
     double* d_offsets;      // surface detectors: device (n_u, n_v, 3) offsets; else nullptr
     double* d_raw;          // device copy of the caller's view records (physical units)
+    int32_t* d_slab_tiles;  // slab-tiled walks: per slab, the (view, v-tile) entries reaching it
+    std::vector<int64_t> slab_off;  // slab s owns d_slab_tiles[slab_off[s] .. slab_off[s + 1])
     std::vector<double> host_views;
+    std::vector<ct::ViewRec> recs;  // host copy of the device records (voxel units)
 };
 
 namespace {
@@ -280,6 +283,113 @@ bool admit_surface(int beam, int32_t n_views, const double* views, int32_t n_u, 
     return true;
 }
 
+// ---- slab tiling of the walks --------------------------------------------------------------
+
+// Slab tiling is opt-in (ct_geometry_set_slabs): measured on the 512^3 spiral it cuts the walks'
+// DRAM traffic about threefold but takes about four times as long, because every slab re-clips
+// its rays in float64 and sloped rays of one detector column enter a slab at different points of
+// their shared column path, so the lanes of a warp lose their lock-step.
+
+// Per (view, detector v-tile), the first and last slab that the tile's rays can reach.  The
+// rays of one detector row of a flat detector lie in one plane (through the source and the row,
+// or through the row along the ray direction); the z of that plane over the box's xy rectangle
+// is affine, so its extremes are at the rectangle's corners.  The union over the tile's rows,
+// widened by two cells, bounds the z of every ray of the tile inside the box.
+std::vector<int2> slab_ranges(const ct_geometry* g, int32_t h, int32_t n_slabs) {
+    const ct_geometry_info& I = g->info;
+    const int tiles_v = g->tiling.tiles_v;
+    std::vector<int2> out((size_t)I.n_views * (size_t)tiles_v);
+    const bool par = g->grid.parallel != 0;
+    const double cx[2] = {0.0, (double)I.nx}, cy[2] = {0.0, (double)I.ny};
+    for (int i = 0; i < I.n_views; ++i) {
+        const ct::ViewRec& R = g->recs[(size_t)i];
+        for (int vt = 0; vt < tiles_v; ++vt) {
+            double zlo = INFINITY, zhi = -INFINITY;
+            const int v1 = std::min(I.n_v, 32 * (vt + 1));
+            for (int v = 32 * vt; v < v1; ++v) {
+                double X0[3], D[3], N[3];
+                for (int a = 0; a < 3; ++a) {
+                    const double row = R.pb[a] + (double)v * R.pv[a];
+                    X0[a] = par ? row : R.q[a];
+                    D[a] = par ? R.q[a] : row;
+                }
+                cross3(D, R.pu, N);
+                const double nn = norm3(N);
+                if (!(nn > 0.0) || !(std::fabs(N[2]) > 1e-9 * nn)) {  // plane (nearly) contains z
+                    zlo = -INFINITY;
+                    zhi = INFINITY;
+                    break;
+                }
+                for (int cxi = 0; cxi < 2; ++cxi)
+                    for (int cyi = 0; cyi < 2; ++cyi) {
+                        const double z = X0[2] - (N[0] * (cx[cxi] - X0[0]) +
+                                                  N[1] * (cy[cyi] - X0[1])) / N[2];
+                        zlo = std::min(zlo, z);
+                        zhi = std::max(zhi, z);
+                    }
+            }
+            int lo, hi;
+            if (!(zhi >= -2.0) || !(zlo <= (double)I.nz + 2.0)) {
+                lo = 1;  // no slab
+                hi = 0;
+            } else {
+                const double a = std::max(zlo - 2.0, 0.0), b = std::min(zhi + 2.0, (double)I.nz);
+                lo = std::min((int)std::floor(a / h), n_slabs - 1);
+                hi = std::min((int)std::floor(b / h), n_slabs - 1);
+            }
+            out[(size_t)i * tiles_v + vt] = make_int2(lo, hi);
+        }
+    }
+    return out;
+}
+
+// Sets the handle's slab height (0: no tiling) and uploads its per-slab tile lists
+// (synchronous).  Within a slab the entries run v-tile first, then view, like the untiled grid.
+ct_status set_slabs(ct_geometry* g, int32_t h) {
+    int32_t* table = nullptr;
+    int32_t n_slabs = 1;
+    std::vector<int64_t> off;
+    if (h > 0) {
+        n_slabs = (int32_t)((g->info.nz + h - 1) / h);
+        const std::vector<int2> r = slab_ranges(g, h, n_slabs);
+        const int tiles_v = g->tiling.tiles_v;
+        std::vector<int32_t> list;
+        off.push_back(0);
+        for (int32_t s = 0; s < n_slabs; ++s) {
+            for (int vt = 0; vt < tiles_v; ++vt)
+                for (int i = 0; i < g->info.n_views; ++i) {
+                    const int2 rg = r[(size_t)i * tiles_v + vt];
+                    if (s >= rg.x && s <= rg.y) list.push_back(i * tiles_v + vt);
+                }
+            off.push_back((int64_t)list.size());
+        }
+        cudaError_t e = cudaMalloc(&table, sizeof(int32_t) * std::max<size_t>(list.size(), 1));
+        if (e == cudaSuccess && !list.empty())
+            e = cudaMemcpy(table, list.data(), sizeof(int32_t) * list.size(),
+                           cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            if (table) cudaFree(table);
+            return from_cuda(e);
+        }
+    }
+    if (g->d_slab_tiles) cudaFree(g->d_slab_tiles);
+    g->d_slab_tiles = table;
+    g->slab_off = std::move(off);
+    g->info.n_slabs = h > 0 ? n_slabs : 1;
+    g->info.slab_cells = h > 0 ? h : g->info.nz;
+    return CT_OK;
+}
+
+ct::SlabArgs slab_args(const ct_geometry* g, int32_t s) {
+    ct::SlabArgs a;
+    a.c0 = s * g->info.slab_cells;
+    a.c1 = std::min(g->info.nz, (s + 1) * g->info.slab_cells);
+    a.tiles = g->d_slab_tiles + g->slab_off[(size_t)s];
+    a.n_tiles = (int32_t)(g->slab_off[(size_t)s + 1] - g->slab_off[(size_t)s]);
+    return a;
+}
+
 ct_status create_impl(ct_beam beam, int32_t n_views, const double* views, int32_t nz, int32_t ny,
                       int32_t nx, const double* spacing_zyx, int32_t n_u, int32_t n_v, double du,
                       double dv, const double* offsets, ct_geometry** out) {
@@ -421,6 +531,9 @@ ct_status create_impl(ct_beam beam, int32_t n_views, const double* views, int32_
     }
     G.offsets = g->d_offsets;
     G.nv = n_v;
+    g->recs = std::move(recs);
+    g->info.n_slabs = 1;
+    g->info.slab_cells = nz;
     *out = g;
     return CT_OK;
 }
@@ -452,6 +565,10 @@ ct_status ct_geometry_destroy(ct_geometry* g) {
     if (g == nullptr) return CT_OK;
     cudaError_t e = cudaSuccess;
     if (g->d_views) e = cudaFree(g->d_views);
+    if (g->d_slab_tiles) {
+        const cudaError_t e2 = cudaFree(g->d_slab_tiles);
+        if (e == cudaSuccess) e = e2;
+    }
     if (g->d_offsets) {
         const cudaError_t e2 = cudaFree(g->d_offsets);
         if (e == cudaSuccess) e = e2;
@@ -470,6 +587,21 @@ ct_status ct_geometry_get_info(const ct_geometry* g, ct_geometry_info* info) {
     return CT_OK;
 }
 
+ct_status ct_geometry_set_slabs(ct_geometry* g, int32_t slab_cells) {
+    if (g == nullptr || slab_cells < 0) return CT_ERR_INVALID_ARGUMENT;
+    if (g->info.volume_layout != ct::LAYOUT_YXZ || g->d_offsets != nullptr)
+        return CT_ERR_INVALID_ARGUMENT;
+    int current = -1;
+    if (cudaGetDevice(&current) != cudaSuccess) {
+        cudaGetLastError();
+        return CT_ERR_CUDA;
+    }
+    if (current != g->device) return CT_ERR_INVALID_ARGUMENT;
+    int64_t h = slab_cells == 0 ? 0 : ((int64_t)slab_cells + 31) / 32 * 32;
+    if (h >= g->info.nz) h = 0;  // one slab: no tiling
+    return set_slabs(g, (int32_t)h);
+}
+
 ct_status ct_project(const ct_geometry* g, const float* d_volume, float* d_sino,
                      void* d_workspace, size_t workspace_bytes, cudaStream_t stream) {
     if (g == nullptr) return CT_ERR_INVALID_ARGUMENT;
@@ -481,6 +613,14 @@ ct_status ct_project(const ct_geometry* g, const float* d_volume, float* d_sino,
         float* tmp = static_cast<float*>(d_workspace);
         if ((st = from_cuda(to_internal(g, d_volume, tmp, stream))) != CT_OK) return st;
         vol = tmp;
+    }
+    if (g->info.n_slabs > 1) {
+        // every ray's partial sums over the slabs are added to its cleared entry, slab by slab
+        cudaError_t e = cudaMemsetAsync(d_sino, 0, sino_bytes(g), stream);
+        for (int32_t s = 0; s < g->info.n_slabs && e == cudaSuccess; ++s)
+            e = ct::launch_project_slab(g->d_views, g->grid, g->tiling, 1, vol, 0, d_sino, 0,
+                                        slab_args(g, s), stream);
+        return from_cuda(e);
     }
     return from_cuda(ct::launch_project(g->d_views, g->grid, g->tiling, vol, d_sino, stream));
 }
@@ -494,9 +634,16 @@ ct_status ct_backproject(const ct_geometry* g, const float* d_sino, float* d_vol
     float* acc = g->info.volume_layout == ct::LAYOUT_ZYX ? d_volume
                                                           : static_cast<float*>(d_workspace);
     if ((st = from_cuda(cudaMemsetAsync(acc, 0, volume_bytes(g), stream))) != CT_OK) return st;
-    if ((st = from_cuda(ct::launch_backproject(g->d_views, g->grid, g->tiling, d_sino, acc,
-                                               stream))) != CT_OK)
+    if (g->info.n_slabs > 1) {
+        cudaError_t e = cudaSuccess;
+        for (int32_t s = 0; s < g->info.n_slabs && e == cudaSuccess; ++s)
+            e = ct::launch_backproject_slab(g->d_views, g->grid, g->tiling, 1, d_sino, 0, acc, 0,
+                                            slab_args(g, s), stream);
+        if ((st = from_cuda(e)) != CT_OK) return st;
+    } else if ((st = from_cuda(ct::launch_backproject(g->d_views, g->grid, g->tiling, d_sino, acc,
+                                                      stream))) != CT_OK) {
         return st;
+    }
     if (acc != d_volume) return from_cuda(from_internal(g, acc, d_volume, stream));
     return CT_OK;
 }
@@ -584,9 +731,16 @@ ct_status ct_project_batch(const ct_geometry* g, int32_t batch, const float* d_v
             vol = ws;
             vstride = wstride;
         }
-        if (e == cudaSuccess)
-            e = ct::launch_project_batch(g->d_views, g->grid, g->tiling, nb, vol, vstride,
-                                         d_sinos + (int64_t)b0 * nray, nray, stream);
+        float* sinos = d_sinos + (int64_t)b0 * nray;
+        if (e == cudaSuccess && g->info.n_slabs > 1) {
+            e = cudaMemsetAsync(sinos, 0, (size_t)nb * sino_bytes(g), stream);
+            for (int32_t s = 0; s < g->info.n_slabs && e == cudaSuccess; ++s)
+                e = ct::launch_project_slab(g->d_views, g->grid, g->tiling, nb, vol, vstride, sinos,
+                                            nray, slab_args(g, s), stream);
+        } else if (e == cudaSuccess) {
+            e = ct::launch_project_batch(g->d_views, g->grid, g->tiling, nb, vol, vstride, sinos,
+                                         nray, stream);
+        }
         b0 += nb;
     }
     return from_cuda(e);
@@ -610,10 +764,15 @@ ct_status ct_backproject_batch(const ct_geometry* g, int32_t batch, const float*
         float* acc = native ? d_volumes + (int64_t)b0 * nvox : ws;
         const int64_t vstride = native ? nvox : wstride;
         e = cudaMemsetAsync(acc, 0, (size_t)((nb - 1) * vstride + nvox) * sizeof(float), stream);
-        if (e == cudaSuccess)
-            e = ct::launch_backproject_batch(g->d_views, g->grid, g->tiling, nb,
-                                             d_sinos + (int64_t)b0 * nray, nray, acc, vstride,
-                                             stream);
+        const float* sinos = d_sinos + (int64_t)b0 * nray;
+        if (e == cudaSuccess && g->info.n_slabs > 1) {
+            for (int32_t s = 0; s < g->info.n_slabs && e == cudaSuccess; ++s)
+                e = ct::launch_backproject_slab(g->d_views, g->grid, g->tiling, nb, sinos, nray, acc,
+                                                vstride, slab_args(g, s), stream);
+        } else if (e == cudaSuccess) {
+            e = ct::launch_backproject_batch(g->d_views, g->grid, g->tiling, nb, sinos, nray, acc,
+                                             vstride, stream);
+        }
         if (!native)
             for (int j = 0; j < nb && e == cudaSuccess; ++j)
                 e = from_internal(g, ws + j * wstride, d_volumes + (int64_t)(b0 + j) * nvox,

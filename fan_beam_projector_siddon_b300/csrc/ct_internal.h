@@ -66,6 +66,16 @@ struct Tiling {
     int32_t two_d;
 };
 
+// One slab of the inner (fastest) axis for the slab-tiled walks: the walks of a launch are
+// restricted to the inner-axis cells [c0, c1), over the detector tiles whose rays can reach the
+// slab: tiles[i] = view * tiles_v + v_tile for i < n_tiles, and block b takes the u-tile
+// b % tiles_u of entry b / tiles_u.
+struct SlabArgs {
+    int32_t c0, c1;
+    const int32_t* tiles;
+    int32_t n_tiles;
+};
+
 // Launchers (kernels in siddon_kernels.cu).  All asynchronous on `stream`.
 cudaError_t launch_project(const ViewRec* views, const Grid& g, const Tiling& t,
                            const float* vol, float* sino, cudaStream_t stream);
@@ -81,6 +91,15 @@ cudaError_t launch_project_batch(const ViewRec* views, const Grid& g, const Tili
 cudaError_t launch_backproject_batch(const ViewRec* views, const Grid& g, const Tiling& t, int nb,
                                      const float* sino, int64_t sstride, float* vol,
                                      int64_t vstride, cudaStream_t stream);
+// Slab-tiled forms (3D, z-fastest internal order only): the projection ADDS each ray's partial
+// line integral over the slab to sino (which the caller clears before the first slab), the
+// backprojection scatters the slab's segments.  nb as for the batched forms.
+cudaError_t launch_project_slab(const ViewRec* views, const Grid& g, const Tiling& t, int nb,
+                                const float* vol, int64_t vstride, float* sino, int64_t sstride,
+                                const SlabArgs& slab, cudaStream_t stream);
+cudaError_t launch_backproject_slab(const ViewRec* views, const Grid& g, const Tiling& t, int nb,
+                                    const float* sino, int64_t sstride, float* vol,
+                                    int64_t vstride, const SlabArgs& slab, cudaStream_t stream);
 cudaError_t launch_project_residual(const ViewRec* views, const Grid& g, const Tiling& t,
                                     const float* x, const float* y, float* r,
                                     cudaStream_t stream);

@@ -41,7 +41,13 @@ constexpr int kThreads = 256;  // 8 warps
 constexpr int kRows = 4;       // 3D tiles: 8 warps x 4 rows = 32 pixels along the warp axis
 constexpr int kTile = 32;      // 3D tiles are 32 x 32 pixels
 constexpr int kTile2D = 256;   // 2D tiles are 256 detector pixels
-constexpr int kMinBlocks = 6;  // resident CTAs per SM the walk kernels are compiled for (<= 51 regs)
+// Resident CTAs per SM the walk kernels are compiled for.  The plain 3D forward projection runs
+// at 8 (32 registers, some set-up values spilled; the extra warps hide the gathers' latency on
+// volumes larger than L2), the scatters, the 2D projection and the fused SIRT/CGLS projections at
+// 6 (40 registers; at 8 the 512^3 reductions and the 2D projection slow down and the fused
+// kernels spill inside the walk).
+constexpr int kMinBlocksGather = 8;
+constexpr int kMinBlocks = 6;
 
 __device__ __forceinline__ float f_inf() { return __int_as_float(0x7f800000); }
 
@@ -56,13 +62,20 @@ __device__ __forceinline__ double rcp64(double d) {
 
 // Walk state of one ray.  Index 0 and 1 are the two "outer" axes, index 2 the "inner" axis,
 // which is the volume axis fastest in memory.
+//
+// The k-th crossing of slot a lies at fmaf(k, dt[a], t0[a]).  A walk takes the crossings with
+// k0[a] <= k < n[a] and runs from tstart to tend; the whole ray has k0 = 0, tstart = 0 and
+// n, tend from the clip (restrict_to_slab narrows them to one slab of the inner axis).
 struct Ray {
     float t0[3];   // distance (voxel units, along the ray) from entry to the first crossing
     float dt[3];   // distance between successive crossings
-    int n[3];      // number of crossings
+    int n[3];      // crossings the walk ends before (the whole ray: number of crossings)
+    float k0[3];   // crossings already behind the walk's start (the whole ray: 0)
     int step[3];   // signed element stride per crossing
-    int idx;       // entry voxel, linear index in the internal layout
-    float tend;    // chord length inside the box (voxel units)
+    int idx;       // voxel at the walk's start, linear index in the internal layout
+    int entry_in;  // entry cell of the whole ray along the inner axis
+    float tstart;  // where the walk starts (the whole ray: 0)
+    float tend;    // where the walk ends (the whole ray: the chord length, voxel units)
     float scale;   // physical length per unit of voxel-space length along this ray
 #ifdef CT_DEBUG_BOUNDS
     int64_t nvox;  // voxels of one volume (bounds-checking builds)
@@ -182,11 +195,130 @@ __device__ __forceinline__ bool setup_ray(const ViewRec& vr, const Grid& g, int 
             r.step[slot] = 0;
         }
         idx += i0 * g.stride[a];
+        if (slot == 2) r.entry_in = i0;
+        r.k0[slot] = 0.0f;
     }
     r.idx = idx;
+    r.tstart = 0.0f;
 #ifdef CT_DEBUG_BOUNDS
     r.nvox = (int64_t)g.n[0] * g.n[1] * g.n[2];
 #endif
+    return true;
+}
+
+// Float32 copy of a view record's flat-detector vectors (slab-tiled launches).
+struct ViewRecF {
+    float pb[3], pu[3], pv[3], q[3];
+};
+
+__device__ __forceinline__ void load_view_f32(const ViewRec& sv, ViewRecF& sf) {
+    if (threadIdx.x < 3) {
+        const int a = threadIdx.x;
+        sf.pb[a] = (float)sv.pb[a];
+        sf.pu[a] = (float)sv.pu[a];
+        sf.pv[a] = (float)sv.pv[a];
+        sf.q[a] = (float)sv.q[a];
+    }
+    __syncthreads();
+}
+
+// Cheap float32 test, before the float64 set-up, of whether the ray of pixel (u, v) can have
+// cells in the inner-axis slab [c0, c1): the ray is clipped against the box widened by one cell
+// on every side and its inner-axis range widened by one more cell, far beyond float32 rounding,
+// so a ray that reaches the slab is never rejected.  F is the inner axis.
+template <int F>
+__device__ __forceinline__ bool may_reach_slab(const ViewRecF& sf, const Grid& g, int u, int v,
+                                               int c0, int c1) {
+    const float fu = (float)u, fv = (float)v;
+    float o[3], d[3];
+    float amin = g.parallel ? -f_inf() : 0.0f, amax = g.parallel ? f_inf() : 1.0f;
+#pragma unroll
+    for (int a = 0; a < 3; ++a) {
+        const float p = __fmaf_rn(fv, sf.pv[a], __fmaf_rn(fu, sf.pu[a], sf.pb[a]));
+        o[a] = g.parallel ? p : sf.q[a];
+        d[a] = g.parallel ? sf.q[a] : p;
+        const float lo = -1.0f, hi = (float)g.n[a] + 1.0f;
+        if (d[a] != 0.0f) {
+            const float r = 1.0f / d[a];
+            const float t1 = (lo - o[a]) * r, t2 = (hi - o[a]) * r;
+            amin = fmaxf(amin, fminf(t1, t2));
+            amax = fminf(amax, fmaxf(t1, t2));
+        } else if (!(o[a] >= lo && o[a] <= hi)) {
+            return false;
+        }
+    }
+    if (!(amax >= amin)) return false;
+    const float z0 = __fmaf_rn(amin, d[F], o[F]), z1 = __fmaf_rn(amax, d[F], o[F]);
+    return fmaxf(z0, z1) >= (float)c0 - 1.0f && fminf(z0, z1) <= (float)c1 + 1.0f;
+}
+
+// Crossings of one axis at or before t (AT = true) or strictly before t, among the first n:
+// #{k < n : fmaf(k, dt, t0) <= t} (or < t), with the walk's own crossing values.
+template <bool AT>
+__device__ __forceinline__ int crossings_before(float t, float t0, float dt, int n) {
+    int k = 0;
+    if (t >= t0) k = min(n, (int)fminf(floorf(__fdiv_rn(__fsub_rn(t, t0), dt)) + 1.0f, (float)n));
+    // the estimate can be off by one either way; settle it on the exact crossing values
+    while (k > 0 && (AT ? __fmaf_rn((float)(k - 1), dt, t0) > t
+                        : __fmaf_rn((float)(k - 1), dt, t0) >= t))
+        --k;
+    while (k < n && (AT ? __fmaf_rn((float)k, dt, t0) <= t : __fmaf_rn((float)k, dt, t0) < t)) ++k;
+    return k;
+}
+
+// Narrows the walk of a whole ray to the inner-axis cells [c0, c1) (one slab): it starts at the
+// crossing into the slab (or at the ray's entry) and ends at the crossing out of it (or at the
+// ray's exit), and keeps the whole ray's crossing values, so every segment it takes has the bits
+// the whole walk gives that segment.  Outer crossings at the slab's entry crossing belong to the
+// slab's start state (the whole walk takes an outer crossing before an inner one at the same
+// value), outer crossings at its exit crossing to the next slab.  Returns false when the ray has
+// no segment of positive length in the slab.
+__device__ __forceinline__ bool restrict_to_slab(Ray& r, int c0, int c1) {
+    const int a = r.entry_in, n = r.n[2];
+    float kstart = 0.0f, tstart = 0.0f, tend = r.tend;
+    int nend = n;
+    if (r.step[2] == 0) {
+        if (a < c0 || a >= c1) return false;
+    } else if (r.step[2] > 0) {  // cells a, a + 1, ..., a + n
+        if (a + n < c0 || a >= c1) return false;
+        if (a < c0) {
+            const int k = c0 - 1 - a;  // crossing from cell c0 - 1 into c0
+            kstart = (float)(k + 1);
+            tstart = __fmaf_rn((float)k, r.dt[2], r.t0[2]);
+        }
+        if (a + n > c1 - 1) {
+            nend = c1 - 1 - a;  // crossing from cell c1 - 1 into c1
+            tend = __fmaf_rn((float)nend, r.dt[2], r.t0[2]);
+        }
+    } else {  // cells a, a - 1, ..., a - n
+        if (a < c0 || a - n >= c1) return false;
+        if (a > c1 - 1) {
+            const int k = a - c1;  // crossing from cell c1 into c1 - 1
+            kstart = (float)(k + 1);
+            tstart = __fmaf_rn((float)k, r.dt[2], r.t0[2]);
+        }
+        if (a - n < c0) {
+            nend = a - c0;  // crossing from cell c0 into c0 - 1
+            tend = __fmaf_rn((float)nend, r.dt[2], r.t0[2]);
+        }
+    }
+    if (!(tend > tstart)) return false;
+    int idx = r.idx + (int)kstart * r.step[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        if (r.n[j] > 0) {
+            const int k = crossings_before<true>(tstart, r.t0[j], r.dt[j], r.n[j]);
+            const int e = crossings_before<false>(tend, r.t0[j], r.dt[j], r.n[j]);
+            idx += k * r.step[j];
+            r.k0[j] = (float)k;
+            r.n[j] = e;
+        }
+    }
+    r.k0[2] = kstart;
+    r.n[2] = nend;
+    r.idx = idx;
+    r.tstart = tstart;
+    r.tend = tend;
     return true;
 }
 
@@ -219,12 +351,12 @@ __device__ __forceinline__ void walk(const Ray& r, const float* __restrict__ vin
     const int s2 = ISIGN != 0 ? ISIGN : r.step[2];
     const float INF = f_inf();
     const float na = (float)r.n[0], nb = (float)r.n[1], nf = (float)r.n[2];
-    float ta = r.n[0] > 0 ? r.t0[0] : INF;
-    float tb = r.n[1] > 0 ? r.t0[1] : INF;
-    float tf = r.n[2] > 0 ? r.t0[2] : INF;
-    float ka = 0.0f, kb = 0.0f, kf = 0.0f;
+    float ka = r.k0[0], kb = r.k0[1], kf = r.k0[2];
+    float ta = ka < na ? __fmaf_rn(ka, r.dt[0], r.t0[0]) : INF;
+    float tb = kb < nb ? __fmaf_rn(kb, r.dt[1], r.t0[1]) : INF;
+    float tf = kf < nf ? __fmaf_rn(kf, r.dt[2], r.t0[2]) : INF;
     int idx = r.idx;
-    float t = 0.0f;
+    float t = r.tstart;
 #pragma unroll
     for (int b = 0; b < NB; ++b) acc[b] = 0.0f;
     // segment [.., .. + seg) in voxel idx: gather from / scatter into every volume of the batch
@@ -253,8 +385,8 @@ __device__ __forceinline__ void walk(const Ray& r, const float* __restrict__ vin
     // Main phase: outer crossings strictly before the earlier of the two outer axes' last
     // crossings, so neither outer axis can run out here and its next crossing needs no check.
     // (The last crossings use the same fmaf as the walk, so the comparison is exact.)
-    const float la = r.n[0] > 0 ? __fmaf_rn(na - 1.0f, r.dt[0], r.t0[0]) : INF;
-    const float lb = r.n[1] > 0 ? __fmaf_rn(nb - 1.0f, r.dt[1], r.t0[1]) : INF;
+    const float la = na > ka ? __fmaf_rn(na - 1.0f, r.dt[0], r.t0[0]) : INF;
+    const float lb = nb > kb ? __fmaf_rn(nb - 1.0f, r.dt[1], r.t0[1]) : INF;
     const float lim = fminf(la, lb);
     float tstop = fminf(ta, tb);
     bool p = tf < tstop;
@@ -394,12 +526,14 @@ __device__ __forceinline__ void walk_dispatch(const Ray& r, const float* __restr
                                               const float (&val)[NB], float (&acc)[NB]) {
     const unsigned m = __activemask();
     const float INF = f_inf();
-    const bool none = r.n[2] == 0;
+    const bool none = !((float)r.n[2] > r.k0[2]);  // no inner crossing to take
     // the crossing after the last inner one, as the walk would compute it, is not before the end
     // of the main phase (the earlier of the two outer axes' last crossings), so the main phase
     // never takes it
-    const float la = r.n[0] > 0 ? __fmaf_rn((float)r.n[0] - 1.0f, r.dt[0], r.t0[0]) : INF;
-    const float lb = r.n[1] > 0 ? __fmaf_rn((float)r.n[1] - 1.0f, r.dt[1], r.t0[1]) : INF;
+    const float la =
+        (float)r.n[0] > r.k0[0] ? __fmaf_rn((float)r.n[0] - 1.0f, r.dt[0], r.t0[0]) : INF;
+    const float lb =
+        (float)r.n[1] > r.k0[1] ? __fmaf_rn((float)r.n[1] - 1.0f, r.dt[1], r.t0[1]) : INF;
     const bool single =
         none || (r.dt[2] > fminf(r.dt[0], r.dt[1]) + __fmaf_rn(r.tend, 1e-5f, 1e-6f) &&
                  __fmaf_rn((float)r.n[2], r.dt[2], r.t0[2]) >= fminf(la, lb));
@@ -466,40 +600,64 @@ __device__ __forceinline__ void pixel_of(const TileCoord& c, const ViewRec& sv, 
     }
 }
 
-// Resident CTAs per SM for the batched walks (more registers per thread for NB values).
-template <int NB>
+// Resident CTAs per SM for the (batched) walks: more registers per thread for NB values.
+template <bool SCATTER, bool TWO_D, int NB>
 struct BatchBlocks {
-    static constexpr int value = NB == 1 ? kMinBlocks : (NB == 2 ? 5 : 4);
+    static constexpr int value = NB == 1 ? (SCATTER || TWO_D ? kMinBlocks : kMinBlocksGather)
+                                         : (NB == 2 ? 5 : 4);
 };
 
+// Block -> (view, pixel tile) of a slab-tiled launch: the slab's list of (view, v-tile) entries,
+// each with its row of u-tiles.
+__device__ __forceinline__ TileCoord tile_of_slab_block(const SlabArgs& sl, const Tiling& t) {
+    const int b = (int)blockIdx.x;
+    const int i = b / t.tiles_u;
+    const int e = __ldg(sl.tiles + i);
+    TileCoord c;
+    c.view = e / t.tiles_v;
+    c.vt = e - c.view * t.tiles_v;
+    c.ut = b - i * t.tiles_u;
+    return c;
+}
+
 // sino[b] = A vol[b] for the NB volumes vol + b * vstride (internal order) and sinograms
-// sino + b * sstride; one walk per ray serves all NB volumes.
-template <bool TWO_D, int F, int NB>
-__global__ void __launch_bounds__(kThreads, BatchBlocks<NB>::value)
+// sino + b * sstride; one walk per ray serves all NB volumes.  SLAB: the walks are restricted to
+// one slab of the inner axis and each ray's partial sum is added to its sinogram entry.
+template <bool TWO_D, int F, int NB, bool SLAB>
+__global__ void __launch_bounds__(kThreads, BatchBlocks<false, TWO_D, NB>::value)
     project_kernel(const ViewRec* __restrict__ views, const Grid g, const Tiling tl,
                    const float* __restrict__ vol, int64_t vstride, float* __restrict__ sino,
-                   int64_t sstride) {
+                   int64_t sstride, const SlabArgs sl) {
     __shared__ ViewRec sv;
-    const TileCoord c = tile_of_block(tl);
+    __shared__ ViewRecF sf;
+    const TileCoord c = SLAB ? tile_of_slab_block(sl, tl) : tile_of_block(tl);
     load_view(views, c.view, sv);
+    if (SLAB) load_view_f32(sv, sf);
 #pragma unroll 1
     for (int row = 0; row < (TWO_D ? 1 : kRows); ++row) {
         int u, v;
         pixel_of<TWO_D>(c, sv, row, u, v);
         if (u >= tl.n_u || v >= tl.n_v) continue;
+        if (SLAB && !may_reach_slab<F>(sf, g, u, v, sl.c0, sl.c1)) continue;
         const int64_t k = ((int64_t)c.view * tl.n_u + u) * tl.n_v + v;
         Ray ray;
-        if (setup_ray<F>(sv, g, u, v, ray)) {
+        bool hit = setup_ray<F>(sv, g, u, v, ray);
+        if (SLAB) hit = hit && restrict_to_slab(ray, sl.c0, sl.c1);
+        if (hit) {
             if (NB == 1) {
-                sino[k] = __fmul_rn(walk_gather(ray, vol), ray.scale);
+                const float y = __fmul_rn(walk_gather(ray, vol), ray.scale);
+                sino[k] = SLAB ? __fadd_rn(sino[k], y) : y;
             } else {
                 const float none[NB] = {};
                 float acc[NB];
                 walk_dispatch<false, NB>(ray, vol, nullptr, vstride, none, acc);
 #pragma unroll
-                for (int b = 0; b < NB; ++b) sino[b * sstride + k] = __fmul_rn(acc[b], ray.scale);
+                for (int b = 0; b < NB; ++b) {
+                    const float y = __fmul_rn(acc[b], ray.scale);
+                    sino[b * sstride + k] = SLAB ? __fadd_rn(sino[b * sstride + k], y) : y;
+                }
             }
-        } else {
+        } else if (!SLAB) {
 #pragma unroll
             for (int b = 0; b < NB; ++b) sino[b * sstride + k] = 0.0f;
         }
@@ -507,20 +665,24 @@ __global__ void __launch_bounds__(kThreads, BatchBlocks<NB>::value)
 }
 
 // MODE 0: scatter sino * (physical length per voxel-space length); MODE 1: the same for a sinogram
-// of ones (A^T 1).  NB volumes/sinograms at strides vstride/sstride, one walk per ray.
-template <bool TWO_D, int F, int MODE, int NB>
-__global__ void __launch_bounds__(kThreads, BatchBlocks<NB>::value)
+// of ones (A^T 1).  NB volumes/sinograms at strides vstride/sstride, one walk per ray.  SLAB: the
+// walks are restricted to one slab of the inner axis.
+template <bool TWO_D, int F, int MODE, int NB, bool SLAB>
+__global__ void __launch_bounds__(kThreads, BatchBlocks<true, TWO_D, NB>::value)
     backproject_kernel(const ViewRec* __restrict__ views, const Grid g, const Tiling tl,
                        const float* __restrict__ sino, int64_t sstride, float* __restrict__ vol,
-                       int64_t vstride) {
+                       int64_t vstride, const SlabArgs sl) {
     __shared__ ViewRec sv;
-    const TileCoord c = tile_of_block(tl);
+    __shared__ ViewRecF sf;
+    const TileCoord c = SLAB ? tile_of_slab_block(sl, tl) : tile_of_block(tl);
     load_view(views, c.view, sv);
+    if (SLAB) load_view_f32(sv, sf);
 #pragma unroll 1
     for (int row = 0; row < (TWO_D ? 1 : kRows); ++row) {
         int u, v;
         pixel_of<TWO_D>(c, sv, row, u, v);
         if (u >= tl.n_u || v >= tl.n_v) continue;
+        if (SLAB && !may_reach_slab<F>(sf, g, u, v, sl.c0, sl.c1)) continue;
         const int64_t k = ((int64_t)c.view * tl.n_u + u) * tl.n_v + v;
         float y[NB];
         bool any = false;
@@ -532,6 +694,7 @@ __global__ void __launch_bounds__(kThreads, BatchBlocks<NB>::value)
         if (!any) continue;
         Ray ray;
         if (!setup_ray<F>(sv, g, u, v, ray)) continue;
+        if (SLAB && !restrict_to_slab(ray, sl.c0, sl.c1)) continue;
         if (NB == 1) {
             walk_scatter(ray, vol, __fmul_rn(y[0], ray.scale));
         } else {
@@ -819,37 +982,44 @@ int device_sm_count() {
 
 #define CT_NO_EXTRA
 
-#define CT_NB1 , 1
-#define CT_NB2 , 2
-#define CT_NB4 , 4
-#define CT_MODE0_NB1 , 0, 1
-#define CT_MODE0_NB2 , 0, 2
-#define CT_MODE0_NB4 , 0, 4
-#define CT_MODE1_NB1 , 1, 1
+#define CT_NB1 , 1, false
+#define CT_NB2 , 2, false
+#define CT_NB4 , 4, false
+#define CT_MODE0_NB1 , 0, 1, false
+#define CT_MODE0_NB2 , 0, 2, false
+#define CT_MODE0_NB4 , 0, 4, false
+#define CT_MODE1_NB1 , 1, 1, false
 
 cudaError_t launch_project(const ViewRec* views, const Grid& g, const Tiling& t, const float* vol,
                            float* sino, cudaStream_t stream) {
-    CT_LAUNCH_BY_AXIS(project_kernel, CT_NB1, views, g, t, vol, (int64_t)0, sino, (int64_t)0);
+    CT_LAUNCH_BY_AXIS(project_kernel, CT_NB1, views, g, t, vol, (int64_t)0, sino, (int64_t)0,
+                      SlabArgs{});
 }
 
 cudaError_t launch_backproject(const ViewRec* views, const Grid& g, const Tiling& t,
                                const float* sino, float* vol, cudaStream_t stream) {
     CT_LAUNCH_BY_AXIS(backproject_kernel, CT_MODE0_NB1, views, g, t, sino, (int64_t)0, vol,
-                      (int64_t)0);
+                      (int64_t)0, SlabArgs{});
 }
 
 cudaError_t launch_backproject_ones(const ViewRec* views, const Grid& g, const Tiling& t,
                                     float* vol, cudaStream_t stream) {
     CT_LAUNCH_BY_AXIS(backproject_kernel, CT_MODE1_NB1, views, g, t, nullptr, (int64_t)0, vol,
-                      (int64_t)0);
+                      (int64_t)0, SlabArgs{});
 }
 
 cudaError_t launch_project_batch(const ViewRec* views, const Grid& g, const Tiling& t, int nb,
                                  const float* vol, int64_t vstride, float* sino, int64_t sstride,
                                  cudaStream_t stream) {
-    if (nb == 4) CT_LAUNCH_BY_AXIS(project_kernel, CT_NB4, views, g, t, vol, vstride, sino, sstride);
-    if (nb == 2) CT_LAUNCH_BY_AXIS(project_kernel, CT_NB2, views, g, t, vol, vstride, sino, sstride);
-    if (nb == 1) CT_LAUNCH_BY_AXIS(project_kernel, CT_NB1, views, g, t, vol, vstride, sino, sstride);
+    if (nb == 4)
+        CT_LAUNCH_BY_AXIS(project_kernel, CT_NB4, views, g, t, vol, vstride, sino, sstride,
+                          SlabArgs{});
+    if (nb == 2)
+        CT_LAUNCH_BY_AXIS(project_kernel, CT_NB2, views, g, t, vol, vstride, sino, sstride,
+                          SlabArgs{});
+    if (nb == 1)
+        CT_LAUNCH_BY_AXIS(project_kernel, CT_NB1, views, g, t, vol, vstride, sino, sstride,
+                          SlabArgs{});
     return cudaErrorInvalidValue;
 }
 
@@ -857,12 +1027,55 @@ cudaError_t launch_backproject_batch(const ViewRec* views, const Grid& g, const 
                                      const float* sino, int64_t sstride, float* vol,
                                      int64_t vstride, cudaStream_t stream) {
     if (nb == 4)
-        CT_LAUNCH_BY_AXIS(backproject_kernel, CT_MODE0_NB4, views, g, t, sino, sstride, vol, vstride);
+        CT_LAUNCH_BY_AXIS(backproject_kernel, CT_MODE0_NB4, views, g, t, sino, sstride, vol, vstride,
+                          SlabArgs{});
     if (nb == 2)
-        CT_LAUNCH_BY_AXIS(backproject_kernel, CT_MODE0_NB2, views, g, t, sino, sstride, vol, vstride);
+        CT_LAUNCH_BY_AXIS(backproject_kernel, CT_MODE0_NB2, views, g, t, sino, sstride, vol, vstride,
+                          SlabArgs{});
     if (nb == 1)
-        CT_LAUNCH_BY_AXIS(backproject_kernel, CT_MODE0_NB1, views, g, t, sino, sstride, vol, vstride);
+        CT_LAUNCH_BY_AXIS(backproject_kernel, CT_MODE0_NB1, views, g, t, sino, sstride, vol, vstride,
+                          SlabArgs{});
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_project_slab(const ViewRec* views, const Grid& g, const Tiling& t, int nb,
+                                const float* vol, int64_t vstride, float* sino, int64_t sstride,
+                                const SlabArgs& slab, cudaStream_t stream) {
+    const unsigned nblk = (unsigned)((int64_t)slab.n_tiles * t.tiles_u);
+    if (nblk == 0) return cudaSuccess;
+    if (t.two_d || g.fast != 2) return cudaErrorInvalidValue;
+    if (nb == 4)
+        project_kernel<false, 2, 4, true><<<nblk, kThreads, 0, stream>>>(views, g, t, vol, vstride,
+                                                                         sino, sstride, slab);
+    else if (nb == 2)
+        project_kernel<false, 2, 2, true><<<nblk, kThreads, 0, stream>>>(views, g, t, vol, vstride,
+                                                                         sino, sstride, slab);
+    else if (nb == 1)
+        project_kernel<false, 2, 1, true><<<nblk, kThreads, 0, stream>>>(views, g, t, vol, vstride,
+                                                                         sino, sstride, slab);
+    else
+        return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_backproject_slab(const ViewRec* views, const Grid& g, const Tiling& t, int nb,
+                                    const float* sino, int64_t sstride, float* vol,
+                                    int64_t vstride, const SlabArgs& slab, cudaStream_t stream) {
+    const unsigned nblk = (unsigned)((int64_t)slab.n_tiles * t.tiles_u);
+    if (nblk == 0) return cudaSuccess;
+    if (t.two_d || g.fast != 2) return cudaErrorInvalidValue;
+    if (nb == 4)
+        backproject_kernel<false, 2, 0, 4, true><<<nblk, kThreads, 0, stream>>>(
+            views, g, t, sino, sstride, vol, vstride, slab);
+    else if (nb == 2)
+        backproject_kernel<false, 2, 0, 2, true><<<nblk, kThreads, 0, stream>>>(
+            views, g, t, sino, sstride, vol, vstride, slab);
+    else if (nb == 1)
+        backproject_kernel<false, 2, 0, 1, true><<<nblk, kThreads, 0, stream>>>(
+            views, g, t, sino, sstride, vol, vstride, slab);
+    else
+        return cudaErrorInvalidValue;
+    return cudaGetLastError();
 }
 
 cudaError_t launch_project_residual(const ViewRec* views, const Grid& g, const Tiling& t,
