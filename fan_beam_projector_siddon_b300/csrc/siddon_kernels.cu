@@ -257,7 +257,7 @@ __device__ __forceinline__ bool may_reach_slab(const ViewRecF& sf, const Grid& g
 template <bool AT>
 __device__ __forceinline__ int crossings_before(float t, float t0, float dt, int n) {
     int k = 0;
-    if (t >= t0) k = min(n, (int)fminf(floorf(__fdiv_rn(__fsub_rn(t, t0), dt)) + 1.0f, (float)n));
+    if (t >= t0) k = min(n, (int)fminf(floorf(__fdividef(__fsub_rn(t, t0), dt)) + 1.0f, (float)n));
     // the estimate can be off by one either way; settle it on the exact crossing values
     while (k > 0 && (AT ? __fmaf_rn((float)(k - 1), dt, t0) > t
                         : __fmaf_rn((float)(k - 1), dt, t0) >= t))
@@ -395,8 +395,20 @@ __device__ __forceinline__ void walk(const Ray& r, const float* __restrict__ vin
         load(idx, v0);
         if (p) load(idx + s2, v1);
     }
-#pragma unroll 2  // two steps per iteration: the loop-carried values are renamed, not copied
-    while (tstop < lim) {
+    // The gather runs the main phase for an exact count of steps: the outer crossings strictly
+    // before lim, counted on the walk's own crossing values, are exactly the ones the value test
+    // tstop < lim admits, and with an integer count the loop unrolled by eight tests once per
+    // eight steps (forward walks: cone 15.6 -> 14.4 ms, 512^3 spiral 122 -> 107 ms, tilt series
+    // 46 -> 42 ms, bit-identical; by four: 14.5, 111, 42 ms).  The scatter keeps the value test
+    // unrolled by two: counted, it ran no faster unrolled by one, four or eight and much slower
+    // by two.  The unrolled loops rename the loop-carried values instead of copying them.
+    int main_steps = 0;
+    if (!SCATTER && lim < INF)
+        main_steps = (na > ka ? crossings_before<false>(lim, r.t0[0], r.dt[0], r.n[0]) - (int)ka : 0) +
+                     (nb > kb ? crossings_before<false>(lim, r.t0[1], r.dt[1], r.n[1]) - (int)kb : 0);
+    constexpr int kMainUnroll = SCATTER ? 2 : 8;
+#pragma unroll kMainUnroll
+    for (int step_no = 0; SCATTER ? tstop < lim : step_no < main_steps; ++step_no) {
         const float seg0 = __fsub_rn(p ? tf : tstop, t);
         if (SCATTER)
             scatter(idx, seg0);
