@@ -344,7 +344,7 @@ __device__ __forceinline__ bool restrict_to_slab(Ray& r, int c0, int c1) {
 // one inner crossing between two outer ones, and none can run out of inner crossings in the main
 // phase (see walk_dispatch), so the main phase needs neither a loop for a second inner crossing
 // nor the exhaustion check.  The specialisations change no arithmetic.
-template <bool SCATTER, int NB, int ISIGN, bool SINGLE>
+template <bool SCATTER, int NB, int ISIGN, bool SINGLE, bool COUNTED>
 __device__ __forceinline__ void walk(const Ray& r, const float* __restrict__ vin,
                                      float* __restrict__ vout, int64_t vstride,
                                      const float (&val)[NB], float (&acc)[NB]) {
@@ -395,20 +395,22 @@ __device__ __forceinline__ void walk(const Ray& r, const float* __restrict__ vin
         load(idx, v0);
         if (p) load(idx + s2, v1);
     }
-    // The gather runs the main phase for an exact count of steps: the outer crossings strictly
+    // COUNTED gathers run the main phase for an exact count of steps: the outer crossings strictly
     // before lim, counted on the walk's own crossing values, are exactly the ones the value test
     // tstop < lim admits, and with an integer count the loop unrolled by eight tests once per
     // eight steps (forward walks: cone 15.6 -> 14.4 ms, 512^3 spiral 122 -> 107 ms, tilt series
-    // 46 -> 42 ms, bit-identical; by four: 14.5, 111, 42 ms).  The scatter keeps the value test
-    // unrolled by two: counted, it ran no faster unrolled by one, four or eight and much slower
-    // by two.  The unrolled loops rename the loop-carried values instead of copying them.
+    // 46 -> 42 ms, bit-identical; by four: 14.5, 111, 42 ms).  The other walks keep the value
+    // test unrolled by two: the scatter ran no faster counted (unrolled by one, four or eight) and
+    // much slower counted by two, and the 2D and batched gathers were slower counted.  The
+    // unrolled loops rename the loop-carried values instead of copying them.
+    static_assert(!(COUNTED && SCATTER), "the scatter walks test values");
     int main_steps = 0;
-    if (!SCATTER && lim < INF)
+    if (COUNTED && lim < INF)
         main_steps = (na > ka ? crossings_before<false>(lim, r.t0[0], r.dt[0], r.n[0]) - (int)ka : 0) +
                      (nb > kb ? crossings_before<false>(lim, r.t0[1], r.dt[1], r.n[1]) - (int)kb : 0);
-    constexpr int kMainUnroll = SCATTER ? 2 : 8;
+    constexpr int kMainUnroll = COUNTED ? 8 : 2;
 #pragma unroll kMainUnroll
-    for (int step_no = 0; SCATTER ? tstop < lim : step_no < main_steps; ++step_no) {
+    for (int step_no = 0; COUNTED ? step_no < main_steps : tstop < lim; ++step_no) {
         const float seg0 = __fsub_rn(p ? tf : tstop, t);
         if (SCATTER)
             scatter(idx, seg0);
@@ -532,7 +534,7 @@ __device__ __forceinline__ void walk(const Ray& r, const float* __restrict__ vin
 // crossings.  Such a gap is at most min(dt_a, dt_b) plus the rounding of two crossing values, and
 // successive inner crossings are at least dt_f minus that rounding apart; each crossing value is
 // one fmaf below tend, so the margin 1e-5 tend (about 80 ulps of tend) covers it.
-template <bool SCATTER, int NB>
+template <bool SCATTER, int NB, bool COUNTED = false>
 __device__ __forceinline__ void walk_dispatch(const Ray& r, const float* __restrict__ vin,
                                               float* __restrict__ vout, int64_t vstride,
                                               const float (&val)[NB], float (&acc)[NB]) {
@@ -550,18 +552,22 @@ __device__ __forceinline__ void walk_dispatch(const Ray& r, const float* __restr
         none || (r.dt[2] > fminf(r.dt[0], r.dt[1]) + __fmaf_rn(r.tend, 1e-5f, 1e-6f) &&
                  __fmaf_rn((float)r.n[2], r.dt[2], r.t0[2]) >= fminf(la, lb));
     if (__all_sync(m, single && (none || r.step[2] == 1)))
-        walk<SCATTER, NB, 1, true>(r, vin, vout, vstride, val, acc);
+        walk<SCATTER, NB, 1, true, COUNTED>(r, vin, vout, vstride, val, acc);
     else if (__all_sync(m, single && (none || r.step[2] == -1)))
-        walk<SCATTER, NB, -1, true>(r, vin, vout, vstride, val, acc);
+        walk<SCATTER, NB, -1, true, COUNTED>(r, vin, vout, vstride, val, acc);
     else
-        walk<SCATTER, NB, 0, false>(r, vin, vout, vstride, val, acc);
+        walk<SCATTER, NB, 0, false, COUNTED>(r, vin, vout, vstride, val, acc);
 }
 
 // Single-volume forms.
+// COUNTED: the main phase runs for a counted number of steps, unrolled by eight (single-volume
+// 3D gathers; the 2D and batched gathers were slower that way: 2D fan 0.42 -> 0.50 ms, four
+// volumes 27.5 -> 35.3 ms).
+template <bool COUNTED>
 __device__ __forceinline__ float walk_gather(const Ray& r, const float* __restrict__ vin) {
     const float none[1] = {0.0f};
     float acc[1];
-    walk_dispatch<false, 1>(r, vin, nullptr, 0, none, acc);
+    walk_dispatch<false, 1, COUNTED>(r, vin, nullptr, 0, none, acc);
     return acc[0];
 }
 __device__ __forceinline__ void walk_scatter(const Ray& r, float* __restrict__ vout, float val) {
@@ -657,7 +663,7 @@ __global__ void __launch_bounds__(kThreads, BatchBlocks<false, TWO_D, NB>::value
         if (SLAB) hit = hit && restrict_to_slab(ray, sl.c0, sl.c1);
         if (hit) {
             if (NB == 1) {
-                const float y = __fmul_rn(walk_gather(ray, vol), ray.scale);
+                const float y = __fmul_rn(walk_gather<!TWO_D>(ray, vol), ray.scale);
                 sino[k] = SLAB ? __fadd_rn(sino[k], y) : y;
             } else {
                 const float none[NB] = {};
@@ -736,7 +742,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
         Ray ray;
         float out = 0.0f;
         if (setup_ray<F>(sv, g, u, v, ray) && ray.tend > 0.0f) {
-            const float ax = __fmul_rn(walk_gather(ray, x), ray.scale);
+            const float ax = __fmul_rn(walk_gather<!TWO_D>(ray, x), ray.scale);
             out = __fdiv_rn(__fsub_rn(__ldg(y + k), ax), __fmul_rn(ray.tend, ray.scale));
         }
         res[k] = out;
@@ -781,7 +787,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
         Ray ray;
         float q = 0.0f;
         if (setup_ray<F>(sv, g, u, v, ray))
-            q = __fmul_rn(walk_gather(ray, vol), ray.scale);
+            q = __fmul_rn(walk_gather<!TWO_D>(ray, vol), ray.scale);
         sino[((int64_t)c.view * tl.n_u + u) * tl.n_v + v] = q;
         sq = __fma_rn((double)q, (double)q, sq);
     }
