@@ -1,7 +1,8 @@
 """Full-size parity of the CUDA path (through the C ABI) against the float64 oracle.
 
-* the cone 256^3 x 360-view workload the benchmark times: EVERY ray of A against the oracle's
-  ray, and the WHOLE volume of A^T against the oracle's backprojection (relative L2);
+* the cone 256^3 x 360-view workload the benchmark times, and the two 2D workloads: EVERY ray of
+  A against the oracle's ray, and the WHOLE volume (image) of A^T against the oracle's
+  backprojection (relative L2);
 * the two 512^3 workloads (jittered spiral, dual-axis tilt series): every ray of full views,
   and a few thousand voxels of A^T computed one by one by the oracle.
 
@@ -140,3 +141,24 @@ def test_large_workloads_full_views_and_voxels(ct, n, views):
     nz = np.abs(want) > 0.1 * np.abs(want).max()
     assert nz.sum() > 100
     assert np.max(np.abs(b_gpu[vox][nz] - want[nz]) / np.abs(want[nz])) <= 1e-3
+
+
+@pytest.mark.parametrize("n", [1, 2])
+def test_2d_workloads_every_ray_and_whole_image(ct, n):
+    """The full 2D parallel (64^2, 90 views) and fan (512^2, 720 views) workloads: every ray of
+    A and the whole image of A^T."""
+    import torch
+    w = W.config(n)
+    x = w.phantom()
+    g = ct.Geometry.from_workload(w)
+    go = oracle.Geometry.from_workload(w)
+    y_gpu = _cpu(g.project(torch_cuda(x)))
+    y_or = go.project(x, threads=CORES)
+    L = _ray_lengths(go, 0, w.n_views)
+    assert (L > 0).mean() > 0.5
+    bad = fp_violations(y_gpu, y_or, L, float(np.abs(x).max()))
+    assert bad.size == 0, (bad.size, bad[:5])
+    y = np.abs(W.random_sinogram(w, 30 + n))
+    b_gpu = _cpu(g.backproject(torch_cuda(y)))
+    torch.cuda.empty_cache()
+    assert rel_l2(b_gpu, go.backproject(y, threads=CORES)) <= BP_RTOL

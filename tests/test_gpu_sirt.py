@@ -28,7 +28,7 @@ def ct():
     return ct
 
 
-@pytest.mark.parametrize("n", [1, 3, 5])
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5])
 def test_sirt_matches_oracle_small(ct, n):
     import torch
     w = W.small_config(n)
