@@ -478,8 +478,8 @@ def fdk_leg(ct, torch, w, peaks, sm_mhz, reps: int = 5, cpu_baseline: bool = Tru
 
 def context_leg(ct, torch):
     """The pages' performance-table workload shape (512^3 volume, circular cone, 360 views,
-    1024x768 detector at pitch 1.25; sid/sdd are not printed, 1000/1500 is this build's
-    reading): one forward projection, one backprojection, one CGLS iteration, CUDA events."""
+    1024x768 detector at pitch 1.25; sid/sdd are not printed and are read as 1000/1500): one
+    forward projection, one backprojection, one CGLS iteration, CUDA events."""
     views = W.circular_cone(360, 1000.0, 1500.0)
     w = W.Workload("cone-512^3-360v-1024x768", W.CONE, views, (512, 512, 512), 1.0, 1024, 768,
                    1.25, 1.25, 0, None)
