@@ -46,7 +46,8 @@ class GeometryInfo(ctypes.Structure):
                 ("volume_layout", ctypes.c_int32),
                 ("n_rays", ctypes.c_int64), ("n_voxels", ctypes.c_int64),
                 ("workspace_bytes", ctypes.c_size_t), ("sirt_workspace_bytes", ctypes.c_size_t),
-                ("n_slabs", ctypes.c_int32), ("slab_cells", ctypes.c_int32)]
+                ("n_slabs", ctypes.c_int32), ("slab_cells", ctypes.c_int32),
+                ("shared_lines", ctypes.c_int32)]
 
 
 _lib = None

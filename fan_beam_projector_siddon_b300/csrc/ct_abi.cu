@@ -507,6 +507,39 @@ ct_status create_impl(ct_beam beam, int32_t n_views, const double* views, int32_
         }
         R.lanes_along_v = (!is_2d(b) && std::fabs(v[fast]) >= std::fabs(u[fast])) ? 1 : 0;
     }
+    // Shared-line forward projections: 3D flat detectors whose lane-axis vector (pv for lanes
+    // along v, else pu) has no component on either outer axis in every view, with the lanes along
+    // the same detector axis in every view, so that the pixels of one detector line share their
+    // outer-axis line; and a volume no larger than L2 (measured: a 256^3 cone projects 22 %
+    // faster, a 512^3 helix 12 % slower, its lines' wider bands outgrowing L2).
+    {
+        const int oa = fast == 0 ? 1 : 0, ob = fast == 2 ? 1 : 2;
+        int dev = 0, l2 = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess) {
+            cudaGetLastError();
+            l2 = 0;
+        }
+        bool line = !is_2d(b) && !surface && nx + ny + nz - G.n[fast] <= ct::kLineMaxCells &&
+                    nvox * (int64_t)sizeof(float) <= (int64_t)l2;
+        for (int i = 0; line && i < n_views; ++i) {
+            const ct::ViewRec& R = recs[(size_t)i];
+            const double* lane = R.lanes_along_v ? R.pv : R.pu;
+            line = lane[oa] == 0.0 && lane[ob] == 0.0 && R.lanes_along_v == recs[0].lanes_along_v;
+        }
+        if (line) {
+            const int64_t n_lane = recs[0].lanes_along_v ? n_v : n_u;
+            const int64_t n_line = recs[0].lanes_along_v ? n_u : n_v;
+            const int64_t lane_tiles = (n_lane + ct::kLinePixels - 1) / ct::kLinePixels;
+            const int64_t line_tiles = (n_line + ct::kLineRows - 1) / ct::kLineRows;
+            if (lane_tiles * line_tiles * n_views <= (int64_t)INT32_MAX) {
+                T.line = recs[0].lanes_along_v ? 1 : 2;
+                I.shared_lines = T.line;
+                T.line_lane_tiles = (int32_t)lane_tiles;
+                T.line_row_tiles = (int32_t)line_tiles;
+            }
+        }
+    }
     cudaError_t e = cudaGetDevice(&g->device);
     if (e == cudaSuccess)
         e = cudaDeviceGetAttribute(&g->sm_count, cudaDevAttrMultiProcessorCount, g->device);
@@ -536,6 +569,14 @@ ct_status create_impl(ct_beam beam, int32_t n_views, const double* views, int32_
     g->info.slab_cells = nz;
     *out = g;
     return CT_OK;
+}
+
+// The handle's tiling with the shared-line walks off: the SIRT and CGLS iterations, whose fused
+// kernels walk per ray, take every walk that way so that their A^T is the transpose of their A.
+ct::Tiling per_ray_tiling(const ct_geometry* g) {
+    ct::Tiling t = g->tiling;
+    t.line = 0;
+    return t;
 }
 
 }  // namespace
@@ -669,12 +710,13 @@ ct_status ct_sirt_iterate(const ct_geometry* g, float* d_x, const float* d_y, vo
     const bool native = g->info.volume_layout == ct::LAYOUT_ZYX;
     float* X = native ? d_x : reinterpret_cast<float*>(ws + 2 * vb);
     float* Rres = reinterpret_cast<float*>(ws + (native ? 2 : 3) * vb);
+    // the fused solver kernels walk per ray, so every walk of the iteration does
+    const ct::Tiling rays = per_ray_tiling(g);
     cudaError_t e = cudaSuccess;
     if (!workspace_initialised) {
         // C = 1 / (A^T 1), b = 0
         e = cudaMemsetAsync(C, 0, volume_bytes(g), stream);
-        if (e == cudaSuccess)
-            e = ct::launch_backproject_ones(g->d_views, g->grid, g->tiling, C, stream);
+        if (e == cudaSuccess) e = ct::launch_backproject_ones(g->d_views, g->grid, rays, C, stream);
         if (e == cudaSuccess) e = ct::launch_invert(C, nvox, stream);
         if (e == cudaSuccess) e = cudaMemsetAsync(B, 0, volume_bytes(g), stream);
         if (e != cudaSuccess) return from_cuda(e);
@@ -682,9 +724,8 @@ ct_status ct_sirt_iterate(const ct_geometry* g, float* d_x, const float* d_y, vo
     if (n_iters == 0) return CT_OK;
     if (!native && (e = to_internal(g, d_x, X, stream)) != cudaSuccess) return from_cuda(e);
     for (int it = 0; it < n_iters && e == cudaSuccess; ++it) {
-        e = ct::launch_project_residual(g->d_views, g->grid, g->tiling, X, d_y, Rres, stream);
-        if (e == cudaSuccess)
-            e = ct::launch_backproject(g->d_views, g->grid, g->tiling, Rres, B, stream);
+        e = ct::launch_project_residual(g->d_views, g->grid, rays, X, d_y, Rres, stream);
+        if (e == cudaSuccess) e = ct::launch_backproject(g->d_views, g->grid, rays, Rres, B, stream);
         if (e == cudaSuccess) e = ct::launch_sirt_update(X, B, C, relaxation, nvox, stream);
     }
     if (e == cudaSuccess && !native) e = from_internal(g, X, d_x, stream);
@@ -830,17 +871,19 @@ ct_status ct_cgls_iterate(const ct_geometry* g, float* d_x, const float* d_y, vo
     float* Q = reinterpret_cast<float*>(ws + L.q);
     double* parts = reinterpret_cast<double*>(ws + L.partials);
     double* scal = reinterpret_cast<double*>(ws + L.scal);
-    const int64_t fp_parts = ct::project_blocks(g->tiling),
+    // the fused solver kernels walk per ray, so every walk of the iteration does
+    const ct::Tiling rays = per_ray_tiling(g);
+    const int64_t fp_parts = ct::project_blocks(rays),
                   nrm_parts = ct::norm_blocks(g->sm_count);
     const ct::ViewRec* V = g->d_views;
     cudaError_t e = cudaSuccess;
     if (!native) e = to_internal(g, d_x, X, stream);
     if (e == cudaSuccess && !workspace_initialised) {
         // r = y - A x;  s = A^T r;  p = s;  gamma = |s|^2
-        e = ct::launch_project(V, g->grid, g->tiling, X, Q, stream);
+        e = ct::launch_project(V, g->grid, rays, X, Q, stream);
         if (e == cudaSuccess) e = ct::launch_sub(R, d_y, Q, nray, stream);
         if (e == cudaSuccess) e = cudaMemsetAsync(S, 0, volume_bytes(g), stream);
-        if (e == cudaSuccess) e = ct::launch_backproject(V, g->grid, g->tiling, R, S, stream);
+        if (e == cudaSuccess) e = ct::launch_backproject(V, g->grid, rays, R, S, stream);
         if (e == cudaSuccess) e = cudaMemsetAsync(P, 0, volume_bytes(g), stream);
         if (e == cudaSuccess) e = ct::launch_norm_partials(S, nvox, parts, g->sm_count, stream);
         if (e == cudaSuccess) e = ct::launch_cgls_scalars(parts, nrm_parts, scal, 2, stream);
@@ -848,11 +891,11 @@ ct_status ct_cgls_iterate(const ct_geometry* g, float* d_x, const float* d_y, vo
     }
     for (int it = 0; it < n_iters && e == cudaSuccess; ++it) {
         // q = A p, delta = |q|^2, alpha = gamma / delta
-        e = ct::launch_project_norm(V, g->grid, g->tiling, P, Q, parts, stream);
+        e = ct::launch_project_norm(V, g->grid, rays, P, Q, parts, stream);
         if (e == cudaSuccess) e = ct::launch_cgls_scalars(parts, fp_parts, scal, 0, stream);
         // r -= alpha q, s = A^T r (s is zero here)
         if (e == cudaSuccess)
-            e = ct::launch_backproject_residual(V, g->grid, g->tiling, R, Q, scal, S, stream);
+            e = ct::launch_backproject_residual(V, g->grid, rays, R, Q, scal, S, stream);
         // beta = |s|^2 / gamma, gamma = |s|^2
         if (e == cudaSuccess) e = ct::launch_norm_partials(S, nvox, parts, g->sm_count, stream);
         if (e == cudaSuccess) e = ct::launch_cgls_scalars(parts, nrm_parts, scal, 1, stream);

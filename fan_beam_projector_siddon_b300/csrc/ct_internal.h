@@ -64,7 +64,19 @@ struct Tiling {
     int32_t n_u, n_v;
     int32_t tiles_u, tiles_v;  // 32 x 32 pixel tiles (2D: 256 x 1)
     int32_t two_d;
+    // Shared-line forward projections (siddon_kernels.cu): 0 off; 1 every view's rays of one
+    // detector column (fixed u) share their outer-axis line, lanes along v; 2 the same for rows
+    // (fixed v), lanes along u.  Blocks take kLinePixels pixels along the lanes times kLineRows
+    // lines.
+    int32_t line;
+    int32_t line_lane_tiles, line_row_tiles;
 };
+
+// Shared-line tiles: pixels along the lanes per block (its threads), lines per block, and the
+// largest outer-axis cell count n_a + n_b whose crossing list (8 bytes per entry) a block keeps.
+constexpr int kLinePixels = 128;
+constexpr int kLineRows = 8;
+constexpr int kLineMaxCells = 6000;
 
 // One slab of the inner (fastest) axis for the slab-tiled walks: the walks of a launch are
 // restricted to the inner-axis cells [c0, c1), over the detector tiles whose rays can reach the

@@ -96,6 +96,13 @@ typedef struct {
     int32_t n_slabs;          /* slabs of the inner axis the projector walks one at a time
                                  (1: the whole volume at once); see ct_geometry_set_slabs  */
     int32_t slab_cells;       /* cells of the inner axis per slab (the last may be shorter) */
+    int32_t shared_lines;     /* 1 (2): in every view the detector's v (u) axis has no
+                                 component on the two outer volume axes, so the rays of one
+                                 detector column (row) share their outer-axis crossings, and the
+                                 volume fits in the device's L2: the untiled forward projection
+                                 reads them from one list per line.  0: per-ray walks only.
+                                 The backprojection always walks per ray; the two walks agree
+                                 within float32 rounding of the crossing positions.        */
 } ct_geometry_info;
 
 /*

@@ -1,0 +1,181 @@
+"""Shared-line walks: when the detector axis along a block's lanes has no component on the two
+outer volume axes (and the volume fits in L2), the rays of one detector line share their
+outer-axis crossings, and the forward projection and the backprojection read them from one merged
+list per line (SIRT and CGLS keep the per-ray walks).
+
+* which handles use them (info.shared_lines) and which keep the per-ray walk;
+* every ray of A and the whole volume of A^T against the oracle, and the adjoint identity, on
+  geometries that exercise the lanes along v and along u, parallel lines at steep elevations,
+  rays entering and leaving through the inner-axis faces (lanes that start part-way along the
+  list, and short chords far along the line, which take the per-ray walk), per-axis pitches and
+  batched calls; SIRT on a shared-line handle against the oracle.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from fan_beam_projector_siddon_b300 import workloads as W
+from tests._parity import ADJ_RTOL, BP_RTOL, adjoint_gap, fp_violations, rel_l2, torch_cuda
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ct():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from fan_beam_projector_siddon_b300 import build
+    build.build()
+    import fan_beam_projector_siddon_b300 as ct
+    return ct
+
+
+def _cpu(t):
+    import torch
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+def _phantom(shape, seed):
+    return W.ellipsoids_3d(8, max(shape), np.random.default_rng(seed),
+                           axis_range=(3.0, 0.45 * min(shape)))[:shape[0], :shape[1], :shape[2]].copy()
+
+
+def _cone_lanes_u():
+    """Circular cone with det_u along z (the lanes run along u)."""
+    views = W.circular_cone(21, 150.0, 300.0).copy()
+    du_vec, dv_vec = views[:, 6:9].copy(), views[:, 9:12].copy()
+    views[:, 6:9], views[:, 9:12] = dv_vec, du_vec
+    shape = (37, 45, 53)
+    return W.Workload("cone-lanes-u", W.CONE, views, shape, 1.0, 47, 69, 1.2, 1.2, 5,
+                      lambda: _phantom(shape, 5))
+
+
+def _cone_through_faces():
+    """Circular cone with the source above the volume and the detector below it: most rays
+    enter through the top face and many leave through the bottom one."""
+    views = W.circular_cone(19, 60.0, 130.0).copy()
+    views[:, 2] += 40.0    # source z
+    views[:, 5] -= 45.0    # detector centre z
+    shape = (41, 39, 35)
+    return W.Workload("cone-faces", W.CONE, views, shape, 1.0, 77, 83, 1.3, 1.1, 6,
+                      lambda: _phantom(shape, 6))
+
+
+def _parallel_lines():
+    """Parallel rays at several azimuths and steep elevations, detector v along z."""
+    views = []
+    for k, (th, ph) in enumerate([(10, 5), (30, 45), (55, 70), (80, 85), (125, -60), (200, -20),
+                                  (290, 30), (345, -80)]):
+        th, ph = math.radians(th), math.radians(ph)
+        r = [math.cos(th) * math.cos(ph), math.sin(th) * math.cos(ph), math.sin(ph)]
+        views.append(r + [0.3 * k, -0.2, 0.1] + [-math.sin(th), math.cos(th), 0.0] + [0.0, 0.0, 1.0])
+    shape = (26, 22, 30)
+    return W.Workload("parallel-lines", W.PARALLEL3D, np.array(views), shape, 1.0, 45, 51, 0.9,
+                      0.8, 7, lambda: _phantom(shape, 7))
+
+
+CASES = [("cone-twin", lambda: W.small_config(3), 1), ("lanes-u", _cone_lanes_u, 2),
+         ("faces", _cone_through_faces, 1), ("parallel", _parallel_lines, 1),
+         ("aniso", lambda: W.anisotropic_config("cone"), 1)]
+
+
+def test_which_handles_share_lines(ct):
+    """Circular cone orbits with an upright detector share lines; 2D beams, the jittered spiral
+    (tilted detector), the dual-axis tilt series and surface detectors keep the per-ray walk."""
+    expect = {1: 0, 2: 0, 3: 1, 4: 0, 5: 0}
+    for n, want in expect.items():
+        assert ct.Geometry.from_workload(W.small_config(n)).info.shared_lines == want, n
+    assert ct.Geometry.from_workload(W.config(3)).info.shared_lines == 1
+    assert ct.Geometry.from_workload(W.config(4)).info.shared_lines == 0
+    w = W.small_config(3)
+    surf = ct.Geometry(w.beam, w.views, w.vol_shape, w.voxel_spacing, w.n_u, w.n_v, w.du, w.dv,
+                       offsets=W.flat_offsets(w.n_u, w.n_v, w.du, w.dv))
+    assert surf.info.shared_lines == 0
+    for _, make, want in CASES:
+        assert ct.Geometry.from_workload(make()).info.shared_lines == want
+
+
+def test_face_case_preconditions(ct):
+    """The face geometry has rays that start part-way along their line (entry through the top
+    face) and rays whose chord is short against their position along the line."""
+    w = _cone_through_faces()
+    go = oracle.Geometry.from_workload(w)
+    starts, short = 0, 0
+    for k in range(0, w.n_views, 3):
+        for iu in range(0, w.n_u, 4):
+            for iv in range(0, w.n_v, 4):
+                idx, seg = go.ray_segments(k, iu, iv)
+                if idx.size:
+                    z_first = idx[0] // (w.vol_shape[1] * w.vol_shape[2])
+                    starts += int(z_first == w.vol_shape[0] - 1)
+                    short += int(seg.sum() < 1.0)
+    assert starts > 200 and short > 2, (starts, short)
+
+
+@pytest.mark.parametrize("name,make,want", CASES)
+def test_lines_against_the_oracle(ct, name, make, want):
+    w = make()
+    g = ct.Geometry.from_workload(w)
+    assert g.info.shared_lines == want
+    go = oracle.Geometry.from_workload(w)
+    x = w.phantom().astype(np.float32)
+    y = _cpu(g.project(torch_cuda(x)))
+    y_or = go.project(x, threads=8)
+    L, _ = go.ray_lengths()
+    assert (L > 0).mean() > 0.3
+    bad = fp_violations(y, y_or, L, float(np.abs(x).max()))
+    assert bad.size == 0, (bad.size, bad[:8])
+    assert np.all(y[L == 0] == 0)
+    yy = np.abs(W.random_sinogram(w, 4))
+    b = _cpu(g.backproject(torch_cuda(yy)))
+    assert rel_l2(b, go.backproject(yy, threads=8)) <= BP_RTOL
+    rng = np.random.default_rng(9)
+    xr = rng.uniform(-1, 1, size=w.volume_shape).astype(np.float32)
+    yr = rng.uniform(-1, 1, size=w.sino_shape).astype(np.float32)
+    gap, lhs, rhs = adjoint_gap(_cpu(g.project(torch_cuda(xr))), yr, xr,
+                                _cpu(g.backproject(torch_cuda(yr))))
+    assert gap <= ADJ_RTOL, (gap, lhs, rhs)
+
+
+@pytest.mark.parametrize("name,make,want", CASES[:3])
+def test_batched_lines_equal_single(ct, name, make, want):
+    import torch
+    w = make()
+    g = ct.Geometry.from_workload(w)
+    rng = np.random.default_rng(2)
+    vols = torch_cuda(rng.uniform(0, 1, size=(7,) + tuple(w.volume_shape)))
+    sinos = g.project(vols)
+    for b in range(7):
+        assert torch.equal(sinos[b], g.project(vols[b].contiguous()))
+    ys = torch_cuda(rng.uniform(-1, 1, size=(7,) + tuple(w.sino_shape)))
+    backs = g.backproject(ys)
+    for b in range(7):
+        assert rel_l2(_cpu(backs[b]), _cpu(g.backproject(ys[b].contiguous()))) <= 1e-6
+
+
+def test_lines_are_deterministic(ct):
+    w = _cone_through_faces()
+    g = ct.Geometry.from_workload(w)
+    x = torch_cuda(w.phantom())
+    a = _cpu(g.project(x))
+    for _ in range(3):
+        assert np.array_equal(_cpu(g.project(x)), a)
+
+
+def test_sirt_on_a_shared_line_handle(ct):
+    """SIRT iterations walk per ray on every handle: on a shared-line handle they match the
+    oracle's SIRT as on any other (relative L2 after 10 iterations, as the SIRT parity tests)."""
+    import torch
+    w = _cone_lanes_u()
+    g = ct.Geometry.from_workload(w)
+    assert g.info.shared_lines == 2
+    go = oracle.Geometry.from_workload(w)
+    y_or = go.project(w.phantom().astype(np.float32), threads=8)
+    x_or, _ = go.sirt(y_or, 10)
+    x = torch.zeros(tuple(w.volume_shape), dtype=torch.float32, device="cuda")
+    g.sirt(x, torch_cuda(y_or), 10, g.new_workspace(sirt=True), initialised=False)
+    assert rel_l2(_cpu(x), x_or) <= 1e-4

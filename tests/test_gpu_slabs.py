@@ -2,8 +2,9 @@
 slab of the inner axis per launch, each ray restarting from its own crossing values.
 
 * forced slabs on small cone and jittered-spiral twins: every ray of A against the oracle, the
-  whole volume of A^T, the adjoint identity, and agreement with the untiled walk (the per-segment
-  weights are the same; the forward sums are added per slab);
+  whole volume of A^T, the adjoint identity, and agreement with the untiled walk (the per-ray
+  walks' segment weights are the same and the forward sums are added per slab; untiled
+  shared-line walks are held to the oracle instead);
 * tall volumes crossed by steep rays, so that rays cross several slabs;
 * batched calls with slabs equal single calls;
 * tiling is opt-in (measured slower on the 512^3 spiral, see include/ct.h).
@@ -70,11 +71,21 @@ def test_slabs_match_the_oracle_and_the_untiled_walk(ct, name, make):
     bad = fp_violations(y, y_or, L, float(np.abs(x).max()))
     assert bad.size == 0, (bad.size, bad[:5])
     assert np.all(y[L == 0] == 0)
-    # the same segments, summed per slab: within float32 rounding of the untiled sums
-    assert np.max(np.abs(y - y_whole)) <= 1e-5 * max(1.0, float(np.abs(y_whole).max()))
+    # Without shared lines the untiled walk takes the same segments, summed per slab: within
+    # float32 rounding of the untiled sums.  With shared lines the untiled walks measure their
+    # crossings along the line instead (other float32 roundings), so both are held to the oracle.
+    same_segments = g.info.shared_lines == 0
+    if same_segments:
+        assert np.max(np.abs(y - y_whole)) <= 1e-5 * max(1.0, float(np.abs(y_whole).max()))
+    else:
+        assert fp_violations(y_whole, y_or, L, float(np.abs(x).max())).size == 0
     b = _cpu(g.backproject(torch_cuda(yy)))
-    assert rel_l2(b, go.backproject(yy, threads=8)) <= BP_RTOL
-    assert rel_l2(b, b_whole) <= 1e-6
+    b_or = go.backproject(yy, threads=8)
+    assert rel_l2(b, b_or) <= BP_RTOL
+    if same_segments:
+        assert rel_l2(b, b_whole) <= 1e-6
+    else:
+        assert rel_l2(b_whole, b_or) <= BP_RTOL
     rng = np.random.default_rng(3)
     xr = rng.uniform(-1, 1, size=w.volume_shape).astype(np.float32)
     yr = rng.uniform(-1, 1, size=w.sino_shape).astype(np.float32)
