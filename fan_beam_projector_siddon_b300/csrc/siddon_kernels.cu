@@ -656,92 +656,6 @@ __device__ __forceinline__ TileCoord tile_of_slab_block(const SlabArgs& sl, cons
     return c;
 }
 
-// sino[b] = A vol[b] for the NB volumes vol + b * vstride (internal order) and sinograms
-// sino + b * sstride; one walk per ray serves all NB volumes.  SLAB: the walks are restricted to
-// one slab of the inner axis and each ray's partial sum is added to its sinogram entry.
-template <bool TWO_D, int F, int NB, bool SLAB>
-__global__ void __launch_bounds__(kThreads, BatchBlocks<false, TWO_D, NB>::value)
-    project_kernel(const ViewRec* __restrict__ views, const Grid g, const Tiling tl,
-                   const float* __restrict__ vol, int64_t vstride, float* __restrict__ sino,
-                   int64_t sstride, const SlabArgs sl) {
-    __shared__ ViewRec sv;
-    __shared__ ViewRecF sf;
-    const TileCoord c = SLAB ? tile_of_slab_block(sl, tl) : tile_of_block(tl);
-    load_view(views, c.view, sv);
-    if (SLAB) load_view_f32(sv, sf);
-#pragma unroll 1
-    for (int row = 0; row < (TWO_D ? 1 : kRows); ++row) {
-        int u, v;
-        pixel_of<TWO_D>(c, sv, row, u, v);
-        if (u >= tl.n_u || v >= tl.n_v) continue;
-        if (SLAB && !may_reach_slab<F>(sf, g, u, v, sl.c0, sl.c1)) continue;
-        const int64_t k = ((int64_t)c.view * tl.n_u + u) * tl.n_v + v;
-        Ray ray;
-        bool hit = setup_ray<F>(sv, g, u, v, ray);
-        if (SLAB) hit = hit && restrict_to_slab(ray, sl.c0, sl.c1);
-        if (hit) {
-            if (NB == 1) {
-                const float y = __fmul_rn(walk_gather<!TWO_D>(ray, vol), ray.scale);
-                sino[k] = SLAB ? __fadd_rn(sino[k], y) : y;
-            } else {
-                const float none[NB] = {};
-                float acc[NB];
-                walk_dispatch<false, NB>(ray, vol, nullptr, vstride, none, acc);
-#pragma unroll
-                for (int b = 0; b < NB; ++b) {
-                    const float y = __fmul_rn(acc[b], ray.scale);
-                    sino[b * sstride + k] = SLAB ? __fadd_rn(sino[b * sstride + k], y) : y;
-                }
-            }
-        } else if (!SLAB) {
-#pragma unroll
-            for (int b = 0; b < NB; ++b) sino[b * sstride + k] = 0.0f;
-        }
-    }
-}
-
-// MODE 0: scatter sino * (physical length per voxel-space length); MODE 1: the same for a sinogram
-// of ones (A^T 1).  NB volumes/sinograms at strides vstride/sstride, one walk per ray.  SLAB: the
-// walks are restricted to one slab of the inner axis.
-template <bool TWO_D, int F, int MODE, int NB, bool SLAB>
-__global__ void __launch_bounds__(kThreads, BatchBlocks<true, TWO_D, NB>::value)
-    backproject_kernel(const ViewRec* __restrict__ views, const Grid g, const Tiling tl,
-                       const float* __restrict__ sino, int64_t sstride, float* __restrict__ vol,
-                       int64_t vstride, const SlabArgs sl) {
-    __shared__ ViewRec sv;
-    __shared__ ViewRecF sf;
-    const TileCoord c = SLAB ? tile_of_slab_block(sl, tl) : tile_of_block(tl);
-    load_view(views, c.view, sv);
-    if (SLAB) load_view_f32(sv, sf);
-#pragma unroll 1
-    for (int row = 0; row < (TWO_D ? 1 : kRows); ++row) {
-        int u, v;
-        pixel_of<TWO_D>(c, sv, row, u, v);
-        if (u >= tl.n_u || v >= tl.n_v) continue;
-        if (SLAB && !may_reach_slab<F>(sf, g, u, v, sl.c0, sl.c1)) continue;
-        const int64_t k = ((int64_t)c.view * tl.n_u + u) * tl.n_v + v;
-        float y[NB];
-        bool any = false;
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {
-            y[b] = MODE == 0 ? __ldg(sino + b * sstride + k) : 1.0f;
-            any |= y[b] != 0.0f;
-        }
-        if (!any) continue;
-        Ray ray;
-        if (!setup_ray<F>(sv, g, u, v, ray)) continue;
-        if (SLAB && !restrict_to_slab(ray, sl.c0, sl.c1)) continue;
-        if (NB == 1) {
-            walk_scatter(ray, vol, __fmul_rn(y[0], ray.scale));
-        } else {
-            float val[NB], unused[NB];
-#pragma unroll
-            for (int b = 0; b < NB; ++b) val[b] = __fmul_rn(y[b], ray.scale);
-            walk_dispatch<true, NB>(ray, nullptr, vol, vstride, val, unused);
-        }
-    }
-}
-
 // ---- Shared-line walks ----------------------------------------------------------------------
 // When the detector axis that a block's lanes run along has no component on either outer axis
 // (det_v along z with the z-fastest order: every circular fan or cone orbit with an upright
@@ -764,14 +678,17 @@ __global__ void __launch_bounds__(kThreads, BatchBlocks<true, TWO_D, NB>::value)
 // moved by the crossings in order, so it lies inside the square; a ray moves along the inner axis
 // at most n times from an entry cell inside the grid, so every index a walk forms is in bounds.
 //
-// The backprojection walks the same lines, so that A^T stays the exact transpose of A (the same
-// segments with the same operations); against the per-ray walk it issues the same reduction
-// sectors and runs 2.5 % slower (its list reads share the L1 unit that the reductions saturate),
-// while pairing the line forward walk with the per-ray backprojection left adjoint gaps of 3e-5.
-// Lines are used only for volumes that fit in L2: on a 512^3 volume (untilted helix) the forward
-// walk took 120 ms against 107 and the backprojection 192 against 143, a block's band of 128
-// detector pixels spanning four times the volume slab of the per-ray tiles.  Blocks walking two,
-// four or eight lines at once (fewer pixels per line) ran slower on both sizes.
+// The backprojection takes the same segments without the list: line_setup_ray gives the per-ray
+// walk the line's parameters (its outer crossings in s, counted from the ray's range, and the
+// ray's own inner crossings), and the per-ray walk visits the merged crossings in the list's order
+// (first axis first on ties) with the same arithmetic, so A^T stays the exact transpose of A.  A
+// list-reading scatter issued the same reduction sectors but ran 2.5 % slower (its list reads
+// share the L1 unit that the reductions saturate); pairing the list forward walk with the
+// backprojection of the per-ray parameters left adjoint gaps of 3e-5 on rays entering through
+// the inner-axis faces.  Lines are used only for volumes that fit in L2: on a 512^3 volume
+// (untilted helix) the forward walk took 120 ms against 107, a block's band of 128 detector pixels
+// spanning four times the volume slab of the per-ray tiles.  Blocks walking two, four or eight
+// lines at once (fewer pixels per line) ran slower on both sizes.
 
 struct LineEntry {
     float s;   // crossing position
@@ -931,19 +848,17 @@ __device__ __forceinline__ bool line_ray(const ViewRec& vr, const Grid& g, const
     return true;
 }
 
-// The walk of one ray along the list entries [j0, j1) (the outer crossings inside its range) and
-// then to its exit.  GATHER: acc = sum_k vol[idx_k] * ds_k for the NB volumes at vin + b * vstride;
-// SCATTER: adds val * ds_k to vol[idx_k] of the NB volumes at vout.  ISIGN and SINGLE as in walk
-// (the inner axis has unit stride); with SINGLE every step takes at most one inner crossing and
-// the crossing after the ray's last one lies at or after entry j1 - 1, so the main loop needs no
-// exhaustion check, and the gather loads the next step's values (the voxel after the outer
-// crossing and, when an inner crossing comes first, the one after it) one step ahead.  All forms
-// take the same segments with the same operations.
-template <bool SCATTER, int NB, int ISIGN, bool SINGLE>
+// The gather of one ray along the list entries [j0, j1) (the outer crossings inside its range) and
+// then to its exit: acc = sum_k vol[idx_k] * ds_k for the NB volumes at vin + b * vstride.  ISIGN
+// and SINGLE as in walk (the inner axis has unit stride); with SINGLE every step takes at most
+// one inner crossing and the crossing after the ray's last one lies at or after entry j1 - 1, so
+// the main loop needs no exhaustion check, and it loads the next step's values (the voxel after
+// the outer crossing and, when an inner crossing comes first, the one after it) one step ahead.
+// Both forms take the same segments with the same operations as walk() on line_setup_ray's Ray.
+template <int NB, int ISIGN, bool SINGLE>
 __device__ __forceinline__ void line_walk(const LineEntry* __restrict__ E, int j0, int j1,
                                           const LineRay& r, const float* __restrict__ vin,
-                                          float* __restrict__ vout, int64_t vstride,
-                                          const float (&val)[NB], float (&acc)[NB]
+                                          int64_t vstride, float (&acc)[NB]
 #ifdef CT_DEBUG_BOUNDS
                                           , int64_t nvox
 #endif
@@ -972,20 +887,12 @@ __device__ __forceinline__ void line_walk(const LineEntry* __restrict__ E, int j
 #pragma unroll
         for (int b = 0; b < NB; ++b) acc[b] = __fmaf_rn(v[b], seg, acc[b]);
     };
-    auto take = [&](int i, float seg) {  // one segment (the gather loads where it takes it)
-        if (SCATTER) {
-#ifdef CT_DEBUG_BOUNDS
-            if (!in_bounds(i, nvox)) return;
-#endif
-#pragma unroll
-            for (int b = 0; b < NB; ++b) atomicAdd(vout + b * vstride + i, __fmul_rn(val[b], seg));
-        } else {
-            float v[NB];
-            load(i, v);
-            gather(v, seg);
-        }
+    auto take = [&](int i, float seg) {  // one segment, loaded where it is taken
+        float v[NB];
+        load(i, v);
+        gather(v, seg);
     };
-    if (SINGLE && !SCATTER) {
+    if (SINGLE) {
         if (j1 > j0) {
             LineEntry e = E[j0];
             int idx = e.cell + zoff;
@@ -1019,39 +926,26 @@ __device__ __forceinline__ void line_walk(const LineEntry* __restrict__ E, int j
             }
             t = e.s;
         }
+        // (the crossing after the last inner one was computed instead of +inf: restore +inf)
+        if (!(kf < nf)) tf = INF;
     } else {
-        // not unrolled: unrolled by two (four) the scatter issued 6 % (14 %) more reduction
-        // sectors for the same requests on the cone 256^3 workload, and ran that much slower
 #pragma unroll 1
         for (int j = j0; j < j1; ++j) {
             const LineEntry e = E[j];
             int idx = e.cell + zoff;
-            if (SINGLE) {
-                const bool p = tf < e.s;
-                take(idx, __fsub_rn(p ? tf : e.s, t));
-                if (p) {
-                    take(idx + s2, __fsub_rn(e.s, tf));
-                    zoff += s2;
-                    kf += 1.0f;
-                    tf = __fmaf_rn(kf, r.dt, r.t0);
-                }
-            } else {
 #pragma unroll 1
-                while (tf < e.s) {
-                    take(idx, __fsub_rn(tf, t));
-                    idx += s2;
-                    zoff += s2;
-                    t = tf;
-                    kf += 1.0f;
-                    tf = kf < nf ? __fmaf_rn(kf, r.dt, r.t0) : INF;
-                }
-                take(idx, __fsub_rn(e.s, t));
+            while (tf < e.s) {
+                take(idx, __fsub_rn(tf, t));
+                idx += s2;
+                zoff += s2;
+                t = tf;
+                kf += 1.0f;
+                tf = kf < nf ? __fmaf_rn(kf, r.dt, r.t0) : INF;
             }
+            take(idx, __fsub_rn(e.s, t));
             t = e.s;
         }
     }
-    // (SINGLE computed the crossing after the last inner one instead of +inf: restore +inf)
-    if (SINGLE && !(kf < nf)) tf = INF;
     int idx = E[j1].cell + zoff;
 #pragma unroll 1
     while (tf < r.s1) {
@@ -1066,13 +960,11 @@ __device__ __forceinline__ void line_walk(const LineEntry* __restrict__ E, int j
 
 // Picks the line walk's specialisation for the lanes that walk together (see walk_dispatch for
 // the one-inner-crossing bound: here the gaps are those between successive list entries).
-template <bool SCATTER, int NB>
+template <int NB>
 __device__ __forceinline__ void line_walk_dispatch(const LineEntry* __restrict__ E, int j0,
                                                    int j1, const LineRow& L, const LineRay& r,
-                                                   const float* __restrict__ vin,
-                                                   float* __restrict__ vout, int64_t vstride,
-                                                   const float (&val)[NB], float (&acc)[NB],
-                                                   int64_t nvox) {
+                                                   const float* __restrict__ vin, int64_t vstride,
+                                                   float (&acc)[NB], int64_t nvox) {
     const unsigned m = __activemask();
     const bool none = r.n == 0;
     const float last = j1 > j0 ? E[j1 - 1].s : -f_inf();
@@ -1086,59 +978,114 @@ __device__ __forceinline__ void line_walk_dispatch(const LineEntry* __restrict__
     (void)nvox;
 #endif
     if (__all_sync(m, single && (none || r.step == 1)))
-        line_walk<SCATTER, NB, 1, true>(E, j0, j1, r, vin, vout, vstride, val, acc CT_LINE_NVOX);
+        line_walk<NB, 1, true>(E, j0, j1, r, vin, vstride, acc CT_LINE_NVOX);
     else if (__all_sync(m, single && (none || r.step == -1)))
-        line_walk<SCATTER, NB, -1, true>(E, j0, j1, r, vin, vout, vstride, val, acc CT_LINE_NVOX);
+        line_walk<NB, -1, true>(E, j0, j1, r, vin, vstride, acc CT_LINE_NVOX);
     else if (__all_sync(m, single))
-        line_walk<SCATTER, NB, 0, true>(E, j0, j1, r, vin, vout, vstride, val, acc CT_LINE_NVOX);
+        line_walk<NB, 0, true>(E, j0, j1, r, vin, vstride, acc CT_LINE_NVOX);
     else
-        line_walk<SCATTER, NB, 0, false>(E, j0, j1, r, vin, vout, vstride, val, acc CT_LINE_NVOX);
+        line_walk<NB, 0, false>(E, j0, j1, r, vin, vstride, acc CT_LINE_NVOX);
 #undef CT_LINE_NVOX
 }
 
-// The per-ray walk of one whole pixel (lines with no extent in the outer plane, short chords far
-// along their line): writes its line integrals, or reads its sinogram values and scatters them.
-// Kept out of line, with no array crossing the call, so that it adds nothing to the register use
-// of the line walk (an accumulator array passed to it by reference had kept the line walk's sums
-// in local memory).
-template <int F, bool SCATTER, int NB>
-__device__ __noinline__ void ray_pixel(const ViewRec& sv, const Grid& g, int u, int v, int64_t k,
-                                       const float* __restrict__ vol_in,
-                                       const float* __restrict__ sino_in,
-                                       float* __restrict__ vol_out, float* __restrict__ sino_out,
-                                       int64_t vstride, int64_t sstride) {
-    Ray ray;
-    const bool hit = setup_ray<F>(sv, g, u, v, ray);
-    float val[NB], acc[NB];
-#pragma unroll
-    for (int c = 0; c < NB; ++c)
-        val[c] = SCATTER ? __fmul_rn(__ldg(sino_in + c * sstride + k), ray.scale) : 0.0f;
-    if (hit) walk_dispatch<SCATTER, NB>(ray, vol_in, vol_out, vstride, val, acc);
-    if (!SCATTER) {
-#pragma unroll
-        for (int c = 0; c < NB; ++c)
-            sino_out[c * sstride + k] = hit ? __fmul_rn(acc[c], ray.scale) : 0.0f;
-    }
+// Rays whose chord is under 1/16 of their exit position along the line take the per-ray
+// parameterisation (setup_ray) in every shared-line walk: positions along the line carry absolute
+// rounding errors of a few ulps of s, too coarse against a short chord far along the line, while
+// setup_ray's positions start at the ray's own entry.
+__device__ __forceinline__ bool short_on_line(const LineRay& r) {
+    return __fsub_rn(r.s1, r.s0) < __fmul_rn(0.0625f, r.s1);
 }
 
-// Resident blocks per SM of the line kernels (kLinePixels threads each): 2048, 1280 or 1024
-// threads per SM for one, two or four volumes, 1536 for the scatter of one.
-template <bool SCATTER, int NB>
+// List entries [j0, j1) of a ray: the line's outer crossings at or before s0 come before its
+// range, those strictly before s1 inside it.
+__device__ __forceinline__ void line_range(const LineRow& L, const LineRay& r, int& ka0, int& kb0,
+                                           int& ka1, int& kb1) {
+    ka0 = 0;
+    kb0 = 0;
+    if (r.s0 > 0.0f) {
+        ka0 = crossings_before<true>(r.s0, L.t0[0], L.dt[0], L.n[0]);
+        kb0 = crossings_before<true>(r.s0, L.t0[1], L.dt[1], L.n[1]);
+    }
+    ka1 = max(ka0, crossings_before<false>(r.s1, L.t0[0], L.dt[0], L.n[0]));
+    kb1 = max(kb0, crossings_before<false>(r.s1, L.t0[1], L.dt[1], L.n[1]));
+}
+
+// The per-ray form of a shared-line walk for pixel (u, v): the Ray whose walk() takes the list
+// walk's segments.  Its outer slots are the line's two axes with their crossings in s, restricted
+// to the ray's range (k0 = crossings at or before s0, n = crossings before s1), its inner slot the
+// ray's own crossings, and it runs from s0 to s1 with the line's physical length factor.  walk()
+// takes the merged outer crossings in the list's order (first axis first on ties) with the same
+// arithmetic, so every segment has the list walk's bits.  Returns 0 when the ray misses, 1 with r
+// set, 2 when the ray takes the per-ray parameterisation (setup_ray) in the list walk as well.
+template <int F>
+__device__ __forceinline__ int line_setup_ray(const ViewRec& sv, const Grid& g, bool along_v,
+                                              int u, int v, Ray& r) {
+    LineRow L;
+    const int st = line_row<F>(sv, g, along_v, along_v ? u : v, L);
+    if (st != 1) return st;
+    LineRay lr;
+    if (!line_ray<F>(sv, g, L, u, v, lr)) return 0;
+    if (short_on_line(lr)) return 2;
+    int ka0, kb0, ka1, kb1;
+    line_range(L, lr, ka0, kb0, ka1, kb1);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        r.t0[j] = L.t0[j];
+        r.dt[j] = L.dt[j];
+        r.step[j] = L.step[j];
+    }
+    r.n[0] = ka1;
+    r.n[1] = kb1;
+    r.k0[0] = (float)ka0;
+    r.k0[1] = (float)kb0;
+    r.t0[2] = lr.t0;
+    r.dt[2] = lr.dt;
+    r.n[2] = lr.n;
+    r.k0[2] = 0.0f;
+    r.step[2] = lr.step;
+    r.idx = L.cell + ka0 * L.step[0] + kb0 * L.step[1] + lr.zoff;
+    r.entry_in = lr.zoff / g.stride[F];
+    r.tstart = lr.s0;
+    r.tend = lr.s1;
+    r.scale = lr.fac;
+#ifdef CT_DEBUG_BOUNDS
+    r.nvox = (int64_t)g.n[0] * g.n[1] * g.n[2];
+#endif
+    return 1;
+}
+
+// The per-ray forward projection of one whole pixel (lines with no extent in the outer plane,
+// short chords far along their line), writing its line integrals.  Kept out of line, with no
+// array crossing the call, so that it adds nothing to the register use of the line walk (an
+// accumulator array passed to it by reference had kept the line walk's sums in local memory).
+template <int F, int NB>
+__device__ __noinline__ void ray_pixel(const ViewRec& sv, const Grid& g, int u, int v, int64_t k,
+                                       const float* __restrict__ vol, int64_t vstride,
+                                       float* __restrict__ sino, int64_t sstride) {
+    Ray ray;
+    const bool hit = setup_ray<F>(sv, g, u, v, ray);
+    const float none[NB] = {};
+    float acc[NB];
+    if (hit) walk_dispatch<false, NB>(ray, vol, nullptr, vstride, none, acc);
+#pragma unroll
+    for (int c = 0; c < NB; ++c) sino[c * sstride + k] = hit ? __fmul_rn(acc[c], ray.scale) : 0.0f;
+}
+
+// Resident blocks per SM of the line kernel (kLinePixels threads each): 2048, 1280 or 1024
+// threads per SM for one, two or four volumes.
+template <int NB>
 struct LineBlocks {
-    static constexpr int value =
-        (NB == 1 ? (SCATTER ? 1536 : 2048) : (NB == 2 ? 1280 : 1024)) / kLinePixels;
+    static constexpr int value = (NB == 1 ? 2048 : (NB == 2 ? 1280 : 1024)) / kLinePixels;
 };
 
-// SCATTER false: sino[b] = A vol[b]; true: vol[b] += A^T sino[b]; NB volumes over shared-line
-// tiles: a block takes kLinePixels pixels of kLineRows successive lines of one view.  Blocks are
-// ordered lane tile first, then view, then line tile (one band of the detector across all views
-// at a time, as tile_of_block).
-template <int F, bool SCATTER, int NB>
-__global__ void __launch_bounds__(kLinePixels, LineBlocks<SCATTER, NB>::value)
-    line_kernel(const ViewRec* __restrict__ views, const Grid g, const Tiling tl,
-                const float* __restrict__ vol_in, const float* __restrict__ sino_in,
-                float* __restrict__ vol_out, float* __restrict__ sino_out, int64_t vstride,
-                int64_t sstride) {
+// sino[b] = A vol[b] for NB volumes over shared-line tiles: a block takes kLinePixels pixels of
+// kLineRows successive lines of one view.  Blocks are ordered lane tile first, then view, then
+// line tile (one band of the detector across all views at a time, as tile_of_block).
+template <int F, int NB>
+__global__ void __launch_bounds__(kLinePixels, LineBlocks<NB>::value)
+    line_project_kernel(const ViewRec* __restrict__ views, const Grid g, const Tiling tl,
+                        const float* __restrict__ vol, int64_t vstride, float* __restrict__ sino,
+                        int64_t sstride) {
     extern __shared__ LineEntry line_list[];
     __shared__ ViewRec sv;
     int b = (int)blockIdx.x;
@@ -1166,53 +1113,124 @@ __global__ void __launch_bounds__(kLinePixels, LineBlocks<SCATTER, NB>::value)
         }
         if (valid) {
             const int64_t k = ((int64_t)view * tl.n_u + u) * tl.n_v + v;
-            float y[NB];
-            bool any = !SCATTER;
-#pragma unroll
-            for (int c = 0; c < NB; ++c) {
-                y[c] = SCATTER ? __ldg(sino_in + c * sstride + k) : 0.0f;
-                any |= y[c] != 0.0f;
-            }
-            bool per_ray = any && st == 2;
-            if (any && st == 1) {
+            bool per_ray = st == 2;
+            if (st == 1) {
                 LineRay r;
                 const bool hit = line_ray<F>(sv, g, L, u, v, r);
-                // Positions along the line carry absolute rounding errors of a few ulps of s;
-                // against a short chord far along the line that is too coarse, so such rays (a
-                // chord under 1/16 of the ray's exit position) take the per-ray walk, whose
-                // positions start at the ray's own entry.
-                per_ray = hit && __fsub_rn(r.s1, r.s0) < __fmul_rn(0.0625f, r.s1);
+                per_ray = hit && short_on_line(r);
                 if (hit && !per_ray) {
-                    int j0 = 0;
-                    if (r.s0 > 0.0f)
-                        j0 = crossings_before<true>(r.s0, L.t0[0], L.dt[0], L.n[0]) +
-                             crossings_before<true>(r.s0, L.t0[1], L.dt[1], L.n[1]);
-                    const int j1 = max(j0, crossings_before<false>(r.s1, L.t0[0], L.dt[0], L.n[0]) +
-                                               crossings_before<false>(r.s1, L.t0[1], L.dt[1],
-                                                                       L.n[1]));
-                    float val[NB], acc[NB];
+                    int ka0, kb0, ka1, kb1;
+                    line_range(L, r, ka0, kb0, ka1, kb1);
+                    float acc[NB];
+                    line_walk_dispatch<NB>(line_list, ka0 + kb0, ka1 + kb1, L, r, vol, vstride,
+                                           acc, nvox);
 #pragma unroll
-                    for (int c = 0; c < NB; ++c) val[c] = __fmul_rn(y[c], r.fac);
-                    line_walk_dispatch<SCATTER, NB>(line_list, j0, j1, L, r, vol_in, vol_out,
-                                                    vstride, val, acc, nvox);
-                    if (!SCATTER) {
+                    for (int c = 0; c < NB; ++c) sino[c * sstride + k] = __fmul_rn(acc[c], r.fac);
+                } else if (!hit) {
 #pragma unroll
-                        for (int c = 0; c < NB; ++c)
-                            sino_out[c * sstride + k] = __fmul_rn(acc[c], r.fac);
-                    }
-                } else if (!hit && !SCATTER) {
-#pragma unroll
-                    for (int c = 0; c < NB; ++c) sino_out[c * sstride + k] = 0.0f;
+                    for (int c = 0; c < NB; ++c) sino[c * sstride + k] = 0.0f;
                 }
-            } else if (st == 0 && !SCATTER) {
+            } else if (st == 0) {
 #pragma unroll
-                for (int c = 0; c < NB; ++c) sino_out[c * sstride + k] = 0.0f;
+                for (int c = 0; c < NB; ++c) sino[c * sstride + k] = 0.0f;
             }
-            if (per_ray)
-                ray_pixel<F, SCATTER, NB>(sv, g, u, v, k, vol_in, sino_in, vol_out, sino_out,
-                                          vstride, sstride);
+            if (per_ray) ray_pixel<F, NB>(sv, g, u, v, k, vol, vstride, sino, sstride);
         }
         if (st == 1) __syncthreads();  // the next line overwrites the list
+    }
+}
+
+// sino[b] = A vol[b] for the NB volumes vol + b * vstride (internal order) and sinograms
+// sino + b * sstride; one walk per ray serves all NB volumes.  SLAB: the walks are restricted to
+// one slab of the inner axis and each ray's partial sum is added to its sinogram entry.
+template <bool TWO_D, int F, int NB, bool SLAB>
+__global__ void __launch_bounds__(kThreads, BatchBlocks<false, TWO_D, NB>::value)
+    project_kernel(const ViewRec* __restrict__ views, const Grid g, const Tiling tl,
+                   const float* __restrict__ vol, int64_t vstride, float* __restrict__ sino,
+                   int64_t sstride, const SlabArgs sl) {
+    __shared__ ViewRec sv;
+    __shared__ ViewRecF sf;
+    const TileCoord c = SLAB ? tile_of_slab_block(sl, tl) : tile_of_block(tl);
+    load_view(views, c.view, sv);
+    if (SLAB) load_view_f32(sv, sf);
+#pragma unroll 1
+    for (int row = 0; row < (TWO_D ? 1 : kRows); ++row) {
+        int u, v;
+        pixel_of<TWO_D>(c, sv, row, u, v);
+        if (u >= tl.n_u || v >= tl.n_v) continue;
+        if (SLAB && !may_reach_slab<F>(sf, g, u, v, sl.c0, sl.c1)) continue;
+        const int64_t k = ((int64_t)c.view * tl.n_u + u) * tl.n_v + v;
+        Ray ray;
+        bool hit = setup_ray<F>(sv, g, u, v, ray);
+        if (SLAB) hit = hit && restrict_to_slab(ray, sl.c0, sl.c1);
+        if (hit) {
+            if (NB == 1) {
+                const float y = __fmul_rn(walk_gather<!TWO_D>(ray, vol), ray.scale);
+                sino[k] = SLAB ? __fadd_rn(sino[k], y) : y;
+            } else {
+                const float none[NB] = {};
+                float acc[NB];
+                walk_dispatch<false, NB>(ray, vol, nullptr, vstride, none, acc);
+#pragma unroll
+                for (int b = 0; b < NB; ++b) {
+                    const float y = __fmul_rn(acc[b], ray.scale);
+                    sino[b * sstride + k] = SLAB ? __fadd_rn(sino[b * sstride + k], y) : y;
+                }
+            }
+        } else if (!SLAB) {
+#pragma unroll
+            for (int b = 0; b < NB; ++b) sino[b * sstride + k] = 0.0f;
+        }
+    }
+}
+
+// MODE 0: scatter sino * (physical length per voxel-space length); MODE 1: the same for a sinogram
+// of ones (A^T 1).  NB volumes/sinograms at strides vstride/sstride, one walk per ray.  SLAB: the
+// walks are restricted to one slab of the inner axis.  LINE: the rays take the shared-line
+// parameters (line_setup_ray), so that this is the exact transpose of line_project_kernel.
+template <bool TWO_D, int F, int MODE, int NB, bool SLAB, bool LINE = false>
+__global__ void __launch_bounds__(kThreads, BatchBlocks<true, TWO_D, NB>::value)
+    backproject_kernel(const ViewRec* __restrict__ views, const Grid g, const Tiling tl,
+                       const float* __restrict__ sino, int64_t sstride, float* __restrict__ vol,
+                       int64_t vstride, const SlabArgs sl) {
+    static_assert(!(LINE && (SLAB || TWO_D)), "shared lines are for untiled 3D walks");
+    __shared__ ViewRec sv;
+    __shared__ ViewRecF sf;
+    const TileCoord c = SLAB ? tile_of_slab_block(sl, tl) : tile_of_block(tl);
+    load_view(views, c.view, sv);
+    if (SLAB) load_view_f32(sv, sf);
+#pragma unroll 1
+    for (int row = 0; row < (TWO_D ? 1 : kRows); ++row) {
+        int u, v;
+        pixel_of<TWO_D>(c, sv, row, u, v);
+        if (u >= tl.n_u || v >= tl.n_v) continue;
+        if (SLAB && !may_reach_slab<F>(sf, g, u, v, sl.c0, sl.c1)) continue;
+        const int64_t k = ((int64_t)c.view * tl.n_u + u) * tl.n_v + v;
+        float y[NB];
+        bool any = false;
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            y[b] = MODE == 0 ? __ldg(sino + b * sstride + k) : 1.0f;
+            any |= y[b] != 0.0f;
+        }
+        if (!any) continue;
+        Ray ray;
+        if (LINE) {
+            // lanes along v walk detector columns (lines of fixed u), as line_project_kernel
+            const int st = line_setup_ray<F>(sv, g, tl.line == 1, u, v, ray);
+            if (st == 0 || (st == 2 && !setup_ray<F>(sv, g, u, v, ray))) continue;
+        } else if (!setup_ray<F>(sv, g, u, v, ray)) {
+            continue;
+        }
+        if (SLAB && !restrict_to_slab(ray, sl.c0, sl.c1)) continue;
+        if (NB == 1) {
+            walk_scatter(ray, vol, __fmul_rn(y[0], ray.scale));
+        } else {
+            float val[NB], unused[NB];
+#pragma unroll
+            for (int b = 0; b < NB; ++b) val[b] = __fmul_rn(y[b], ray.scale);
+            walk_dispatch<true, NB>(ray, nullptr, vol, vstride, val, unused);
+        }
     }
 }
 
@@ -1500,12 +1518,12 @@ int device_sm_count() {
 #define CT_MODE0_NB4 , 0, 4, false
 #define CT_MODE1_NB1 , 1, 1, false
 
-// Shared-line walks (t.line != 0, 3D): one block per kLinePixels x kLineRows pixel tile, the
-// line's crossing list in dynamic shared memory (8 bytes per outer-axis cell).
-template <bool SCATTER, int NB>
-cudaError_t launch_line(const ViewRec* views, const Grid& g, const Tiling& t, const float* vol_in,
-                        const float* sino_in, float* vol_out, float* sino_out, int64_t vstride,
-                        int64_t sstride, cudaStream_t stream) {
+// Shared-line forward projections (t.line != 0, 3D): one block per kLinePixels x kLineRows pixel
+// tile, the line's crossing list in dynamic shared memory (8 bytes per outer-axis cell).
+template <int NB>
+cudaError_t launch_line_project(const ViewRec* views, const Grid& g, const Tiling& t,
+                                const float* vol, int64_t vstride, float* sino, int64_t sstride,
+                                cudaStream_t stream) {
     const int64_t nblk = (int64_t)t.line_lane_tiles * t.n_views * t.line_row_tiles;
     if (nblk == 0) return cudaSuccess;
     const int a = g.fast == 0 ? 1 : 0, b = g.fast == 2 ? 1 : 2;
@@ -1513,29 +1531,47 @@ cudaError_t launch_line(const ViewRec* views, const Grid& g, const Tiling& t, co
     const size_t smem = sizeof(LineEntry) * (size_t)(g.n[a] + g.n[b]);
     const unsigned nb = (unsigned)nblk;
     if (g.fast == 2)
-        line_kernel<2, SCATTER, NB><<<nb, kLinePixels, smem, stream>>>(
-            views, g, t, vol_in, sino_in, vol_out, sino_out, vstride, sstride);
+        line_project_kernel<2, NB><<<nb, kLinePixels, smem, stream>>>(views, g, t, vol, vstride,
+                                                                      sino, sstride);
     else if (g.fast == 1)
-        line_kernel<1, SCATTER, NB><<<nb, kLinePixels, smem, stream>>>(
-            views, g, t, vol_in, sino_in, vol_out, sino_out, vstride, sstride);
+        line_project_kernel<1, NB><<<nb, kLinePixels, smem, stream>>>(views, g, t, vol, vstride,
+                                                                      sino, sstride);
     else
-        line_kernel<0, SCATTER, NB><<<nb, kLinePixels, smem, stream>>>(
-            views, g, t, vol_in, sino_in, vol_out, sino_out, vstride, sstride);
+        line_project_kernel<0, NB><<<nb, kLinePixels, smem, stream>>>(views, g, t, vol, vstride,
+                                                                      sino, sstride);
+    return cudaGetLastError();
+}
+
+// The backprojection over the same lines (per-ray tiles, line parameters).
+template <int NB>
+cudaError_t launch_line_backproject(const ViewRec* views, const Grid& g, const Tiling& t,
+                                    const float* sino, int64_t sstride, float* vol,
+                                    int64_t vstride, cudaStream_t stream) {
+    const unsigned nb = (unsigned)grid_for(t);
+    if (nb == 0) return cudaSuccess;
+    if (t.two_d) return cudaErrorInvalidValue;
+    if (g.fast == 2)
+        backproject_kernel<false, 2, 0, NB, false, true><<<nb, kThreads, 0, stream>>>(
+            views, g, t, sino, sstride, vol, vstride, SlabArgs{});
+    else if (g.fast == 1)
+        backproject_kernel<false, 1, 0, NB, false, true><<<nb, kThreads, 0, stream>>>(
+            views, g, t, sino, sstride, vol, vstride, SlabArgs{});
+    else
+        backproject_kernel<false, 0, 0, NB, false, true><<<nb, kThreads, 0, stream>>>(
+            views, g, t, sino, sstride, vol, vstride, SlabArgs{});
     return cudaGetLastError();
 }
 
 cudaError_t launch_project(const ViewRec* views, const Grid& g, const Tiling& t, const float* vol,
                            float* sino, cudaStream_t stream) {
-    if (t.line)
-        return launch_line<false, 1>(views, g, t, vol, nullptr, nullptr, sino, 0, 0, stream);
+    if (t.line) return launch_line_project<1>(views, g, t, vol, 0, sino, 0, stream);
     CT_LAUNCH_BY_AXIS(project_kernel, CT_NB1, views, g, t, vol, (int64_t)0, sino, (int64_t)0,
                       SlabArgs{});
 }
 
 cudaError_t launch_backproject(const ViewRec* views, const Grid& g, const Tiling& t,
                                const float* sino, float* vol, cudaStream_t stream) {
-    if (t.line)
-        return launch_line<true, 1>(views, g, t, nullptr, sino, vol, nullptr, 0, 0, stream);
+    if (t.line) return launch_line_backproject<1>(views, g, t, sino, 0, vol, 0, stream);
     CT_LAUNCH_BY_AXIS(backproject_kernel, CT_MODE0_NB1, views, g, t, sino, (int64_t)0, vol,
                       (int64_t)0, SlabArgs{});
 }
@@ -1550,15 +1586,9 @@ cudaError_t launch_project_batch(const ViewRec* views, const Grid& g, const Tili
                                  const float* vol, int64_t vstride, float* sino, int64_t sstride,
                                  cudaStream_t stream) {
     if (t.line) {
-        if (nb == 4)
-            return launch_line<false, 4>(views, g, t, vol, nullptr, nullptr, sino, vstride,
-                                         sstride, stream);
-        if (nb == 2)
-            return launch_line<false, 2>(views, g, t, vol, nullptr, nullptr, sino, vstride,
-                                         sstride, stream);
-        if (nb == 1)
-            return launch_line<false, 1>(views, g, t, vol, nullptr, nullptr, sino, vstride,
-                                         sstride, stream);
+        if (nb == 4) return launch_line_project<4>(views, g, t, vol, vstride, sino, sstride, stream);
+        if (nb == 2) return launch_line_project<2>(views, g, t, vol, vstride, sino, sstride, stream);
+        if (nb == 1) return launch_line_project<1>(views, g, t, vol, vstride, sino, sstride, stream);
         return cudaErrorInvalidValue;
     }
     if (nb == 4)
@@ -1577,15 +1607,9 @@ cudaError_t launch_backproject_batch(const ViewRec* views, const Grid& g, const 
                                      const float* sino, int64_t sstride, float* vol,
                                      int64_t vstride, cudaStream_t stream) {
     if (t.line) {
-        if (nb == 4)
-            return launch_line<true, 4>(views, g, t, nullptr, sino, vol, nullptr, vstride, sstride,
-                                        stream);
-        if (nb == 2)
-            return launch_line<true, 2>(views, g, t, nullptr, sino, vol, nullptr, vstride, sstride,
-                                        stream);
-        if (nb == 1)
-            return launch_line<true, 1>(views, g, t, nullptr, sino, vol, nullptr, vstride, sstride,
-                                        stream);
+        if (nb == 4) return launch_line_backproject<4>(views, g, t, sino, sstride, vol, vstride, stream);
+        if (nb == 2) return launch_line_backproject<2>(views, g, t, sino, sstride, vol, vstride, stream);
+        if (nb == 1) return launch_line_backproject<1>(views, g, t, sino, sstride, vol, vstride, stream);
         return cudaErrorInvalidValue;
     }
     if (nb == 4)
