@@ -380,19 +380,24 @@ FDK_L1_BYTES_PER_VOXEL_VIEW = 16  # the four bilinear taps of the filtered sinog
 FP32_LANES_PER_SM = 128
 
 
+# The cone workload's walk kernels (its detector columns share their outer-axis lines, and the
+# 256^3 volume fits in L2, so the forward projection reads one crossing list per line).
+FP_KERNEL, BP_KERNEL = "line_project_kernel", "backproject_kernel"
+
+
 def ncu_sol():
     """Figures COPIED from the committed ncu summaries under profiles/ (hand-kept notes of
     earlier captures of the same kernel source; not measured in this run): per walk kernel the
     ncu memory SOL, L1TEX, L2 and DRAM throughput percentages, and the pair's L2-only and
     memory-SOL fractions weighted by the captured durations.  None when a summary is missing or
     its recorded source hash differs from the current kernel source."""
-    fp, bp = profiled_sol("project_kernel"), profiled_sol("backproject_kernel")
+    fp, bp = profiled_sol(FP_KERNEL), profiled_sol(BP_KERNEL)
     if not fp or not bp or None in (fp["ms"], bp["ms"], fp["memory_sol_pct"],
                                     bp["memory_sol_pct"], fp["l2_pct"], bp["l2_pct"]):
         return None
     tot = fp["ms"] + bp["ms"]
     return {"source": "copied from committed profiles/*.md (not measured in this run)",
-            "project_kernel": fp, "backproject_kernel": bp,
+            FP_KERNEL: fp, BP_KERNEL: bp,
             "pair_l2_throughput_pct": (fp["l2_pct"] * fp["ms"] + bp["l2_pct"] * bp["ms"]) / tot,
             "pair_memory_sol_pct":
                 (fp["memory_sol_pct"] * fp["ms"] + bp["memory_sol_pct"] * bp["ms"]) / tot,
@@ -785,7 +790,7 @@ def run_ours(args, rank, world):
     fp_avg, bp_avg = sum(fp_ms) / len(fp_ms), sum(bp_ms) / len(bp_ms)
     walks = walk_roofline(U, fp_avg, bp_avg, peaks)
     dom = "bp" if bp_avg >= fp_avg else "fp"
-    kname = "backproject_kernel" if dom == "bp" else "project_kernel"
+    kname = BP_KERNEL if dom == "bp" else FP_KERNEL
     traffic, traffic_src = profiled_traffic(kname)
     clocks = clk.summary()
     line = {

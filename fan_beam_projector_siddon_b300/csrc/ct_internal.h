@@ -70,6 +70,11 @@ struct Tiling {
     // lines.
     int32_t line;
     int32_t line_lane_tiles, line_row_tiles;
+    // 3D backprojection tiles whose warps take every second pixel along the lanes' axis (two
+    // warps interleave over 64 pixels): 0 off; 1 lanes along v in every view, 16 (u) x 64 (v)
+    // tiles; 2 lanes along u, 64 x 16 tiles.  Counts of those tiles.
+    int32_t spread;
+    int32_t spread_tiles_u, spread_tiles_v;
 };
 
 // Shared-line tiles: pixels along the lanes per block (its threads), lines per block, and the

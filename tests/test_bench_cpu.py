@@ -96,8 +96,8 @@ def test_profile_figures_parse_or_are_withheld():
     """Traffic and ncu speed-of-light figures come from the committed profiles only while the
     kernel source matches the capture; otherwise they are None (never stale numbers)."""
     import bench
-    for kern, src in (("project_kernel", "siddon_kernels.cu"),
-                      ("backproject_kernel", "siddon_kernels.cu"),
+    for kern, src in ((bench.FP_KERNEL, "siddon_kernels.cu"),
+                      (bench.BP_KERNEL, "siddon_kernels.cu"),
                       ("fdk_gather_kernel", "fbp_kernels.cu")):
         traffic, path = bench.profiled_traffic(kern, src)
         sol = bench.profiled_sol(kern, src)
@@ -109,8 +109,9 @@ def test_profile_figures_parse_or_are_withheld():
         assert sol["ms"] > 0
     pair = bench.ncu_sol()
     if pair is not None:
-        lo = min(pair["project_kernel"]["memory_sol_pct"], pair["backproject_kernel"]["memory_sol_pct"])
-        hi = max(pair["project_kernel"]["memory_sol_pct"], pair["backproject_kernel"]["memory_sol_pct"])
+        fp, bp = pair[bench.FP_KERNEL], pair[bench.BP_KERNEL]
+        lo = min(fp["memory_sol_pct"], bp["memory_sol_pct"])
+        hi = max(fp["memory_sol_pct"], bp["memory_sol_pct"])
         assert lo <= pair["pair_memory_sol_pct"] <= hi
 
 
@@ -124,14 +125,14 @@ def test_l2_figures_of_the_walk_profiles():
     if pair is None:
         pytest.skip("walk summaries do not match the current kernel source")
     assert "not measured in this run" in pair["source"]
-    for name in ("project_kernel", "backproject_kernel"):
+    for name in (bench.FP_KERNEL, bench.BP_KERNEL):
         d = pair[name]
         text = open(os.path.join(bench.ROOT, d["source"])).read()
         pct = float(re.search(r"= ([0-9.]+) % of the L2 sector peak", text).group(1))
         assert 0 < d["l2_sector_gbs"] < d["l2_sector_peak_gbs"]
         assert abs(100 * d["l2_sector_gbs"] / d["l2_sector_peak_gbs"] - pct) < 0.1
-    lo = min(pair["project_kernel"]["l2_pct"], pair["backproject_kernel"]["l2_pct"])
-    hi = max(pair["project_kernel"]["l2_pct"], pair["backproject_kernel"]["l2_pct"])
+    lo = min(pair[bench.FP_KERNEL]["l2_pct"], pair[bench.BP_KERNEL]["l2_pct"])
+    hi = max(pair[bench.FP_KERNEL]["l2_pct"], pair[bench.BP_KERNEL]["l2_pct"])
     assert lo <= pair["pair_l2_throughput_pct"] <= hi
 
 
