@@ -1119,6 +1119,10 @@ __global__ void __launch_bounds__(kLinePixels, LineBlocks<NB>::value)
                         int64_t sstride) {
     extern __shared__ LineEntry line_list[];
     __shared__ ViewRec sv;
+    // the line's set-up, computed once per line by one thread (it is the same for the whole
+    // block; computed by every thread it cost register spills in every walk)
+    __shared__ LineRow L;
+    __shared__ int line_status;
     int b = (int)blockIdx.x;
     const int per_band = tl.n_views * tl.line_row_tiles;
     const int lane_tile = b / per_band;
@@ -1136,8 +1140,9 @@ __global__ void __launch_bounds__(kLinePixels, LineBlocks<NB>::value)
         const int line = line_tile * kLineRows + rr;
         if (line >= n_line) break;  // the same for the whole block
         const int u = along_v ? line : lane_px, v = along_v ? lane_px : line;
-        LineRow L;
-        const int st = line_row<F>(sv, g, along_v, line, L);  // the same for the whole block
+        if (threadIdx.x == 0) line_status = line_row<F>(sv, g, along_v, line, L);
+        __syncthreads();
+        const int st = line_status;
         if (st == 1) {
             build_line(L, line_list, (int)threadIdx.x, kLinePixels);
             __syncthreads();
@@ -1167,7 +1172,7 @@ __global__ void __launch_bounds__(kLinePixels, LineBlocks<NB>::value)
             }
             if (per_ray) ray_pixel<F, NB>(sv, g, u, v, k, vol, vstride, sino, sstride);
         }
-        if (st == 1) __syncthreads();  // the next line overwrites the list
+        __syncthreads();  // the next line overwrites the set-up and the list
     }
 }
 
