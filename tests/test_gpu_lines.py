@@ -97,6 +97,15 @@ def test_which_handles_share_lines(ct):
     assert surf.info.shared_lines == 0
     for _, make, want in CASES:
         assert ct.Geometry.from_workload(make()).info.shared_lines == want
+    # a volume larger than L2 (untilted 512^3 helix): per-ray walks
+    w4 = W.config(4)
+    helix = ct.Geometry(w4.beam, W.spiral_cone(8, 320.0, 512.0, 40.0, 2.0), w4.vol_shape,
+                        w4.voxel_spacing, w4.n_u, w4.n_v, w4.du, w4.dv)
+    assert helix.info.shared_lines == 0
+    # more outer-axis cells than a block's list holds (n_x + n_y > 6000), small enough for L2
+    wide = ct.Geometry(W.CONE, W.circular_cone(4, 5000.0, 9000.0), (2, 3100, 3100), 1.0, 64, 8,
+                       1.0, 1.0)
+    assert wide.info.shared_lines == 0
 
 
 def test_face_case_preconditions(ct):
@@ -196,3 +205,49 @@ def test_line_backprojection_is_the_exact_transpose(ct):
         gap, lhs, rhs = adjoint_gap(_cpu(g.project(torch_cuda(xr))), yr, xr,
                                     _cpu(g.backproject(torch_cuda(yr))))
         assert gap <= 1e-6, (seed, gap, lhs, rhs)
+
+
+@pytest.mark.parametrize("shape", [(2, 1, 1), (2, 2, 3), (3, 1, 2), (2, 3, 1), (5, 4, 6), (7, 1, 1)])
+def test_tiny_volumes_on_shared_lines(ct, shape):
+    """1-7-voxel volumes under a circular cone with an upright detector (shared lines; a volume
+    one cell high keeps the caller's x-fastest order, whose lanes do not share lines): every ray
+    against the oracle, the whole volume of A^T, and exact zeros for rays that miss."""
+    views = W.circular_cone(11, 12.0, 24.0)
+    args = (W.CONE, views, shape, 1.0, 19, 13, 0.9, 0.7)
+    g, go = ct.Geometry(*args), oracle.Geometry(*args)
+    assert g.info.shared_lines == 1
+    rng = np.random.default_rng(sum(shape))
+    x = rng.uniform(0.1, 1.0, size=shape).astype(np.float32)
+    y = _cpu(g.project(torch_cuda(x)))
+    L, _ = go.ray_lengths()
+    assert (L > 0).any()
+    bad = fp_violations(y, go.project(x), L, float(x.max()))
+    assert bad.size == 0, bad[:8]
+    yy = rng.uniform(0.1, 1.0, size=go.sino_shape).astype(np.float32)
+    assert rel_l2(_cpu(g.backproject(torch_cuda(yy))), go.backproject(yy)) <= BP_RTOL
+
+
+def test_lines_entering_through_a_face(ct):
+    """A short, wide volume seen from far above: every ray of a line enters through the top face
+    at its own position along the line, so no lane starts at the line's entry (each finds its
+    first list entry by counting), and many chords are short (the per-ray fallback)."""
+    views = W.circular_cone(13, 40.0, 90.0).copy()
+    views[:, 2] += 60.0     # source z, far above the slab
+    views[:, 5] -= 20.0     # detector centre z
+    shape = (6, 47, 53)
+    args = (W.CONE, views, shape, 1.0, 61, 67, 1.1, 1.4)
+    g, go = ct.Geometry(*args), oracle.Geometry(*args)
+    assert g.info.shared_lines == 1
+    x = W.ellipsoids_3d(6, 53, np.random.default_rng(4), axis_range=(3.0, 20.0))[:6, :47, :53]
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    y = _cpu(g.project(torch_cuda(x)))
+    L, _ = go.ray_lengths()
+    assert (L > 0).mean() > 0.3
+    bad = fp_violations(y, go.project(x, threads=8), L, float(np.abs(x).max()))
+    assert bad.size == 0, (bad.size, bad[:8])
+    rng = np.random.default_rng(5)
+    xr = rng.uniform(-1, 1, size=shape).astype(np.float32)
+    yr = rng.uniform(-1, 1, size=go.sino_shape).astype(np.float32)
+    gap, lhs, rhs = adjoint_gap(_cpu(g.project(torch_cuda(xr))), yr, xr,
+                                _cpu(g.backproject(torch_cuda(yr))))
+    assert gap <= 1e-6, (gap, lhs, rhs)
