@@ -697,8 +697,8 @@ __device__ __forceinline__ TileCoord tile_of_slab_block(const SlabArgs& sl, cons
 // memory, each entry holding the crossing's position and the cell (outer-axis part of the index)
 // before it; each thread then walks its own ray along the list and takes only its own inner-axis
 // crossings, so a step costs a shared-memory read instead of choosing between the two outer axes
-// (cone 256^3 x 360 views, forward: 25.5 -> 18.2 warp instructions per 32 updates, 14.6 ->
-// 11.4 ms).
+// (cone 256^3 x 360 views, forward: 25.5 -> 16.8 warp instructions per 32 updates, 14.6 -> 10.45
+// ms).
 //
 // Positions are measured along the line's outer-plane projection from its entry into the square,
 // s = (a - a_in) |d_outer| (voxel units; a is the ray parameter), so every ray of the line reads the
