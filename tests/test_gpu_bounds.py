@@ -148,3 +148,39 @@ def test_slab_tiled_walks_stay_in_bounds(pair, w, cells):
     torch.cuda.synchronize()
     assert _violations(lib) == 0
     assert torch.equal(fp, fpd)
+
+
+def _line_cases():
+    from tests.test_gpu_lines import CASES, _cone_through_faces
+    cases = [make() for _, make, _ in CASES]
+    views = W.circular_cone(13, 40.0, 90.0).copy()
+    views[:, 2] += 60.0
+    views[:, 5] -= 20.0
+    cases.append(W.Workload("faces-slab", W.CONE, views, (6, 47, 53), 1.0, 61, 67, 1.1, 1.4, 0,
+                            None))
+    for shape in [(2, 1, 1), (2, 2, 3), (7, 1, 1), (3, 4, 2)]:
+        cases.append(W.Workload(f"tiny-lines-{shape}", W.CONE, W.circular_cone(11, 12.0, 24.0),
+                                shape, 1.0, 19, 13, 0.9, 0.7, 0, None))
+    return cases
+
+
+@pytest.mark.parametrize("w", _line_cases(), ids=lambda w: w.name)
+def test_shared_line_walks_stay_in_bounds(pair, w):
+    """The shared-line walks (list projection, the backprojection over the line parameters, the
+    batched forms and the per-ray fallback of short chords): every voxel index stays in bounds,
+    and the forward results equal the release build's bit for bit."""
+    import torch
+    ct, dbg, lib = pair
+    _violations(lib)
+    g, gd = ct.Geometry.from_workload(w), dbg.Geometry.from_workload(w)
+    assert g.info.shared_lines > 0 and gd.info.shared_lines == g.info.shared_lines
+    x = torch_cuda(np.random.default_rng(1).uniform(0, 1, size=w.volume_shape))
+    y = torch_cuda(np.random.default_rng(2).uniform(0, 1, size=w.sino_shape))
+    fp, fpd = g.project(x), gd.project(x)
+    gd.backproject(y)
+    fb, fbd = g.project(torch.stack([x, x])), gd.project(torch.stack([x, x]))
+    gd.backproject(torch.stack([y, y, y, y]))
+    torch.cuda.synchronize()
+    assert _violations(lib) == 0
+    assert torch.equal(fp, fpd) and torch.equal(fb, fbd)
+    assert torch.equal(fb[1], fp)
