@@ -8,7 +8,8 @@ list per line (SIRT and CGLS keep the per-ray walks).
   geometries that exercise the lanes along v and along u, parallel lines at steep elevations,
   rays entering and leaving through the inner-axis faces (lanes that start part-way along the
   list, and short chords far along the line, which take the per-ray walk), per-axis pitches and
-  batched calls; SIRT on a shared-line handle against the oracle.
+  batched calls; SIRT on a shared-line handle against the oracle; ten random shared-line
+  geometries (cone orbits with offsets, steep parallel rays, random shapes and pitches).
 """
 import math
 
@@ -251,3 +252,60 @@ def test_lines_entering_through_a_face(ct):
     gap, lhs, rhs = adjoint_gap(_cpu(g.project(torch_cuda(xr))), yr, xr,
                                 _cpu(g.backproject(torch_cuda(yr))))
     assert gap <= 1e-6, (gap, lhs, rhs)
+
+
+def _random_line_geometry(seed):
+    """Random geometry whose detector v axis is exactly z in every view (so its lines share
+    their xy path): cone orbits with random radii, source and detector offsets (z included) and
+    in-plane detector rotations, or parallel rays at random elevations; random volume shape,
+    per-axis pitches, detector size and pitches."""
+    rng = np.random.default_rng(5000 + seed)
+    nz, ny, nx = (int(v) for v in rng.integers(3, 40, size=3))
+    sp = tuple(float(v) for v in rng.uniform(0.6, 1.4, size=3))
+    n_views = int(rng.integers(3, 12))
+    n_u, n_v = int(rng.integers(20, 90)), int(rng.integers(20, 90))
+    du, dv = float(rng.uniform(0.5, 1.5)), float(rng.uniform(0.5, 1.5))
+    views = []
+    for _ in range(n_views):
+        th = rng.uniform(0, 2 * math.pi)
+        c, s = math.cos(th), math.sin(th)
+        rot = rng.uniform(-0.3, 0.3)                      # detector turned about z
+        du_vec = [-math.sin(th + rot), math.cos(th + rot), 0.0]
+        if seed % 2 == 0:
+            sid = rng.uniform(40, 90)
+            sdd = sid + rng.uniform(20, 60)
+            src = [sid * c, sid * s, rng.uniform(-10, 10)]
+            det = [-(sdd - sid) * c + rng.uniform(-3, 3), -(sdd - sid) * s + rng.uniform(-3, 3),
+                   rng.uniform(-10, 10)]
+            views.append(src + det + du_vec + [0.0, 0.0, 1.0])
+        else:
+            ph = rng.uniform(-1.2, 1.2)                  # elevation of the rays
+            ray = [c * math.cos(ph), s * math.cos(ph), math.sin(ph)]
+            views.append(ray + list(rng.uniform(-2, 2, size=3)) + du_vec + [0.0, 0.0, 1.0])
+    beam = W.CONE if seed % 2 == 0 else W.PARALLEL3D
+    return W.Workload(f"random-lines-{seed}", beam, np.array(views), (nz, ny, nx), sp, n_u, n_v,
+                      du, dv, seed, None)
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_random_shared_line_geometries(ct, seed):
+    w = _random_line_geometry(seed)
+    g = ct.Geometry.from_workload(w)
+    go = oracle.Geometry.from_workload(w)
+    rng = np.random.default_rng(seed)
+    x = rng.uniform(0.1, 1.0, size=w.volume_shape).astype(np.float32)
+    L, _ = go.ray_lengths()
+    if g.info.volume_layout != 1:
+        pytest.skip("the volume order chosen for this shape is not z-fastest")
+    assert g.info.shared_lines == 1
+    assert (L > 0).mean() > 0.02
+    y = _cpu(g.project(torch_cuda(x)))
+    bad = fp_violations(y, go.project(x, threads=8), L, float(x.max()))
+    assert bad.size == 0, (bad.size, bad[:8])
+    yy = rng.uniform(0.1, 1.0, size=w.sino_shape).astype(np.float32)
+    assert rel_l2(_cpu(g.backproject(torch_cuda(yy))), go.backproject(yy, threads=8)) <= BP_RTOL
+    xr = rng.uniform(-1, 1, size=w.volume_shape).astype(np.float32)
+    yr = rng.uniform(-1, 1, size=w.sino_shape).astype(np.float32)
+    gap, lhs, rhs = adjoint_gap(_cpu(g.project(torch_cuda(xr))), yr, xr,
+                                _cpu(g.backproject(torch_cuda(yr))))
+    assert gap <= ADJ_RTOL, (gap, lhs, rhs)
