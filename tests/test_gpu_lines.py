@@ -1,7 +1,8 @@
 """Shared-line walks: when the detector axis along a block's lanes has no component on the two
 outer volume axes (and the volume fits in L2), the rays of one detector line share their
-outer-axis crossings, and the forward projection and the backprojection read them from one merged
-list per line (SIRT and CGLS keep the per-ray walks).
+outer-axis crossings: the forward projection reads them from one merged list per line, and the
+backprojection walks the same segments per ray over the line's parameters (SIRT and CGLS keep the
+per-ray walks).
 
 * which handles use them (info.shared_lines) and which keep the per-ray walk;
 * every ray of A and the whole volume of A^T against the oracle, and the adjoint identity, on
