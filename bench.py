@@ -621,10 +621,12 @@ def workload_leg(ct, torch, n: int, peaks, cpu_baseline: bool, reps: int = 3,
             fps.append(e[0].elapsed_time(e[1]))
             bps.append(e[2].elapsed_time(e[3]))
     fp, bp = statistics.median(fps), statistics.median(bps)
+    shared_lines = int(g.info.shared_lines)
     del vol, meas, sino, back, ws, flush
     torch.cuda.empty_cache()
     out = {"workload": w.name, "volume": list(w.vol_shape), "views": w.n_views,
-           "detector": [w.n_u, w.n_v], "updates_per_pass": U, "fp_ms": fp, "bp_ms": bp,
+           "detector": [w.n_u, w.n_v], "shared_lines": shared_lines, "updates_per_pass": U,
+           "fp_ms": fp, "bp_ms": bp,
            "views_per_s": {"fp": w.n_views / (fp * 1e-3), "bp": w.n_views / (bp * 1e-3)},
            "fp_updates_per_s": U / (fp * 1e-3), "bp_updates_per_s": U / (bp * 1e-3),
            "pair_updates_per_s": 2 * U / ((fp + bp) * 1e-3),
@@ -800,7 +802,8 @@ def run_ours(args, rank, world):
         "config": {"workload": w.name, "volume": list(w.vol_shape), "views": w.n_views,
                    "detector": [w.n_u, w.n_v], "updates_per_pass": U,
                    "l2": "flushed before each step (256 MiB write outside the timed events)",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}",
+                   "shared_lines": int(g.info.shared_lines)},
         "fp_ms": statistics.mean(fp_ms), "bp_ms": statistics.mean(bp_ms),
         "fp_updates_per_s": U / (fp_avg * 1e-3), "bp_updates_per_s": U / (bp_avg * 1e-3),
         "views_per_s": {"fp": w.n_views / (fp_avg * 1e-3), "bp": w.n_views / (bp_avg * 1e-3)},
