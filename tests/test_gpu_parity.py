@@ -540,3 +540,34 @@ def test_random_geometries_against_the_oracle(ct, seed):
     assert bad.size == 0, bad[:10]
     yy = rng.uniform(-1.0, 1.0, size=go.sino_shape).astype(np.float32)
     assert rel_l2(_cpu(g.backproject(torch_cuda(yy))), go.backproject(yy)) <= BP_RTOL
+
+
+@pytest.mark.parametrize("make", [lambda: W.small_config(1), lambda: W.small_config(2),
+                                  lambda: W.small_config(3), lambda: W.small_config(4),
+                                  lambda: W.small_config(5), lambda: W.anisotropic_config("cone"),
+                                  lambda: W.anisotropic_config("tilt"),
+                                  lambda: W.anisotropic_config("fan")],
+                         ids=["parallel2d", "fan2d", "cone", "spiral", "tilt", "cone-aniso",
+                              "tilt-aniso", "fan-aniso"])
+def test_matched_transpose_entry_by_entry(ct, make):
+    """A^T is the transpose of A entry by entry, bit for bit: the projection of a unit voxel e_i
+    read at ray r equals the backprojection of the unit ray e_r read at voxel i (the forward and
+    adjoint walks take the same segments with the same operations; each entry is one segment
+    length times the ray's length factor, rounded once, and the zero terms add nothing)."""
+    w = make()
+    g = ct.Geometry.from_workload(w)
+    nvox, nray = int(np.prod(w.volume_shape)), int(np.prod(w.sino_shape))
+    rng = np.random.default_rng(17)
+    checked = 0
+    for i in rng.choice(nvox, size=8, replace=False):
+        e = np.zeros(nvox, np.float32)
+        e[i] = 1.0
+        col = _cpu(g.project(torch_cuda(e.reshape(w.volume_shape)))).reshape(-1)
+        rays = np.nonzero(col)[0]
+        for r in rng.choice(rays, size=min(6, rays.size), replace=False):
+            er = np.zeros(nray, np.float32)
+            er[r] = 1.0
+            row = _cpu(g.backproject(torch_cuda(er.reshape(w.sino_shape)))).reshape(-1)
+            assert row[i] == col[r], (int(i), int(r), float(row[i]), float(col[r]))
+            checked += 1
+    assert checked >= 12, checked
