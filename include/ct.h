@@ -100,9 +100,11 @@ typedef struct {
                                  component on the two outer volume axes, so the rays of one
                                  detector column (row) share their outer-axis crossings, and the
                                  volume fits in the device's L2: the untiled forward projection
-                                 reads them from one list per line.  0: per-ray walks only.
-                                 The backprojection always walks per ray; the two walks agree
-                                 within float32 rounding of the crossing positions.        */
+                                 reads them from one list per line, and the backprojection
+                                 walks the same segments per ray (still the exact transpose).
+                                 0: per-ray parameters only.  The two parameterisations agree
+                                 within float32 rounding of the crossing positions; SIRT and
+                                 CGLS always use the per-ray one.                          */
 } ct_geometry_info;
 
 /*
