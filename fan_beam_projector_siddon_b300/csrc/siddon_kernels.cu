@@ -82,26 +82,31 @@ struct Ray {
 #endif
 };
 
-// Crossings of one axis by a walk that enters at coordinate ci, leaves at co (voxel units) and
-// advances the coordinate by dh per unit of its parameter: the entry cell i0 and the exit cell,
-// both clamped into [0, top], the number n of planes between them, the first crossing t0 and the
-// pitch dt (parameter units) and the signed element step of a crossing.
+// Crossings of one axis by a walk that enters at coordinate ci, leaves at co (voxel units,
+// float64) and advances the coordinate by dh per unit of its parameter: the entry cell i0 and the
+// exit cell, both clamped into [0, top], the number n of planes between them, the first crossing
+// t0 and the pitch dt (parameter units) and the signed element step of a crossing.  The cells and
+// the distance from the entry to the first plane are taken in float64 and only that distance (at
+// most one cell) is rounded to float32: a float32 entry coordinate is off by up to half an ulp of
+// the coordinate (1e-6 cells near cell 30), which t0 = distance / |dh| multiplies by 1 / |dh|, so on
+// an axis the ray crosses at a grazing angle it moved the crossing by 2e-4 cells.
 struct AxisWalk {
     float t0, dt;
     int n, step, i0;
 };
 
-__device__ __forceinline__ AxisWalk axis_walk(float ci, float co, float dh, int top, int stride) {
+__device__ __forceinline__ AxisWalk axis_walk(double ci, double co, float dh, int top,
+                                              int stride) {
     AxisWalk w;
     int i0, i1;
     if (dh > 0.0f) {
-        i0 = (int)floorf(ci);
-        i1 = (int)ceilf(co) - 1;
+        i0 = (int)floor(ci);
+        i1 = (int)ceil(co) - 1;
     } else if (dh < 0.0f) {
-        i0 = (int)ceilf(ci) - 1;
-        i1 = (int)floorf(co);
+        i0 = (int)ceil(ci) - 1;
+        i1 = (int)floor(co);
     } else {
-        i0 = (int)floorf(ci);
+        i0 = (int)floor(ci);
         i1 = i0;
     }
     i0 = min(max(i0, 0), top);
@@ -113,13 +118,13 @@ __device__ __forceinline__ AxisWalk axis_walk(float ci, float co, float dh, int 
         const float inv = fminf(1.0f / dh, 1e28f);
         w.n = max(0, i1 - i0);
         w.dt = inv;
-        w.t0 = __fmul_rn(__fsub_rn((float)(i0 + 1), ci), inv);
+        w.t0 = __fmul_rn((float)((double)(i0 + 1) - ci), inv);
         w.step = stride;
     } else if (dh < 0.0f) {
         const float inv = fminf(-1.0f / dh, 1e28f);
         w.n = max(0, i0 - i1);
         w.dt = inv;
-        w.t0 = __fmul_rn(__fsub_rn(ci, (float)i0), inv);
+        w.t0 = __fmul_rn((float)(ci - (double)i0), inv);
         w.step = -stride;
     } else {
         w.n = 0;
@@ -205,9 +210,8 @@ __device__ __forceinline__ bool setup_ray(const ViewRec& vr, const Grid& g, int 
 #pragma unroll
     for (int a = 0; a < 3; ++a) {
         const int slot = a == F ? 2 : (a == A ? 0 : 1);
-        const AxisWalk w = axis_walk((float)__fma_rn(amin, d[a], o[a]),
-                                     (float)__fma_rn(amax, d[a], o[a]), __fmul_rn(df[a], inv_dl),
-                                     g.n[a] - 1, g.stride[a]);
+        const AxisWalk w = axis_walk(__fma_rn(amin, d[a], o[a]), __fma_rn(amax, d[a], o[a]),
+                                     __fmul_rn(df[a], inv_dl), g.n[a] - 1, g.stride[a]);
         r.n[slot] = w.n;
         r.dt[slot] = w.dt;
         r.t0[slot] = w.t0;
@@ -786,8 +790,7 @@ __device__ __forceinline__ int line_row(const ViewRec& vr, const Grid& g, bool a
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
         const int a = j == 0 ? A : B;
-        const AxisWalk w = axis_walk((float)__fma_rn(amin, d[j], o[j]),
-                                     (float)__fma_rn(amax, d[j], o[j]),
+        const AxisWalk w = axis_walk(__fma_rn(amin, d[j], o[j]), __fma_rn(amax, d[j], o[j]),
                                      __fmul_rn(L.df[j], L.inv_dl), g.n[a] - 1, g.stride[a]);
         L.t0[j] = w.t0;
         L.dt[j] = w.dt;
@@ -869,7 +872,7 @@ __device__ __forceinline__ bool line_ray(const ViewRec& vr, const Grid& g, const
     r.fac = __fmul_rn(phys, L.inv_dl);
     r.s0 = __fmul_rn((float)(amin - L.amin), L.dl);
     r.s1 = __fmul_rn((float)(amax - L.amin), L.dl);
-    const AxisWalk w = axis_walk((float)__fma_rn(amin, d, o), (float)__fma_rn(amax, d, o),
+    const AxisWalk w = axis_walk(__fma_rn(amin, d, o), __fma_rn(amax, d, o),
                                  __fmul_rn(df[F], L.inv_dl), g.n[F] - 1, g.stride[F]);
     r.n = w.n;
     r.dt = w.dt;

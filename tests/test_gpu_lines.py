@@ -10,7 +10,8 @@ per-ray walks).
   rays entering and leaving through the inner-axis faces (lanes that start part-way along the
   list, and short chords far along the line, which take the per-ray walk), per-axis pitches and
   batched calls; SIRT on a shared-line handle against the oracle; ten random shared-line
-  geometries (cone orbits with offsets, steep parallel rays, random shapes and pitches).
+  geometries (cone orbits with offsets, steep parallel rays, random shapes and pitches), and the
+  geometries whose short chords cross a plane at a grazing angle far along an axis.
 """
 import math
 
@@ -319,3 +320,19 @@ def test_random_shared_line_geometries(ct, seed):
     gap, lhs, rhs = adjoint_gap(_cpu(g.project(torch_cuda(xr))), yr, xr,
                                 _cpu(g.backproject(torch_cuda(yr))))
     assert gap <= ADJ_RTOL, (gap, lhs, rhs)
+
+
+# Seeds whose geometries have short chords with a crossing taken at a grazing angle far from the
+# volume's corner (z cell 30 of 35 at 1/|dh| = 430 on seed 458): a float32 entry coordinate moved
+# such a crossing by 2e-4 cells, two to four times the per-ray tolerance of those chords.
+@pytest.mark.parametrize("seed", [458, 603, 649, 665, 982, 1096, 1245, 1990])
+def test_grazing_crossings_far_along_an_axis(ct, seed):
+    w = _random_line_geometry(seed)
+    g = ct.Geometry.from_workload(w)
+    go = oracle.Geometry.from_workload(w)
+    x = np.random.default_rng(seed).uniform(0.1, 1.0, size=w.volume_shape).astype(np.float32)
+    L, _ = go.ray_lengths()
+    y = _cpu(g.project(torch_cuda(x)))
+    bad = fp_violations(y, go.project(x, threads=8), L, float(x.max()))
+    assert bad.size == 0, (bad.size, bad[:8])
+

@@ -505,7 +505,8 @@ def _random_frames_2d(rng, n, beam):
     return np.array(views)
 
 
-@pytest.mark.parametrize("seed", range(8))
+# (seed 493: a short chord with a grazing crossing, see test_grazing_crossings_far_along_an_axis)
+@pytest.mark.parametrize("seed", [*range(8), 493])
 def test_random_geometries_against_the_oracle(ct, seed):
     """Random frames, volume shapes, per-axis pitches and detectors for the four beams: every
     ray of A against the oracle and A^T in relative L2 (exercises the walk's specialised and
