@@ -603,6 +603,36 @@ def test_anisotropic_adjoint_and_rows(kind):
                                    rtol=0, atol=1e-13)
 
 
+def test_grazing_crossings_far_along_an_axis():
+    """Short chords that cross a plane at a grazing angle far from the volume's corner (the
+    crossing's position along the ray is the plane distance over a tiny direction component):
+    the oracle's segments equal the pure-Python per-voxel clip.  The first ray is a corner clip of
+    a 6 x 9 x 35 volume that crosses z plane 30 at 1/|dz| = 430 voxel lengths per cell.  Both
+    sides round plane positions of ~10 units in float64 and a grazing crossing multiplies that by
+    up to 1/|dz| = 1000, hence 1e-10 (a float32 plane position would be off by 1e-4)."""
+    vol_shape, s_zyx = (35, 9, 6), (0.6582214119560114, 1.1847855166608365, 0.8213995296135223)
+    s_xyz = s_zyx[::-1]
+    rays = [(np.array([78.47037568, -29.22880575, 8.03421051]),
+             np.array([-112.59456299, 50.87213812, 0.28538153]))]
+    rng = np.random.default_rng(29)
+    half = 0.5 * np.array(vol_shape[::-1], dtype=float) * np.array(s_xyz)
+    for _ in range(12):
+        # through a point near a vertical edge of the box, almost level, crossing a high z plane
+        th = rng.uniform(0, 2 * math.pi)
+        d = np.array([math.cos(th), math.sin(th), rng.choice([-1, 1]) * rng.uniform(1e-3, 3e-3)])
+        edge = np.array([rng.choice([-1, 1]) * half[0], rng.choice([-1, 1]) * half[1],
+                         (rng.integers(20, 34) - vol_shape[0] / 2) * s_zyx[0]])
+        p = edge + rng.uniform(-0.3, 0.3, 3) * np.array([1, 1, 0]) + np.array([0, 0, 1e-4])
+        rays.append((p - 40.0 * d, d))
+    hit = 0
+    for e, d in rays:
+        idx, w = oracle.line_segments(e, d, -np.inf, np.inf, vol_shape, s_zyx)
+        ref = _brute_row_python_aniso(e, d, -np.inf, np.inf, vol_shape, s_xyz, 3)
+        np.testing.assert_allclose(_dense(idx, w, vol_shape), ref, rtol=0, atol=1e-10)
+        hit += int(len(set((np.nonzero(ref.reshape(-1))[0] // (9 * 6)).tolist())) >= 2)
+    assert hit >= 4   # rays whose chord crosses a z plane
+
+
 # ---------------------------------------------------------------------------------------------
 # parameterized detector surfaces
 # ---------------------------------------------------------------------------------------------
