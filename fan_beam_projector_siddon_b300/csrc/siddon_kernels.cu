@@ -7,9 +7,10 @@
 //
 // Per ray:
 //   1. float64: pixel point, ray origin/direction, slab clip of the parameter range against the
-//      box [0, nx] x [0, ny] x [0, nz] (voxel units), entry and exit points;
-//   2. float32: per-axis first-crossing distance t0, crossing pitch dt and crossing count n from
-//      the entry/exit voxels, then the incremental Siddon walk.  The k-th crossing of axis a is
+//      box [0, nx] x [0, ny] x [0, nz] (voxel units), entry and exit points, and per axis the
+//      entry and exit cells (hence the crossing count n) and the distance to the first plane;
+//   2. float32: per-axis first-crossing distance t0 (that distance over the direction component)
+//      and crossing pitch dt, then the incremental Siddon walk.  The k-th crossing of axis a is
 //      always fmaf(k, dt_a, t0_a) (no running sums), so any kernel that walks the same ray gets
 //      bit-identical crossing positions and therefore bit-identical chord weights.
 // The walk takes exactly n_x + n_y + n_z steps and moves each axis at most n_a times from an

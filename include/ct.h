@@ -204,8 +204,10 @@ CT_API ct_status ct_geometry_set_slabs(ct_geometry *geom, int32_t slab_cells);
  * d_workspace, workspace_bytes
  *            device scratch of at least info.workspace_bytes (may be NULL when that is 0);
  *            used for the kernels' internal volume order.  Must not overlap the other buffers.
- * Float32 walk with float64 entry/exit clipping; per-ray results match the float64 definition
- * within 1e-4 of (ray chord length x max |x|).
+ * Float32 walk with float64 entry/exit clipping (the entry and exit cells and the distance to
+ * each axis's first plane are also taken in float64, so a plane crossed at a grazing angle keeps
+ * its position); per-ray results match the float64 definition within 1e-4 of (ray chord length
+ * x max |x|).
  */
 CT_API ct_status ct_project(const ct_geometry *geom, const float *d_volume, float *d_sino,
                      void *d_workspace, size_t workspace_bytes, struct CUstream_st *stream);
