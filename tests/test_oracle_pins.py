@@ -471,6 +471,31 @@ def _dense_matrix(g):
     return np.array(rows)
 
 
+def test_sirt_converges_to_the_weighted_least_squares_solution():
+    """SIRT from x = 0 with relaxation in (0, 2) converges to the minimiser of the R-weighted
+    residual ||A x - y||_R (R = 1 / row sums); with A of full column rank and inconsistent data
+    that is the unique solution of A^T R A x = A^T R y.  A and R come from the per-voxel brute
+    force; the unweighted least-squares solution differs by ~0.7 here, so a wrong R fails."""
+    rng = np.random.default_rng(31)
+    rec = []
+    for th in np.linspace(0.1, 3.0, 7):
+        r = np.array([math.cos(th), math.sin(th), 0.35])
+        r /= np.linalg.norm(r)
+        u = np.array([-math.sin(th), math.cos(th), 0.0])
+        rec.append(np.concatenate([r, rng.uniform(-0.2, 0.2, 3), u, np.cross(r, u)]))
+    g = _geom(W.PARALLEL3D, np.array(rec), (2, 3, 3), 1.0, 6, 5, 0.7, 0.7)
+    A = _dense_matrix(g)
+    assert np.linalg.matrix_rank(A) == A.shape[1]
+    y = rng.uniform(0.5, 1.5, size=g.sino_shape)
+    rs = A.sum(axis=1)
+    R = np.where(rs > 0, 1.0 / np.where(rs > 0, rs, 1.0), 0.0)
+    x_ls = np.linalg.solve(A.T @ (R[:, None] * A), A.T @ (R * y.reshape(-1)))
+    x, _ = g.sirt(y, 6000)
+    np.testing.assert_allclose(x.reshape(-1), x_ls, rtol=0, atol=1e-9)
+    x_un = np.linalg.lstsq(A, y.reshape(-1), rcond=None)[0]
+    assert np.abs(x_un - x_ls).max() > 0.1
+
+
 def test_cgls_reaches_the_least_squares_solution():
     """In exact arithmetic CGLS from x = 0 reaches the minimum-norm least-squares solution of
     min ||A x - y|| within rank(A) steps; checked against numpy's SVD-based lstsq of the explicit
